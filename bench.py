@@ -1,0 +1,363 @@
+"""Benchmark: one block-quantized MoE layer on the T=4 MTP verify batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full layer forward (router, top-k, permutation, gate/up +
+SwiGLU, down, combine) over one synthetic batch, through the library's C ABI.
+Prints ONE JSON line (rank 0).  Multi-GPU runs are independent replicas, one
+per rank (the layer has no data-path exchange): value = max-over-ranks time /
+layers processed by all ranks.
+
+L2 hygiene: the timed loop rotates over ``--copies`` separately allocated
+copies of the layer weights (each copy's bytes exceed the 129 MB L2).
+
+--impl reference times the oracle (plain numpy CPU code) on the same
+workload, extrapolated from bounded samples; it is a deliberately slow
+baseline, not a competitor.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/MoE layer and effective HBM GB/s (T=4 verify, 352×top-8) vs 8 TB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--workload", default="verify_q8")
+    p.add_argument("--copies", type=int, default=4)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w, n_unique):
+    """Router weight + bias + unique routed experts + shared expert + x + y,
+    at the serialised sizes of their formats."""
+    def mat(fmt, rows, cols):
+        return rows * (cols // 32 * 34 if fmt == 2 else cols // 256 * 144)
+    per_expert = 2 * mat(w.routed_fmt, w.I, w.H) + mat(w.routed_fmt, w.H, w.I)
+    shared = 2 * mat(w.shared_fmt, w.I_shared, w.H) + mat(w.shared_fmt, w.H, w.I_shared) if w.I_shared else 0
+    router = w.E * w.H * 4 + (w.E * 4 if w.bias_std is not None else 0)
+    act = 2 * w.T * w.H * 2
+    return router + n_unique * per_expert + shared + act
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 8 for i in range(4)
+                          if r[4 + i].lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+def traffic_record(kernel_src):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    rec = d.get(h)
+    return rec
+
+
+def cpu_baseline_sample(w, budget_s=20.0):
+    """The oracle on a bounded sample of the workload (one layer forward on a
+    T-token batch per repetition), on this host's cores; returns µs/layer."""
+    import torch
+    from oracle import moe as omoe
+    from tests._oracle_layer import synth_oracle_layer
+    from block_quantized_moe_layer_gb300 import synth
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    times = []
+    variant = 0
+    t_end = time.time() + budget_s
+    while time.time() < t_end and variant < 8:
+        ol = synth_oracle_layer(w, dev)
+        x = synth.activations(w, "cpu", variant=variant).float().numpy()
+        r = omoe.route(x, ol)
+        for e in r["act"]:          # quantise outside the timed part (weight preparation)
+            ol.expert(int(e))
+        t0 = time.perf_counter()
+        omoe.forward(x, ol)
+        times.append(time.perf_counter() - t0)
+        variant += 1
+    return statistics.median(times) * 1e6, len(times)
+
+
+def run_ours(args):
+    import torch
+    import block_quantized_moe_layer_gb300 as pkg
+    from block_quantized_moe_layer_gb300 import synth
+    from block_quantized_moe_layer_gb300.workloads import synthetic_layer
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = synth.WORKLOADS[args.workload]
+    layers = [synthetic_layer(w, pkg.ACT_BF16, T_max=w.T)[0] for _ in range(args.copies)]
+    x = synth.activations(w, "cuda")
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    for i in range(max(args.warmup, 3)):
+        layers[i % len(layers)].forward(x, y)
+    torch.cuda.synchronize()
+    for L in layers:
+        L.status()
+    offs = layers[0].routing(w.T)[2]
+    n_unique = int((offs[1:] > offs[:-1]).sum().item())
+    alg = algorithmic_bytes(w, n_unique)
+
+    # timed region: exactly K steps; every 8th launch is bracketed by events
+    sample_every = 8
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps // sample_every + 1)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        L = layers[i % len(layers)]
+        if i % sample_every == 0:
+            a, b = evs[i // sample_every]
+            a.record(stream)
+            L.forward(x, y)
+            b.record(stream)
+        else:
+            L.forward(x, y)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    for L in layers:
+        L.status()
+    total_ms = t_start.elapsed_time(t_stop)
+    launch_us = [a.elapsed_time(b) * 1e3 for (a, b) in evs[: (args.steps + sample_every - 1) // sample_every]]
+    kern_us = statistics.mean(launch_us)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = t.item()
+    us_per_layer = total_ms * 1e3 / (args.steps * world)
+
+    # end to end: pinned host x -> device, forward, device -> pinned host y, every step
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(x)
+    e2e_steps = min(args.e2e_steps, args.steps)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        layers[i % len(layers)].forward(xd, y)
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1e3 / e2e_steps
+    assert torch.equal(yh.cuda(), y)
+
+    peak, peak_src = measured_peaks()
+    achieved = alg / (kern_us * 1e-6) / 1e9
+    src = os.path.join(ROOT, "block_quantized_moe_layer_gb300", "csrc", "small_t.cu")
+    tr = traffic_record(src)
+    out = {
+        "metric": METRIC,
+        "value": round(us_per_layer, 3),
+        "unit": "us/layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "q8_0 weights x bf16 activations (int dp4a, fp32 accumulate)",
+        "data": "synthetic (seeded, random-init weights of the workload's shapes)",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.top_k, "I": w.I,
+                   "I_shared": w.I_shared, "routed_fmt": ["f32", "bf16", "q8_0", "q4ks"][w.routed_fmt],
+                   "unique_experts": n_unique, "algorithmic_bytes": alg,
+                   "l2": f"rotating {len(layers)} weight copies of {layers[0].weight_bytes / 1e9:.2f} GB (> L2)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(w.T / (us_per_layer * 1e-6), 1),
+        "effective_gbs": round(alg / (us_per_layer * 1e-6) / 1e9, 1),
+        "frac_of_8tbs": round(alg / (us_per_layer * 1e-6) / 8e12, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": tr["bytes_per_launch"] if tr else None,
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "moe_small_t_kernel", "kernel_us": round(kern_us, 3)},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+                "d2h_bytes_per_step": yh.numel() * yh.element_size(), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, n = cpu_baseline_sample(w)
+        out["cpu_baseline"] = {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(),
+                               "kind": "oracle",
+                               "sample": f"{n} full layer forwards (T={w.T}, distinct x), median; numpy fp64, "
+                                         f"BLAS on up to {os.cpu_count()} threads"}
+    for L in layers:
+        L.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def run_reference(args):
+    """The oracle on bounded samples of the workload: each step runs the
+    oracle's routing for the batch plus the FFN of a slice of the touched
+    row blocks; µs/layer is extrapolated from time per row block."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from oracle import moe as omoe
+    from tests._oracle_layer import synth_oracle_layer
+    from block_quantized_moe_layer_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ol = synth_oracle_layer(w, dev)
+    x = synth.activations(w, "cpu").float().numpy()
+    r = omoe.route(x, ol)
+    # work list: 32-row blocks of every touched matrix with the rows they multiply
+    def sub(q, r0):
+        rb = q.data.shape[1]
+        return omoe.QTensor(q.fmt, 32, q.cols, q.data[r0:r0 + 32].reshape(32, rb))
+    blocks = []
+    items = []
+    for e in r["act"]:
+        e = int(e)
+        sl = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
+        items.append((ol.expert(e), x[sl // w.top_k]))
+    items.append((ol.shared, x))
+    for ex, xr in items:
+        u = xr @ ex.gate.dense().T
+        h = omoe.silu(u) * (xr @ ex.up.dense().T)
+        blocks += [(ex.gate, r0, xr) for r0 in range(0, ex.gate.rows, 32)]
+        blocks += [(ex.up, r0, xr) for r0 in range(0, ex.up.rows, 32)]
+        blocks += [(ex.down, r0, h) for r0 in range(0, ex.down.rows, 32)]
+
+    def block(i):
+        q, r0, inp = blocks[i % len(blocks)]
+        return inp @ sub(q, r0).dense().T
+    n_blocks = len(blocks)
+    t0 = time.perf_counter()
+    omoe.route(x, ol)
+    t_route = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    block(0)
+    t_blk = max(time.perf_counter() - t0, 1e-5)
+    budget = 90.0
+    per_step = int(max(1, min(n_blocks, budget / max(1, args.steps + args.warmup) / t_blk)))
+    i = 0
+    for _ in range(args.warmup):
+        for _ in range(per_step):
+            block(i)
+            i += 1
+    samples = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for _ in range(per_step):
+            block(i)
+            i += 1
+        samples.append((time.perf_counter() - t0) / per_step)
+    us = (t_route + statistics.median(samples) * n_blocks) * 1e6
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp64 (numpy oracle)", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.top_k, "I": w.I},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"routing of the batch once + {per_step} of the layer's {n_blocks} "
+                                   f"32-row weight blocks (dequantise + multiply) per step; "
+                                   f"time per block x blocks per layer"},
+        "e2e": {"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

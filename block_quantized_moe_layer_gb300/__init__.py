@@ -1,0 +1,216 @@
+"""Block-quantized MoE layer for MTP verify batches on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/moe_layer.h``: argument
+marshalling only.  Every step of the layer runs in the library's CUDA kernels;
+there is no CPU fallback, and importing the binding's functions fails loudly
+when the library has not been built (``python -m
+block_quantized_moe_layer_gb300._build``).  PyTorch provides device memory
+and streams.
+"""
+import ctypes
+import os
+
+from ._build import LIB
+
+MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_EFORMAT, MOE_ETIMEOUT, MOE_ECUDA = 0, -1, -2, -3, -4, -5
+FMT_F32, FMT_BF16, FMT_Q8_0, FMT_Q4KS = 0, 1, 2, 3
+ACT_BF16, ACT_F32 = 0, 1
+
+_c = ctypes
+EXPORTS = (
+    "moe_layer_create", "moe_forward", "moe_get_routing", "moe_layer_status",
+    "moe_layer_weight_bytes", "moe_layer_workspace_bytes", "moe_layer_destroy",
+    "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
+    "mtp_verify_accept", "moe_last_error",
+)
+
+
+class MoeTensor(_c.Structure):
+    _fields_ = [("fmt", _c.c_int32), ("reserved", _c.c_int32), ("rows", _c.c_int64),
+                ("cols", _c.c_int64), ("data", _c.c_void_p), ("nbytes", _c.c_size_t)]
+
+
+class MoeLayerDesc(_c.Structure):
+    _fields_ = [("H", _c.c_int32), ("E", _c.c_int32), ("top_k", _c.c_int32), ("I", _c.c_int32),
+                ("I_shared", _c.c_int32), ("T_max", _c.c_int32), ("act_dtype", _c.c_int32),
+                ("reserved", _c.c_int32), ("router_w", MoeTensor), ("router_b", MoeTensor),
+                ("gate", _c.POINTER(MoeTensor)), ("up", _c.POINTER(MoeTensor)),
+                ("down", _c.POINTER(MoeTensor)), ("sh_gate", MoeTensor), ("sh_up", MoeTensor),
+                ("sh_down", MoeTensor)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise ImportError(f"CUDA library not built: {LIB} is missing")
+        L = _c.CDLL(LIB)
+        vp, i32, i64, sz = _c.c_void_p, _c.c_int32, _c.c_int64, _c.c_size_t
+        sig = {
+            "moe_layer_create": (_c.c_int, [_c.POINTER(MoeLayerDesc), vp, _c.POINTER(vp)]),
+            "moe_forward": (_c.c_int, [vp, vp, i32, vp, vp]),
+            "moe_get_routing": (_c.c_int, [vp, vp, vp, vp, vp, vp]),
+            "moe_layer_status": (_c.c_int, [vp, vp]),
+            "moe_layer_weight_bytes": (sz, [vp]),
+            "moe_layer_workspace_bytes": (sz, [vp]),
+            "moe_layer_destroy": (None, [vp]),
+            "moe_quantized_bytes": (sz, [i32, i64, i64]),
+            "moe_quantize": (_c.c_int, [i32, vp, i64, i64, vp, vp]),
+            "mtp_verify_accept_workspace_bytes": (sz, [i32, i32]),
+            "mtp_verify_accept": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp, sz, vp]),
+            "moe_last_error": (_c.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != MOE_OK:
+        raise MoEError(rc, lib().moe_last_error().decode())
+    return rc
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def quantized_bytes(fmt, rows, cols):
+    return lib().moe_quantized_bytes(fmt, rows, cols)
+
+
+def quantize(fmt, w, out=None, stream=None):
+    """fp32 [rows, cols] CUDA tensor -> serialised uint8 CUDA tensor."""
+    import torch
+    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous()
+    rows, cols = w.shape
+    n = quantized_bytes(fmt, rows, cols)
+    if n == 0:
+        raise MoEError(MOE_EFORMAT, f"shape {tuple(w.shape)} does not fit format {fmt}")
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=w.device)
+    _check(lib().moe_quantize(fmt, w.data_ptr(), rows, cols, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def _tensor(fmt, rows, cols, t):
+    if t is None:
+        return MoeTensor(fmt, 0, rows, cols, None, 0)
+    return MoeTensor(fmt, 0, rows, cols, t.data_ptr(), t.numel() * t.element_size())
+
+
+class Layer:
+    """One MoE layer resident on the current CUDA device.
+
+    experts: list of E tuples (fmt, gate, up, down) of serialised byte
+    tensors (host or device); shared: one such tuple or None.
+    """
+
+    def __init__(self, H, E, top_k, I, I_shared, T_max, act, router_w, router_b, experts, shared,
+                 stream=None):
+        self.H, self.E, self.top_k, self.I, self.I_shared = H, E, top_k, I, I_shared
+        self.T_max, self.act = T_max, act
+        gate = (MoeTensor * E)()
+        up = (MoeTensor * E)()
+        down = (MoeTensor * E)()
+        for e, (fmt, g, u, d) in enumerate(experts):
+            gate[e] = _tensor(fmt, I, H, g)
+            up[e] = _tensor(fmt, I, H, u)
+            down[e] = _tensor(fmt, H, I, d)
+        desc = MoeLayerDesc()
+        desc.H, desc.E, desc.top_k, desc.I, desc.I_shared = H, E, top_k, I, I_shared
+        desc.T_max, desc.act_dtype, desc.reserved = T_max, act, 0
+        desc.router_w = _tensor(FMT_F32, E, H, router_w)
+        desc.router_b = _tensor(FMT_F32, 1, E, router_b)
+        desc.gate, desc.up, desc.down = gate, up, down
+        if shared is not None:
+            sfmt, g, u, d = shared
+            desc.sh_gate = _tensor(sfmt, I_shared, H, g)
+            desc.sh_up = _tensor(sfmt, I_shared, H, u)
+            desc.sh_down = _tensor(sfmt, H, I_shared, d)
+        h = _c.c_void_p()
+        _check(lib().moe_layer_create(_c.byref(desc), _stream(stream), _c.byref(h)))
+        self.handle = h
+
+    @property
+    def weight_bytes(self):
+        return lib().moe_layer_weight_bytes(self.handle)
+
+    @property
+    def workspace_bytes(self):
+        return lib().moe_layer_workspace_bytes(self.handle)
+
+    def forward(self, x, y=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        _check(lib().moe_forward(self.handle, x.data_ptr() if T else None, T,
+                                 y.data_ptr() if T else None, _stream(stream)))
+        return y
+
+    def routing(self, T, stream=None):
+        """(ids [T,k] int32, gates [T,k] fp32, offsets [E+1] int32, perm [T*k] int32)."""
+        import torch
+        dev = torch.device("cuda")
+        ids = torch.empty(T, self.top_k, dtype=torch.int32, device=dev)
+        gates = torch.empty(T, self.top_k, dtype=torch.float32, device=dev)
+        offs = torch.empty(self.E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(T * self.top_k, dtype=torch.int32, device=dev)
+        _check(lib().moe_get_routing(self.handle, ids.data_ptr(), gates.data_ptr(), offs.data_ptr(),
+                                     perm.data_ptr(), _stream(stream)))
+        return ids, gates, offs, perm
+
+    def status(self, stream=None):
+        """Raises MoEError(MOE_ETIMEOUT) if a device-side wait gave up."""
+        _check(lib().moe_layer_status(self.handle, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def accept_workspace(k, V, device="cuda"):
+    import torch
+    n = lib().mtp_verify_accept_workspace_bytes(k, V)
+    if n == 0:
+        raise MoEError(MOE_EINVAL, f"k={k}, V={V} out of range")
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def verify_accept(draft_ids, logits, workspace=None, out=None, stream=None):
+    """Greedy acceptance; returns a device int32 tensor [n_accepted, next_token]."""
+    import torch
+    k = draft_ids.numel()
+    V = logits.shape[1]
+    assert logits.shape[0] == k + 1 and logits.dtype == torch.float32 and logits.is_contiguous()
+    if workspace is None:
+        workspace = accept_workspace(k, V, logits.device)
+    if out is None:
+        out = torch.empty(2, dtype=torch.int32, device=logits.device)
+    _check(lib().mtp_verify_accept(draft_ids.data_ptr() if k else None, k, logits.data_ptr(), V,
+                                   out.data_ptr(), out.data_ptr() + 4, workspace.data_ptr(),
+                                   workspace.numel(), _stream(stream)))
+    return out

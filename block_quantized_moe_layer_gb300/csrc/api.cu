@@ -1,0 +1,443 @@
+// api.cu -- the extern "C" entry points of include/moe_layer.h.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "layer.cuh"
+
+namespace moe {
+cudaError_t repack_matrix(int fmt, const uint8_t* src, uint8_t* dst, int rows, int K, int rows_per_tile, int lr_off,
+                          Chunking ch, cudaStream_t st);
+cudaError_t repack_router(const float* src, float* dst, int E, int E_pad, int H, cudaStream_t st);
+cudaError_t quantize_launch(int fmt, const float* w, int64_t rows, int64_t cols, void* out, cudaStream_t st);
+size_t accept_workspace_bytes(int k, int V);
+cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int V, int32_t* out_n, int32_t* out_next,
+                          void* ws, cudaStream_t st);
+int small_t_smem_bytes(const SmallParams& P);
+cudaError_t small_t_configure(int L, int smem_bytes);
+cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st);
+int large_t_setup(moe_layer* L, cudaStream_t st);
+int large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st);
+void large_t_release(moe_layer* L);
+int large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, cudaStream_t st);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_err = "no error";
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(call, what)                           \
+  do {                                           \
+    cudaError_t e_ = (call);                     \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+size_t fmt_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  if (fmt == MOE_Q8_0) return cols % 32 ? 0 : (size_t)rows * (size_t)(cols / 32) * 34;
+  if (fmt == MOE_Q4KS) return cols % 256 ? 0 : (size_t)rows * (size_t)(cols / 256) * 144;
+  if (fmt == MOE_F32) return (size_t)rows * (size_t)cols * 4;
+  return 0;
+}
+
+int check_tensor(const moe_tensor& t, int64_t rows, int64_t cols, bool quant, const char* name) {
+  if (t.reserved != 0) return fail(MOE_EINVAL, "%s: reserved field must be 0", name);
+  if (t.rows != rows || t.cols != cols)
+    return fail(MOE_EINVAL, "%s: shape [%lld, %lld], expected [%lld, %lld]", name, (long long)t.rows,
+                (long long)t.cols, (long long)rows, (long long)cols);
+  if (quant && t.fmt != MOE_Q8_0 && t.fmt != MOE_Q4KS)
+    return fail(MOE_EFORMAT, "%s: format %d not supported (Q8_0 or Q4KS)", name, t.fmt);
+  if (!quant && t.fmt != MOE_F32) return fail(MOE_EFORMAT, "%s: must be MOE_F32", name);
+  const size_t nb = fmt_bytes(t.fmt, rows, cols);
+  if (nb == 0) return fail(MOE_EFORMAT, "%s: %lld columns do not fit format %d", name, (long long)cols, t.fmt);
+  if (t.nbytes != nb) return fail(MOE_EINVAL, "%s: nbytes %zu, expected %zu", name, t.nbytes, nb);
+  if (!t.data) return fail(MOE_EINVAL, "%s: data is NULL", name);
+  return MOE_OK;
+}
+
+// Copies a source tensor to a device staging buffer when it lives on the host.
+struct Stager {
+  uint8_t* buf = nullptr;
+  size_t cap = 0;
+  ~Stager() {
+    if (buf) cudaFree(buf);
+  }
+  int get(const void* src, size_t n, cudaStream_t st, const uint8_t** out) {
+    if (is_device_ptr(src)) {
+      *out = static_cast<const uint8_t*>(src);
+      return MOE_OK;
+    }
+    if (n > cap) {
+      CK(cudaStreamSynchronize(st), "staging sync");
+      if (buf) cudaFree(buf);
+      buf = nullptr;
+      CK(cudaMalloc(&buf, n), "staging alloc");
+      cap = n;
+    }
+    CK(cudaMemcpyAsync(buf, src, n, cudaMemcpyHostToDevice, st), "staging copy");
+    *out = buf;
+    return MOE_OK;
+  }
+};
+
+void free_layer(moe_layer* L) {
+  if (!L) return;
+  large_t_release(L);
+  cudaFree(L->router);
+  cudaFree(L->router_b);
+  cudaFree(L->gu);
+  cudaFree(L->dn);
+  cudaFree(L->sgu);
+  cudaFree(L->sdn);
+  cudaFree(L->ws);
+  delete L;
+}
+
+int64_t tile_bytes_total(int fmt, int rows_tiles, Chunking ch) {
+  return (int64_t)rows_tiles * ch.n * chunk_bytes(fmt, ch.Kc);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+size_t moe_quantized_bytes(int32_t fmt, int64_t rows, int64_t cols) {
+  if (fmt != MOE_Q8_0 && fmt != MOE_Q4KS) return 0;
+  return fmt_bytes(fmt, rows, cols);
+}
+
+int moe_quantize(int32_t fmt, const float* w, int64_t rows, int64_t cols, void* out, void* stream) {
+  if (fmt != MOE_Q8_0 && fmt != MOE_Q4KS) return fail(MOE_EFORMAT, "moe_quantize: format %d", fmt);
+  if (!w || !out) return fail(MOE_EINVAL, "moe_quantize: NULL pointer");
+  if (fmt_bytes(fmt, rows, cols) == 0) return fail(MOE_EFORMAT, "moe_quantize: shape does not fit format");
+  if ((reinterpret_cast<uintptr_t>(w) & 3) != 0) return fail(MOE_EINVAL, "moe_quantize: w not 4-byte aligned");
+  CK(quantize_launch(fmt, w, rows, cols, out, static_cast<cudaStream_t>(stream)), "moe_quantize launch");
+  return MOE_OK;
+}
+
+int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
+  if (!d || !out) return fail(MOE_EINVAL, "moe_layer_create: NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d->reserved != 0) return fail(MOE_EINVAL, "reserved must be 0");
+  if (d->H <= 0 || d->H % 256) return fail(MOE_EINVAL, "H=%d must be a positive multiple of 256", d->H);
+  if (d->E < 1 || d->E > 1024) return fail(MOE_EINVAL, "E=%d out of range 1..1024", d->E);
+  if (d->top_k < 1 || d->top_k > std::min(d->E, 16)) return fail(MOE_EINVAL, "top_k=%d out of range", d->top_k);
+  if (d->I <= 0 || d->I % 32) return fail(MOE_EINVAL, "I=%d must be a positive multiple of 32", d->I);
+  if (d->I_shared < 0 || d->I_shared % 32) return fail(MOE_EINVAL, "I_shared=%d must be a multiple of 32", d->I_shared);
+  if (d->T_max < 1 || d->T_max > 8192) return fail(MOE_EINVAL, "T_max=%d out of range 1..8192", d->T_max);
+  if (d->act_dtype != MOE_ACT_BF16 && d->act_dtype != MOE_ACT_F32)
+    return fail(MOE_EINVAL, "act_dtype=%d", d->act_dtype);
+  if (!d->gate || !d->up || !d->down) return fail(MOE_EINVAL, "gate/up/down descriptor arrays are NULL");
+  int rc;
+  if ((rc = check_tensor(d->router_w, d->E, d->H, false, "router_w"))) return rc;
+  const bool has_bias = d->router_b.data != nullptr;
+  if (has_bias && (rc = check_tensor(d->router_b, 1, d->E, false, "router_b"))) return rc;
+  const int fmt = d->gate[0].fmt;
+  for (int e = 0; e < d->E; ++e) {
+    char nm[64];
+    snprintf(nm, sizeof nm, "gate[%d]", e);
+    if ((rc = check_tensor(d->gate[e], d->I, d->H, true, nm))) return rc;
+    snprintf(nm, sizeof nm, "up[%d]", e);
+    if ((rc = check_tensor(d->up[e], d->I, d->H, true, nm))) return rc;
+    snprintf(nm, sizeof nm, "down[%d]", e);
+    if ((rc = check_tensor(d->down[e], d->H, d->I, true, nm))) return rc;
+    if (d->gate[e].fmt != fmt || d->up[e].fmt != fmt || d->down[e].fmt != fmt)
+      return fail(MOE_EFORMAT, "expert %d: all routed matrices must share one format", e);
+  }
+  const bool has_sh = d->I_shared > 0;
+  int sfmt = fmt;
+  if (has_sh) {
+    if ((rc = check_tensor(d->sh_gate, d->I_shared, d->H, true, "sh_gate"))) return rc;
+    if ((rc = check_tensor(d->sh_up, d->I_shared, d->H, true, "sh_up"))) return rc;
+    if ((rc = check_tensor(d->sh_down, d->H, d->I_shared, true, "sh_down"))) return rc;
+    sfmt = d->sh_gate.fmt;
+    if (d->sh_up.fmt != sfmt || d->sh_down.fmt != sfmt)
+      return fail(MOE_EFORMAT, "shared expert: all matrices must share one format");
+  }
+
+  moe_layer* L = new moe_layer();
+  L->H = d->H; L->E = d->E; L->k = d->top_k; L->I = d->I; L->Ish = d->I_shared;
+  L->T_max = d->T_max; L->act = d->act_dtype; L->fmt = fmt; L->sfmt = sfmt;
+  struct Guard {
+    moe_layer* L;
+    bool keep = false;
+    ~Guard() {
+      if (!keep) free_layer(L);
+    }
+  } guard{L};
+
+  CK(cudaGetDevice(&L->dev), "cudaGetDevice");
+  CK(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->dev), "SM count");
+  L->gu_ch = choose_chunking(fmt, d->H);
+  L->dn_ch = choose_chunking(fmt, d->I);
+  if (L->gu_ch.n == 0 || L->dn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for format %d", fmt);
+  if (has_sh) {
+    L->sgu_ch = choose_chunking(sfmt, d->H);
+    L->sdn_ch = choose_chunking(sfmt, d->I_shared);
+    if (L->sgu_ch.n == 0 || L->sdn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for shared format %d", sfmt);
+  }
+  const int n_rg = (d->E + 31) / 32, n_ks = d->H / kRouterKc;
+  const int E_pad = n_rg * 32;
+  L->gu_stride = tile_bytes_total(fmt, d->I / 16, L->gu_ch);
+  L->dn_stride = tile_bytes_total(fmt, d->H / 32, L->dn_ch);
+  const size_t router_bytes = (size_t)E_pad * d->H * 4;
+  CK(cudaMalloc(&L->router, router_bytes), "alloc router");
+  if (has_bias) CK(cudaMalloc(&L->router_b, (size_t)d->E * 4), "alloc bias");
+  CK(cudaMalloc(&L->gu, (size_t)L->gu_stride * d->E), "alloc gate/up");
+  CK(cudaMalloc(&L->dn, (size_t)L->dn_stride * d->E), "alloc down");
+  size_t sgu_b = 0, sdn_b = 0;
+  if (has_sh) {
+    sgu_b = tile_bytes_total(sfmt, d->I_shared / 16, L->sgu_ch);
+    sdn_b = tile_bytes_total(sfmt, d->H / 32, L->sdn_ch);
+    CK(cudaMalloc(&L->sgu, sgu_b), "alloc shared gate/up");
+    CK(cudaMalloc(&L->sdn, sdn_b), "alloc shared down");
+  }
+  L->weight_bytes = router_bytes + (has_bias ? d->E * 4 : 0) + (size_t)(L->gu_stride + L->dn_stride) * d->E +
+                    sgu_b + sdn_b;
+
+  // upload + repack
+  Stager stg;
+  const uint8_t* src = nullptr;
+  if ((rc = stg.get(d->router_w.data, d->router_w.nbytes, st, &src))) return rc;
+  CK(repack_router(reinterpret_cast<const float*>(src), reinterpret_cast<float*>(L->router), d->E, E_pad, d->H, st),
+     "repack router");
+  if (has_bias) {
+    const cudaMemcpyKind kind = is_device_ptr(d->router_b.data) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    CK(cudaMemcpyAsync(L->router_b, d->router_b.data, (size_t)d->E * 4, kind, st), "copy bias");
+  }
+  for (int e = 0; e < d->E; ++e) {
+    uint8_t* gu = L->gu + (int64_t)e * L->gu_stride;
+    uint8_t* dn = L->dn + (int64_t)e * L->dn_stride;
+    if ((rc = stg.get(d->gate[e].data, d->gate[e].nbytes, st, &src))) return rc;
+    CK(repack_matrix(fmt, src, gu, d->I, d->H, 16, 0, L->gu_ch, st), "repack gate");
+    if ((rc = stg.get(d->up[e].data, d->up[e].nbytes, st, &src))) return rc;
+    CK(repack_matrix(fmt, src, gu, d->I, d->H, 16, 16, L->gu_ch, st), "repack up");
+    if ((rc = stg.get(d->down[e].data, d->down[e].nbytes, st, &src))) return rc;
+    CK(repack_matrix(fmt, src, dn, d->H, d->I, 32, 0, L->dn_ch, st), "repack down");
+  }
+  if (has_sh) {
+    if ((rc = stg.get(d->sh_gate.data, d->sh_gate.nbytes, st, &src))) return rc;
+    CK(repack_matrix(sfmt, src, L->sgu, d->I_shared, d->H, 16, 0, L->sgu_ch, st), "repack shared gate");
+    if ((rc = stg.get(d->sh_up.data, d->sh_up.nbytes, st, &src))) return rc;
+    CK(repack_matrix(sfmt, src, L->sgu, d->I_shared, d->H, 16, 16, L->sgu_ch, st), "repack shared up");
+    if ((rc = stg.get(d->sh_down.data, d->sh_down.nbytes, st, &src))) return rc;
+    CK(repack_matrix(sfmt, src, L->sdn, d->H, d->I_shared, 32, 0, L->sdn_ch, st), "repack shared down");
+  }
+
+  // small-T workspace
+  const int L_limbs = d->act_dtype == MOE_ACT_BF16 ? 2 : 4;
+  const int RB = rec_bytes(L_limbs);
+  const int Tm = std::min(d->T_max, kMaxSmallT);
+  const int k = d->top_k;
+  const int P = Tm * k + Tm;
+  const int Imax = std::max(d->I, d->I_shared);
+  const int w_max = (Tm + kGroup - 1) / kGroup + Tm * k;
+  const int n_rbd = d->H / 32;
+  SmallParams& sp = L->sp;
+  sp = SmallParams{};
+  sp.H = d->H; sp.E = d->E; sp.k = k; sp.I = d->I; sp.Ish = d->I_shared;
+  sp.n_rg = n_rg; sp.n_ks = n_ks; sp.n_rb = d->I / 16; sp.n_rb_sh = d->I_shared / 16; sp.n_rbd = n_rbd;
+  sp.Imax = Imax; sp.E_pad = E_pad; sp.w_max = w_max;
+  sp.router = L->router; sp.router_b = L->router_b;
+  sp.gu = L->gu; sp.dn = L->dn; sp.sgu = L->sgu; sp.sdn = L->sdn;
+  sp.gu_stride = L->gu_stride; sp.dn_stride = L->dn_stride;
+  sp.fmt = fmt; sp.sfmt = sfmt;
+  sp.gu_nch = L->gu_ch.n; sp.gu_kc = L->gu_ch.Kc; sp.dn_nch = L->dn_ch.n; sp.dn_kc = L->dn_ch.Kc;
+  sp.sgu_nch = L->sgu_ch.n; sp.sgu_kc = L->sgu_ch.Kc; sp.sdn_nch = L->sdn_ch.n; sp.sdn_kc = L->sdn_ch.Kc;
+  sp.timeout_ns = 2000000000ull;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_sync = take(sizeof(Sync));
+  const size_t o_gucnt = take((size_t)w_max * 4);
+  const size_t o_ready = take((size_t)w_max * 4);
+  const size_t o_dcnt = take((size_t)n_rbd * 4);
+  const size_t counters_end = off;
+  const size_t o_status = take(16);
+  const size_t o_part = take((size_t)n_ks * E_pad * Tm * 4);
+  const size_t o_ids = take((size_t)Tm * k * 4);
+  const size_t o_gates = take((size_t)Tm * k * 4);
+  const size_t o_pos = take((size_t)Tm * k * 4);
+  const size_t o_offs = take((size_t)(d->E + 1) * 4);
+  const size_t o_perm = take((size_t)Tm * k * 4);
+  const size_t o_ent = take((size_t)w_max * sizeof(Entry));
+  const size_t o_xrec = take((size_t)Tm * (d->H / 32) * RB);
+  const size_t o_h = take((size_t)P * Imax * 4);
+  const size_t o_hrec = take((size_t)P * (Imax / 32) * RB);
+  const size_t o_z = take((size_t)P * d->H * 4);
+  L->ws_bytes = off;
+  CK(cudaMalloc(&L->ws, L->ws_bytes), "alloc workspace");
+  CK(cudaMemsetAsync(L->ws, 0, L->ws_bytes, st), "zero workspace");
+  uint8_t* w = static_cast<uint8_t*>(L->ws);
+  sp.sync = reinterpret_cast<Sync*>(w + o_sync);
+  sp.gu_cnt = reinterpret_cast<int*>(w + o_gucnt);
+  sp.entry_ready = reinterpret_cast<int*>(w + o_ready);
+  sp.d_cnt = reinterpret_cast<int*>(w + o_dcnt);
+  sp.status = reinterpret_cast<int*>(w + o_status);
+  sp.partials = reinterpret_cast<float*>(w + o_part);
+  sp.ids = reinterpret_cast<int*>(w + o_ids);
+  sp.gates = reinterpret_cast<float*>(w + o_gates);
+  sp.pos = reinterpret_cast<int*>(w + o_pos);
+  sp.offsets = reinterpret_cast<int*>(w + o_offs);
+  sp.perm = reinterpret_cast<int*>(w + o_perm);
+  sp.entries = reinterpret_cast<Entry*>(w + o_ent);
+  sp.xrec = w + o_xrec;
+  sp.h = reinterpret_cast<float*>(w + o_h);
+  sp.hrec = w + o_hrec;
+  sp.z = reinterpret_cast<float*>(w + o_z);
+  (void)counters_end;
+
+  // shared-memory plan: stages hold a weight chunk plus up to kGroup records
+  auto stage_need = [&](int f, Chunking ch) {
+    return chunk_bytes(f, ch.Kc) + (int64_t)kGroup * (ch.Kc / 32) * RB;
+  };
+  int64_t stage = chunk_bytes(MOE_F32, kRouterKc);
+  stage = std::max(stage, stage_need(fmt, L->gu_ch));
+  stage = std::max(stage, stage_need(fmt, L->dn_ch));
+  if (has_sh) {
+    stage = std::max(stage, stage_need(sfmt, L->sgu_ch));
+    stage = std::max(stage, stage_need(sfmt, L->sdn_ch));
+  }
+  stage = align_up(stage, 128);
+  const int Tk = Tm * k;
+  const size_t fin = align_up((size_t)Tm * d->E * 4, 16) + 4 * (align_up(d->E, 4) + 3 * align_up(Tk, 4));
+  sp.misc_bytes = (int)align_up(std::max((size_t)Tm * kRouterKc * 4, fin), 16);
+  int max_optin = 0;
+  CK(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->dev), "smem attr");
+  sp.stage_bytes = (int)stage;
+  int ns = 4;
+  for (; ns >= 2; --ns) {
+    sp.n_stages = ns;
+    if (small_t_smem_bytes(sp) <= max_optin) break;
+  }
+  if (ns < 2) return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has");
+  L->smem_bytes = small_t_smem_bytes(sp);
+  CK(small_t_configure(L_limbs, L->smem_bytes), "configure small-T kernel");
+
+  if ((rc = large_t_setup(L, st))) return rc;
+  CK(cudaStreamSynchronize(st), "create sync");
+  guard.keep = true;
+  *out = L;
+  g_err = "no error";
+  return MOE_OK;
+}
+
+int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
+  if (!L) return fail(MOE_EINVAL, "moe_forward: NULL layer");
+  if (T < 0 || T > L->T_max) return fail(MOE_EINVAL, "moe_forward: T=%d outside 0..%d", T, L->T_max);
+  if (T == 0) return MOE_OK;
+  if (!x || !y) return fail(MOE_EINVAL, "moe_forward: NULL x or y");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
+    return fail(MOE_EINVAL, "moe_forward: x and y must be 16-byte aligned");
+  const size_t esz = L->act == MOE_ACT_BF16 ? 2 : 4;
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x), yb = reinterpret_cast<uintptr_t>(y);
+  const size_t nb = (size_t)T * L->H * esz;
+  if (xb < yb + nb && yb < xb + nb) return fail(MOE_EINVAL, "moe_forward: x and y overlap");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  L->last_T = T;
+  if (T > kMaxSmallT) return large_t_forward(L, x, T, y, st);
+  SmallParams P = L->sp;
+  P.T = T;
+  P.n_sh = L->Ish > 0 ? (T + kGroup - 1) / kGroup : 0;
+  P.x = x;
+  P.y = y;
+  CK(small_t_launch(P, L->act == MOE_ACT_BF16 ? 2 : 4, L->num_sms, L->smem_bytes, st), "moe_forward launch");
+  return MOE_OK;
+}
+
+int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, void* stream) {
+  if (!L) return fail(MOE_EINVAL, "moe_get_routing: NULL layer");
+  if (L->last_T <= 0) return fail(MOE_EINVAL, "moe_get_routing: no forward yet");
+  if (L->last_T > kMaxSmallT) {
+    return large_t_get_routing(L, ids, gates, offsets, perm, static_cast<cudaStream_t>(stream));
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t Tk = (size_t)L->last_T * L->k;
+  if (ids) CK(cudaMemcpyAsync(ids, L->sp.ids, Tk * 4, cudaMemcpyDeviceToDevice, st), "routing ids");
+  if (gates) CK(cudaMemcpyAsync(gates, L->sp.gates, Tk * 4, cudaMemcpyDeviceToDevice, st), "routing gates");
+  if (offsets)
+    CK(cudaMemcpyAsync(offsets, L->sp.offsets, (size_t)(L->E + 1) * 4, cudaMemcpyDeviceToDevice, st), "offsets");
+  if (perm) CK(cudaMemcpyAsync(perm, L->sp.perm, Tk * 4, cudaMemcpyDeviceToDevice, st), "routing perm");
+  return MOE_OK;
+}
+
+int moe_layer_status(moe_layer* L, void* stream) {
+  if (!L) return fail(MOE_EINVAL, "moe_layer_status: NULL layer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaStreamSynchronize(st), "status sync");
+  int word[4] = {0, 0, 0, 0};
+  CK(cudaMemcpy(word, L->sp.status, 16, cudaMemcpyDeviceToHost), "status read");
+  if (word[0] == 0) return MOE_OK;
+  // clear the word and every cross-CTA counter so the next call starts clean
+  const size_t counters = reinterpret_cast<uint8_t*>(L->sp.status) - static_cast<uint8_t*>(L->ws);
+  CK(cudaMemset(L->ws, 0, counters + 16), "status reset");
+  static const char* sites[] = {"?", "routing flag", "x records", "entry ready", "free stage", "full stage",
+                                 "end marker", "copy drain"};
+  const int site = (word[1] >= 0 && word[1] <= 7) ? word[1] : 0;
+  return fail(MOE_ETIMEOUT, "a device-side wait timed out: %s (detail %d, block %d)", sites[site], word[2], word[3]);
+}
+
+size_t moe_layer_weight_bytes(const moe_layer* L) { return L ? L->weight_bytes : 0; }
+size_t moe_layer_workspace_bytes(const moe_layer* L) { return L ? L->ws_bytes + L->lws_bytes : 0; }
+
+void moe_layer_destroy(moe_layer* L) { free_layer(L); }
+
+size_t mtp_verify_accept_workspace_bytes(int32_t k, int32_t V) {
+  if (k < 0 || k > 15 || V < 1 || V > (1 << 24)) return 0;
+  return accept_workspace_bytes(k, V);
+}
+
+int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V, int32_t* out_n_accepted,
+                      int32_t* out_next_token, void* workspace, size_t workspace_bytes, void* stream) {
+  if (k < 0 || k > 15) return fail(MOE_EINVAL, "mtp_verify_accept: k=%d outside 0..15", k);
+  if (V < 1 || V > (1 << 24)) return fail(MOE_EINVAL, "mtp_verify_accept: V=%d outside 1..2^24", V);
+  if ((k > 0 && !draft_ids) || !logits || !out_n_accepted || !out_next_token || !workspace)
+    return fail(MOE_EINVAL, "mtp_verify_accept: NULL pointer");
+  if (reinterpret_cast<uintptr_t>(workspace) & 15)
+    return fail(MOE_EINVAL, "mtp_verify_accept: workspace must be 16-byte aligned");
+  if (workspace_bytes < accept_workspace_bytes(k, V))
+    return fail(MOE_EINVAL, "mtp_verify_accept: workspace %zu bytes, need %zu", workspace_bytes,
+                accept_workspace_bytes(k, V));
+  CK(accept_launch(draft_ids, k, logits, V, out_n_accepted, out_next_token, workspace,
+                   static_cast<cudaStream_t>(stream)),
+     "mtp_verify_accept launch");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,192 @@
+// common.cuh -- device helpers and the internal weight / activation layouts.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe_layer.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Tiling constants of the small-T (GEMV) path.
+//   A weight chunk holds 32 rows (one per lane) x Kc columns of one matrix; the
+//   8 consumer warps split the chunk's 32-column blocks between them.
+// ---------------------------------------------------------------------------
+constexpr int kRows = 32;           // rows per chunk (= lanes)
+constexpr int kConsumerWarps = 8;   // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kGroup = 4;           // activation vectors per tile (token group)
+constexpr int kRouterKc = 256;      // router chunk columns
+constexpr int kQ8KcMax = 1280;      // largest Q8_0 chunk (columns)
+constexpr int kQ4KcMax = 2048;      // largest Q4KS chunk (columns)
+constexpr int kMaxSmallT = 8;       // largest T of the GEMV path
+
+// Activation record of one 32-value block: L limb planes of 32 bytes each
+// (byte i of limb l = bits [8l, 8l+8) of the block fixed-point integer X_i,
+// lower limbs unsigned, the top limb signed), then fp32 ascale = 2^-s and
+// fp32 sumx = ascale * sum_i X_i, then 8 bytes of padding.  X_i =
+// round(v_i * 2^s) with s chosen so that max |X_i| <= 2^(8L-2).
+__host__ __device__ constexpr int rec_bytes(int L) { return 32 * L + 16; }
+
+// Bytes of one weight chunk: 32 rows x Kc columns.
+//   Q8_0 : quants [Kc/32 blocks][2 halves][32 rows][16 B], then
+//          scales [Kc/32][32 rows] fp16
+//   Q4KS : quants [Kc/32 sub-blocks][32 rows][16 B] (nibbles permuted so that
+//          (word & 0x0F0F0F0F) holds weights 8w..8w+3 and
+//          ((word >> 4) & 0x0F0F0F0F) weights 8w+4..8w+7), then the
+//          serialised 16-byte superblock headers [Kc/256][32 rows][16 B]
+//   F32  : [Kc/4][32 rows][4 floats]
+__host__ __device__ inline int64_t chunk_bytes(int fmt, int Kc) {
+  if (fmt == MOE_Q8_0) return (int64_t)(Kc / 32) * 1088;
+  if (fmt == MOE_Q4KS) return (int64_t)(Kc / 32) * 512 + (int64_t)(Kc / 256) * 512;
+  return (int64_t)Kc * kRows * 4;
+}
+
+// Chunking of a reduction dimension K for a format: n chunks of Kc columns.
+struct Chunking {
+  int n, Kc;
+};
+inline Chunking choose_chunking(int fmt, int K) {
+  const int unit = fmt == MOE_Q4KS ? 256 : (fmt == MOE_Q8_0 ? 32 : kRouterKc);
+  const int kmax = fmt == MOE_Q4KS ? kQ4KcMax : (fmt == MOE_Q8_0 ? kQ8KcMax : kRouterKc);
+  int n = (K + kmax - 1) / kmax;
+  for (; n <= K / unit; ++n)
+    if (K % n == 0 && (K / n) % unit == 0) return {n, K / n};
+  return {0, 0};
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and
+// both addresses must be multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (bulk copy) accesses: records written with st.global by one CTA and read
+// with cp.async.bulk by another need it on both sides of the flag hand-off.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Named barrier over the consumer warps only (the producer warp keeps going).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// dp4a variants: a = weight bytes, b = activation limb bytes.
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp converts 32 values (lane i holds v) into an activation record.
+template <int L>
+__device__ __forceinline__ void write_record(float v, uint8_t* rec) {
+  const int lane = threadIdx.x & 31;
+  const float amax = warp_max(fabsf(v));
+  int s = 0;
+  if (amax > 0.f) {
+    s = (8 * L - 3) - ilogbf(amax);
+    s = max(-100, min(120, s));
+  }
+  const int X = __float2int_rn(ldexpf(v, s));
+#pragma unroll
+  for (int l = 0; l < L; ++l) rec[l * 32 + lane] = (uint8_t)((X >> (8 * l)) & 0xFF);
+  const double sx = warp_sum_d((double)X);
+  if (lane == 0) {
+    float* meta = reinterpret_cast<float*>(rec + 32 * L);
+    meta[0] = ldexpf(1.f, -s);
+    meta[1] = (float)ldexp(sx, -s);
+    meta[2] = 0.f;
+    meta[3] = 0.f;
+  }
+}
+
+// Status bits written into the layer's status word.
+constexpr int kStatusTimeout = 1;
+
+}  // namespace moe

@@ -1,0 +1,100 @@
+// layer.cuh -- the layer object and the parameter block of the small-T kernel.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+// One unit of expert work: up to kGroup activation vectors routed to one
+// expert (e == -1 for the shared expert).  Slots index the activation /
+// intermediate rows: routed slots are positions in perm[], the shared
+// expert's slot for token t is T*k + t.
+struct Entry {
+  int e;
+  int slot0;
+  int M;
+  int tok[kGroup];
+};
+
+// Cross-CTA counters of the fused kernel.  All zero between launches: the
+// last CTA to leave resets them.
+struct Sync {
+  int queue;          // next tile to claim
+  int router_done;    // router tiles finished
+  int x_done;         // x slices converted to activation records
+  int routing_ready;  // routing published
+  int exit_cnt;       // CTAs that left
+  int n_rent;         // routed entries (written with the routing)
+  int pad[2];
+};
+
+struct SmallParams {
+  // shapes
+  int H, E, k, I, Ish, T;
+  int n_rg, n_ks;         // router: row groups of 32 experts, 256-column slices
+  int n_rb, n_rb_sh;      // gate/up tiles per routed / shared expert (16 outputs each)
+  int n_rbd;              // down tiles per expert (32 outputs each)
+  int n_sh;               // shared entries for this T
+  int Imax;               // max(I, Ish): row stride of h / h records
+  int E_pad;              // n_rg * 32
+  int w_max;              // capacity of the entry arrays
+  // weights (repacked)
+  const uint8_t* router;  // [n_rg][n_ks][32 rows x 256 cols fp32]
+  const float* router_b;  // [E] or nullptr
+  const uint8_t* gu;      // routed gate/up, expert stride gu_stride
+  const uint8_t* dn;      // routed down, expert stride dn_stride
+  const uint8_t* sgu;     // shared gate/up (nullptr if none)
+  const uint8_t* sdn;     // shared down
+  int64_t gu_stride, dn_stride;
+  int fmt, sfmt;
+  int gu_nch, gu_kc, dn_nch, dn_kc, sgu_nch, sgu_kc, sdn_nch, sdn_kc;
+  // activations
+  const void* x;  // [T, H] bf16 (L = 2) or fp32 (L = 4)
+  void* y;        // [T, H] same type
+  // workspace
+  Sync* sync;
+  int* status;
+  int* gu_cnt;       // [w_max]
+  int* entry_ready;  // [w_max]
+  int* d_cnt;        // [n_rbd]
+  float* partials;   // [n_ks][E_pad][T]
+  int* ids;          // [T*k]
+  float* gates;      // [T*k]
+  int* pos;          // [T*k]
+  int* offsets;      // [E+1]
+  int* perm;         // [T*k]
+  Entry* entries;    // [w_max]
+  uint8_t* xrec;     // [T][H/32] records
+  float* h;          // [P][Imax]
+  uint8_t* hrec;     // [P][Imax/32] records
+  float* z;          // [P][H]
+  // shared-memory plan
+  int n_stages, stage_bytes, misc_bytes;
+  uint64_t timeout_ns;
+};
+
+}  // namespace moe
+
+struct moe_layer {
+  int dev = 0;
+  int H = 0, E = 0, k = 0, I = 0, Ish = 0, T_max = 0, act = 0;
+  int fmt = 0, sfmt = 0;
+  uint8_t* router = nullptr;
+  float* router_b = nullptr;
+  uint8_t* gu = nullptr;
+  uint8_t* dn = nullptr;
+  uint8_t* sgu = nullptr;
+  uint8_t* sdn = nullptr;
+  int64_t gu_stride = 0, dn_stride = 0;
+  moe::Chunking gu_ch{}, dn_ch{}, sgu_ch{}, sdn_ch{};
+  size_t weight_bytes = 0;
+  // small-T workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  moe::SmallParams sp{};  // pointers filled at create; T-dependent fields per call
+  int num_sms = 0;
+  int smem_bytes = 0;
+  int last_T = 0;
+  // large-T workspace
+  void* lws = nullptr;
+  size_t lws_bytes = 0;
+};

@@ -1,0 +1,171 @@
+/*
+ * moe_layer.h -- C ABI of the block-quantized MoE layer library (sm_103a).
+ *
+ * One sparse MoE FFN layer as the Step-5 / Step-3.7 pages describe it
+ * ("Step-5 Preview GGUF", "Model background" table: hidden 4096, 352 routed
+ * experts, 8 selected per token, shared experts; "Precision distribution"
+ * table and "Step 3.7 Flash Mixed-Quant GGUF", "Tensor recipe" table: routed
+ * experts in low-bit block types such as Q4_K, shared experts in Q8_0, the
+ * router in F32), run on the small token batch of MTP verification
+ * ("Support Step3.5/3.7 flash mtp3", llama.cpp PR #24340, "Overview",
+ * Round 1 step 1: [id_last, d1, d2, d3], all logits on), plus the greedy
+ * acceptance of that PR's steps 4 and 5.
+ *
+ * Layer definition (the pages name the tensors but print no formula; this is
+ * the plain reading the library implements):
+ *   l[t,e] = sum_h x[t,h] Wr[e,h] + b[e];  p = softmax_e(l[t,:]);
+ *   ids[t,0..k-1] = the k largest p (descending, ties to the lower e);
+ *   g[t,j] = p[t,ids[t,j]] / sum_j' p[t,ids[t,j']];
+ *   FFN_e(v) = Wd_e (silu(Wg_e v) * (Wu_e v)),  silu(u) = u / (1 + e^-u);
+ *   y[t] = sum_j g[t,j] FFN_ids[t,j](x[t]) + FFN_shared(x[t]).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless a comment says "host".
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  The caller owns every buffer it passes.
+ *   - Return value: MOE_OK or a negative MOE_E* code.  On error nothing is
+ *     launched unless the code is MOE_ECUDA; moe_last_error() then describes
+ *     the failure.  No call aborts or throws.
+ *   - Arguments are validated on the host before anything touches the GPU.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_EINVAL (-1)   /* bad argument (null, size, alignment, T out of range) */
+#define MOE_ENOMEM (-2)   /* device allocation failed */
+#define MOE_EFORMAT (-3)  /* unsupported format, or a shape the format cannot hold */
+#define MOE_ETIMEOUT (-4) /* a bounded device-side wait gave up (see moe_layer_status) */
+#define MOE_ECUDA (-5)    /* a CUDA runtime call failed */
+
+/* Weight formats.  Serialised layouts (blocks run along a row, i.e. along
+ * the reduction dimension K = cols):
+ *   MOE_F32  : row-major fp32.
+ *   MOE_Q8_0 : 32 weights -> 34 bytes: fp16 d (little endian), 32 x int8 q;
+ *              w = d * q.  The pages name Q8_0 without a layout; this is the
+ *              library's reading of it.
+ *   MOE_Q4KS : the library's Q4_K-style type.  256 weights -> 144 bytes:
+ *              fp16 d, fp16 dmin, sixteen 6-bit fields (sc[0..7], m[0..7]) as
+ *              one little-endian bit stream in 12 bytes, then 128 bytes of
+ *              4-bit codes (weight i in byte 16 + i/2, low nibble for even i);
+ *              w = (d*sc[s]) * q - dmin*m[s] for sub-block s = i/32.
+ *   MOE_BF16 : reserved (not accepted for weights). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4KS = 3 } moe_fmt;
+
+/* Activation / output type of moe_forward.
+ *   MOE_ACT_BF16: x and y are bf16.  Inside, x and the SwiGLU outputs enter
+ *                 the integer dot products as 16-bit block fixed point
+ *                 (per 32 values: a power-of-two scale and 16-bit integers).
+ *   MOE_ACT_F32 : "check mode": x and y are fp32, block fixed point has 32
+ *                 bits.  Slower; meant for verification. */
+typedef enum { MOE_ACT_BF16 = 0, MOE_ACT_F32 = 1 } moe_act;
+
+/* A serialised weight matrix [rows, cols].  `data` may be a host or a device
+ * pointer; it is read only during moe_layer_create. */
+typedef struct {
+  int32_t fmt;      /* moe_fmt */
+  int32_t reserved; /* must be 0 */
+  int64_t rows, cols;
+  const void* data;
+  size_t nbytes; /* must equal moe_quantized_bytes(fmt, rows, cols) */
+} moe_tensor;
+
+typedef struct {
+  int32_t H;         /* hidden size; multiple of 256 */
+  int32_t E;         /* routed experts, 1..1024 */
+  int32_t top_k;     /* experts per token, 1..min(E, 16) */
+  int32_t I;         /* routed expert intermediate size; multiple of 32 (256 for MOE_Q4KS) */
+  int32_t I_shared;  /* shared expert intermediate size; 0 = no shared expert */
+  int32_t T_max;     /* largest token count moe_forward will be given, 1..8192 */
+  int32_t act_dtype; /* moe_act */
+  int32_t reserved;  /* must be 0 */
+  moe_tensor router_w; /* [E, H], MOE_F32 */
+  moe_tensor router_b; /* [1, E], MOE_F32; data == NULL for no bias */
+  const moe_tensor* gate; /* HOST array of E descriptors, each [I, H] */
+  const moe_tensor* up;   /* HOST array of E descriptors, each [I, H] */
+  const moe_tensor* down; /* HOST array of E descriptors, each [H, I] */
+  moe_tensor sh_gate, sh_up, sh_down; /* [I_shared, H], [I_shared, H], [H, I_shared];
+                                         the format may differ from the routed one */
+} moe_layer_desc;
+
+typedef struct moe_layer moe_layer;
+
+/* Uploads and repacks every weight into the library's device layout and
+ * allocates all workspace, on the current device.  The caller may free the
+ * source buffers once the call returns (it synchronises `stream`).
+ * Errors: MOE_EINVAL (null pointers, sizes), MOE_EFORMAT (format/shape),
+ * MOE_ENOMEM, MOE_ECUDA.  *out is set only on success. */
+int moe_layer_create(const moe_layer_desc* desc, void* stream, moe_layer** out);
+
+/* y[T, H] = MoE(x[T, H]) for 0 <= T <= T_max, in the layer's act_dtype.
+ * x and y must be 16-byte aligned and must not overlap.  T == 0 returns
+ * MOE_OK and launches nothing.  No allocation happens here.  Calls on one
+ * layer must not run concurrently (they share the layer's workspace).
+ * Device-side wait failures are reported by moe_layer_status(). */
+int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
+
+/* Copies the routing of the last moe_forward (device-to-device, async on
+ * `stream`): ids int32 [T, k] and gates fp32 [T, k] in slot order, offsets
+ * int32 [E+1], perm int32 [T*k] (pair ids t*k+j grouped by expert, ascending
+ * within an expert).  Any pointer may be NULL to skip it. */
+int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm,
+                    void* stream);
+
+/* Synchronises `stream` and reads the layer's device status word: MOE_OK, or
+ * MOE_ETIMEOUT if a bounded device-side wait gave up in some earlier call
+ * (the word is then cleared and the workspace re-zeroed). */
+int moe_layer_status(moe_layer* L, void* stream);
+
+/* Bytes of weights resident on the device (repacked), and of workspace. */
+size_t moe_layer_weight_bytes(const moe_layer* L);
+size_t moe_layer_workspace_bytes(const moe_layer* L);
+
+void moe_layer_destroy(moe_layer* L);
+
+/* Serialised size of a [rows, cols] matrix in `fmt`; 0 if the shape does not
+ * fit the format. */
+size_t moe_quantized_bytes(int32_t fmt, int64_t rows, int64_t cols);
+
+/* Quantises fp32 w [rows, cols] (device) into serialised `fmt` bytes at out
+ * (device, moe_quantized_bytes(...) bytes).  MOE_Q8_0: d = max|w|/127 in
+ * fp32, stored as fp16; q = clamp(round_half_away(w / d), -127, 127).
+ * MOE_Q4KS: the closed-form min/max quantiser (per sub-block A = (hi - lo)/15
+ * with lo = min(0, min w), B = -lo; d, dmin = fp16(max A / 63), fp16(max B / 63);
+ * sc, m = round(A / d), round(B / dmin) clamped to [0, 63];
+ * q = clamp(round((w + dmin*m) / (d*sc)), 0, 15)).  Bit-exact and
+ * deterministic. */
+int moe_quantize(int32_t fmt, const float* w, int64_t rows, int64_t cols, void* out, void* stream);
+
+/* Greedy verification of k drafted tokens against the target's logits over
+ * the verify batch ("Support Step3.5/3.7 flash mtp3", "Overview", Round 1
+ * steps 4-5): a_i = argmax_v logits[i, v] (ties to the lowest v) for
+ * i = 0..k; *out_n_accepted = the largest n <= k with a_i == draft_ids[i]
+ * for all i < n; *out_next_token = a_n (the correction token, or the bonus
+ * token when all drafts match).  The caller hands pending_h =
+ * verify_h[*out_n_accepted] to the next round.
+ *   draft_ids int32 [k] (device), logits fp32 [k+1, V] row-major (device,
+ *   finite values), outputs int32 (device).  0 <= k <= 15, 1 <= V <= 2^24.
+ *   workspace: device scratch of mtp_verify_accept_workspace_bytes(k, V)
+ *   bytes, 16-byte aligned, owned by the caller; it must be zero-filled
+ *   before its first use and is left zero-filled by every call that
+ *   completes.  Calls sharing one workspace must not overlap on the GPU. */
+size_t mtp_verify_accept_workspace_bytes(int32_t k, int32_t V);
+int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V,
+                      int32_t* out_n_accepted, int32_t* out_next_token, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Message for the last error on the calling thread; valid until the next
+ * call on that thread.  Never NULL. */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H */

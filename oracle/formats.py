@@ -22,7 +22,7 @@ Q4KS -- 256 weights along a row (8 sub-blocks of 32), serialised as 144 bytes:
   Decoding: a = d*sc, b = dmin*m (both exact in fp32), w = fp32(a*q - b) with
   a*q exact, so one round-to-nearest on the subtraction.
   Quantiser (closed form, no search), per sub-block s:
-    lo = min(0, min w), hi = max w, A_s = (hi - lo)/15, B_s = -lo   (fp32)
+    lo = min(0, min w), hi = max w, A_s = (hi - lo)/15, B_s = 0 - lo  (fp32)
     d = fp16(max_s A_s / 63), dmin = fp16(max_s B_s / 63)
     sc = clamp(round_half_away(A_s / d), 0, 63), m likewise from B_s / dmin
         (d and dmin are the decoded fp16 values; a zero divisor gives 0)
@@ -126,7 +126,7 @@ def q4ks_quantize(w):
     lo = np.minimum(F32(0), sub.min(axis=3))
     hi = sub.max(axis=3)
     A = ((hi - lo) / F32(15)).astype(F32)
-    B = (-lo).astype(F32)
+    B = (F32(0) - lo).astype(F32)
     d16 = (A.max(axis=2) / F32(63)).astype(F32).astype("<f2")
     m16 = (B.max(axis=2) / F32(63)).astype(F32).astype("<f2")
     dF = d16.astype(F32)[..., None]
