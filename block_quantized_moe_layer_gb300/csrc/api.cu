@@ -151,7 +151,8 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if (!d || !out) return fail(MOE_EINVAL, "moe_layer_create: NULL argument");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (d->reserved != 0) return fail(MOE_EINVAL, "reserved must be 0");
-  if (d->H <= 0 || d->H % 256) return fail(MOE_EINVAL, "H=%d must be a positive multiple of 256", d->H);
+  if (d->H <= 0 || d->H % 256 || d->H > 128 * kMaxDownTiles)
+    return fail(MOE_EINVAL, "H=%d must be a positive multiple of 256, at most %d", d->H, 128 * kMaxDownTiles);
   if (d->E < 1 || d->E > 1024) return fail(MOE_EINVAL, "E=%d out of range 1..1024", d->E);
   if (d->top_k < 1 || d->top_k > std::min(d->E, 16)) return fail(MOE_EINVAL, "top_k=%d out of range", d->top_k);
   if (d->I <= 0 || d->I % 32) return fail(MOE_EINVAL, "I=%d must be a positive multiple of 32", d->I);
@@ -200,13 +201,33 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
 
   CK(cudaGetDevice(&L->dev), "cudaGetDevice");
   CK(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->dev), "SM count");
-  L->gu_ch = choose_chunking(fmt, d->H);
-  L->dn_ch = choose_chunking(fmt, d->I);
-  if (L->gu_ch.n == 0 || L->dn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for format %d", fmt);
-  if (has_sh) {
-    L->sgu_ch = choose_chunking(sfmt, d->H);
-    L->sdn_ch = choose_chunking(sfmt, d->I_shared);
-    if (L->sgu_ch.n == 0 || L->sdn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for shared format %d", sfmt);
+  // chunk sizes: the largest that let the shared-memory ring hold two stages
+  int max_optin = 0;
+  CK(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->dev), "smem attr");
+  const int L_limbs = d->act_dtype == MOE_ACT_BF16 ? 2 : 4;
+  const int RB = rec_bytes(L_limbs);
+  auto stage_need = [&](int f, Chunking ch) {
+    return chunk_bytes(f, ch.Kc) + (int64_t)kGroup * (ch.Kc / 32) * RB;
+  };
+  int64_t stage = 0;
+  for (int shift = 0; shift < 6; ++shift) {
+    L->gu_ch = choose_chunking(fmt, d->H, shift);
+    L->dn_ch = choose_chunking(fmt, d->I, shift);
+    if (L->gu_ch.n == 0 || L->dn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for format %d", fmt);
+    if (has_sh) {
+      L->sgu_ch = choose_chunking(sfmt, d->H, shift);
+      L->sdn_ch = choose_chunking(sfmt, d->I_shared, shift);
+      if (L->sgu_ch.n == 0 || L->sdn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for shared format %d", sfmt);
+    }
+    stage = chunk_bytes(MOE_F32, kRouterCc) + (int64_t)std::min(d->T_max, kMaxSmallT) * kRouterCc * (L_limbs == 2 ? 2 : 4);
+    stage = std::max(stage, stage_need(fmt, L->gu_ch));
+    stage = std::max(stage, stage_need(fmt, L->dn_ch));
+    if (has_sh) {
+      stage = std::max(stage, stage_need(sfmt, L->sgu_ch));
+      stage = std::max(stage, stage_need(sfmt, L->sdn_ch));
+    }
+    stage = align_up(stage, 128);
+    if (2 * stage + 40 * 1024 <= max_optin) break;
   }
   const int n_rg = (d->E + 31) / 32, n_ks = d->H / kRouterKc;
   const int E_pad = n_rg * 32;
@@ -257,18 +278,17 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   }
 
   // small-T workspace
-  const int L_limbs = d->act_dtype == MOE_ACT_BF16 ? 2 : 4;
-  const int RB = rec_bytes(L_limbs);
   const int Tm = std::min(d->T_max, kMaxSmallT);
   const int k = d->top_k;
   const int P = Tm * k + Tm;
   const int Imax = std::max(d->I, d->I_shared);
   const int w_max = (Tm + kGroup - 1) / kGroup + Tm * k;
-  const int n_rbd = d->H / 32;
+  const int n_dt = d->H / 128;
   SmallParams& sp = L->sp;
   sp = SmallParams{};
   sp.H = d->H; sp.E = d->E; sp.k = k; sp.I = d->I; sp.Ish = d->I_shared;
-  sp.n_rg = n_rg; sp.n_ks = n_ks; sp.n_rb = d->I / 16; sp.n_rb_sh = d->I_shared / 16; sp.n_rbd = n_rbd;
+  sp.n_rg = n_rg; sp.n_ks = n_ks; sp.n_rc = d->H / kRouterCc;
+  sp.n_kt = (sp.n_rc + kRouterTileChunks - 1) / kRouterTileChunks; sp.n_gu = d->I / 32; sp.n_gu_sh = d->I_shared / 32; sp.n_dt = n_dt;
   sp.Imax = Imax; sp.E_pad = E_pad; sp.w_max = w_max;
   sp.router = L->router; sp.router_b = L->router_b;
   sp.gu = L->gu; sp.dn = L->dn; sp.sgu = L->sgu; sp.sdn = L->sdn;
@@ -287,10 +307,10 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_sync = take(sizeof(Sync));
   const size_t o_gucnt = take((size_t)w_max * 4);
   const size_t o_ready = take((size_t)w_max * 4);
-  const size_t o_dcnt = take((size_t)n_rbd * 4);
+  const size_t o_dcnt = take((size_t)n_dt * 4);
   const size_t counters_end = off;
   const size_t o_status = take(16);
-  const size_t o_part = take((size_t)n_ks * E_pad * Tm * 4);
+  const size_t o_part = take((size_t)((d->H / kRouterCc + kRouterTileChunks - 1) / kRouterTileChunks) * E_pad * 8 * 4);
   const size_t o_ids = take((size_t)Tm * k * 4);
   const size_t o_gates = take((size_t)Tm * k * 4);
   const size_t o_pos = take((size_t)Tm * k * 4);
@@ -298,7 +318,6 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_perm = take((size_t)Tm * k * 4);
   const size_t o_ent = take((size_t)w_max * sizeof(Entry));
   const size_t o_xrec = take((size_t)Tm * (d->H / 32) * RB);
-  const size_t o_h = take((size_t)P * Imax * 4);
   const size_t o_hrec = take((size_t)P * (Imax / 32) * RB);
   const size_t o_z = take((size_t)P * d->H * 4);
   L->ws_bytes = off;
@@ -318,35 +337,21 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.perm = reinterpret_cast<int*>(w + o_perm);
   sp.entries = reinterpret_cast<Entry*>(w + o_ent);
   sp.xrec = w + o_xrec;
-  sp.h = reinterpret_cast<float*>(w + o_h);
   sp.hrec = w + o_hrec;
   sp.z = reinterpret_cast<float*>(w + o_z);
   (void)counters_end;
 
-  // shared-memory plan: stages hold a weight chunk plus up to kGroup records
-  auto stage_need = [&](int f, Chunking ch) {
-    return chunk_bytes(f, ch.Kc) + (int64_t)kGroup * (ch.Kc / 32) * RB;
-  };
-  int64_t stage = chunk_bytes(MOE_F32, kRouterKc);
-  stage = std::max(stage, stage_need(fmt, L->gu_ch));
-  stage = std::max(stage, stage_need(fmt, L->dn_ch));
-  if (has_sh) {
-    stage = std::max(stage, stage_need(sfmt, L->sgu_ch));
-    stage = std::max(stage, stage_need(sfmt, L->sdn_ch));
-  }
-  stage = align_up(stage, 128);
   const int Tk = Tm * k;
   const size_t fin = align_up((size_t)Tm * d->E * 4, 16) + 4 * (align_up(d->E, 4) + 3 * align_up(Tk, 4));
-  sp.misc_bytes = (int)align_up(std::max((size_t)Tm * kRouterKc * 4, fin), 16);
-  int max_optin = 0;
-  CK(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->dev), "smem attr");
-  sp.stage_bytes = (int)stage;
-  int ns = 4;
-  for (; ns >= 2; --ns) {
-    sp.n_stages = ns;
-    if (small_t_smem_bytes(sp) <= max_optin) break;
-  }
-  if (ns < 2) return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has");
+  sp.misc_bytes = (int)align_up(fin, 16);
+  // every byte not needed elsewhere goes to the stage ring; it must hold at
+  // least two of the largest stages
+  sp.n_stages = kMaxSlots;
+  sp.ring_bytes = 0;
+  const int fixed = small_t_smem_bytes(sp);
+  sp.ring_bytes = (int)((max_optin - fixed) / 128 * 128);
+  if (sp.ring_bytes < 2 * stage)
+    return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has (stage %lld B)", (long long)stage);
   L->smem_bytes = small_t_smem_bytes(sp);
   CK(small_t_configure(L_limbs, L->smem_bytes), "configure small-T kernel");
 
@@ -374,6 +379,7 @@ int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
   if (T > kMaxSmallT) return large_t_forward(L, x, T, y, st);
   SmallParams P = L->sp;
   P.T = T;
+  P.Tp = (T + 3) & ~3;
   P.n_sh = L->Ish > 0 ? (T + kGroup - 1) / kGroup : 0;
   P.x = x;
   P.y = y;

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/moe_layer.h"
 
 namespace moe {
@@ -15,13 +17,22 @@ namespace moe {
 //   8 consumer warps split the chunk's 32-column blocks between them.
 // ---------------------------------------------------------------------------
 constexpr int kRows = 32;           // rows per chunk (= lanes)
-constexpr int kConsumerWarps = 8;   // warps that compute
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kConsumerWarps = 8;   // warps that compute (warps 0-7)
+constexpr int kProducerWarp = 8;    // issues the bulk copies (one thread)
+constexpr int kEpilogueWarp = 9;    // reduces finished row groups, does the bookkeeping
+constexpr int kThreads = 10 * 32;
 constexpr int kGroup = 4;           // activation vectors per tile (token group)
-constexpr int kRouterKc = 256;      // router chunk columns
-constexpr int kQ8KcMax = 1280;      // largest Q8_0 chunk (columns)
-constexpr int kQ4KcMax = 2048;      // largest Q4KS chunk (columns)
+constexpr int kRowsPerWarp = kRows / kConsumerWarps;  // 4 rows of a chunk per consumer warp
+constexpr int kRouterKc = 256;      // router repack block columns
+constexpr int kRouterCc = 128;      // router chunk columns (half a repack block)
+constexpr int kRouterTileChunks = 4;  // router chunks per router tile (512 columns)
+constexpr int kQ8KcMax = 2048;      // largest Q8_0 chunk (columns)
+constexpr int kQ4KcMax = 4096;      // largest Q4KS chunk (columns)
 constexpr int kMaxSmallT = 8;       // largest T of the GEMV path
+constexpr int kMaxTopK = 16;        // largest top_k
+constexpr int kMaxE = 1024;         // largest expert count
+constexpr int kMaxDownTiles = 256;  // largest H / 128
+constexpr int kMaxSlots = 8;        // stage descriptor slots of the small-T ring
 
 // Activation record of one 32-value block: L limb planes of 32 bytes each
 // (byte i of limb l = bits [8l, 8l+8) of the block fixed-point integer X_i,
@@ -30,27 +41,28 @@ constexpr int kMaxSmallT = 8;       // largest T of the GEMV path
 // round(v_i * 2^s) with s chosen so that max |X_i| <= 2^(8L-2).
 __host__ __device__ constexpr int rec_bytes(int L) { return 32 * L + 16; }
 
-// Bytes of one weight chunk: 32 rows x Kc columns.
-//   Q8_0 : quants [Kc/32 blocks][2 halves][32 rows][16 B], then
-//          scales [Kc/32][32 rows] fp16
-//   Q4KS : quants [Kc/32 sub-blocks][32 rows][16 B] (nibbles permuted so that
+// Bytes of one weight chunk: 32 rows x Kc columns (nbc = Kc/32 blocks).
+//   Q8_0 : quants [32 rows][2 halves][nbc][16 B], then scales [32 rows][nbc] fp16
+//   Q4KS : quants [32 rows][nbc sub-blocks][16 B] (nibbles permuted so that
 //          (word & 0x0F0F0F0F) holds weights 8w..8w+3 and
 //          ((word >> 4) & 0x0F0F0F0F) weights 8w+4..8w+7), then the
-//          serialised 16-byte superblock headers [Kc/256][32 rows][16 B]
-//   F32  : [Kc/4][32 rows][4 floats]
+//          serialised 16-byte superblock headers [32 rows][nbc/8][16 B]
+//   F32  : [Kc/4][32 rows][4 floats]   (router; lane = row)
 __host__ __device__ inline int64_t chunk_bytes(int fmt, int Kc) {
   if (fmt == MOE_Q8_0) return (int64_t)(Kc / 32) * 1088;
   if (fmt == MOE_Q4KS) return (int64_t)(Kc / 32) * 512 + (int64_t)(Kc / 256) * 512;
   return (int64_t)Kc * kRows * 4;
 }
 
-// Chunking of a reduction dimension K for a format: n chunks of Kc columns.
+// Chunking of a reduction dimension K for a format: n chunks of Kc columns,
+// Kc at most the format's largest chunk >> shift (shift > 0 when shared
+// memory cannot hold two stages of the largest chunks).
 struct Chunking {
   int n, Kc;
 };
-inline Chunking choose_chunking(int fmt, int K) {
+inline Chunking choose_chunking(int fmt, int K, int shift = 0) {
   const int unit = fmt == MOE_Q4KS ? 256 : (fmt == MOE_Q8_0 ? 32 : kRouterKc);
-  const int kmax = fmt == MOE_Q4KS ? kQ4KcMax : (fmt == MOE_Q8_0 ? kQ8KcMax : kRouterKc);
+  const int kmax = std::max(unit, (fmt == MOE_Q4KS ? kQ4KcMax : (fmt == MOE_Q8_0 ? kQ8KcMax : kRouterKc)) >> shift);
   int n = (K + kmax - 1) / kmax;
   for (; n <= K / unit; ++n)
     if (K % n == 0 && (K / n) % unit == 0) return {n, K / n};
@@ -80,14 +92,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Waits for the phase with the given parity; the thread may be suspended (it
+// takes no issue slots) for up to 0.5 ms before the call returns false.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(500000)
       : "memory");
   return ok != 0;
 }

@@ -30,11 +30,13 @@ struct Sync {
 struct SmallParams {
   // shapes
   int H, E, k, I, Ish, T;
-  int n_rg, n_ks;         // router: row groups of 32 experts, 256-column slices
-  int n_rb, n_rb_sh;      // gate/up tiles per routed / shared expert (16 outputs each)
-  int n_rbd;              // down tiles per expert (32 outputs each)
+  int n_rg, n_ks, n_kt;   // router: row groups of 32 experts, 256-column repack blocks, 512-column tiles
+  int n_rc;               // router: 128-column chunks (H / 128)
+  int Tp;                 // T rounded up to 4 (partial-logit row stride)
+  int n_gu, n_gu_sh;      // gate/up tiles per routed / shared entry (32 outputs each)
+  int n_dt;               // down tiles per entry (128 outputs each)
   int n_sh;               // shared entries for this T
-  int Imax;               // max(I, Ish): row stride of h / h records
+  int Imax;               // max(I, Ish): row stride of the h records
   int E_pad;              // n_rg * 32
   int w_max;              // capacity of the entry arrays
   // weights (repacked)
@@ -55,8 +57,8 @@ struct SmallParams {
   int* status;
   int* gu_cnt;       // [w_max]
   int* entry_ready;  // [w_max]
-  int* d_cnt;        // [n_rbd]
-  float* partials;   // [n_ks][E_pad][T]
+  int* d_cnt;        // [n_dt]
+  float* partials;   // [n_kt][E_pad][Tp]
   int* ids;          // [T*k]
   float* gates;      // [T*k]
   int* pos;          // [T*k]
@@ -64,11 +66,10 @@ struct SmallParams {
   int* perm;         // [T*k]
   Entry* entries;    // [w_max]
   uint8_t* xrec;     // [T][H/32] records
-  float* h;          // [P][Imax]
   uint8_t* hrec;     // [P][Imax/32] records
   float* z;          // [P][H]
   // shared-memory plan
-  int n_stages, stage_bytes, misc_bytes;
+  int n_stages, ring_bytes, misc_bytes;  // descriptor slots, bytes of the stage ring, router scratch
   uint64_t timeout_ns;
 };
 

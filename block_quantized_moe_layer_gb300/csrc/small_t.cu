@@ -1,34 +1,39 @@
 // small_t.cu -- the fused MoE layer for the MTP verify batch (1 <= T <= 8).
 //
-// One persistent kernel per forward, one CTA per SM.  Warp 8 (one thread) is
-// a producer that claims tiles from a global queue and streams each tile's
-// weight chunks, plus the activation records they need, into a ring of
-// shared-memory stages with 1-D TMA bulk copies.  Warps 0-7 consume: lane =
-// weight row, warp = a slice of the chunk's 32-column blocks.
+// One persistent kernel per forward, one CTA per SM, three warp roles:
+//   producer (warp 8, one thread): claims tiles from a global queue (one claim
+//     ahead) and streams each tile's weight chunks, plus the activation
+//     records they need, into a ring of shared-memory stages with 1-D bulk
+//     copies;
+//   consumers (warps 0-7): lane = weight row, warp = a slice of the chunk's
+//     32-column blocks; integer dot products per block;
+//   epilogue (warp 9): takes each finished 32-row group's partial sums from a
+//     small ring, reduces them and does the bookkeeping (SwiGLU and
+//     activation records, down outputs, counters, the combine), so the
+//     consumers never wait on global-memory round trips.
 //
 // Tile order in the queue (each kind only waits on kinds before it, so every
 // tile another tile waits for has already been claimed by a running CTA):
 //   router tiles     32 experts x 256 columns; partial logits to global.  The
-//                    tiles of row group 0 also convert x into activation
-//                    records.  The last router tile to finish computes the
-//                    routing (top-k, gates, permutation, expert work list).
-//   shared gate/up   16 outputs x full K per tile, tokens of the shared expert
-//   routed gate/up   same, per routed work entry (<= 4 tokens of one expert)
-//   down tiles       32 outputs x full I per tile, per entry (shared first)
-// Hand-offs use last-arriver counters: the last gate/up tile of an entry turns
-// its SwiGLU outputs into activation records and publishes the entry; the last
-// down tile of a 32-row block combines that block of y in slot order.  No
-// floating-point atomics: every sum has a fixed order, so results are
-// bit-reproducible.  Every spin-wait is bounded; on timeout the kernel sets
-// the status word and drains its own copies before leaving.
+//                    tiles of row group 0 also turn x into activation records.
+//                    The last router tile to finish computes the routing
+//                    (top-k, gates, permutation, expert work entries).
+//   shared gate/up   32 outputs (16+16 gate/up rows, twice) x full K
+//   shared down      128 outputs x full I
+//   routed gate/up   per routed work entry (<= 4 tokens of one expert)
+//   routed down
+// Hand-offs use last-arriver counters: the last gate/up tile of an entry
+// publishes it (its activation records are complete); the last down tile of
+// a 128-row block combines that block of y in slot order.  No floating-point
+// atomics: every sum has a fixed order, so results are bit-reproducible.
+// Every spin-wait is bounded; on timeout the kernel records where in the
+// status word, drains its own copies and leaves.
 //
 // Arithmetic: weights enter as their integer codes; activations as block
 // fixed point (32 values share a power-of-two scale, L bytes per value);
 // dp4a gives exact integer block dot products, scaled once per block:
-//   Q8_0 : sum_i d q_i v_i   = d * ascale * sum_i q_i X_i
+//   Q8_0 : sum_i d q_i v_i       = d * ascale * sum_i q_i X_i
 //   Q4KS : sum_i (a q_i - b) v_i = a * ascale * sum_i q_i X_i - b * sumx
-#include <cstdio>
-
 #include "layer.cuh"
 
 namespace moe {
@@ -36,26 +41,40 @@ namespace moe {
 enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3 };
 
 struct Desc {
-  int kind, chunk, nch, M;
-  int entry, rb, nbc, fmt;
-  int slot0, n_ent, n_tiles_entry, rg;
-  int ks, pad0, pad1, pad2;
+  int kind, chunk, nch, M;         // read by every consumer thread
+  int nbc, fmt, rgks, off;         //   " (rgks = router row group << 16 | chunk; off = ring offset)
+  int entry, rbt, group, ngroups;  // read by the epilogue warp
+  int slot0, n_ent, n_tiles_entry, pad;
 };
 
 struct SmemPlan {
-  int ring, bars, descs, red, misc, flags, total;
+  int ring, bars, rbars, descs, metas, rred, red, misc, ecache, escr, pend, flags, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int n_stages, int stage_bytes, int misc_bytes) {
+constexpr int kRedSlots = 8;
+constexpr int kRedSlotBytes = 32 * kGroup * 4;  // sums of one 32-row group: [32 rows][kGroup]
+
+// The ring holds variable-size stages back to back (ring_bytes); n_slots
+// descriptor slots, each with a full / empty barrier pair.
+__host__ __device__ inline SmemPlan smem_plan(int n_stages, int ring_bytes, int misc_bytes, int w_max) {
   SmemPlan p;
   p.ring = 0;
-  p.bars = n_stages * stage_bytes;
-  p.descs = p.bars + 2 * n_stages * 8;
-  p.red = p.descs + n_stages * (int)sizeof(Desc);
-  p.red = (p.red + 15) & ~15;
-  p.misc = p.red + kConsumerWarps * kMaxSmallT * 32 * 4;
-  p.flags = p.misc + misc_bytes;
-  p.total = p.flags + 64;
+  p.bars = ring_bytes;
+  p.rbars = p.bars + 2 * n_stages * 8;
+  p.descs = p.rbars + 2 * kRedSlots * 8;
+  p.metas = p.descs + n_stages * (int)sizeof(Desc);
+  // the router's scratch (rred, misc) shares bytes with the epilogue ring: a
+  // CTA's router tiles and the routing come before any of its gate/up or down
+  // tiles, so the two are never live at once
+  p.red = (p.metas + kRedSlots * (int)sizeof(Desc) + 15) & ~15;
+  p.rred = p.red;
+  p.misc = p.rred + kConsumerWarps * kMaxSmallT * 32 * 4;
+  const int region = max(kRedSlots * kRedSlotBytes, kConsumerWarps * kMaxSmallT * 32 * 4 + misc_bytes);
+  p.ecache = p.red + ((region + 15) & ~15);
+  p.escr = p.ecache + ((w_max * (int)sizeof(Entry) + 15) & ~15);
+  p.pend = p.escr + 2 * kMaxSmallT * kMaxTopK * 4;
+  p.flags = p.pend + 4 * (1 + kMaxDownTiles);
+  p.total = p.flags + 64;  // flags[0..3] and the producer's published-entry bits [4..11]
   return p;
 }
 
@@ -71,7 +90,7 @@ __device__ inline void record_timeout(int* status, int site, int detail) {
 }
 
 enum WaitSite : int { kSiteRouting = 1, kSiteX = 2, kSiteEntry = 3, kSiteEmpty = 4, kSiteFull = 5, kSiteEnd = 6,
-                      kSiteDrain = 7 };
+                      kSiteDrain = 7, kSiteRedEmpty = 8, kSiteRedFull = 9 };
 
 // Bounded spin on a global flag (acquire).  Returns false on timeout.
 __device__ inline bool wait_flag_geq(const int* p, int v, uint64_t limit_ns, int* status, int site, int detail) {
@@ -86,7 +105,7 @@ __device__ inline bool wait_flag_geq(const int* p, int v, uint64_t limit_ns, int
       return false;
     }
     __nanosleep(ns);
-    ns = min(ns * 2, 1024);
+    ns = min(ns * 2, 512);
   }
 }
 
@@ -103,240 +122,212 @@ __device__ inline bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_
   return true;
 }
 
-__device__ inline void entry_info(const SmallParams& P, int entry, Entry& en) {
-  if (entry < P.n_sh) {
-    en.e = -1;
-    en.slot0 = P.T * P.k + kGroup * entry;
-    en.M = min(kGroup, P.T - kGroup * entry);
-    for (int m = 0; m < kGroup; ++m) en.tok[m] = kGroup * entry + m;
-  } else {
-    const int* src = reinterpret_cast<const int*>(P.entries + entry);
-    en.e = __ldcg(src + 0);
-    en.slot0 = __ldcg(src + 1);
-    en.M = __ldcg(src + 2);
-    for (int m = 0; m < kGroup; ++m) en.tok[m] = __ldcg(src + 3 + m);
-  }
+__device__ inline void shared_entry(const SmallParams& P, int entry, Entry& en) {
+  en.e = -1;
+  en.slot0 = P.T * P.k + kGroup * entry;
+  en.M = min(kGroup, P.T - kGroup * entry);
+  for (int m = 0; m < kGroup; ++m) en.tok[m] = kGroup * entry + m;
 }
 
 // ---------------------------------------------------------------------------
 // producer
 // ---------------------------------------------------------------------------
+// Waits until stage j (issue order) has been released by the consumers.
+__device__ __forceinline__ bool wait_released(uint64_t* empty, int NS, int j, const SmallParams& P) {
+  return mbar_wait_bounded(&empty[j % NS], (uint32_t)((j / NS) & 1), P.timeout_ns, P.status, kSiteEmpty, j);
+}
+
+// The producer is one thread; everything it keeps per stage lives in
+// registers or shared memory (no local arrays, no captured locals), since a
+// single thread pays the full latency of every dependent access.
 template <int L>
 __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + P.n_stages;
   Desc* descs = reinterpret_cast<Desc*>(smem + plan.descs);
+  Entry* ecache = reinterpret_cast<Entry*>(smem + plan.ecache);
+  uint32_t* readybits = reinterpret_cast<uint32_t*>(smem + plan.flags) + 4;  // [8] entries seen published
   constexpr int RB = rec_bytes(L);
-  const int NR = P.n_rg * P.n_ks;
-  const int NSG = P.n_sh * P.n_rb_sh;
-  int s = 0;
-  uint32_t ph = 0;
-  int last_ph[8];
-  for (int i = 0; i < 8; ++i) last_ph[i] = -1;
+  constexpr int XEL = L == 2 ? 2 : 4;  // bytes of one x element
+  const int NR = P.n_rg * P.n_kt;
+  const int NSG = P.n_sh * P.n_gu_sh, NSD = P.n_sh * P.n_dt;
+  const int NS = P.n_stages;
+  // Stage j (in issue order) uses descriptor slot j % NS and `need` bytes of
+  // the ring placed right after stage j-1 (or at 0 when the end is reached).
+  // Stages [oldest, issued) may still be in flight; their bytes form one arc
+  // of the ring that starts at descs[oldest % NS].off and ends at head.
+  int issued = 0, oldest = 0, head = 0;
   bool ok = true;
   int n_rent = -1;
+  for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
+  int t = atomicAdd(&P.sync->queue, 1);
   while (ok) {
-    const int t = atomicAdd(&P.sync->queue, 1);
-    Desc d{};
-    Entry en{};
-    const uint8_t* wbase = nullptr;
-    int64_t cbytes = 0;
+    const int t_next = atomicAdd(&P.sync->queue, 1);  // claim one ahead: its latency overlaps this tile
+    int kind, rgk = 0, rbt, entry = 0, ngroups = 1, nch = 1, nbc, fmt, M, slot0 = 0, n_tiles = 0;
+    const Entry* ep = nullptr;
+    bool shared_e = false;
     if (t < NR) {
-      d.kind = kRouter;
-      d.rg = t / P.n_ks;
-      d.ks = t % P.n_ks;
-      d.nch = 1;
-      d.fmt = MOE_F32;
-      d.nbc = kRouterKc / 32;
-      wbase = P.router + (int64_t)t * chunk_bytes(MOE_F32, kRouterKc);
-      cbytes = chunk_bytes(MOE_F32, kRouterKc);
+      kind = kRouter;
+      rgk = (t / P.n_kt) << 16;
+      rbt = t % P.n_kt;  // router: index of the 512-column slice
+      nch = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);
+      fmt = MOE_F32;
+      nbc = kRouterCc / 32;
+      M = P.T;
     } else if (t < NR + NSG) {
-      d.kind = kGateUp;
-      d.entry = (t - NR) / P.n_rb_sh;
-      d.rb = (t - NR) % P.n_rb_sh;
+      kind = kGateUp;
+      entry = (t - NR) / P.n_gu_sh;
+      rbt = (t - NR) % P.n_gu_sh;
+    } else if (t < NR + NSG + NSD) {
+      kind = kDown;
+      entry = (t - NR - NSG) / P.n_dt;
+      rbt = (t - NR - NSG) % P.n_dt;
     } else {
       if (n_rent < 0) {
         if (!wait_flag_geq(&P.sync->routing_ready, 1, P.timeout_ns, P.status, kSiteRouting, t)) { ok = false; break; }
         fence_proxy_async_global();
         n_rent = __ldcg(&P.sync->n_rent);
+        const int* src = reinterpret_cast<const int*>(P.entries + P.n_sh);
+        int* dst = reinterpret_cast<int*>(ecache + P.n_sh);
+        for (int i = 0; i < n_rent * (int)(sizeof(Entry) / 4); ++i) dst[i] = __ldcg(src + i);
       }
-      const int A = NR + NSG;
-      const int NG = n_rent * P.n_rb;
-      const int ND = (P.n_sh + n_rent) * P.n_rbd;
+      const int A = NR + NSG + NSD;
+      const int NG = n_rent * P.n_gu, ND = n_rent * P.n_dt;
       if (t < A + NG) {
-        d.kind = kGateUp;
-        d.entry = P.n_sh + (t - A) / P.n_rb;
-        d.rb = (t - A) % P.n_rb;
+        kind = kGateUp;
+        entry = P.n_sh + (t - A) / P.n_gu;
+        rbt = (t - A) % P.n_gu;
       } else if (t < A + NG + ND) {
-        d.kind = kDown;
-        d.entry = (t - A - NG) / P.n_rbd;
-        d.rb = (t - A - NG) % P.n_rbd;
+        kind = kDown;
+        entry = P.n_sh + (t - A - NG) / P.n_dt;
+        rbt = (t - A - NG) % P.n_dt;
       } else {
         break;  // queue exhausted
       }
     }
-    if (d.kind != kRouter) {
-      entry_info(P, d.entry, en);
-      const bool sh = en.e < 0;
-      d.M = en.M;
-      d.slot0 = en.slot0;
-      if (d.kind == kGateUp) {
-        d.fmt = sh ? P.sfmt : P.fmt;
-        d.nch = sh ? P.sgu_nch : P.gu_nch;
-        const int kc = sh ? P.sgu_kc : P.gu_kc;
-        d.nbc = kc / 32;
-        cbytes = chunk_bytes(d.fmt, kc);
-        wbase = (sh ? P.sgu : P.gu + (int64_t)en.e * P.gu_stride) + (int64_t)d.rb * d.nch * cbytes;
-        d.n_tiles_entry = sh ? P.n_rb_sh : P.n_rb;
+    const uint8_t* wbase;
+    int64_t cbytes;
+    int e_id = -1;
+    if (kind == kRouter) {
+      cbytes = chunk_bytes(MOE_F32, kRouterCc);
+      wbase = P.router + ((int64_t)(rgk >> 16) * P.n_rc + kRouterTileChunks * rbt) * cbytes;
+    } else {
+      shared_e = entry < P.n_sh;
+      if (shared_e) {
+        slot0 = P.T * P.k + kGroup * entry;
+        M = min(kGroup, P.T - kGroup * entry);
       } else {
-        d.fmt = sh ? P.sfmt : P.fmt;
-        d.nch = sh ? P.sdn_nch : P.dn_nch;
-        const int kc = sh ? P.sdn_kc : P.dn_kc;
-        d.nbc = kc / 32;
-        cbytes = chunk_bytes(d.fmt, kc);
-        wbase = (sh ? P.sdn : P.dn + (int64_t)en.e * P.dn_stride) + (int64_t)d.rb * d.nch * cbytes;
-        d.n_ent = P.n_sh + n_rent;
+        ep = ecache + entry;
+        e_id = ep->e;
+        slot0 = ep->slot0;
+        M = ep->M;
+      }
+      fmt = shared_e ? P.sfmt : P.fmt;
+      if (kind == kGateUp) {
+        ngroups = 2;
+        nch = shared_e ? P.sgu_nch : P.gu_nch;
+        const int kc = shared_e ? P.sgu_kc : P.gu_kc;
+        nbc = kc / 32;
+        cbytes = chunk_bytes(fmt, kc);
+        wbase = (shared_e ? P.sgu : P.gu + (int64_t)e_id * P.gu_stride) + (int64_t)(2 * rbt) * nch * cbytes;
+        n_tiles = shared_e ? P.n_gu_sh : P.n_gu;
+      } else {
+        ngroups = 4;
+        nch = shared_e ? P.sdn_nch : P.dn_nch;
+        const int kc = shared_e ? P.sdn_kc : P.dn_kc;
+        nbc = kc / 32;
+        cbytes = chunk_bytes(fmt, kc);
+        wbase = (shared_e ? P.sdn : P.dn + (int64_t)e_id * P.dn_stride) + (int64_t)(4 * rbt) * nch * cbytes;
       }
     }
-    bool dep_ok = false;  // activation dependency satisfied for this tile
-    for (int c = 0; c < d.nch && ok; ++c) {
-      if (!mbar_wait_bounded(&empty[s], ph ^ 1u, P.timeout_ns, P.status, kSiteEmpty, t)) { ok = false; break; }
-      d.chunk = c;
-      uint8_t* stage = smem + plan.ring + s * P.stage_bytes;
-      const uint32_t wb = (uint32_t)cbytes;
-      const uint32_t ab = (d.kind == kRouter) ? 0u : (uint32_t)(d.M * d.nbc * RB);
-      descs[s] = d;
-      mbar_arrive_expect_tx(&full[s], wb + ab);
-      bulk_g2s(stage, wbase + (int64_t)c * cbytes, wb, &full[s]);
-      if (d.kind != kRouter) {
-        if (!dep_ok) {
-          if (d.kind == kGateUp) {
-            // shared gate/up needs the x records; routed ones were gated by the routing flag
-            if (en.e < 0) dep_ok = wait_flag_geq(&P.sync->x_done, P.n_ks, P.timeout_ns, P.status, kSiteX, t);
-            else dep_ok = true;
-          } else {
-            dep_ok = wait_flag_geq(&P.entry_ready[d.entry], 1, P.timeout_ns, P.status, kSiteEntry,
-                                   d.entry * 65536 + (t & 0xFFFF));
-          }
+    const uint32_t per = kind == kRouter ? (uint32_t)(kRouterCc * XEL) : (uint32_t)(nbc * RB);
+    const uint32_t wb = (uint32_t)cbytes;
+    const int need = (int)((wb + (uint32_t)M * per + 127u) & ~127u);
+    // activation sources of this tile at chunk 0, and their step per chunk
+    const uint8_t* asrc[kMaxSmallT];
+    int64_t astep;
+    if (kind == kRouter) {
+      astep = (int64_t)kRouterCc * XEL;
+#pragma unroll
+      for (int m = 0; m < kMaxSmallT; ++m)
+        asrc[m] = static_cast<const uint8_t*>(P.x) + ((int64_t)m * P.H + (int64_t)kRouterTileChunks * rbt * kRouterCc) * XEL;
+    } else {
+      astep = (int64_t)nbc * RB;
+#pragma unroll
+      for (int m = 0; m < kMaxSmallT; ++m) {
+        const int mm = m < kGroup ? m : 0;
+        asrc[m] = kind == kGateUp
+                      ? P.xrec + (int64_t)(shared_e ? kGroup * entry + mm : ep->tok[mm]) * (P.H / 32) * RB
+                      : P.hrec + (int64_t)(slot0 + mm) * (P.Imax / 32) * RB;
+      }
+    }
+    const int4 h3 = make_int4(slot0, P.n_sh + max(n_rent, 0), n_tiles, 0);
+    bool dep_ok = kind == kRouter;
+    const int nstages = ngroups * nch;
+    for (int q = 0; q < nstages && ok; ++q) {
+      const int g = q / nch, c = q - g * nch;
+      // ring space: a free slot, then free bytes
+      while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
+      int pos = 0;
+      while (ok) {
+        pos = head + need <= P.ring_bytes ? head : 0;
+        if (oldest == issued) break;
+        const int A = descs[oldest & (NS - 1)].off;
+        if (A < head ? (pos + need <= A || pos >= head) : (pos >= head && pos + need <= A)) break;
+        ok = wait_released(empty, NS, oldest++, P);
+      }
+      if (!ok) break;
+      head = pos + need;
+      const int s = issued & (NS - 1);
+      const int kch = kind == kRouter ? kRouterTileChunks * rbt + c : 0;
+      int4* dd = reinterpret_cast<int4*>(descs + s);
+      dd[0] = make_int4(kind, c, nch, M);
+      dd[1] = make_int4(nbc, fmt, rgk | kch, pos);
+      dd[2] = make_int4(entry, rbt, g, ngroups);
+      dd[3] = h3;
+      uint8_t* stage = smem + plan.ring + pos;
+      mbar_arrive_expect_tx(&full[s], wb + (uint32_t)M * per);
+      bulk_g2s(stage, wbase + (int64_t)q * cbytes, wb, &full[s]);
+      if (!dep_ok) {
+        if (kind == kGateUp) {
+          // shared gate/up needs the x records; routed ones were gated by the routing flag
+          dep_ok = !shared_e || wait_flag_geq(&P.sync->x_done, P.T * P.n_rc, P.timeout_ns, P.status, kSiteX, t);
+        } else if (readybits[entry >> 5] & (1u << (entry & 31))) {
+          dep_ok = true;
+        } else {
+          dep_ok = wait_flag_geq(&P.entry_ready[entry], 1, P.timeout_ns, P.status, kSiteEntry,
+                                 entry * 65536 + (t & 0xFFFF));
+          if (dep_ok) readybits[entry >> 5] |= 1u << (entry & 31);
         }
         if (dep_ok) fence_proxy_async_global();
-        if (!dep_ok) {
-          // keep the stage's byte count consistent: fill the activation part
-          // with weight bytes again (the consumers see the status and stop)
-          ok = false;
-        }
-        uint8_t* adst = stage + wb;
-        const int kc = d.nbc * 32;
-        for (int m = 0; m < d.M; ++m) {
-          const uint8_t* src;
-          if (!dep_ok) {
-            src = wbase;  // harmless in-bounds bytes, only to complete the phase
-          } else if (d.kind == kGateUp) {
-            src = P.xrec + ((int64_t)en.tok[m] * (P.H / 32) + (int64_t)c * d.nbc) * RB;
-          } else {
-            src = P.hrec + ((int64_t)(en.slot0 + m) * (P.Imax / 32) + (int64_t)c * d.nbc) * RB;
-          }
-          (void)kc;
-          bulk_g2s(adst + m * d.nbc * RB, src, (uint32_t)(d.nbc * RB), &full[s]);
-        }
+        else ok = false;  // the consumers see the status word; the stage is still completed below
       }
-      last_ph[s] = (int)ph;
-      if (++s == P.n_stages) { s = 0; ph ^= 1u; }
+      uint8_t* adst = stage + wb;
+      const int64_t aoff = (int64_t)(kind == kRouter ? c : c) * astep;
+#pragma unroll
+      for (int m = 0; m < kMaxSmallT; ++m)
+        if (m < M) bulk_g2s(adst + m * per, dep_ok ? asrc[m] + aoff : wbase, per, &full[s]);
+      ++issued;
     }
+    t = t_next;
   }
-  // end marker (or error): hand the consumers an END descriptor
-  if (mbar_wait_bounded(&empty[s], ph ^ 1u, P.timeout_ns, P.status, kSiteEnd, s)) {
-    Desc d{};
-    d.kind = kEnd;
-    descs[s] = d;
-    mbar_arrive(&full[s]);
-    // the consumers released this stage's previous fill, so its copies have
-    // landed; the END arrival moved its barrier one phase on, so it must not
-    // be waited for below
-    last_ph[s] = -1;
+  // end marker (or error): hand the consumers an END descriptor in the next slot
+  const int n_data = issued;
+  bool have_slot = true;
+  while (have_slot && oldest <= issued - NS) have_slot = wait_released(empty, NS, oldest++, P);
+  if (have_slot) {
+    reinterpret_cast<int4*>(descs + issued % NS)[0] = make_int4(kEnd, 0, 0, 0);
+    mbar_arrive(&full[issued % NS]);
   }
   // drain: every bulk copy this CTA issued must have landed before it exits
-  // (a stage's barrier only advances past its last fill when that fill lands)
-  for (int i = 0; i < P.n_stages; ++i)
-    if (last_ph[i] >= 0) mbar_wait_bounded(&full[i], (uint32_t)last_ph[i], P.timeout_ns, P.status, kSiteDrain, i);
+  for (int j = oldest; j < n_data; ++j)
+    mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), P.timeout_ns, P.status, kSiteDrain, j);
 }
 
 // ---------------------------------------------------------------------------
 // consumer: chunk compute
 // ---------------------------------------------------------------------------
-template <int L>
-__device__ __forceinline__ int block_dot_q8(uint4 q0, uint4 q1, const uint8_t* rec) {
-  const uint4 a0 = *reinterpret_cast<const uint4*>(rec);
-  const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 16);
-  int s0 = 0;
-  s0 = dp4a_su(q0.x, a0.x, s0); s0 = dp4a_su(q0.y, a0.y, s0);
-  s0 = dp4a_su(q0.z, a0.z, s0); s0 = dp4a_su(q0.w, a0.w, s0);
-  s0 = dp4a_su(q1.x, a1.x, s0); s0 = dp4a_su(q1.y, a1.y, s0);
-  s0 = dp4a_su(q1.z, a1.z, s0); s0 = dp4a_su(q1.w, a1.w, s0);
-  return s0;
-}
-template <int L>
-__device__ __forceinline__ int block_dot_q8_top(uint4 q0, uint4 q1, const uint8_t* rec) {
-  const uint4 a0 = *reinterpret_cast<const uint4*>(rec);
-  const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 16);
-  int s = 0;
-  s = dp4a_ss(q0.x, a0.x, s); s = dp4a_ss(q0.y, a0.y, s);
-  s = dp4a_ss(q0.z, a0.z, s); s = dp4a_ss(q0.w, a0.w, s);
-  s = dp4a_ss(q1.x, a1.x, s); s = dp4a_ss(q1.y, a1.y, s);
-  s = dp4a_ss(q1.z, a1.z, s); s = dp4a_ss(q1.w, a1.w, s);
-  return s;
-}
-
-// sum over limbs of the block dot product, as float
-template <int L>
-__device__ __forceinline__ float limbs_q8(uint4 q0, uint4 q1, const uint8_t* rec) {
-  if constexpr (L == 2) {
-    const int s0 = block_dot_q8<L>(q0, q1, rec);
-    const int s1 = block_dot_q8_top<L>(q0, q1, rec + 32);
-    return (float)(s1 * 256 + s0);
-  } else {
-    const int s0 = block_dot_q8<L>(q0, q1, rec);
-    const int s1 = block_dot_q8<L>(q0, q1, rec + 32);
-    const int s2 = block_dot_q8<L>(q0, q1, rec + 64);
-    const int s3 = block_dot_q8_top<L>(q0, q1, rec + 96);
-    return fmaf((float)s3, 16777216.f, fmaf((float)s2, 65536.f, fmaf((float)s1, 256.f, (float)s0)));
-  }
-}
-
-__device__ __forceinline__ int q4_dot(const uint32_t (&w)[8], const uint8_t* rec, bool top) {
-  const uint4 a0 = *reinterpret_cast<const uint4*>(rec);
-  const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 16);
-  int s = 0;
-  if (!top) {
-    s = dp4a_uu(w[0], a0.x, s); s = dp4a_uu(w[1], a0.y, s);
-    s = dp4a_uu(w[2], a0.z, s); s = dp4a_uu(w[3], a0.w, s);
-    s = dp4a_uu(w[4], a1.x, s); s = dp4a_uu(w[5], a1.y, s);
-    s = dp4a_uu(w[6], a1.z, s); s = dp4a_uu(w[7], a1.w, s);
-  } else {
-    s = dp4a_us(w[0], a0.x, s); s = dp4a_us(w[1], a0.y, s);
-    s = dp4a_us(w[2], a0.z, s); s = dp4a_us(w[3], a0.w, s);
-    s = dp4a_us(w[4], a1.x, s); s = dp4a_us(w[5], a1.y, s);
-    s = dp4a_us(w[6], a1.z, s); s = dp4a_us(w[7], a1.w, s);
-  }
-  return s;
-}
-
-template <int L>
-__device__ __forceinline__ float limbs_q4(const uint32_t (&w)[8], const uint8_t* rec) {
-  if constexpr (L == 2) {
-    const int s0 = q4_dot(w, rec, false);
-    const int s1 = q4_dot(w, rec + 32, true);
-    return (float)(s1 * 256 + s0);
-  } else {
-    const int s0 = q4_dot(w, rec, false);
-    const int s1 = q4_dot(w, rec + 32, false);
-    const int s2 = q4_dot(w, rec + 64, false);
-    const int s3 = q4_dot(w, rec + 96, true);
-    return fmaf((float)s3, 16777216.f, fmaf((float)s2, 65536.f, fmaf((float)s1, 256.f, (float)s0)));
-  }
-}
-
 __device__ __forceinline__ uint32_t field6(uint32_t w0, uint32_t w1, uint32_t w2, int f) {
   const int p = 6 * f;
   const int wi = p >> 5, sh = p & 31;
@@ -345,60 +336,130 @@ __device__ __forceinline__ uint32_t field6(uint32_t w0, uint32_t w1, uint32_t w2
   return __funnelshift_r(lo, hi, sh) & 63u;
 }
 
+// Integer dot product of one 32-weight Q8_0 block (codes q0 | q1) with one
+// activation record: four independent dp4a chains of four, then the limbs
+// combined exactly (L = 2) or in fp32 (L = 4).
 template <int L>
-__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, const Desc& d, float (&acc)[kGroup]) {
+__device__ __forceinline__ float q8_block(const uint4 q0, const uint4 q1, const uint8_t* rec) {
+  int c[2 * L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
+    if (l == L - 1) {  // top limb: signed
+      c[2 * l] = dp4a_ss(q0.w, a0.w, dp4a_ss(q0.z, a0.z, dp4a_ss(q0.y, a0.y, dp4a_ss(q0.x, a0.x, 0))));
+      c[2 * l + 1] = dp4a_ss(q1.w, a1.w, dp4a_ss(q1.z, a1.z, dp4a_ss(q1.y, a1.y, dp4a_ss(q1.x, a1.x, 0))));
+    } else {
+      c[2 * l] = dp4a_su(q0.w, a0.w, dp4a_su(q0.z, a0.z, dp4a_su(q0.y, a0.y, dp4a_su(q0.x, a0.x, 0))));
+      c[2 * l + 1] = dp4a_su(q1.w, a1.w, dp4a_su(q1.z, a1.z, dp4a_su(q1.y, a1.y, dp4a_su(q1.x, a1.x, 0))));
+    }
+  }
+  if constexpr (L == 2) {
+    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
+  } else {
+    return fmaf((float)(c[6] + c[7]), 16777216.f,
+                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
+  }
+}
+
+// Same for one 32-weight Q4KS sub-block; w[2j] holds codes 8j..8j+3 and
+// w[2j+1] codes 8j+4..8j+7, one per byte.
+template <int L>
+__device__ __forceinline__ float q4_block(const uint32_t (&w)[8], const uint8_t* rec) {
+  int c[2 * L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
+    if (l == L - 1) {
+      c[2 * l] = dp4a_us(w[3], a0.w, dp4a_us(w[2], a0.z, dp4a_us(w[1], a0.y, dp4a_us(w[0], a0.x, 0))));
+      c[2 * l + 1] = dp4a_us(w[7], a1.w, dp4a_us(w[6], a1.z, dp4a_us(w[5], a1.y, dp4a_us(w[4], a1.x, 0))));
+    } else {
+      c[2 * l] = dp4a_uu(w[3], a0.w, dp4a_uu(w[2], a0.z, dp4a_uu(w[1], a0.y, dp4a_uu(w[0], a0.x, 0))));
+      c[2 * l + 1] = dp4a_uu(w[7], a1.w, dp4a_uu(w[6], a1.z, dp4a_uu(w[5], a1.y, dp4a_uu(w[4], a1.x, 0))));
+    }
+  }
+  if constexpr (L == 2) {
+    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
+  } else {
+    return fmaf((float)(c[6] + c[7]), 16777216.f,
+                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
+  }
+}
+
+__device__ __forceinline__ void q4_unpack(const uint4 qv, uint32_t (&w)[8]) {
+  w[0] = qv.x & 0x0F0F0F0Fu; w[1] = (qv.x >> 4) & 0x0F0F0F0Fu;
+  w[2] = qv.y & 0x0F0F0F0Fu; w[3] = (qv.y >> 4) & 0x0F0F0F0Fu;
+  w[4] = qv.z & 0x0F0F0F0Fu; w[5] = (qv.z >> 4) & 0x0F0F0F0Fu;
+  w[6] = qv.w & 0x0F0F0F0Fu; w[7] = (qv.w >> 4) & 0x0F0F0F0Fu;
+}
+
+// a = d * sc[s], b = dmin * m[s] of sub-block s from a 16-byte superblock header
+__device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float& b) {
+  const float dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+  a = dd * (float)field6(hd.y, hd.z, hd.w, s);
+  b = dmin * (float)field6(hd.y, hd.z, hd.w, 8 + s);
+}
+
+// One chunk.  Warp w owns rows 4w..4w+3 of the chunk; lane l owns blocks l,
+// l+32, ...  Per block a lane loads its activation record once and reuses it
+// for the warp's four rows, so the shared-memory traffic is the weights once
+// plus one record read per warp.  acc[r][m] collects this lane's share of
+// row r's dot product with vector m; the lanes are summed when the row group
+// is complete.
+template <int L>
+__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M,
+                                           float (&acc)[kRowsPerWarp][kGroup]) {
   constexpr int RB = rec_bytes(L);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nbc = d.nbc;
-  const int nbw = (nbc + kConsumerWarps - 1) / kConsumerWarps;
-  const int b0 = warp * nbw, b1 = min(nbc, b0 + nbw);
-  const int M = d.M;
-  const uint8_t* A = stage + chunk_bytes(d.fmt, nbc * 32);
-  if (d.fmt == MOE_Q8_0) {
+  const int r0 = warp * kRowsPerWarp;
+  const uint8_t* A = stage + chunk_bytes(fmt, nbc * 32);
+  if (fmt == MOE_Q8_0) {
     const __half* sc = reinterpret_cast<const __half*>(stage + nbc * 1024);
-    for (int b = b0; b < b1; ++b) {
-      const uint4 q0 = *reinterpret_cast<const uint4*>(stage + ((b * 2 + 0) * 32 + lane) * 16);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(stage + ((b * 2 + 1) * 32 + lane) * 16);
-      const float dq = __half2float(sc[b * 32 + lane]);
+    for (int b = lane; b < nbc; b += 32) {
+      uint4 q0[kRowsPerWarp], q1[kRowsPerWarp];
+      float dq[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        q0[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)((r0 + r) * 2 + 0) * nbc + b) * 16);
+        q1[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)((r0 + r) * 2 + 1) * nbc + b) * 16);
+        dq[r] = __half2float(sc[(r0 + r) * nbc + b]);
+      }
 #pragma unroll
       for (int m = 0; m < kGroup; ++m) {
         if (m < M) {
           const uint8_t* rec = A + (m * nbc + b) * RB;
           const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
-          acc[m] = fmaf(dq * asc, limbs_q8<L>(q0, q1, rec), acc[m]);
+#pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r) acc[r][m] = fmaf(dq[r] * asc, q8_block<L>(q0[r], q1[r], rec), acc[r][m]);
         }
       }
     }
   } else {  // MOE_Q4KS
-    const uint8_t* hdr_base = stage + nbc * 512;
-    int cur_sb = -1;
-    float dd = 0.f, dmin = 0.f;
-    uint32_t f0 = 0, f1 = 0, f2 = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int sb = b >> 3;
-      if (sb != cur_sb) {
-        const uint4 hd = *reinterpret_cast<const uint4*>(hdr_base + (sb * 32 + lane) * 16);
-        dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-        dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-        f0 = hd.y; f1 = hd.z; f2 = hd.w;
-        cur_sb = sb;
+    const uint8_t* hdr = stage + nbc * 512;
+    const int nsup = nbc / 8;
+    for (int b = lane; b < nbc; b += 32) {
+      uint4 qv[kRowsPerWarp];
+      float sa[kRowsPerWarp], sb[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        qv[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)(r0 + r) * nbc + b) * 16);
+        const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((r0 + r) * nsup + (b >> 3)) * 16);
+        q4_scales(hd, b & 7, sa[r], sb[r]);
       }
-      const int sidx = b & 7;
-      const float a = dd * (float)field6(f0, f1, f2, sidx);
-      const float bq = dmin * (float)field6(f0, f1, f2, 8 + sidx);
-      const uint4 qv = *reinterpret_cast<const uint4*>(stage + (b * 32 + lane) * 16);
-      uint32_t w[8];
-      w[0] = qv.x & 0x0F0F0F0Fu; w[1] = (qv.x >> 4) & 0x0F0F0F0Fu;
-      w[2] = qv.y & 0x0F0F0F0Fu; w[3] = (qv.y >> 4) & 0x0F0F0F0Fu;
-      w[4] = qv.z & 0x0F0F0F0Fu; w[5] = (qv.z >> 4) & 0x0F0F0F0Fu;
-      w[6] = qv.w & 0x0F0F0F0Fu; w[7] = (qv.w >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
       for (int m = 0; m < kGroup; ++m) {
         if (m < M) {
           const uint8_t* rec = A + (m * nbc + b) * RB;
-          const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
-          const float sx = *reinterpret_cast<const float*>(rec + 32 * L + 4);
-          acc[m] = fmaf(a * asc, limbs_q4<L>(w, rec), fmaf(-bq, sx, acc[m]));
+          const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
+          const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
+#pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r) {
+            uint32_t w[8];
+            q4_unpack(qv[r], w);
+            acc[r][m] = fmaf(sa[r] * asc, q4_block<L>(w, rec), fmaf(-sb[r], sx, acc[r][m]));
+          }
         }
       }
     }
@@ -408,6 +469,39 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, const Desc& d, 
 // ---------------------------------------------------------------------------
 // consumer: routing (last router tile)
 // ---------------------------------------------------------------------------
+// The k largest of row[0..E) by (value desc, index asc), one warp; lane l
+// holds experts l, l+32, ... (NPER of them) in registers.  Writes ids and
+// values in slot order.
+template <int NPER>
+__device__ __forceinline__ void topk_token(const float* row, int E, int k, int* ids, float* vals_out) {
+  const int lane = threadIdx.x & 31;
+  float v[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -INFINITY;
+  }
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && v[i] > best) { best = v[i]; bi = e; }  // ascending e: the first wins ties
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    }
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+      if (lane + 32 * i == bi) v[i] = -INFINITY;
+    if (lane == 0) { ids[j] = bi; vals_out[j] = best; }
+  }
+}
+
 __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   const int tid = threadIdx.x;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
@@ -418,37 +512,42 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   int* sperm = reinterpret_cast<int*>(sl + ((Tk + 3) & ~3));         // [Tk]
 
   __threadfence();
-  for (int i = tid; i < T * E; i += kConsumerWarps * 32) {
-    const int t = i / E, e = i % E;
-    float v = 0.f;
-    for (int ks = 0; ks < P.n_ks; ++ks) v += __ldcg(&P.partials[((int64_t)ks * P.E_pad + e) * T + t]);
-    if (P.router_b) v += P.router_b[e];
-    lg[t * E + e] = v;
+  // logits: thread i sums, in slice order, the partials of experts e = i,
+  // i + 256, ... (the loads of one expert are all in flight before the adds)
+  for (int e = tid; e < E; e += kConsumerWarps * 32) {
+    const float bias = P.router_b ? P.router_b[e] : 0.f;
+    for (int q = 0; q < P.Tp / 4; ++q) {
+      float4 a[8];
+#pragma unroll
+      for (int kt = 0; kt < 8; ++kt)
+        if (kt < P.n_kt)
+          a[kt] = __ldcg(reinterpret_cast<const float4*>(P.partials + ((int64_t)kt * P.E_pad + e) * P.Tp) + q);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int kt = 0; kt < 8; ++kt)
+        if (kt < P.n_kt) { v.x += a[kt].x; v.y += a[kt].y; v.z += a[kt].z; v.w += a[kt].w; }
+      for (int kt = 8; kt < P.n_kt; ++kt) {  // H > 4096: further slices, one at a time
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(P.partials + ((int64_t)kt * P.E_pad + e) * P.Tp) + q);
+        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+      }
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 4; ++c)
+        if (4 * q + c < T) lg[(4 * q + c) * E + e] = vv[c] + bias;
+    }
   }
   for (int e = tid; e < E; e += kConsumerWarps * 32) cnt[e] = 0;
   consumer_sync();
 
-  // top-k per token (one warp per token): (value desc, index asc)
+  // top-k per token (one warp per token): (value desc, index asc).  Each lane
+  // keeps its experts' logits (e = lane + 32 i) in registers.
   const int lane = tid & 31, warp = tid >> 5;
+  const int nper = (E + 31) / 32;
   for (int t = warp; t < T; t += kConsumerWarps) {
-    uint32_t chosen = 0;  // bit i <-> expert lane + 32 i
-    for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int i = 0, e = lane; e < E; ++i, e += 32) {
-        if (chosen & (1u << i)) continue;
-        const float v = lg[t * E + e];
-        if (v > best || (v == best && e < bi)) { best = v; bi = e; }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-      }
-      if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
-      if (lane == 0) { sid[t * k + j] = bi; sl[t * k + j] = best; }
-    }
+    if (nper <= 4) topk_token<4>(lg + t * E, E, k, sid + t * k, sl + t * k);
+    else if (nper <= 8) topk_token<8>(lg + t * E, E, k, sid + t * k, sl + t * k);
+    else if (nper <= 12) topk_token<12>(lg + t * E, E, k, sid + t * k, sl + t * k);
+    else if (nper <= 16) topk_token<16>(lg + t * E, E, k, sid + t * k, sl + t * k);
+    else topk_token<kMaxE / 32>(lg + t * E, E, k, sid + t * k, sl + t * k);
     __syncwarp();
     if (lane < k) {
       const float l0 = sl[t * k];
@@ -462,19 +561,23 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   consumer_sync();
 
   if (warp == 0) {
-    // ranks of pairs within their expert (stable), histogram
+    // rank of each pair among the earlier pairs of its expert (stable), and
+    // the histogram: 32 pairs at a time, equal experts found with match_any
     int rank[4], ep[4];
     for (int r = 0; r < 4; ++r) {
       const int p = lane + 32 * r;
+      const int e = p < Tk ? sid[p] : -1 - lane;
+      const unsigned mask = __match_any_sync(0xffffffffu, e);
       rank[r] = 0;
       ep[r] = -1;
       if (p < Tk) {
-        ep[r] = sid[p];
-        for (int q = 0; q < p; ++q) rank[r] += (sid[q] == ep[r]);
-        atomicAdd(&cnt[ep[r]], 1);
+        ep[r] = e;
+        rank[r] = cnt[e] + __popc(mask & ((1u << lane) - 1u));
       }
+      __syncwarp();
+      if (p < Tk && (mask & ((1u << lane) - 1u)) == 0) cnt[e] += __popc(mask);  // one lane per expert
+      __syncwarp();
     }
-    __syncwarp();
     // exclusive scans over experts: pair offsets, entry counts
     const int nper = (E + 31) / 32;
     const int e0 = lane * nper, e1 = min(E, e0 + nper);
@@ -531,187 +634,297 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
 }
 
 // ---------------------------------------------------------------------------
-// consumer loop
+// consumers
 // ---------------------------------------------------------------------------
 template <int L>
 __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + P.n_stages;
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + plan.rbars);
+  uint64_t* rempty = rfull + kRedSlots;
   const Desc* descs = reinterpret_cast<const Desc*>(smem + plan.descs);
-  float* red = reinterpret_cast<float*>(smem + plan.red);  // [8 warps][8][32]
+  Desc* metas = reinterpret_cast<Desc*>(smem + plan.metas);
+  float* rred = reinterpret_cast<float*>(smem + plan.rred);  // [8 warps][8 tokens][32]
+  float* red = reinterpret_cast<float*>(smem + plan.red);    // [slot][8 warps][4][32]
   uint8_t* misc = smem + plan.misc;
   int* flags = reinterpret_cast<int*>(smem + plan.flags);
   constexpr int RB = rec_bytes(L);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = P.T;
-  int s = 0;
-  uint32_t ph = 0;
-  float acc[kGroup] = {0.f, 0.f, 0.f, 0.f};
+  int s = 0, rs = 0;
+  uint32_t ph = 0, rph = 0;
+  float acc[kRowsPerWarp][kGroup];
   float racc[kMaxSmallT];
 
   while (true) {
     if (!mbar_wait_bounded(&full[s], ph, P.timeout_ns, P.status, kSiteFull, s)) break;
-    const Desc d = descs[s];
-    if (d.kind == kEnd) break;
-    const uint8_t* stage = smem + plan.ring + s * P.stage_bytes;
+    Desc d;  // consumers need only the first 32 bytes; thread 0 copies the rest for the epilogue
+    {
+      const int4* src = reinterpret_cast<const int4*>(descs + s);
+      const int4 h0 = src[0], h1 = src[1];
+      d.kind = h0.x; d.chunk = h0.y; d.nch = h0.z; d.M = h0.w;
+      d.nbc = h1.x; d.fmt = h1.y; d.rgks = h1.z; d.off = h1.w;
+      if (tid == 0) {
+        const int4 h2 = src[2], h3 = src[3];
+        d.entry = h2.x; d.rbt = h2.y; d.group = h2.z; d.ngroups = h2.w;
+        d.slot0 = h3.x; d.n_ent = h3.y; d.n_tiles_entry = h3.z; d.pad = h3.w;
+      }
+    }
+    if (d.kind == kEnd) {
+      // pass the end marker on to the epilogue warp
+      if (mbar_wait_bounded(&rempty[rs], rph ^ 1u, P.timeout_ns, P.status, kSiteRedEmpty, rs)) {
+        if (tid == 0) metas[rs] = d;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rfull[rs]);
+      }
+      break;
+    }
+    const uint8_t* stage = smem + plan.ring + d.off;
+    const int d_rg = d.rgks >> 16, d_ks = d.rgks & 0xFFFF;  // router tiles
 
     if (d.kind == kRouter) {
-      // stage x[:, 256-column slice] as fp32
-      float* xs = reinterpret_cast<float*>(misc);  // [T][256]
-      const int col0 = d.ks * kRouterKc;
-      for (int t = 0; t < T; ++t) {
-        float v;
-        if constexpr (L == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + col0 + tid]);
-        else v = reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + col0 + tid];
-        xs[t * kRouterKc + tid] = v;
-      }
-      consumer_sync();
-      if (d.rg == 0) {
-        // x slice -> activation records (warp w: block ks*8 + w)
-        for (int t = 0; t < T; ++t)
-          write_record<L>(xs[t * kRouterKc + warp * 32 + lane],
-                          P.xrec + ((int64_t)t * (P.H / 32) + d.ks * 8 + warp) * RB);
+      const uint8_t* xs = stage + chunk_bytes(MOE_F32, kRouterCc);  // [T][128] x slice
+      auto xval = [&](int t, int c) -> float {
+        if constexpr (L == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xs)[t * kRouterCc + c]);
+        else return reinterpret_cast<const float*>(xs)[t * kRouterCc + c];
+      };
+      if (d_rg < T && warp < kRouterCc / 32) {
+        // x slice -> activation records for tokens t = rg, rg + n_rg, ... (warp w: block 4*ks + w)
+        for (int t = d_rg; t < T; t += P.n_rg)
+          write_record<L>(xval(t, warp * 32 + lane),
+                          P.xrec + ((int64_t)t * (P.H / 32) + d_ks * (kRouterCc / 32) + warp) * RB);
         __threadfence();
         fence_proxy_async_global();
       }
-      for (int t = 0; t < kMaxSmallT; ++t) racc[t] = 0.f;
-      for (int k4 = warp * 8; k4 < warp * 8 + 8; ++k4) {
+      if (d.chunk == 0)
+        for (int t = 0; t < kMaxSmallT; ++t) racc[t] = 0.f;
+      for (int k4 = warp * 4; k4 < warp * 4 + 4; ++k4) {
         const float4 w = *reinterpret_cast<const float4*>(stage + (k4 * 32 + lane) * 16);
 #pragma unroll
         for (int t = 0; t < kMaxSmallT; ++t) {
           if (t < T) {
-            const float4 xv = *reinterpret_cast<const float4*>(xs + t * kRouterKc + k4 * 4);
+            float4 xv;
+            if constexpr (L == 2) {
+              const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * kRouterCc + k4 * 4) * 2);
+              xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                               __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+            } else {
+              xv = *reinterpret_cast<const float4*>(xs + (t * kRouterCc + k4 * 4) * 4);
+            }
             racc[t] = fmaf(w.x, xv.x, fmaf(w.y, xv.y, fmaf(w.z, xv.z, fmaf(w.w, xv.w, racc[t]))));
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (d.chunk == d.nch - 1) {
 #pragma unroll
-      for (int t = 0; t < kMaxSmallT; ++t)
-        if (t < T) red[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
-      consumer_sync();
-      if (tid < T * 32) {
-        const int t = tid >> 5, r = tid & 31;
-        float v = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * kMaxSmallT + t) * 32 + r];
-        const int e = d.rg * 32 + r;
-        P.partials[((int64_t)d.ks * P.E_pad + e) * T + t] = v;
+        for (int t = 0; t < kMaxSmallT; ++t)
+          if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
+        consumer_sync();
+        if (tid < T * 32) {
+          const int t = tid >> 5, r = tid & 31;
+          float v = 0.f;
+          for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
+          P.partials[((int64_t)(d_ks / kRouterTileChunks) * P.E_pad + d_rg * 32 + r) * P.Tp + t] = v;
+        }
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) {
+          if (d_rg < T) atomicAdd(&P.sync->x_done, d.nch * ((T - 1 - d_rg) / P.n_rg + 1));
+          const int old = atomicAdd(&P.sync->router_done, 1);
+          flags[0] = (old == P.n_rg * P.n_kt - 1);
+        }
+        consumer_sync();
+        if (flags[0]) finalize_routing(P, misc);
+        consumer_sync();
       }
-      __threadfence();
-      consumer_sync();
-      if (tid == 0) {
-        if (d.rg == 0) atomicAdd(&P.sync->x_done, 1);
-        const int old = atomicAdd(&P.sync->router_done, 1);
-        flags[0] = (old == P.n_rg * P.n_ks - 1);
-      }
-      consumer_sync();
-      if (flags[0]) finalize_routing(P, misc);
-      consumer_sync();
     } else {
-      if (d.chunk == 0)
-        for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
-      gemv_chunk<L>(stage, d, acc);
+      if (d.chunk == 0) {
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+          for (int m = 0; m < kGroup; ++m) acc[r][m] = 0.f;
+      }
+      gemv_chunk<L>(stage, d.nbc, d.fmt, d.M, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (d.chunk == d.nch - 1) {
-        for (int m = 0; m < kGroup; ++m) red[(warp * kMaxSmallT + m) * 32 + lane] = acc[m];
-        consumer_sync();
-        if (d.kind == kGateUp) {
-          const bool sh = d.entry < P.n_sh;
-          if (tid < 16 * d.M) {
-            const int i = tid & 15, m = tid >> 4;
-            float g = 0.f, u = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              g += red[(w * kMaxSmallT + m) * 32 + i];
-              u += red[(w * kMaxSmallT + m) * 32 + 16 + i];
-            }
-            const float hv = g / (1.f + expf(-g)) * u;
-            P.h[(int64_t)(d.slot0 + m) * P.Imax + d.rb * 16 + i] = hv;
-          }
-          __threadfence();
-          consumer_sync();
-          if (tid == 0) {
-            const int old = atomicAdd(&P.gu_cnt[d.entry], 1);
-            flags[0] = (old == d.n_tiles_entry - 1);
-          }
-          consumer_sync();
-          if (flags[0]) {
-            __threadfence();
-            const int Ie = sh ? P.Ish : P.I;
-            const int nblk = Ie / 32;
-            for (int wi = warp; wi < d.M * nblk; wi += kConsumerWarps) {
-              const int m = wi / nblk, b = wi % nblk;
-              const float v = __ldcg(&P.h[(int64_t)(d.slot0 + m) * P.Imax + b * 32 + lane]);
-              write_record<L>(v, P.hrec + ((int64_t)(d.slot0 + m) * (P.Imax / 32) + b) * RB);
-            }
-            __threadfence();
-            fence_proxy_async_global();
-            consumer_sync();
-            if (tid == 0) st_release(&P.entry_ready[d.entry], 1);
-          }
-        } else {  // kDown
-          if (tid < 32 * d.M) {
-            const int r = tid & 31, m = tid >> 5;
-            float v = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * kMaxSmallT + m) * 32 + r];
-            P.z[(int64_t)(d.slot0 + m) * P.H + d.rb * 32 + r] = v;
-          }
-          __threadfence();
-          consumer_sync();
-          if (tid == 0) {
-            const int old = atomicAdd(&P.d_cnt[d.rb], 1);
-            flags[0] = (old == d.n_ent - 1);
-          }
-          consumer_sync();
-          if (flags[0]) {
-            __threadfence();
-            const int k = P.k;
-            if (tid < T * 32) {
-              const int t = tid >> 5, r = tid & 31;
-              const int hh = d.rb * 32 + r;
-              float v = 0.f;
-              for (int j = 0; j < k; ++j) {
-                const float g = __ldcg(&P.gates[t * k + j]);
-                const int sl = __ldcg(&P.pos[t * k + j]);
-                v = fmaf(g, __ldcg(&P.z[(int64_t)sl * P.H + hh]), v);
-              }
-              if (P.n_sh > 0) v += __ldcg(&P.z[(int64_t)(T * k + t) * P.H + hh]);
-              if constexpr (L == 2) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + hh] = __float2bfloat16_rn(v);
-              else reinterpret_cast<float*>(P.y)[(int64_t)t * P.H + hh] = v;
-            }
-          }
-        }
-        consumer_sync();
+        // a 32-row group is complete: sum the lanes and hand the group's
+        // results to the epilogue warp (the descriptor is copied before the
+        // stage is released, since the producer reuses it)
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+          for (int m = 0; m < kGroup; ++m)
+#pragma unroll
+            for (int o = 16; o; o >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], o);
+        if (!mbar_wait_bounded(&rempty[rs], rph ^ 1u, P.timeout_ns, P.status, kSiteRedEmpty, rs)) break;
+        float mine = 0.f;
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+          for (int m = 0; m < kGroup; ++m)
+            if (lane == r * kGroup + m) mine = acc[r][m];
+        float* slot = red + rs * (kRedSlotBytes / 4);
+        if (lane < kRowsPerWarp * kGroup) slot[warp * kRowsPerWarp * kGroup + lane] = mine;
+        if (tid == 0) metas[rs] = d;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rfull[rs]);
+        if (++rs == kRedSlots) { rs = 0; rph ^= 1u; }
       }
     }
     if (++s == P.n_stages) { s = 0; ph ^= 1u; }
   }
 }
 
+// ---------------------------------------------------------------------------
+// epilogue warp
+// ---------------------------------------------------------------------------
+template <int L>
+__device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + plan.rbars);
+  uint64_t* rempty = rfull + kRedSlots;
+  const Desc* metas = reinterpret_cast<const Desc*>(smem + plan.metas);
+  const float* red = reinterpret_cast<const float*>(smem + plan.red);
+  constexpr int RB = rec_bytes(L);
+  const int lane = threadIdx.x & 31;
+  const int T = P.T, k = P.k;
+  int rs = 0;
+  uint32_t rph = 0;
+  float keep[kGroup] = {0.f, 0.f, 0.f, 0.f};
+  while (true) {
+    if (!mbar_wait_bounded(&rfull[rs], rph, P.timeout_ns, P.status, kSiteRedFull, rs)) break;
+    const Desc d = metas[rs];
+    if (d.kind == kEnd) break;
+    const float4 vv = reinterpret_cast<const float4*>(red + rs * (kRedSlotBytes / 4))[lane];  // row = lane
+    const float v[kGroup] = {vv.x, vv.y, vv.z, vv.w};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rempty[rs]);
+    if (++rs == kRedSlots) { rs = 0; rph ^= 1u; }
+
+    if (d.kind == kGateUp) {
+      // lanes 0-15: gate rows, lanes 16-31: up rows of outputs 32*rbt + 16*group + (0..15)
+#pragma unroll
+      for (int m = 0; m < kGroup; ++m) {
+        const float u = __shfl_down_sync(0xffffffffu, v[m], 16);
+        const float hv = v[m] / (1.f + expf(-v[m])) * u;  // meaningful on lanes 0-15
+        if (d.group == 0) {
+          keep[m] = hv;
+        } else {
+          const float hi = __shfl_up_sync(0xffffffffu, hv, 16);
+          const float vec = lane < 16 ? keep[m] : hi;
+          if (m < d.M)
+            write_record<L>(vec, P.hrec + ((int64_t)(d.slot0 + m) * (P.Imax / 32) + d.rbt) * RB);
+        }
+      }
+      if (d.group == d.ngroups - 1) {
+        __threadfence();
+        fence_proxy_async_global();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = (atomicAdd(&P.gu_cnt[d.entry], 1) == d.n_tiles_entry - 1);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && lane == 0) {
+          __threadfence();
+          st_release(&P.entry_ready[d.entry], 1);
+        }
+      }
+    } else {  // kDown
+      const int row = d.rbt * 128 + d.group * 32 + lane;
+      for (int m = 0; m < d.M; ++m) P.z[(int64_t)(d.slot0 + m) * P.H + row] = v[m];
+      if (d.group == d.ngroups - 1) {
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int old = atomicAdd(&P.d_cnt[d.rbt], 1);
+          // a shared down tile may finish before the routing is published; the
+          // routed down tiles only run after it, so it cannot be last then
+          int n_ent = d.n_ent;
+          if (d.entry < P.n_sh)
+            n_ent = ld_acquire(&P.sync->routing_ready) ? P.n_sh + __ldcg(&P.sync->n_rent) : 0x7fffffff;
+          last = (old == n_ent - 1);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && lane == 0) {
+          // this CTA combines the block when it leaves (with all its threads)
+          int* pend = reinterpret_cast<int*>(smem + plan.pend);
+          pend[1 + pend[0]] = d.rbt;
+          pend[0] += 1;
+        }
+      }
+    }
+  }
+}
+
+// y rows of the 128-row blocks this CTA completed last, in slot order:
+// y[t] = sum_{j<k} g[t,j] z[pos[t,j]] + z_shared[t], all threads of the CTA.
+template <int L>
+__device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, const int* pend) {
+  float* sg = reinterpret_cast<float*>(smem + plan.escr);                       // [T*k] gates
+  int* sp = reinterpret_cast<int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);  // [T*k] slots
+  const int T = P.T, k = P.k;
+  __threadfence();
+  for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
+    sg[q] = __ldcg(&P.gates[q]);
+    sp[q] = __ldcg(&P.pos[q]);
+  }
+  __syncthreads();
+  const int n = pend[0];
+  for (int o = threadIdx.x; o < n * 128 * T; o += blockDim.x) {
+    const int b = o / (128 * T), rem = o % (128 * T), t = rem / 128;
+    const int r = pend[1 + b] * 128 + rem % 128;
+    float zv[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) zv[j] = __ldcg(&P.z[(int64_t)sp[t * k + j] * P.H + r]);
+    const float zs = P.n_sh > 0 ? __ldcg(&P.z[(int64_t)(T * k + t) * P.H + r]) : 0.f;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) acc = fmaf(sg[t * k + j], zv[j], acc);
+    acc += zs;
+    if constexpr (L == 2) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + r] = __float2bfloat16_rn(acc);
+    else reinterpret_cast<float*>(P.y)[(int64_t)t * P.H + r] = acc;
+  }
+}
+
 template <int L>
 __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_constant__ SmallParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemPlan plan = smem_plan(P.n_stages, P.stage_bytes, P.misc_bytes);
+  const SmemPlan plan = smem_plan(P.n_stages, P.ring_bytes, P.misc_bytes, P.w_max);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + P.n_stages;
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + plan.rbars);
+  uint64_t* rempty = rfull + kRedSlots;
   int* flags = reinterpret_cast<int*>(smem + plan.flags);
+  int* pend = reinterpret_cast<int*>(smem + plan.pend);
   if (threadIdx.x == 0) {
+    pend[0] = 0;
     for (int i = 0; i < P.n_stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kRedSlots; ++i) {
+      mbar_init(&rfull[i], kConsumerWarps);
+      mbar_init(&rempty[i], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
   const int warp = threadIdx.x >> 5;
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     if ((threadIdx.x & 31) == 0) producer_loop<L>(P, smem, plan);
+  } else if (warp == kEpilogueWarp) {
+    epilogue_loop<L>(P, smem, plan);
   } else {
     consumer_loop<L>(P, smem, plan);
   }
 
+  __syncthreads();
+  if (pend[0] > 0) combine_blocks<L>(P, smem, plan, pend);
   // the last CTA out resets the cross-CTA counters for the next launch
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -726,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.gu_cnt[i] = 0;
       P.entry_ready[i] = 0;
     }
-    for (int i = threadIdx.x; i < P.n_rbd; i += blockDim.x) P.d_cnt[i] = 0;
+    for (int i = threadIdx.x; i < P.n_dt; i += blockDim.x) P.d_cnt[i] = 0;
     if (threadIdx.x == 0) {
       P.sync->queue = 0;
       P.sync->router_done = 0;
@@ -743,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
 // host side
 // ---------------------------------------------------------------------------
 int small_t_smem_bytes(const SmallParams& P) {
-  return smem_plan(P.n_stages, P.stage_bytes, P.misc_bytes).total;
+  return smem_plan(P.n_stages, P.ring_bytes, P.misc_bytes, P.w_max).total;
 }
 
 cudaError_t small_t_configure(int L, int smem_bytes) {
