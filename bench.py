@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--experts", type=int, default=0,
+                   help="override the expert count (smaller resident layer for profiler captures)")
     return p.parse_args()
 
 
@@ -163,6 +165,9 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        w = dataclasses.replace(w, E=args.experts)
     layers = [synthetic_layer(w, pkg.ACT_BF16, T_max=w.T)[0] for _ in range(args.copies)]
     x = synth.activations(w, "cuda")
     y = torch.empty_like(x)
