@@ -21,7 +21,7 @@ EXPORTS = (
     "moe_layer_create", "moe_forward", "moe_get_routing", "moe_layer_status",
     "moe_layer_weight_bytes", "moe_layer_workspace_bytes", "moe_layer_destroy",
     "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
-    "mtp_verify_accept", "moe_last_error",
+    "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_last_error",
 )
 
 
@@ -68,6 +68,7 @@ def lib():
             "moe_quantize": (_c.c_int, [i32, vp, i64, i64, vp, vp]),
             "mtp_verify_accept_workspace_bytes": (sz, [i32, i32]),
             "mtp_verify_accept": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp, sz, vp]),
+            "mtp_verify_accept_noalloc": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp]),
             "moe_last_error": (_c.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -213,4 +214,19 @@ def verify_accept(draft_ids, logits, workspace=None, out=None, stream=None):
     _check(lib().mtp_verify_accept(draft_ids.data_ptr() if k else None, k, logits.data_ptr(), V,
                                    out.data_ptr(), out.data_ptr() + 4, workspace.data_ptr(),
                                    workspace.numel(), _stream(stream)))
+    return out
+
+
+def verify_accept_noalloc(draft_ids, logits, out=None, stream=None):
+    """Greedy acceptance through the entry point that uses the library's
+    static scratch (no workspace); returns the device int32 tensor
+    [n_accepted, next_token]."""
+    import torch
+    k = draft_ids.numel()
+    V = logits.shape[1]
+    assert logits.shape[0] == k + 1 and logits.dtype == torch.float32 and logits.is_contiguous()
+    if out is None:
+        out = torch.empty(2, dtype=torch.int32, device=logits.device)
+    _check(lib().mtp_verify_accept_noalloc(draft_ids.data_ptr() if k else None, k, logits.data_ptr(), V,
+                                           out.data_ptr(), out.data_ptr() + 4, _stream(stream)))
     return out

@@ -9,6 +9,8 @@
 // (max, argmax) to the caller's workspace, and the last CTA to finish (a
 // counter in the workspace) reduces the partials in split order, counts the
 // matching prefix and writes the two outputs.  The counter is left at zero.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -101,6 +103,42 @@ cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int 
   ArgPart* parts = reinterpret_cast<ArgPart*>(static_cast<uint8_t*>(ws) + 16);
   accept_kernel<<<(k + 1) * S, kAcceptThreads, 0, st>>>(draft, k, logits, V, S, out_n, out_next, counter, parts);
   return cudaGetLastError();
+}
+
+// Scratch of the allocation-free entry point (mtp_verify_accept_noalloc).
+// A C runtime that drives the draft/verify loop itself may hold no device
+// allocator at all (no torch, no pool), and cudaMalloc / cudaFree would
+// synchronise the device between two verify rounds, so that caller gets a
+// fixed scratch that lives in the library's own module instead.  Every call
+// on a device uses this one array: the counter at its start must be zero
+// when a call begins (it is zero at module load and every completed call
+// leaves it at zero); the partials behind it are written before they are
+// read.  Two calls whose kernels overlap on the GPU race on it.
+constexpr size_t kAcceptStaticBytes = 4096;
+static __device__ __align__(256) uint8_t g_accept_scratch[kAcceptStaticBytes];
+
+size_t accept_static_bytes() { return kAcceptStaticBytes; }
+
+// Device address of g_accept_scratch on the current device, looked up once
+// per device (the lookup loads the module on that device, so the first call
+// on a device belongs before any stream capture on it).
+cudaError_t accept_static_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t rc = cudaGetDevice(&dev);
+  if (rc != cudaSuccess) return rc;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    rc = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (rc != cudaSuccess) return rc;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -16,6 +16,8 @@ cudaError_t quantize_launch(int fmt, const float* w, int64_t rows, int64_t cols,
 size_t accept_workspace_bytes(int k, int V);
 cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int V, int32_t* out_n, int32_t* out_next,
                           void* ws, cudaStream_t st);
+size_t accept_static_bytes();
+cudaError_t accept_static_scratch(void** out);
 int small_t_smem_bytes(const SmallParams& P);
 cudaError_t small_t_configure(int L, int smem_bytes);
 cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st);
@@ -443,6 +445,26 @@ int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, 
   CK(accept_launch(draft_ids, k, logits, V, out_n_accepted, out_next_token, workspace,
                    static_cast<cudaStream_t>(stream)),
      "mtp_verify_accept launch");
+  return MOE_OK;
+}
+
+int mtp_verify_accept_noalloc(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V,
+                              int32_t* out_n_accepted, int32_t* out_next_token, void* stream) {
+  if (k < 0 || k > 15) return fail(MOE_EINVAL, "mtp_verify_accept_noalloc: k=%d outside 0..15", k);
+  if (V < 1 || V > (1 << 24)) return fail(MOE_EINVAL, "mtp_verify_accept_noalloc: V=%d outside 1..2^24", V);
+  if ((k > 0 && !draft_ids) || !logits || !out_n_accepted || !out_next_token)
+    return fail(MOE_EINVAL, "mtp_verify_accept_noalloc: NULL pointer");
+  const size_t need = accept_workspace_bytes(k, V);
+  if (need > accept_static_bytes())
+    return fail(MOE_EINVAL,
+                "mtp_verify_accept_noalloc: k=%d, V=%d needs %zu bytes of scratch but the static scratch holds "
+                "%zu; use mtp_verify_accept with a caller workspace",
+                k, V, need, accept_static_bytes());
+  void* scratch = nullptr;
+  CK(accept_static_scratch(&scratch), "mtp_verify_accept_noalloc: static scratch lookup");
+  CK(accept_launch(draft_ids, k, logits, V, out_n_accepted, out_next_token, scratch,
+                   static_cast<cudaStream_t>(stream)),
+     "mtp_verify_accept_noalloc launch");
   return MOE_OK;
 }
 

@@ -161,6 +161,25 @@ int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, 
                       int32_t* out_n_accepted, int32_t* out_next_token, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* The same greedy verification as mtp_verify_accept, for callers that cannot
+ * allocate device memory: a C runtime driving the draft/verify loop without a
+ * device allocator of its own, for which cudaMalloc / cudaFree would also
+ * synchronise the device between verify rounds.  The source pages have no
+ * counterpart to this call; it only changes where the scratch lives.
+ *   Arguments, outputs and results are those of mtp_verify_accept; the
+ *   scratch is a 4096-byte array inside the library (one per device), so
+ *   the call accepts only 16 + 8 * (k+1) * ceil(V / 16384) <= 4096 (every
+ *   V <= 507904 for every k <= 15) and returns MOE_EINVAL, with a message
+ *   naming the sizes, beyond that.  It allocates nothing and calls no
+ *   allocating library.  The first call on a device looks the array's
+ *   address up (this loads the library's module on that device), so make
+ *   it before any stream capture on that device.  All calls on a device
+ *   share the array: calls whose kernels overlap on the GPU (different
+ *   streams, other host threads) race and must be ordered by the caller,
+ *   e.g. by issuing them on one stream. */
+int mtp_verify_accept_noalloc(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V,
+                              int32_t* out_n_accepted, int32_t* out_next_token, void* stream);
+
 /* Message for the last error on the calling thread; valid until the next
  * call on that thread.  Never NULL. */
 const char* moe_last_error(void);
