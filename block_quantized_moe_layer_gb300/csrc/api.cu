@@ -21,10 +21,18 @@ cudaError_t accept_static_scratch(void** out);
 int small_t_smem_bytes(const SmallParams& P);
 cudaError_t small_t_configure(int L, int smem_bytes);
 cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st);
-int large_t_setup(moe_layer* L, cudaStream_t st);
-int large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st);
+bool large_t_enabled(const moe_layer* L);
+cudaError_t large_t_alloc(moe_layer* L);
+cudaError_t large_t_repack(moe_layer* L, int which, int e, const uint8_t* src, cudaStream_t st);
+cudaError_t large_t_repack_router(moe_layer* L, const float* src, cudaStream_t st);
+size_t large_t_weight_bytes(const moe_layer* L);
+size_t large_t_workspace_bytes(const moe_layer* L);
+int* large_t_status_word(const moe_layer* L);
+int* large_t_counters(const moe_layer* L);
+cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st);
+cudaError_t large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm,
+                                cudaStream_t st);
 void large_t_release(moe_layer* L);
-int large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, cudaStream_t st);
 }  // namespace moe
 
 using namespace moe;
@@ -163,6 +171,15 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if (d->act_dtype != MOE_ACT_BF16 && d->act_dtype != MOE_ACT_F32)
     return fail(MOE_EINVAL, "act_dtype=%d", d->act_dtype);
   if (!d->gate || !d->up || !d->down) return fail(MOE_EINVAL, "gate/up/down descriptor arrays are NULL");
+  if (d->T_max > kMaxSmallT) {
+    // the tensor-core path: 128-row weight tiles, 64-column K-blocks, bf16 operands
+    if (d->act_dtype != MOE_ACT_BF16)
+      return fail(MOE_EINVAL, "T_max=%d: batches above %d tokens run in bf16 only (act_dtype must be MOE_ACT_BF16)",
+                  d->T_max, kMaxSmallT);
+    if (d->I % 64 || d->I_shared % 64)
+      return fail(MOE_EINVAL, "T_max=%d: I=%d and I_shared=%d must be multiples of 64 for batches above %d tokens",
+                  d->T_max, d->I, d->I_shared, kMaxSmallT);
+  }
   int rc;
   if ((rc = check_tensor(d->router_w, d->E, d->H, false, "router_w"))) return rc;
   const bool has_bias = d->router_b.data != nullptr;
@@ -249,6 +266,11 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   }
   L->weight_bytes = router_bytes + (has_bias ? d->E * 4 : 0) + (size_t)(L->gu_stride + L->dn_stride) * d->E +
                     sgu_b + sdn_b;
+  if (large_t_enabled(L)) {
+    CK(large_t_alloc(L), "allocate the prefill-sized path");
+    L->weight_bytes += large_t_weight_bytes(L);
+  }
+  const bool lt = L->lt != nullptr;
 
   // upload + repack
   Stager stg;
@@ -256,6 +278,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if ((rc = stg.get(d->router_w.data, d->router_w.nbytes, st, &src))) return rc;
   CK(repack_router(reinterpret_cast<const float*>(src), reinterpret_cast<float*>(L->router), d->E, E_pad, d->H, st),
      "repack router");
+  if (lt) CK(large_t_repack_router(L, reinterpret_cast<const float*>(src), st), "repack router (tensor-core path)");
   if (has_bias) {
     const cudaMemcpyKind kind = is_device_ptr(d->router_b.data) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
     CK(cudaMemcpyAsync(L->router_b, d->router_b.data, (size_t)d->E * 4, kind, st), "copy bias");
@@ -265,18 +288,24 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
     uint8_t* dn = L->dn + (int64_t)e * L->dn_stride;
     if ((rc = stg.get(d->gate[e].data, d->gate[e].nbytes, st, &src))) return rc;
     CK(repack_matrix(fmt, src, gu, d->I, d->H, 16, 0, L->gu_ch, st), "repack gate");
+    if (lt) CK(large_t_repack(L, 0, e, src, st), "repack gate (tensor-core path)");
     if ((rc = stg.get(d->up[e].data, d->up[e].nbytes, st, &src))) return rc;
     CK(repack_matrix(fmt, src, gu, d->I, d->H, 16, 16, L->gu_ch, st), "repack up");
+    if (lt) CK(large_t_repack(L, 1, e, src, st), "repack up (tensor-core path)");
     if ((rc = stg.get(d->down[e].data, d->down[e].nbytes, st, &src))) return rc;
     CK(repack_matrix(fmt, src, dn, d->H, d->I, 32, 0, L->dn_ch, st), "repack down");
+    if (lt) CK(large_t_repack(L, 2, e, src, st), "repack down (tensor-core path)");
   }
   if (has_sh) {
     if ((rc = stg.get(d->sh_gate.data, d->sh_gate.nbytes, st, &src))) return rc;
     CK(repack_matrix(sfmt, src, L->sgu, d->I_shared, d->H, 16, 0, L->sgu_ch, st), "repack shared gate");
+    if (lt) CK(large_t_repack(L, 3, 0, src, st), "repack shared gate (tensor-core path)");
     if ((rc = stg.get(d->sh_up.data, d->sh_up.nbytes, st, &src))) return rc;
     CK(repack_matrix(sfmt, src, L->sgu, d->I_shared, d->H, 16, 16, L->sgu_ch, st), "repack shared up");
+    if (lt) CK(large_t_repack(L, 4, 0, src, st), "repack shared up (tensor-core path)");
     if ((rc = stg.get(d->sh_down.data, d->sh_down.nbytes, st, &src))) return rc;
     CK(repack_matrix(sfmt, src, L->sdn, d->H, d->I_shared, 32, 0, L->sdn_ch, st), "repack shared down");
+    if (lt) CK(large_t_repack(L, 5, 0, src, st), "repack shared down (tensor-core path)");
   }
 
   // small-T workspace
@@ -357,7 +386,6 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   L->smem_bytes = small_t_smem_bytes(sp);
   CK(small_t_configure(L_limbs, L->smem_bytes), "configure small-T kernel");
 
-  if ((rc = large_t_setup(L, st))) return rc;
   CK(cudaStreamSynchronize(st), "create sync");
   guard.keep = true;
   *out = L;
@@ -378,7 +406,10 @@ int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
   if (xb < yb + nb && yb < xb + nb) return fail(MOE_EINVAL, "moe_forward: x and y overlap");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   L->last_T = T;
-  if (T > kMaxSmallT) return large_t_forward(L, x, T, y, st);
+  if (T > kMaxSmallT) {
+    CK(large_t_forward(L, x, T, y, st), "moe_forward (tensor-core path)");
+    return MOE_OK;
+  }
   SmallParams P = L->sp;
   P.T = T;
   P.Tp = (T + 3) & ~3;
@@ -393,7 +424,8 @@ int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, 
   if (!L) return fail(MOE_EINVAL, "moe_get_routing: NULL layer");
   if (L->last_T <= 0) return fail(MOE_EINVAL, "moe_get_routing: no forward yet");
   if (L->last_T > kMaxSmallT) {
-    return large_t_get_routing(L, ids, gates, offsets, perm, static_cast<cudaStream_t>(stream));
+    CK(large_t_get_routing(L, ids, gates, offsets, perm, static_cast<cudaStream_t>(stream)), "moe_get_routing");
+    return MOE_OK;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t Tk = (size_t)L->last_T * L->k;
@@ -411,18 +443,33 @@ int moe_layer_status(moe_layer* L, void* stream) {
   CK(cudaStreamSynchronize(st), "status sync");
   int word[4] = {0, 0, 0, 0};
   CK(cudaMemcpy(word, L->sp.status, 16, cudaMemcpyDeviceToHost), "status read");
-  if (word[0] == 0) return MOE_OK;
-  // clear the word and every cross-CTA counter so the next call starts clean
-  const size_t counters = reinterpret_cast<uint8_t*>(L->sp.status) - static_cast<uint8_t*>(L->ws);
-  CK(cudaMemset(L->ws, 0, counters + 16), "status reset");
-  static const char* sites[] = {"?", "routing flag", "x records", "entry ready", "free stage", "full stage",
-                                 "end marker", "copy drain"};
-  const int site = (word[1] >= 0 && word[1] <= 7) ? word[1] : 0;
-  return fail(MOE_ETIMEOUT, "a device-side wait timed out: %s (detail %d, block %d)", sites[site], word[2], word[3]);
+  if (word[0] != 0) {
+    // clear the word and every cross-CTA counter so the next call starts clean
+    const size_t counters = reinterpret_cast<uint8_t*>(L->sp.status) - static_cast<uint8_t*>(L->ws);
+    CK(cudaMemset(L->ws, 0, counters + 16), "status reset");
+    static const char* sites[] = {"?", "routing flag", "x records", "entry ready", "free stage", "full stage",
+                                   "end marker", "copy drain"};
+    const int site = (word[1] >= 0 && word[1] <= 7) ? word[1] : 0;
+    return fail(MOE_ETIMEOUT, "a device-side wait timed out: %s (detail %d, block %d)", sites[site], word[2],
+                word[3]);
+  }
+  if (int* lw = large_t_status_word(L)) {
+    CK(cudaMemcpy(word, lw, 16, cudaMemcpyDeviceToHost), "status read");
+    if (word[0] != 0) {
+      CK(cudaMemset(lw, 0, 16), "status reset");
+      CK(cudaMemset(large_t_counters(L), 0, 16 * 4), "counter reset");
+      static const char* sites[] = {"?", "free stage", "full stage", "dequantised stage", "accumulator",
+                                     "work item", "copy drain"};
+      const int site = (word[1] >= 0 && word[1] <= 6) ? word[1] : 0;
+      return fail(MOE_ETIMEOUT, "a device-side wait of the tensor-core path timed out: %s (detail %d, block %d)",
+                  sites[site], word[2], word[3]);
+    }
+  }
+  return MOE_OK;
 }
 
 size_t moe_layer_weight_bytes(const moe_layer* L) { return L ? L->weight_bytes : 0; }
-size_t moe_layer_workspace_bytes(const moe_layer* L) { return L ? L->ws_bytes + L->lws_bytes : 0; }
+size_t moe_layer_workspace_bytes(const moe_layer* L) { return L ? L->ws_bytes + large_t_workspace_bytes(L) : 0; }
 
 void moe_layer_destroy(moe_layer* L) { free_layer(L); }
 

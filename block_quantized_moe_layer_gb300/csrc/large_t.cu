@@ -1,24 +1,653 @@
 // large_t.cu -- the layer for prefill-sized batches (T > 8).
-#include "layer.cuh"
+//
+// The steps of the layer (router, top-k and gates, permutation, SwiGLU
+// experts, combine; see the layer definition in moe_layer.h) run as a
+// sequence of launches on the caller's stream:
+//   1. lt_prep    : x -> token tiles of the shared expert / router (bf16 MMA
+//                   operand image), the work lists that need no routing;
+//   2. GEMM       : router logits (three bf16 planes of the fp32 router, so
+//                   the logits keep fp32 accuracy) + shared-expert gate/up;
+//   3. lt_topk    : per token top-k (descending, ties to the lower index) and
+//                   renormalised gates;
+//   4. lt_perm    : histogram, scan, stable scatter -> offsets, perm, pos,
+//                   routed token tiles and the remaining work lists;
+//   5. lt_gather  : routed token tiles' activations (operand image);
+//   6. GEMM       : routed gate/up + SwiGLU;
+//   7. GEMM       : routed and shared down projections -> z (bf16);
+//   8. lt_combine : y[t] = sum_j g[t,j] z[pos[t,j]] + z[shared t], in slot order.
+// No step depends on atomics for its result; every result is deterministic.
+#include <algorithm>
+
+#include "large_t.cuh"
 
 namespace moe {
 
-int large_t_setup(moe_layer* L, cudaStream_t st) {
-  (void)L;
-  (void)st;
-  return MOE_OK;
+struct LtState {
+  // weights in the LT layout
+  uint8_t* gu = nullptr;
+  uint8_t* dn = nullptr;
+  uint8_t* sgu = nullptr;
+  uint8_t* sdn = nullptr;
+  uint8_t* router = nullptr;
+  int64_t gu_stride = 0, dn_stride = 0, router_plane = 0;
+  size_t weight_bytes = 0;
+  int E_pad128 = 0, Imax = 0, max_tiles = 0, max_rows = 0;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* counters = nullptr;  // [0..2] queues, [3..5] exit counters, [6..8] item counts, [9] routed tiles
+  int* status = nullptr;    // [4]
+  float* logits = nullptr;  // [planes][T_max][E_pad128]
+  int* ids = nullptr;
+  float* gates = nullptr;
+  int* pos = nullptr;
+  int* perm = nullptr;
+  int* offsets = nullptr;
+  LtTile* tiles = nullptr;
+  LtItem* items1 = nullptr;
+  LtItem* items2 = nullptr;
+  LtItem* items3 = nullptr;
+  uint8_t* xg = nullptr;
+  uint8_t* h = nullptr;
+  __nv_bfloat16* z = nullptr;
+  int max_items1 = 0, max_items2 = 0, max_items3 = 0;
+  int perm_smem = 0;
+};
+
+namespace {
+
+constexpr int kPermThreads = 1024;
+
+__host__ __device__ inline int round16(int v) { return (v + 15) & ~15; }
+
+// ---------------------------------------------------------------------------
+// Weight repacking into the LT layout (create time)
+// ---------------------------------------------------------------------------
+
+// Source row `o` of a [rows, K] matrix -> (row tile, tile row).
+//   mode 0: down (128 rows per tile); mode 1: gate; mode 2: up.
+__device__ __forceinline__ void lt_row(int mode, int o, int& rt, int& r) {
+  if (mode == 0) {
+    rt = o / 128;
+    r = o % 128;
+  } else {
+    rt = o / 64;
+    const int rem = o % 64;
+    r = 32 * (rem / 16) + rem % 16 + (mode == 2 ? 16 : 0);
+  }
 }
 
-int large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st) {
-  (void)L; (void)x; (void)T; (void)y; (void)st;
-  return MOE_EINVAL;
+__global__ void lt_repack_q8_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int rows, int K,
+                                    int mode) {
+  const int nb = K / 32;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)rows * nb) return;
+  const int o = (int)(i / nb), b = (int)(i % nb);
+  int rt, r;
+  lt_row(mode, o, rt, r);
+  const int kb = b / 2, h = b % 2;
+  uint8_t* chunk = dst + rt * lt_tile_bytes(MOE_Q8_0, K) + (int64_t)kb * kLtQ8Chunk;
+  const uint8_t* s = src + i * 34;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    uint8_t* q = chunk + ((h * 2 + p) * 128 + r) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = s[2 + 16 * p + j];
+  }
+  chunk[8192 + (h * 128 + r) * 2] = s[0];
+  chunk[8192 + (h * 128 + r) * 2 + 1] = s[1];
 }
 
-int large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, cudaStream_t st) {
-  (void)L; (void)ids; (void)gates; (void)offsets; (void)perm; (void)st;
-  return MOE_EINVAL;
+__global__ void lt_repack_q4ks_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int rows, int K,
+                                      int mode) {
+  const int ns = K / 256;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)rows * ns) return;
+  const int o = (int)(i / ns), sb = (int)(i % ns);
+  int rt, r;
+  lt_row(mode, o, rt, r);
+  uint8_t* sup = dst + rt * lt_tile_bytes(MOE_Q4KS, K) + (int64_t)sb * kLtQ4Super;
+  const uint8_t* s = src + i * 144;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sup[r * 16 + j] = s[j];
+  for (int sub = 0; sub < 8; ++sub) {
+    uint8_t* c = sup + kLtQ4Hdr + (sub / 2) * kLtQ4Codes + ((sub % 2) * 128 + r) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c[j] = s[16 + 16 * sub + j];
+  }
 }
 
-void large_t_release(moe_layer* L) { (void)L; }
+// fp32 router [E, H] -> three bf16 planes (W1 = bf16(W), W2 = bf16(W - W1),
+// W3 = bf16(W - W1 - W2)), rows zero-padded to E_pad128, LT BF16 layout.
+__global__ void lt_repack_router_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int E, int E_pad,
+                                        int H, int64_t plane_bytes) {
+  const int n8 = H / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)E_pad * n8) return;
+  const int row = (int)(i / n8), g = (int)(i % n8);
+  const int k0 = g * 8, kb = k0 / 64, h = (k0 % 64) / 32, pc = (k0 % 32) / 8;
+  const int rt = row / 128, r = row % 128;
+  const int64_t off = rt * lt_tile_bytes(MOE_BF16, H) + (int64_t)kb * kLtBf16Chunk + ((h * 4 + pc) * 128 + r) * 16;
+  uint32_t w[3][4];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    float v0 = row < E ? src[(int64_t)row * H + k0 + j] : 0.f;
+    float v1 = row < E ? src[(int64_t)row * H + k0 + j + 1] : 0.f;
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl) {
+      const __nv_bfloat16 b0 = __float2bfloat16_rn(v0), b1 = __float2bfloat16_rn(v1);
+      w[pl][j / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+      v0 -= __bfloat162float(b0);
+      v1 -= __bfloat162float(b1);
+    }
+  }
+#pragma unroll
+  for (int pl = 0; pl < 3; ++pl)
+    *reinterpret_cast<uint4*>(dst + pl * plane_bytes + off) = make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
+}
+
+// ---------------------------------------------------------------------------
+// Forward kernels
+// ---------------------------------------------------------------------------
+
+struct PrepParams {
+  const __nv_bfloat16* x;
+  int T, H, k, Ish, E_pad128, n_sh;
+  LtTile* tiles;
+  LtItem* items1;
+  LtItem* items3;
+  int* counters;
+  uint8_t* xg;
+};
+
+// Block b tiles x rows [128 b, 128 b + 128) into the operand image; block 0
+// also writes the plain token tiles and the work lists that need no routing.
+__global__ void lt_prep_kernel(const PrepParams P) {
+  const int tt = blockIdx.x;
+  const int n = min(128, P.T - 128 * tt), n_pad = round16(n);
+  if (tt == 0) {
+    const int n_rt_r = P.E_pad128 / 128, n_gu_sh = P.Ish / 64, n_dn = P.H / 128;
+    const int n_rt_items = kLtPlanes * n_rt_r * P.n_sh;
+    for (int i = threadIdx.x; i < P.n_sh; i += blockDim.x) {
+      const int ni = min(128, P.T - 128 * i);
+      P.tiles[i] = LtTile{-1, P.T * P.k + 128 * i, ni, round16(ni), 128 * i, {0, 0, 0}};
+    }
+    // router items first (they gate the routing), then shared gate/up
+    for (int i = threadIdx.x; i < n_rt_items; i += blockDim.x) {
+      const int pl = i / (n_rt_r * P.n_sh), rem = i % (n_rt_r * P.n_sh);
+      P.items1[i] = LtItem{kItemRT, rem % n_rt_r, rem / n_rt_r, pl};
+    }
+    for (int i = threadIdx.x; i < n_gu_sh * P.n_sh; i += blockDim.x)
+      P.items1[n_rt_items + i] = LtItem{kItemGU, i % n_gu_sh, i / n_gu_sh, 0};
+    if (P.Ish > 0)
+      for (int i = threadIdx.x; i < n_dn * P.n_sh; i += blockDim.x)
+        P.items3[i] = LtItem{kItemDN, i % n_dn, i / n_dn, 0};
+    if (threadIdx.x == 0) P.counters[6] = n_rt_items + n_gu_sh * P.n_sh;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)128 * tt * P.H * 2);
+  const int nc = P.H / 8;
+  for (int idx = threadIdx.x; idx < n_pad * nc; idx += blockDim.x) {
+    const int r = idx % n_pad, c = idx / n_pad;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < n) v = *reinterpret_cast<const uint4*>(P.x + (int64_t)(128 * tt + r) * P.H + 8 * c);
+    dst[(int64_t)c * n_pad + r] = v;
+  }
+}
+
+__device__ __forceinline__ bool topk_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// One warp per token.  NPER = experts per lane (lane l holds e = l + 32 i).
+template <int NPER>
+__global__ void lt_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
+                               int E_pad, int k, int* __restrict__ ids, float* __restrict__ gates) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int64_t plane = (int64_t)T * E_pad;
+  const float* l0 = logits + (int64_t)t * E_pad;
+  float v[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    float x = -INFINITY;
+    if (e < E) {
+      x = ((l0[e] + l0[plane + e]) + l0[2 * plane + e]) + (bias ? bias[e] : 0.f);
+      if (x != x) x = -INFINITY;
+    }
+    v[i] = x;
+  }
+  uint32_t taken = 0;
+  float sel[kMaxTopK];
+  int seli[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && topk_better(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (topk_better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      sel[j] = bv;
+      seli[j] = bi;
+    }
+  }
+  if (lane == 0) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) s += expf(sel[j] - sel[0]);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        ids[t * k + j] = seli[j];
+        gates[t * k + j] = expf(sel[j] - sel[0]) / s;
+      }
+  }
+}
+
+// Exclusive scan of one int per thread over the block (blockDim.x == 1024).
+__device__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int r = x - v + warp_tot[warp];
+  *total = warp_tot[32];
+  __syncthreads();
+  return r;
+}
+
+struct PermParams {
+  const int* ids;
+  int T, E, k, H, I, Ish, n_sh, prow_sh;
+  int* offsets;
+  int* perm;
+  int* pos;
+  LtTile* tiles;
+  LtItem* items2;
+  LtItem* items3;
+  int* counters;
+};
+
+// Single CTA of 1024 threads.  Pair p = t*k + j goes to slot
+// offsets[e] + (number of pairs p' < p with the same expert e).
+__global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermParams P) {
+  extern __shared__ int psm[];
+  const int E = P.E, Tk = P.T * P.k;
+  int* cnt = psm;               // [E]
+  int* off = cnt + E;           // [E]
+  int* run = off + E;           // [E]
+  int* wc = run + E;            // [32][E]
+  __shared__ int wtot[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kPermThreads) {
+    cnt[e] = 0;
+    run[e] = 0;
+  }
+  __syncthreads();
+  for (int p = tid; p < Tk; p += kPermThreads) atomicAdd(&cnt[P.ids[p]], 1);
+  __syncthreads();
+  int total;
+  {
+    const int c = tid < E ? cnt[tid] : 0;
+    const int ex = block_excl_scan(c, wtot, &total);
+    if (tid < E) {
+      off[tid] = ex;
+      P.offsets[tid] = ex;
+    }
+    if (tid == 0) P.offsets[E] = total;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < Tk; c0 += kPermThreads) {
+    for (int i = tid; i < 32 * E; i += kPermThreads) wc[i] = 0;
+    __syncthreads();
+    const int p = c0 + tid;
+    const bool valid = p < Tk;
+    const int e = valid ? P.ids[p] : -1;
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(mask & ((1u << lane) - 1u));
+    if (valid && lrank == 0) wc[warp * E + e] = __popc(mask);
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermThreads) {
+      int s = run[x];
+      for (int w = 0; w < 32; ++w) {
+        const int t = wc[w * E + x];
+        wc[w * E + x] = s;
+        s += t;
+      }
+      run[x] = s;
+    }
+    __syncthreads();
+    if (valid) {
+      const int dest = off[e] + wc[warp * E + e] + lrank;
+      P.perm[dest] = p;
+      P.pos[p] = dest;
+    }
+    __syncthreads();
+  }
+  // routed token tiles and the work lists of the gate/up and down launches
+  // (E <= 1024: thread e handles expert e)
+  const int n_gu = P.I / 64, n_dn = P.H / 128, sh_dn = P.Ish > 0 ? P.n_sh * n_dn : 0;
+  const int e = tid;
+  const int M = e < E ? cnt[e] : 0;
+  const int ntt = (M + 127) / 128;
+  const int rows = M > 0 ? 128 * (ntt - 1) + round16(M - 128 * (ntt - 1)) : 0;
+  int n_tiles, n_rows;
+  const int tb = block_excl_scan(ntt, wtot, &n_tiles);
+  const int pb = block_excl_scan(rows, wtot, &n_rows);
+  for (int i = 0; i < ntt; ++i) {
+    const int ti = P.n_sh + tb + i;
+    const int ni = min(128, M - 128 * i);
+    P.tiles[ti] = LtTile{e, off[e] + 128 * i, ni, round16(ni), P.prow_sh + pb + 128 * i, {0, 0, 0}};
+    for (int rt = 0; rt < n_gu; ++rt) P.items2[(tb + i) * n_gu + rt] = LtItem{kItemGU, rt, ti, 0};
+    for (int rt = 0; rt < n_dn; ++rt) P.items3[sh_dn + (tb + i) * n_dn + rt] = LtItem{kItemDN, rt, ti, 0};
+  }
+  if (tid == 0) {
+    P.counters[7] = n_tiles * n_gu;
+    P.counters[8] = sh_dn + n_tiles * n_dn;
+    P.counters[9] = n_tiles;
+  }
+}
+
+// Block b gathers routed tile n_sh + b (if it exists) into the operand image.
+__global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm,
+                                 const LtTile* __restrict__ tiles, const int* __restrict__ counters, int n_sh, int k,
+                                 int H, uint8_t* __restrict__ xg) {
+  if ((int)blockIdx.x >= counters[9]) return;
+  const LtTile tl = tiles[n_sh + blockIdx.x];
+  uint4* dst = reinterpret_cast<uint4*>(xg + (int64_t)tl.prow0 * H * 2);
+  const int nc = H / 8;
+  for (int idx = threadIdx.x; idx < tl.n_pad * nc; idx += blockDim.x) {
+    const int r = idx % tl.n_pad, c = idx / tl.n_pad;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < tl.n) {
+      const int tok = perm[tl.slot0 + r] / k;
+      v = *reinterpret_cast<const uint4*>(x + (int64_t)tok * H + 8 * c);
+    }
+    dst[(int64_t)c * tl.n_pad + r] = v;
+  }
+}
+
+// y[t] = sum_j g[t,j] z[pos[t,j]] + z[T k + t]; one block per token, 8 columns per thread step.
+__global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const float* __restrict__ gates,
+                                  const int* __restrict__ pos, int T, int k, int H, bool shared,
+                                  __nv_bfloat16* __restrict__ y) {
+  const int t = blockIdx.x;
+  __shared__ float g[kMaxTopK];
+  __shared__ int ps[kMaxTopK];
+  if (threadIdx.x < k) {
+    g[threadIdx.x] = gates[t * k + threadIdx.x];
+    ps[threadIdx.x] = pos[t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)ps[j] * H + 8 * c);
+      const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] += g[j] * __bfloat162float(b[m]);
+    }
+    if (shared) {
+      const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)(T * k + t) * H + 8 * c);
+      const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] += __bfloat162float(b[m]);
+    }
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * m], acc[2 * m + 1]);
+      ow[m] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(y + (int64_t)t * H + 8 * c) = o;
+  }
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+#define LT_CK(call)                       \
+  do {                                    \
+    cudaError_t e_ = (call);              \
+    if (e_ != cudaSuccess) return e_;     \
+  } while (0)
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+bool large_t_enabled(const moe_layer* L) { return L->T_max > kMaxSmallT; }
+
+// Allocates the LT weight copies and the workspace.  Shapes were validated by
+// the caller (H % 128 == 0, I and I_shared multiples of 64).
+cudaError_t large_t_alloc(moe_layer* L) {
+  LtState* S = new LtState();
+  L->lt = S;
+  const int H = L->H, E = L->E, I = L->I, Ish = L->Ish, k = L->k, Tm = L->T_max;
+  S->E_pad128 = (E + 127) / 128 * 128;
+  S->Imax = std::max(I, Ish);
+  S->gu_stride = (int64_t)(I / 64) * lt_tile_bytes(L->fmt, H);
+  S->dn_stride = (int64_t)(H / 128) * lt_tile_bytes(L->fmt, I);
+  S->router_plane = (int64_t)(S->E_pad128 / 128) * lt_tile_bytes(MOE_BF16, H);
+  LT_CK(cudaMalloc(&S->gu, (size_t)S->gu_stride * E));
+  LT_CK(cudaMalloc(&S->dn, (size_t)S->dn_stride * E));
+  LT_CK(cudaMalloc(&S->router, (size_t)S->router_plane * kLtPlanes));
+  size_t wb = (size_t)(S->gu_stride + S->dn_stride) * E + (size_t)S->router_plane * kLtPlanes;
+  if (Ish > 0) {
+    const size_t a = (size_t)(Ish / 64) * lt_tile_bytes(L->sfmt, H), b = (size_t)(H / 128) * lt_tile_bytes(L->sfmt, Ish);
+    LT_CK(cudaMalloc(&S->sgu, a));
+    LT_CK(cudaMalloc(&S->sdn, b));
+    wb += a + b;
+  }
+  S->weight_bytes = wb;
+
+  const int n_sh_max = (Tm + 127) / 128;
+  const int Tk = Tm * k;
+  S->max_tiles = n_sh_max + std::min(E, Tk) + Tk / 128 + 1;
+  S->max_rows = Tm + Tk + 16 * S->max_tiles;
+  S->max_items1 = (kLtPlanes * (S->E_pad128 / 128) + Ish / 64) * n_sh_max;
+  S->max_items2 = S->max_tiles * (I / 64);
+  S->max_items3 = S->max_tiles * (H / 128);
+  size_t off = 0;
+  auto take = [&](size_t b) {
+    const size_t o = off;
+    off = align256(off + b);
+    return o;
+  };
+  const size_t o_cnt = take(16 * 4);
+  const size_t o_status = take(16);
+  const size_t o_logits = take((size_t)kLtPlanes * Tm * S->E_pad128 * 4);
+  const size_t o_ids = take((size_t)Tk * 4);
+  const size_t o_gates = take((size_t)Tk * 4);
+  const size_t o_pos = take((size_t)Tk * 4);
+  const size_t o_perm = take((size_t)Tk * 4);
+  const size_t o_offs = take((size_t)(E + 1) * 4);
+  const size_t o_tiles = take((size_t)S->max_tiles * sizeof(LtTile));
+  const size_t o_i1 = take((size_t)S->max_items1 * sizeof(LtItem));
+  const size_t o_i2 = take((size_t)S->max_items2 * sizeof(LtItem));
+  const size_t o_i3 = take((size_t)S->max_items3 * sizeof(LtItem));
+  const size_t o_xg = take((size_t)S->max_rows * H * 2);
+  const size_t o_h = take((size_t)S->max_rows * S->Imax * 2);
+  const size_t o_z = take((size_t)(Tk + Tm) * H * 2);
+  S->ws_bytes = off;
+  LT_CK(cudaMalloc(&S->ws, S->ws_bytes));
+  LT_CK(cudaMemset(S->ws, 0, o_status + 16));
+  uint8_t* w = static_cast<uint8_t*>(S->ws);
+  S->counters = reinterpret_cast<int*>(w + o_cnt);
+  S->status = reinterpret_cast<int*>(w + o_status);
+  S->logits = reinterpret_cast<float*>(w + o_logits);
+  S->ids = reinterpret_cast<int*>(w + o_ids);
+  S->gates = reinterpret_cast<float*>(w + o_gates);
+  S->pos = reinterpret_cast<int*>(w + o_pos);
+  S->perm = reinterpret_cast<int*>(w + o_perm);
+  S->offsets = reinterpret_cast<int*>(w + o_offs);
+  S->tiles = reinterpret_cast<LtTile*>(w + o_tiles);
+  S->items1 = reinterpret_cast<LtItem*>(w + o_i1);
+  S->items2 = reinterpret_cast<LtItem*>(w + o_i2);
+  S->items3 = reinterpret_cast<LtItem*>(w + o_i3);
+  S->xg = w + o_xg;
+  S->h = w + o_h;
+  S->z = reinterpret_cast<__nv_bfloat16*>(w + o_z);
+  S->perm_smem = (3 * E + 32 * E) * 4;
+  LT_CK(cudaFuncSetAttribute(lt_perm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S->perm_smem));
+  LT_CK(lt_gemm_configure());
+  return cudaSuccess;
+}
+
+// which: 0 gate, 1 up, 2 down, 3 shared gate, 4 shared up, 5 shared down.
+cudaError_t large_t_repack(moe_layer* L, int which, int e, const uint8_t* src, cudaStream_t st) {
+  LtState* S = L->lt;
+  const bool sh = which >= 3;
+  const int fmt = sh ? L->sfmt : L->fmt;
+  const int kind = which % 3;
+  const int I = sh ? L->Ish : L->I;
+  const int rows = kind == 2 ? L->H : I, K = kind == 2 ? I : L->H;
+  uint8_t* dst = kind == 2 ? (sh ? S->sdn : S->dn + (int64_t)e * S->dn_stride)
+                           : (sh ? S->sgu : S->gu + (int64_t)e * S->gu_stride);
+  const int mode = kind == 2 ? 0 : (kind == 0 ? 1 : 2);
+  const int64_t n = (int64_t)rows * (fmt == MOE_Q8_0 ? K / 32 : K / 256);
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  if (fmt == MOE_Q8_0)
+    lt_repack_q8_kernel<<<grid, 256, 0, st>>>(src, dst, rows, K, mode);
+  else
+    lt_repack_q4ks_kernel<<<grid, 256, 0, st>>>(src, dst, rows, K, mode);
+  return cudaGetLastError();
+}
+
+cudaError_t large_t_repack_router(moe_layer* L, const float* src, cudaStream_t st) {
+  LtState* S = L->lt;
+  const int64_t n = (int64_t)S->E_pad128 * (L->H / 8);
+  lt_repack_router_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, S->router, L->E, S->E_pad128, L->H,
+                                                                       S->router_plane);
+  return cudaGetLastError();
+}
+
+size_t large_t_weight_bytes(const moe_layer* L) { return L->lt ? L->lt->weight_bytes : 0; }
+size_t large_t_workspace_bytes(const moe_layer* L) { return L->lt ? L->lt->ws_bytes : 0; }
+int* large_t_status_word(const moe_layer* L) { return L->lt ? L->lt->status : nullptr; }
+int* large_t_counters(const moe_layer* L) { return L->lt ? L->lt->counters : nullptr; }
+
+cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st) {
+  LtState* S = L->lt;
+  const int H = L->H, E = L->E, k = L->k, Tk = T * k;
+  const int n_sh = (T + 127) / 128;
+  const int prow_sh = 128 * (n_sh - 1) + round16(T - 128 * (n_sh - 1));
+
+  PrepParams pp{static_cast<const __nv_bfloat16*>(x), T, H, k, L->Ish, S->E_pad128, n_sh, S->tiles, S->items1,
+                S->items3, S->counters, S->xg};
+  lt_prep_kernel<<<n_sh, 256, 0, st>>>(pp);
+  LT_CK(cudaGetLastError());
+
+  LtGemmParams g{};
+  g.tiles = S->tiles;
+  g.status = S->status;
+  g.gu = S->gu; g.dn = S->dn; g.sgu = S->sgu; g.sdn = S->sdn; g.router = S->router;
+  g.gu_stride = S->gu_stride; g.dn_stride = S->dn_stride; g.router_plane = S->router_plane;
+  g.fmt = L->fmt; g.sfmt = L->sfmt;
+  g.H = H; g.I = L->I; g.Ish = L->Ish; g.Imax = S->Imax; g.E_pad128 = S->E_pad128; g.T = T; g.k = k;
+  g.xg = S->xg; g.h = S->h; g.z = S->z; g.logits = S->logits;
+  g.timeout_ns = 2000000000ull;
+  const int grid = L->num_sms;
+
+  g.items = S->items1; g.n_items = S->counters + 6; g.queue = S->counters + 0; g.exit_cnt = S->counters + 3;
+  LT_CK(lt_gemm_launch(g, grid, st));
+
+  const int warps = 8;
+  const unsigned tgrid = (unsigned)((T + warps - 1) / warps);
+  const int nper = (E + 31) / 32;
+#define LT_TOPK(NP) \
+  lt_topk_kernel<NP><<<tgrid, warps * 32, 0, st>>>(S->logits, L->router_b, T, E, S->E_pad128, k, S->ids, S->gates)
+  if (nper <= 4) LT_TOPK(4);
+  else if (nper <= 8) LT_TOPK(8);
+  else if (nper <= 12) LT_TOPK(12);
+  else if (nper <= 16) LT_TOPK(16);
+  else LT_TOPK(32);
+#undef LT_TOPK
+  LT_CK(cudaGetLastError());
+
+  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, S->offsets, S->perm, S->pos,
+               S->tiles, S->items2, S->items3, S->counters};
+  lt_perm_kernel<<<1, kPermThreads, S->perm_smem, st>>>(P);
+  LT_CK(cudaGetLastError());
+
+  const int max_routed = S->max_tiles - (L->T_max + 127) / 128;
+  lt_gather_kernel<<<max_routed, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), S->perm, S->tiles, S->counters,
+                                                n_sh, k, H, S->xg);
+  LT_CK(cudaGetLastError());
+
+  g.items = S->items2; g.n_items = S->counters + 7; g.queue = S->counters + 1; g.exit_cnt = S->counters + 4;
+  LT_CK(lt_gemm_launch(g, grid, st));
+  g.items = S->items3; g.n_items = S->counters + 8; g.queue = S->counters + 2; g.exit_cnt = S->counters + 5;
+  LT_CK(lt_gemm_launch(g, grid, st));
+
+  lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, T, k, H, L->Ish > 0,
+                                       static_cast<__nv_bfloat16*>(y));
+  LT_CK(cudaGetLastError());
+  (void)Tk;
+  return cudaSuccess;
+}
+
+cudaError_t large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm,
+                                cudaStream_t st) {
+  LtState* S = L->lt;
+  const size_t Tk = (size_t)L->last_T * L->k;
+  if (ids) LT_CK(cudaMemcpyAsync(ids, S->ids, Tk * 4, cudaMemcpyDeviceToDevice, st));
+  if (gates) LT_CK(cudaMemcpyAsync(gates, S->gates, Tk * 4, cudaMemcpyDeviceToDevice, st));
+  if (offsets) LT_CK(cudaMemcpyAsync(offsets, S->offsets, (size_t)(L->E + 1) * 4, cudaMemcpyDeviceToDevice, st));
+  if (perm) LT_CK(cudaMemcpyAsync(perm, S->perm, Tk * 4, cudaMemcpyDeviceToDevice, st));
+  return cudaSuccess;
+}
+
+void large_t_release(moe_layer* L) {
+  LtState* S = L->lt;
+  if (!S) return;
+  cudaFree(S->gu);
+  cudaFree(S->dn);
+  cudaFree(S->sgu);
+  cudaFree(S->sdn);
+  cudaFree(S->router);
+  cudaFree(S->ws);
+  delete S;
+  L->lt = nullptr;
+}
 
 }  // namespace moe

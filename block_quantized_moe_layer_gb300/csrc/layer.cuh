@@ -4,6 +4,8 @@
 
 namespace moe {
 
+struct LtState;  // the prefill-sized path's weights and workspace (large_t.cu)
+
 // One unit of expert work: up to kGroup activation vectors routed to one
 // expert (e == -1 for the shared expert).  Slots index the activation /
 // intermediate rows: routed slots are positions in perm[], the shared
@@ -95,7 +97,6 @@ struct moe_layer {
   int num_sms = 0;
   int smem_bytes = 0;
   int last_T = 0;
-  // large-T workspace
-  void* lws = nullptr;
-  size_t lws_bytes = 0;
+  // prefill-sized path (T > kMaxSmallT), present when T_max > kMaxSmallT
+  moe::LtState* lt = nullptr;
 };

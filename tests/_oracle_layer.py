@@ -37,6 +37,6 @@ def synth_oracle_layer(w, device="cpu", fetch=None):
 
     def ex(e):
         return tuple(to_np(t) for t in synth.expert(w, e, device))
-    sh = tuple(to_np(t) for t in synth.shared(w, device))
+    sh = tuple(to_np(t) for t in synth.shared(w, device)) if w.I_shared else None
     return layer_from_fp32(w.H, w.E, w.top_k, w.I, w.I_shared, to_np(Wr),
                            None if b is None else to_np(b), ex, sh, w.routed_fmt, w.shared_fmt)
