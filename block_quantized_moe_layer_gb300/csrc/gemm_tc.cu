@@ -3,17 +3,23 @@
 // One persistent CTA per SM (512 threads) claims work items from a global
 // queue.  An item multiplies one 128-row tile of a block-quantized weight
 // matrix (dequantised to bf16) by the bf16 activations of one token tile
-// (n_pad <= 128 tokens), accumulating in fp32 in tensor memory:
-//   warp 0      producer: 1-D bulk copies of the raw weight K-block and the
-//               activation K-block into a 6-stage shared-memory ring;
+// (n_pad <= 64 tokens), accumulating in fp32 in tensor memory (TMEM).
+//   warp 0      producer: 1-D bulk copies of raw weight stages (A ring) and
+//               activation K-slices (B ring);
 //   warp 1      allocates the 512 TMEM columns; lane 0 issues the MMAs
 //               (M = 128, N = n_pad, K = 16, A from TMEM, B from shared memory);
-//   warps 4-11  dequantise: thread (row r, half h) turns its 32 weights of the
-//               stage into bf16 pairs and stores them to TMEM (A operand);
-//   warps 12-15 epilogue: read the accumulator (double-buffered in TMEM) and
-//               write SwiGLU outputs (gate/up), bf16 partial outputs z (down) or
-//               fp32 router logits.
-// TMEM columns: A stages at 32 s (s < 6), accumulators at 256 and 384.
+//   warps 4-11  dequantise, as two groups of four warps that take alternate A
+//               stages: thread (group, row r) turns its row's weights of the
+//               stage into bf16 pairs and stores them to TMEM;
+//   warps 12-15 epilogue: read the accumulator (double-buffered) and write
+//               SwiGLU outputs (gate/up), bf16 partial outputs z (down) or fp32
+//               router logits.
+// The three rings are released independently: a raw weight slot as soon as
+// its group holds the data in registers, an activation slot and a TMEM stage
+// when the MMAs that read them complete.  An A stage is 128 columns of Q8_0,
+// one 256-column superblock of Q4KS (two TMEM stages) or 64 columns of a
+// router plane.
+// TMEM columns: A stages at 64 s (s < 6), accumulators at 384 and 448.
 // Every wait is bounded; a timeout records its site in the status word, sets
 // an abort flag that the other roles see, and every role then leaves after
 // its own in-flight copies and MMAs have completed.
@@ -24,27 +30,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 6;
-constexpr int kStageA = 16384;
-constexpr int kStageBytes = 32768;
+constexpr int kNA = 7;            // raw weight slots
+constexpr int kNB = 5;            // activation slots
+constexpr int kNT = 6;            // TMEM A stages of 64 columns
+constexpr int kASlot = kLtQ4Super;  // 18432 >= Q8_0 (17408) >= a router K-block (16384)
+constexpr int kBSlot = kLtMaxN * 128 * 2;
 constexpr int kGemmThreads = 512;
 constexpr int kDequantWarp0 = 4;
 constexpr int kEpiWarp0 = 12;
-constexpr int kTmemAcc = 256;
+constexpr int kTmemAcc = 384;
 
 // dynamic shared-memory plan
-constexpr int kOffStaging = kStages * kStageBytes;        // 4 warps x 4 KB
-constexpr int kOffBars = kOffStaging + 4 * 4096;
-constexpr int kNumBars = 3 * kStages + 2 + 2 + 4 + 4 + 1;
+constexpr int kOffB = kNA * kASlot;
+constexpr int kOffStaging = kOffB + kNB * kBSlot;          // 4 warps x 2 chunks x 64 rows x 16 B
+constexpr int kOffBars = kOffStaging + 4 * 2048;
+constexpr int kNumBars = 2 * kNA + 2 * kNB + 2 * kNT + 2 + 2 + 4 + 4 + 1;
 constexpr int kOffDescs = kOffBars + kNumBars * 8;
-constexpr int kOffInfos = kOffDescs + kStages * 16;
+constexpr int kOffTdescs = kOffDescs + kNA * 48;
+constexpr int kOffInfos = kOffTdescs + kNT * 16;
 constexpr int kOffMisc = kOffInfos + 4 * 48;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory plan");
 
-enum { kFlagEnd = 1, kFlagFirst = 2, kFlagLast = 4, kFlagHdr = 8 };
+enum { kFlagEnd = 1, kFlagFwdEnd = 2, kFlagFirst = 4, kFlagLast = 8 };
 
-struct StageDesc {
-  int flags, fmt, n_pad, kb;
+struct StageDesc {  // one A stage
+  int flags, fmt, n_pad, cols, nt0, nts, tflags[2], pad[4];
+};
+struct TDesc {  // one TMEM stage, for the MMA issuer
+  int flags, n_pad, nk, pad;
 };
 struct ItemInfo {
   int end, kind, rt, e, slot0, n, n_pad, prow0, plane, pad[3];
@@ -60,9 +74,16 @@ __device__ __forceinline__ void record_timeout(int* status, int site, int detail
   }
 }
 
+// Waits spin on the non-blocking test first (a suspended thread takes a few
+// hundred cycles to resume, which would sit on the per-stage critical path),
+// then fall back to the suspending try_wait.
+constexpr int kSpin = 256;
+
 // Single-thread bounded wait.
 __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t par, volatile int* abort, const LtGemmParams& p,
                                       int site, int detail) {
+  for (int i = 0; i < kSpin; ++i)
+    if (mbar_test_wait(bar, par)) return true;
   uint64_t t0 = 0;
   while (!mbar_try_wait(bar, par)) {
     if (*abort) return false;
@@ -80,7 +101,9 @@ __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t par, volatile int*
 
 // Whole-warp bounded wait with a warp-uniform result.
 __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t par, volatile int* abort, const LtGemmParams& p,
-                                      int site, int detail) {
+                                      int site, int detail, int spin = kSpin) {
+  for (int i = 0; i < spin; ++i)
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, par))) return true;
   uint64_t t0 = 0;
   for (;;) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, par))) return true;
@@ -103,78 +126,116 @@ __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t par, volatile int*
   }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+__device__ __forceinline__ uint64_t pack2(float a) {
+  const uint32_t u = __float_as_uint(a);
+  return ((uint64_t)u << 32) | u;
 }
 
-// 32 Q8_0 codes (8 words) times the block scale d -> 16 bf16 pairs.  A code
-// byte b becomes the fp32 2^23 + (b ^ 0x80) by placing it under the exponent
-// of 2^23; subtracting 2^23 + 128 recovers the signed code exactly, and
-// q * d is exact in fp32 (8 x 11 significant bits); the only rounding is
-// the conversion to bf16.
+// Two Q8_0 codes held as the fp32 bit patterns 2^23 + 128 + q (the code byte
+// with its sign bit flipped, placed under the exponent of 2^23): subtracting
+// 2^23 + 128 gives q exactly, q * d is exact in fp32 (8 x 11 significant
+// bits), and the only rounding is the conversion to bf16.  Packed f32x2 math.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t m0, uint32_t m1, uint64_t c2, uint64_t d2) {
+  uint32_t out;
+  asm("{\n\t.reg .b64 x;\n\t.reg .b32 lo, hi;\n\t"
+      "mov.b64 x, {%1, %2};\n\t"
+      "sub.rn.f32x2 x, x, %3;\n\t"
+      "mul.rn.f32x2 x, x, %4;\n\t"
+      "mov.b64 {lo, hi}, x;\n\t"
+      "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+      : "=r"(out)
+      : "r"(m0), "r"(m1), "l"(c2), "l"(d2));
+  return out;
+}
+
+// Two Q4KS codes as 2^23 + q: w = a*q - b with one fp32 rounding (as the
+// format defines it), then bf16.
+__device__ __forceinline__ uint32_t q4_pair(uint32_t m0, uint32_t m1, uint64_t c2, uint64_t a2, uint64_t nb2) {
+  uint32_t out;
+  asm("{\n\t.reg .b64 x;\n\t.reg .b32 lo, hi;\n\t"
+      "mov.b64 x, {%1, %2};\n\t"
+      "sub.rn.f32x2 x, x, %3;\n\t"
+      "fma.rn.f32x2 x, x, %4, %5;\n\t"
+      "mov.b64 {lo, hi}, x;\n\t"
+      "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+      : "=r"(out)
+      : "r"(m0), "r"(m1), "l"(c2), "l"(a2), "l"(nb2));
+  return out;
+}
+
+// 32 Q8_0 codes (8 words) of one block with scale d -> 16 bf16 pairs.
 __device__ __forceinline__ void dq_q8(const uint4& a, const uint4& b, float d, uint32_t (&v)[16]) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint64_t c2 = pack2(8388736.f), d2 = pack2(d);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t f = w[i] ^ 0x80808080u;
-    const float q0 = __int_as_float((int)__byte_perm(f, 0x4B000000u, 0x7440)) - 8388736.f;
-    const float q1 = __int_as_float((int)__byte_perm(f, 0x4B000000u, 0x7441)) - 8388736.f;
-    const float q2 = __int_as_float((int)__byte_perm(f, 0x4B000000u, 0x7442)) - 8388736.f;
-    const float q3 = __int_as_float((int)__byte_perm(f, 0x4B000000u, 0x7443)) - 8388736.f;
-    v[2 * i] = pack_bf16(q0 * d, q1 * d);
-    v[2 * i + 1] = pack_bf16(q2 * d, q3 * d);
+    v[2 * i] = q8_pair(__byte_perm(f, 0x4B000000u, 0x7440), __byte_perm(f, 0x4B000000u, 0x7441), c2, d2);
+    v[2 * i + 1] = q8_pair(__byte_perm(f, 0x4B000000u, 0x7442), __byte_perm(f, 0x4B000000u, 0x7443), c2, d2);
   }
 }
 
 // 32 Q4KS codes of one sub-block (16 bytes, weight 2j in the low nibble of
-// byte j) -> 16 bf16 pairs of a*q - b, rounded once in fp32 (as the format
-// defines it) and once to bf16.
+// byte j) -> 16 bf16 pairs of a*q - b.
 __device__ __forceinline__ void dq_q4(const uint4& c, float a, float b, uint32_t (&v)[16]) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  const uint64_t c2 = pack2(8388608.f), a2 = pack2(a), nb2 = pack2(-b);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float qe = __int_as_float((int)__byte_perm(lo, 0x4B000000u, 0x7440 + j)) - 8388608.f;
-      const float qo = __int_as_float((int)__byte_perm(hi, 0x4B000000u, 0x7440 + j)) - 8388608.f;
-      v[4 * i + j] = pack_bf16(fmaf(qe, a, -b), fmaf(qo, a, -b));
-    }
+    for (int j = 0; j < 4; ++j)
+      v[4 * i + j] = q4_pair(__byte_perm(lo, 0x4B000000u, 0x7440 + j), __byte_perm(hi, 0x4B000000u, 0x7440 + j),
+                             c2, a2, nb2);
   }
 }
 
-// 6-bit field f of a serialised Q4KS header (bits 32 + 6f .. of the 16 bytes).
-__device__ __forceinline__ int q4_field(const uint32_t (&hw)[4], int f) {
-  const int P = 32 + 6 * f, wi = P >> 5, sh = P & 31;
-  uint32_t v = hw[wi] >> sh;
-  if (sh > 26) v |= hw[wi + 1] << (32 - sh);
-  return (int)(v & 63u);
+// 6-bit field f of a serialised Q4KS header (bits 32 + 6f .. of the 16 bytes;
+// w1..w3 are its words 1..3).
+__device__ __forceinline__ int q4_field(uint32_t w1, uint32_t w2, uint32_t w3, int f) {
+  const int P = 6 * f;
+  if (P < 32) {
+    const uint64_t lo = ((uint64_t)w2 << 32) | w1;
+    return (int)((lo >> P) & 63u);
+  }
+  const uint64_t hi = ((uint64_t)w3 << 32) | w2;
+  return (int)((hi >> (P - 32)) & 63u);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
-  uint64_t* full = bars;
-  uint64_t* afull = bars + kStages;
-  uint64_t* empty = bars + 2 * kStages;
-  uint64_t* dfull = bars + 3 * kStages;
+  uint64_t* afull = bars;
+  uint64_t* aempty = afull + kNA;
+  uint64_t* bfull = aempty + kNA;
+  uint64_t* bempty = bfull + kNB;
+  uint64_t* tfull = bempty + kNB;
+  uint64_t* tempty = tfull + kNT;
+  uint64_t* dfull = tempty + kNT;
   uint64_t* dempty = dfull + 2;
   uint64_t* ifull = dempty + 2;
   uint64_t* iempty = ifull + 4;
   uint64_t* finbar = iempty + 4;
   StageDesc* descs = reinterpret_cast<StageDesc*>(sm + kOffDescs);
+  TDesc* tdescs = reinterpret_cast<TDesc*>(sm + kOffTdescs);
   ItemInfo* infos = reinterpret_cast<ItemInfo*>(sm + kOffInfos);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&afull[s], 8);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kNA; ++s) {
+      mbar_init(&afull[s], 1);
+      mbar_init(&aempty[s], 4);
+    }
+    for (int s = 0; s < kNB; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int s = 0; s < kNT; ++s) {
+      mbar_init(&tfull[s], 4);
+      mbar_init(&tempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&dfull[a], 1);
@@ -197,70 +258,99 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
-      uint32_t n = 0, i = 0;
+      uint32_t na = 0, nt = 0, i = 0;
       const int count = *p.n_items;
+      const int n_rt_items = p.n_rt_items;
       int item = atomicAdd(p.queue, 1);
       bool ok = true;
       while (ok && item < count) {
         const int next = atomicAdd(p.queue, 1);
-        const LtItem it = p.items[item];
-        const LtTile tl = p.tiles[it.tile];
+        // decode the item: router items first, then tile items (tile-major)
+        int kind, rt, tile, plane = 0;
+        if (item < n_rt_items) {
+          kind = kItemRT;
+          plane = item / (p.n_rt_router * p.n_router_tiles);
+          const int rem = item % (p.n_rt_router * p.n_router_tiles);
+          tile = rem / p.n_rt_router;
+          rt = rem % p.n_rt_router;
+        } else {
+          kind = p.tile_kind;
+          tile = p.tile0 + (item - n_rt_items) / p.n_rt_tile;
+          rt = (item - n_rt_items) % p.n_rt_tile;
+        }
+        const LtTile tl = p.tiles[tile];
         const uint8_t* A;
         const uint8_t* B;
-        int fmt, nkb;
-        if (it.kind == kItemGU) {
+        int fmt, K;
+        if (kind == kItemGU) {
           fmt = tl.e >= 0 ? p.fmt : p.sfmt;
-          A = (tl.e >= 0 ? p.gu + (int64_t)tl.e * p.gu_stride : p.sgu) + it.rt * lt_tile_bytes(fmt, p.H);
-          nkb = p.H / kLtKb;
+          K = p.H;
+          A = (tl.e >= 0 ? p.gu + (int64_t)tl.e * p.gu_stride : p.sgu) + rt * lt_tile_bytes(fmt, K);
           B = p.xg + (int64_t)tl.prow0 * p.H * 2;
-        } else if (it.kind == kItemDN) {
+        } else if (kind == kItemDN) {
           fmt = tl.e >= 0 ? p.fmt : p.sfmt;
-          const int K = tl.e >= 0 ? p.I : p.Ish;
-          A = (tl.e >= 0 ? p.dn + (int64_t)tl.e * p.dn_stride : p.sdn) + it.rt * lt_tile_bytes(fmt, K);
-          nkb = K / kLtKb;
+          K = tl.e >= 0 ? p.I : p.Ish;
+          A = (tl.e >= 0 ? p.dn + (int64_t)tl.e * p.dn_stride : p.sdn) + rt * lt_tile_bytes(fmt, K);
           B = p.h + (int64_t)tl.prow0 * p.Imax * 2;
         } else {
           fmt = MOE_BF16;
-          A = p.router + it.plane * p.router_plane + it.rt * lt_tile_bytes(MOE_BF16, p.H);
-          nkb = p.H / kLtKb;
+          K = p.H;
+          A = p.router + plane * p.router_plane + rt * lt_tile_bytes(MOE_BF16, K);
           B = p.xg + (int64_t)tl.prow0 * p.H * 2;
         }
         // item information for the epilogue
         const uint32_t j = i & 3;
         if (i >= 4 && !(ok = wait1(&iempty[j], ((i >> 2) - 1) & 1, abort, p, kSiteItem, (int)i))) break;
-        infos[j] = ItemInfo{0, it.kind, it.rt, tl.e, tl.slot0, tl.n, tl.n_pad, tl.prow0, it.plane, {0, 0, 0}};
+        infos[j] = ItemInfo{0, kind, rt, tl.e, tl.slot0, tl.n, tl.n_pad, tl.prow0, plane, {0, 0, 0}};
         mbar_arrive(&ifull[j]);
-        const uint32_t bbytes = (uint32_t)tl.n_pad * 128;
-        for (int kb = 0; kb < nkb; ++kb, ++n) {
-          const uint32_t s = n % kStages;
-          if (n >= kStages && !(ok = wait1(&empty[s], ((n / kStages) - 1) & 1, abort, p, kSiteFree, (int)n))) break;
-          uint8_t* sa = sm + s * kStageBytes;
-          uint8_t* sb = sa + kStageA;
-          int flags = (kb == 0 ? kFlagFirst : 0) | (kb == nkb - 1 ? kFlagLast : 0);
-          const uint8_t* asrc;
+        const int span = fmt == MOE_Q8_0 ? 128 : (fmt == MOE_Q4KS ? 256 : 64);  // columns per A stage
+        const int nst = (K + span - 1) / span;
+        for (int st = 0; st < nst; ++st, ++na) {
+          const int c0 = st * span, cols = min(span, K - c0);
+          const uint32_t sa = na % kNA;
+          if (na >= kNA && !(ok = wait1(&aempty[sa], ((na / kNA) - 1) & 1, abort, p, kSiteFree, (int)na))) break;
+          const int nts = cols > 128 ? 2 : 1;
+          StageDesc d;
+          d.flags = 0;
+          d.fmt = fmt;
+          d.n_pad = tl.n_pad;
+          d.cols = cols;
+          d.nt0 = (int)nt;
+          d.nts = nts;
+          d.tflags[0] = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 && nts == 1 ? kFlagLast : 0);
+          d.tflags[1] = st == nst - 1 ? kFlagLast : 0;
+          descs[sa] = d;
           uint32_t abytes;
+          const uint8_t* asrc;
           if (fmt == MOE_Q8_0) {
-            asrc = A + (int64_t)kb * kLtQ8Chunk;
-            abytes = kLtQ8Chunk;
+            asrc = A + (int64_t)(c0 / 64) * kLtQ8Chunk;
+            abytes = (uint32_t)(cols / 64) * kLtQ8Chunk;
           } else if (fmt == MOE_Q4KS) {
-            asrc = A + (int64_t)(kb >> 2) * kLtQ4Super + kLtQ4Hdr + (kb & 3) * kLtQ4Codes;
-            abytes = kLtQ4Codes;
-            if ((kb & 3) == 0) flags |= kFlagHdr;
+            asrc = A + (int64_t)(c0 / 256) * kLtQ4Super;
+            abytes = kLtQ4Super;
           } else {
-            asrc = A + (int64_t)kb * kLtBf16Chunk;
+            asrc = A + (int64_t)(c0 / 64) * kLtBf16Chunk;
             abytes = kLtBf16Chunk;
           }
-          descs[s] = StageDesc{flags, fmt, tl.n_pad, kb};
-          const uint32_t hbytes = (flags & kFlagHdr) ? kLtQ4Hdr : 0;
-          mbar_arrive_expect_tx(&full[s], abytes + hbytes + bbytes);
-          bulk_g2s(sa, asrc, abytes, &full[s]);
-          if (hbytes) bulk_g2s(sa + kLtQ4Codes, A + (int64_t)(kb >> 2) * kLtQ4Super, hbytes, &full[s]);
-          bulk_g2s(sb, B + (int64_t)kb * bbytes, bbytes, &full[s]);
+          mbar_arrive_expect_tx(&afull[sa], abytes);
+          bulk_g2s(sm + sa * kASlot, asrc, abytes, &afull[sa]);
+          // activation K-slices, one per TMEM stage
+          for (int t = 0; t < nts; ++t, ++nt) {
+            const int tc0 = c0 + 128 * t, tcols = min(128, cols - 128 * t);
+            const uint32_t sb = nt % kNB;
+            if (nt >= kNB && !(ok = wait1(&bempty[sb], ((nt / kNB) - 1) & 1, abort, p, kSiteFree, -(int)nt)))
+              break;
+            const uint32_t bbytes = (uint32_t)tl.n_pad * tcols * 2;
+            mbar_arrive_expect_tx(&bfull[sb], bbytes);
+            bulk_g2s(sm + kOffB + sb * kBSlot, B + (int64_t)(tc0 / 64) * tl.n_pad * 128, bbytes, &bfull[sb]);
+          }
+          if (!ok) break;
         }
         ++i;
         item = next;
       }
-      // end markers
+      // end markers: one A stage for each dequant group; the first forwards
+      // the end to the MMA issuer
       if (ok) {
         const uint32_t j = i & 3;
         if (i < 4 || (ok = wait1(&iempty[j], ((i >> 2) - 1) & 1, abort, p, kSiteItem, (int)i))) {
@@ -268,21 +358,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           mbar_arrive(&ifull[j]);
         }
       }
-      if (ok) {
-        const uint32_t s = n % kStages;
-        if (n < kStages || (ok = wait1(&empty[s], ((n / kStages) - 1) & 1, abort, p, kSiteFree, (int)n))) {
-          descs[s].flags = kFlagEnd;
-          mbar_arrive(&full[s]);
-          ++n;
-        }
+      for (int e = 0; e < 2 && ok; ++e, ++na) {
+        const uint32_t sa = na % kNA;
+        if (na >= kNA && !(ok = wait1(&aempty[sa], ((na / kNA) - 1) & 1, abort, p, kSiteFree, (int)na))) break;
+        descs[sa].flags = kFlagEnd | (e == 0 ? kFlagFwdEnd : 0);
+        descs[sa].nt0 = (int)nt;
+        mbar_arrive(&afull[sa]);
       }
       // every copy this thread issued has landed before the CTA leaves
-      const uint32_t n0 = n > kStages ? n - kStages : 0;
-      for (uint32_t m = n0; m < n; ++m) {
-        uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[m % kStages], (m / kStages) & 1)) {
+      const uint32_t a0 = na > kNA ? na - kNA : 0;
+      for (uint32_t m = a0; m < na; ++m) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&afull[m % kNA], (m / kNA) & 1)) {
           if (globaltimer_ns() - t0 > p.timeout_ns) {
             record_timeout(p.status, kSiteDrain, (int)m);
+            break;
+          }
+        }
+      }
+      const uint32_t b0 = nt > kNB ? nt - kNB : 0;
+      for (uint32_t m = b0; m < nt; ++m) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&bfull[m % kNB], (m / kNB) & 1)) {
+          if (globaltimer_ns() - t0 > p.timeout_ns) {
+            record_timeout(p.status, kSiteDrain, -(int)m);
             break;
           }
         }
@@ -291,29 +390,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      uint32_t n = 0, i = 0, a = 0;
-      for (;; ++n) {
-        const uint32_t s = n % kStages, par = (n / kStages) & 1;
-        if (!wait1(&full[s], par, abort, p, kSiteFull, (int)n)) break;
-        const StageDesc d = descs[s];
+      uint32_t i = 0, a = 0;
+      for (uint32_t nt = 0;; ++nt) {
+        const uint32_t st = nt % kNT;
+        if (!wait1(&tfull[st], (nt / kNT) & 1, abort, p, kSiteDq, (int)nt)) break;
+        const TDesc d = tdescs[st];
         if (d.flags & kFlagEnd) break;
         if (d.flags & kFlagFirst) {
           a = i & 1;
           const uint32_t u = i >> 1;
           if (u >= 1 && !wait1(&dempty[a], (u - 1) & 1, abort, p, kSiteAcc, (int)i)) break;
         }
-        if (!wait1(&afull[s], par, abort, p, kSiteDq, (int)n)) break;
+        const uint32_t sb = nt % kNB;
+        if (!wait1(&bfull[sb], (nt / kNB) & 1, abort, p, kSiteFull, (int)nt)) break;
         tc::fence_after();
         const uint32_t idesc = tc::idesc_bf16(kLtRows, d.n_pad);
-        const uint32_t bsm = smem_u32(sm + s * kStageBytes + kStageA);
+        const uint32_t bsm = smem_u32(sm + kOffB + sb * kBSlot);
         const uint32_t lbo = (uint32_t)d.n_pad * 16;
-#pragma unroll
-        for (int j = 0; j < kLtKb / 16; ++j) {
+        for (int j = 0; j < d.nk; ++j) {
           const uint64_t bdesc = tc::smem_desc(bsm + j * 2 * lbo, lbo, 128);
-          tc::mma_ts(tbase + kTmemAcc + 128 * a, tbase + 32 * s + 8 * j, bdesc, idesc,
+          tc::mma_ts(tbase + kTmemAcc + 64 * a, tbase + 64 * st + 8 * j, bdesc, idesc,
                      ((d.flags & kFlagFirst) && j == 0) ? 0u : 1u);
         }
-        tc::commit(&empty[s]);
+        tc::commit(&tempty[st]);
+        tc::commit(&bempty[sb]);
         if (d.flags & kFlagLast) {
           tc::commit(&dfull[a]);
           ++i;
@@ -321,7 +421,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
       }
       // all MMAs of this thread complete before the accumulators are freed
       tc::commit(finbar);
-      uint64_t t0 = globaltimer_ns();
+      const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(finbar, 0)) {
         if (globaltimer_ns() - t0 > p.timeout_ns) {
           record_timeout(p.status, kSiteDrain, -1);
@@ -331,61 +431,132 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
     }
   } else if (warp >= kDequantWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------------ dequantise
-    const int q = warp & 3, h = (warp - kDequantWarp0) >> 2, r = 32 * q + lane;
-    uint32_t hw[4] = {0, 0, 0, 0};
-    for (uint32_t n = 0;; ++n) {
-      const uint32_t s = n % kStages, par = (n / kStages) & 1;
-      if (!waitw(&full[s], par, abort, p, kSiteFull, (int)n)) break;
-      const StageDesc d = descs[s];
-      if (d.flags & kFlagEnd) break;
-      // the MMAs that read this TMEM stage last time have completed
-      if (n >= kStages && !waitw(&empty[s], ((n / kStages) - 1) & 1, abort, p, kSiteFree, (int)n)) break;
-      tc::fence_after();
-      const uint8_t* sa = sm + s * kStageBytes;
-      uint32_t v[16];
-      if (d.fmt == MOE_Q8_0) {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(sa + ((h * 2 + 0) * 128 + r) * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(sa + ((h * 2 + 1) * 128 + r) * 16);
-        const float dsc = __half2float(*reinterpret_cast<const __half*>(sa + 8192 + (h * 128 + r) * 2));
-        dq_q8(c0, c1, dsc, v);
-      } else if (d.fmt == MOE_Q4KS) {
-        if (d.flags & kFlagHdr) {
-          const uint4 hv = *reinterpret_cast<const uint4*>(sa + kLtQ4Codes + r * 16);
-          hw[0] = hv.x; hw[1] = hv.y; hw[2] = hv.z; hw[3] = hv.w;
+    const int q = warp & 3, g = (warp - kDequantWarp0) >> 2, r = 32 * q + lane;
+    const bool leader = warp == kDequantWarp0 + 4 * g && lane == 0;
+    const uint32_t tlane = (uint32_t)(32 * q) << 16;
+    for (uint32_t na = g;; na += 2) {
+      const uint32_t sa = na % kNA;
+      if (!waitw(&afull[sa], (na / kNA) & 1, abort, p, kSiteFull, (int)na)) break;
+      const StageDesc d = descs[sa];
+      const uint8_t* s = sm + sa * kASlot;
+      if (d.flags & kFlagEnd) {
+        if (d.flags & kFlagFwdEnd) {
+          const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
+          if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
+          if (leader) tdescs[ts] = TDesc{kFlagEnd, 0, 0, 0};
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tfull[ts]);
         }
-        const int sub = 2 * (d.kb & 3) + h;
-        const float dd = __half2float(__ushort_as_half((unsigned short)(hw[0] & 0xFFFFu)));
-        const float dm = __half2float(__ushort_as_half((unsigned short)(hw[0] >> 16)));
-        const float av = dd * (float)q4_field(hw, sub);
-        const float bv = dm * (float)q4_field(hw, 8 + sub);
-        const uint4 c = *reinterpret_cast<const uint4*>(sa + (h * 128 + r) * 16);
-        dq_q4(c, av, bv, v);
-      } else {
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const uint4 c = *reinterpret_cast<const uint4*>(sa + ((h * 4 + pc) * 128 + r) * 16);
-          v[4 * pc + 0] = c.x; v[4 * pc + 1] = c.y; v[4 * pc + 2] = c.z; v[4 * pc + 3] = c.w;
-        }
+        break;
       }
-      tc::st_32x32b_x16(tbase + ((uint32_t)(32 * q) << 16) + 32 * s + 16 * h, v);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[s]);
+      if (d.fmt == MOE_Q8_0) {
+        // up to 4 blocks (two 64-column K-blocks x two halves)
+        const int nb = d.cols / 32;
+        uint4 c[4][2];
+        float sc[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (b < nb) {
+            const uint8_t* kbp = s + (b >> 1) * kLtQ8Chunk;
+            const int h = b & 1;
+            c[b][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
+            c[b][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
+            sc[b] = __half2float(*reinterpret_cast<const __half*>(kbp + 8192 + (h * 128 + r) * 2));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[sa]);
+        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
+        if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
+        tc::fence_after();
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (b < nb) {
+            uint32_t v[16];
+            dq_q8(c[b][0], c[b][1], sc[b], v);
+            tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16 * b, v);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before();
+        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nb * 2, 0};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfull[ts]);
+      } else if (d.fmt == MOE_Q4KS) {
+        // one superblock: header, then 8 sub-blocks over two TMEM stages
+        const uint4 hv = *reinterpret_cast<const uint4*>(s + r * 16);
+        uint4 c[8];
+#pragma unroll
+        for (int sb = 0; sb < 8; ++sb)
+          c[sb] = *reinterpret_cast<const uint4*>(s + kLtQ4Hdr + (sb >> 1) * kLtQ4Codes + ((sb & 1) * 128 + r) * 16);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[sa]);
+        const float dd = __half2float(__ushort_as_half((unsigned short)(hv.x & 0xFFFFu)));
+        const float dm = __half2float(__ushort_as_half((unsigned short)(hv.x >> 16)));
+        bool good = true;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t t = (uint32_t)d.nt0 + half, ts = t % kNT;
+          if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) {
+            good = false;
+            break;
+          }
+          tc::fence_after();
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int sb = 4 * half + k4;
+            uint32_t v[16];
+            dq_q4(c[sb], dd * (float)q4_field(hv.y, hv.z, hv.w, sb), dm * (float)q4_field(hv.y, hv.z, hv.w, 8 + sb),
+                  v);
+            tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16 * k4, v);
+          }
+          tc::wait_st();
+          tc::fence_before();
+          if (leader) tdescs[ts] = TDesc{d.tflags[half], d.n_pad, 8, 0};
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tfull[ts]);
+        }
+        if (!good) break;
+      } else {
+        // router plane: 64 columns of bf16, copied as they are
+        uint32_t v[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc) {
+            const uint4 x = *reinterpret_cast<const uint4*>(s + ((h * 4 + pc) * 128 + r) * 16);
+            v[h][4 * pc + 0] = x.x;
+            v[h][4 * pc + 1] = x.y;
+            v[h][4 * pc + 2] = x.z;
+            v[h][4 * pc + 3] = x.w;
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[sa]);
+        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
+        if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
+        tc::fence_after();
+        tc::st_32x32b_x16(tbase + tlane + 64 * ts, v[0]);
+        tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16, v[1]);
+        tc::wait_st();
+        tc::fence_before();
+        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, 4, 0};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfull[ts]);
+      }
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3, r = 32 * q + lane;
-    uint8_t* stg = sm + kOffStaging + q * 4096;
+    uint8_t* stg = sm + kOffStaging + q * 2048;
     for (uint32_t i = 0;; ++i) {
       const uint32_t j = i & 3;
-      if (!waitw(&ifull[j], (i >> 2) & 1, abort, p, kSiteItem, (int)i)) break;
+      if (!waitw(&ifull[j], (i >> 2) & 1, abort, p, kSiteItem, (int)i, 0)) break;
       const ItemInfo info = infos[j];
       if (info.end) break;
       const uint32_t a = i & 1;
-      if (!waitw(&dfull[a], (i >> 1) & 1, abort, p, kSiteAcc, (int)i)) break;
+      if (!waitw(&dfull[a], (i >> 1) & 1, abort, p, kSiteAcc, (int)i, 0)) break;
       tc::fence_after();
-      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + kTmemAcc + 128 * a;
+      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + kTmemAcc + 64 * a;
       for (int c = 0; c < info.n_pad; c += 16) {
         uint32_t v[16];
         tc::ld_32x32b_x16(tacc + c, v);
@@ -393,12 +564,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         if (info.kind == kItemGU) {
 #pragma unroll
           for (int m = 0; m < 16; ++m) {
-            const float g = __uint_as_float(v[m]);
-            const float u = __shfl_down_sync(0xffffffffu, g, 16);
+            const float gt = __uint_as_float(v[m]);
+            const float u = __shfl_down_sync(0xffffffffu, gt, 16);
             if (lane < 16) {
-              const float hv = g / (1.f + expf(-g)) * u;
-              const int nn = c + m;
-              *reinterpret_cast<__nv_bfloat16*>(stg + ((lane >> 3) * info.n_pad + nn) * 16 + (lane & 7) * 2) =
+              const float hv = gt / (1.f + expf(-gt)) * u;
+              *reinterpret_cast<__nv_bfloat16*>(stg + ((lane >> 3) * info.n_pad + c + m) * 16 + (lane & 7) * 2) =
                   __float2bfloat16_rn(hv);
             }
           }

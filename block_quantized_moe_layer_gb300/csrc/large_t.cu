@@ -44,13 +44,9 @@ struct LtState {
   int* perm = nullptr;
   int* offsets = nullptr;
   LtTile* tiles = nullptr;
-  LtItem* items1 = nullptr;
-  LtItem* items2 = nullptr;
-  LtItem* items3 = nullptr;
   uint8_t* xg = nullptr;
   uint8_t* h = nullptr;
   __nv_bfloat16* z = nullptr;
-  int max_items1 = 0, max_items2 = 0, max_items3 = 0;
   int perm_smem = 0;
 };
 
@@ -152,44 +148,33 @@ __global__ void lt_repack_router_kernel(const float* __restrict__ src, uint8_t* 
 
 struct PrepParams {
   const __nv_bfloat16* x;
-  int T, H, k, Ish, E_pad128, n_sh;
+  int T, H, k, n_sh, n_items1;
   LtTile* tiles;
-  LtItem* items1;
-  LtItem* items3;
   int* counters;
   uint8_t* xg;
 };
 
-// Block b tiles x rows [128 b, 128 b + 128) into the operand image; block 0
-// also writes the plain token tiles and the work lists that need no routing.
+constexpr int kColSlices = 8;  // column slices per token tile in the operand-image kernels
+
+// Block (tt, cs) writes column slice cs of plain token tile tt (x rows
+// [64 tt, 64 tt + 64)) into the operand image; block (0, 0) also writes the
+// plain token tiles, which the router and the shared expert use.
 __global__ void lt_prep_kernel(const PrepParams P) {
-  const int tt = blockIdx.x;
-  const int n = min(128, P.T - 128 * tt), n_pad = round16(n);
-  if (tt == 0) {
-    const int n_rt_r = P.E_pad128 / 128, n_gu_sh = P.Ish / 64, n_dn = P.H / 128;
-    const int n_rt_items = kLtPlanes * n_rt_r * P.n_sh;
+  const int tt = blockIdx.x, cs = blockIdx.y;
+  const int n = min(kLtMaxN, P.T - kLtMaxN * tt), n_pad = round16(n);
+  if (tt == 0 && cs == 0) {
     for (int i = threadIdx.x; i < P.n_sh; i += blockDim.x) {
-      const int ni = min(128, P.T - 128 * i);
-      P.tiles[i] = LtTile{-1, P.T * P.k + 128 * i, ni, round16(ni), 128 * i, {0, 0, 0}};
+      const int ni = min(kLtMaxN, P.T - kLtMaxN * i);
+      P.tiles[i] = LtTile{-1, P.T * P.k + kLtMaxN * i, ni, round16(ni), kLtMaxN * i, {0, 0, 0}};
     }
-    // router items first (they gate the routing), then shared gate/up
-    for (int i = threadIdx.x; i < n_rt_items; i += blockDim.x) {
-      const int pl = i / (n_rt_r * P.n_sh), rem = i % (n_rt_r * P.n_sh);
-      P.items1[i] = LtItem{kItemRT, rem % n_rt_r, rem / n_rt_r, pl};
-    }
-    for (int i = threadIdx.x; i < n_gu_sh * P.n_sh; i += blockDim.x)
-      P.items1[n_rt_items + i] = LtItem{kItemGU, i % n_gu_sh, i / n_gu_sh, 0};
-    if (P.Ish > 0)
-      for (int i = threadIdx.x; i < n_dn * P.n_sh; i += blockDim.x)
-        P.items3[i] = LtItem{kItemDN, i % n_dn, i / n_dn, 0};
-    if (threadIdx.x == 0) P.counters[6] = n_rt_items + n_gu_sh * P.n_sh;
+    if (threadIdx.x == 0) P.counters[6] = P.n_items1;
   }
-  uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)128 * tt * P.H * 2);
-  const int nc = P.H / 8;
+  uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)kLtMaxN * tt * P.H * 2);
+  const int nc = P.H / 8 / kColSlices, c0 = cs * nc;
   for (int idx = threadIdx.x; idx < n_pad * nc; idx += blockDim.x) {
-    const int r = idx % n_pad, c = idx / n_pad;
+    const int r = idx % n_pad, c = c0 + idx / n_pad;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = *reinterpret_cast<const uint4*>(P.x + (int64_t)(128 * tt + r) * P.H + 8 * c);
+    if (r < n) v = *reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c);
     dst[(int64_t)c * n_pad + r] = v;
   }
 }
@@ -298,28 +283,34 @@ struct PermParams {
   int* perm;
   int* pos;
   LtTile* tiles;
-  LtItem* items2;
-  LtItem* items3;
   int* counters;
 };
 
+constexpr int kPermChunk = 512;  // tokens per pass (16 bitmap words per expert)
+
 // Single CTA of 1024 threads.  Pair p = t*k + j goes to slot
-// offsets[e] + (number of pairs p' < p with the same expert e).
+// offsets[e] + (number of tokens t' < t that chose e): an expert's tokens
+// are a bitmap over the tokens of a pass, and a pair's rank is the popcount
+// of the bits below its token plus the expert's count in earlier words and
+// passes.  The k experts of one token are distinct, so the order of pairs
+// within an expert is the order of their tokens.
 __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermParams P) {
   extern __shared__ int psm[];
-  const int E = P.E, Tk = P.T * P.k;
-  int* cnt = psm;               // [E]
-  int* off = cnt + E;           // [E]
-  int* run = off + E;           // [E]
-  int* wc = run + E;            // [32][E]
+  const int E = P.E, k = P.k, T = P.T;
+  constexpr int W = kPermChunk / 32;
+  int* cnt = psm;                                      // [E]
+  int* off = cnt + E;                                  // [E]
+  int* run = off + E;                                  // [E] tokens of e in earlier passes
+  unsigned* bits = reinterpret_cast<unsigned*>(run + E);  // [E][W]
+  int* pre = reinterpret_cast<int*>(bits + E * W);     // [E][W] exclusive word prefix
   __shared__ int wtot[33];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   for (int e = tid; e < E; e += kPermThreads) {
     cnt[e] = 0;
     run[e] = 0;
   }
   __syncthreads();
-  for (int p = tid; p < Tk; p += kPermThreads) atomicAdd(&cnt[P.ids[p]], 1);
+  for (int p = tid; p < T * k; p += kPermThreads) atomicAdd(&cnt[P.ids[p]], 1);
   __syncthreads();
   int total;
   {
@@ -332,72 +323,70 @@ __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermPara
     if (tid == 0) P.offsets[E] = total;
   }
   __syncthreads();
-  for (int c0 = 0; c0 < Tk; c0 += kPermThreads) {
-    for (int i = tid; i < 32 * E; i += kPermThreads) wc[i] = 0;
+  for (int t0 = 0; t0 < T; t0 += kPermChunk) {
+    const int nt = min(kPermChunk, T - t0);
+    for (int i = tid; i < E * W; i += kPermThreads) bits[i] = 0u;
     __syncthreads();
-    const int p = c0 + tid;
-    const bool valid = p < Tk;
-    const int e = valid ? P.ids[p] : -1;
-    const unsigned mask = __match_any_sync(0xffffffffu, e);
-    const int lrank = __popc(mask & ((1u << lane) - 1u));
-    if (valid && lrank == 0) wc[warp * E + e] = __popc(mask);
-    __syncthreads();
-    for (int x = tid; x < E; x += kPermThreads) {
-      int s = run[x];
-      for (int w = 0; w < 32; ++w) {
-        const int t = wc[w * E + x];
-        wc[w * E + x] = s;
-        s += t;
-      }
-      run[x] = s;
+    for (int p = tid; p < nt * k; p += kPermThreads) {
+      const int tl = p / k;
+      atomicOr(&bits[P.ids[t0 * k + p] * W + (tl >> 5)], 1u << (tl & 31));
     }
     __syncthreads();
-    if (valid) {
-      const int dest = off[e] + wc[warp * E + e] + lrank;
-      P.perm[dest] = p;
-      P.pos[p] = dest;
+    for (int e = tid; e < E; e += kPermThreads) {
+      int s = run[e];
+      for (int w = 0; w < W; ++w) {
+        pre[e * W + w] = s;
+        s += __popc(bits[e * W + w]);
+      }
+      run[e] = s;
+    }
+    __syncthreads();
+    for (int p = tid; p < nt * k; p += kPermThreads) {
+      const int tl = p / k, e = P.ids[t0 * k + p];
+      const unsigned below = bits[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u);
+      const int dest = off[e] + pre[e * W + (tl >> 5)] + __popc(below);
+      P.perm[dest] = t0 * k + p;
+      P.pos[t0 * k + p] = dest;
     }
     __syncthreads();
   }
-  // routed token tiles and the work lists of the gate/up and down launches
-  // (E <= 1024: thread e handles expert e)
-  const int n_gu = P.I / 64, n_dn = P.H / 128, sh_dn = P.Ish > 0 ? P.n_sh * n_dn : 0;
+  // routed token tiles (E <= 1024: thread e handles expert e)
   const int e = tid;
   const int M = e < E ? cnt[e] : 0;
-  const int ntt = (M + 127) / 128;
-  const int rows = M > 0 ? 128 * (ntt - 1) + round16(M - 128 * (ntt - 1)) : 0;
+  const int ntt = (M + kLtMaxN - 1) / kLtMaxN;
+  const int rows = M > 0 ? kLtMaxN * (ntt - 1) + round16(M - kLtMaxN * (ntt - 1)) : 0;
   int n_tiles, n_rows;
   const int tb = block_excl_scan(ntt, wtot, &n_tiles);
   const int pb = block_excl_scan(rows, wtot, &n_rows);
   for (int i = 0; i < ntt; ++i) {
-    const int ti = P.n_sh + tb + i;
-    const int ni = min(128, M - 128 * i);
-    P.tiles[ti] = LtTile{e, off[e] + 128 * i, ni, round16(ni), P.prow_sh + pb + 128 * i, {0, 0, 0}};
-    for (int rt = 0; rt < n_gu; ++rt) P.items2[(tb + i) * n_gu + rt] = LtItem{kItemGU, rt, ti, 0};
-    for (int rt = 0; rt < n_dn; ++rt) P.items3[sh_dn + (tb + i) * n_dn + rt] = LtItem{kItemDN, rt, ti, 0};
+    const int ni = min(kLtMaxN, M - kLtMaxN * i);
+    P.tiles[P.n_sh + tb + i] =
+        LtTile{e, off[e] + kLtMaxN * i, ni, round16(ni), P.prow_sh + pb + kLtMaxN * i, {0, 0, 0}};
   }
   if (tid == 0) {
-    P.counters[7] = n_tiles * n_gu;
-    P.counters[8] = sh_dn + n_tiles * n_dn;
+    const int n_gu = P.I / 64, n_dn = P.H / 128;
+    P.counters[7] = n_tiles * n_gu;                                   // routed gate/up items
+    P.counters[8] = (P.Ish > 0 ? P.n_sh : 0) * n_dn + n_tiles * n_dn;  // down items
     P.counters[9] = n_tiles;
   }
 }
 
-// Block b gathers routed tile n_sh + b (if it exists) into the operand image.
+// Block (b, cs) gathers column slice cs of routed tile n_sh + b (if it exists)
+// into the operand image.
 __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm,
                                  const LtTile* __restrict__ tiles, const int* __restrict__ counters, int n_sh, int k,
                                  int H, uint8_t* __restrict__ xg) {
   if ((int)blockIdx.x >= counters[9]) return;
   const LtTile tl = tiles[n_sh + blockIdx.x];
+  __shared__ int tok[kLtMaxN];
+  for (int r = threadIdx.x; r < tl.n; r += blockDim.x) tok[r] = perm[tl.slot0 + r] / k;
+  __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>(xg + (int64_t)tl.prow0 * H * 2);
-  const int nc = H / 8;
+  const int nc = H / 8 / kColSlices, c0 = blockIdx.y * nc;
   for (int idx = threadIdx.x; idx < tl.n_pad * nc; idx += blockDim.x) {
-    const int r = idx % tl.n_pad, c = idx / tl.n_pad;
+    const int r = idx % tl.n_pad, c = c0 + idx / tl.n_pad;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < tl.n) {
-      const int tok = perm[tl.slot0 + r] / k;
-      v = *reinterpret_cast<const uint4*>(x + (int64_t)tok * H + 8 * c);
-    }
+    if (r < tl.n) v = *reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c);
     dst[(int64_t)c * tl.n_pad + r] = v;
   }
 }
@@ -480,13 +469,11 @@ cudaError_t large_t_alloc(moe_layer* L) {
   }
   S->weight_bytes = wb;
 
-  const int n_sh_max = (Tm + 127) / 128;
+  const int n_sh_max = (Tm + kLtMaxN - 1) / kLtMaxN;
   const int Tk = Tm * k;
-  S->max_tiles = n_sh_max + std::min(E, Tk) + Tk / 128 + 1;
+  // routed tiles: sum over experts of ceil(M_e / 64) <= T k / 64 + min(E, T k)
+  S->max_tiles = n_sh_max + std::min(E, Tk) + Tk / kLtMaxN + 1;
   S->max_rows = Tm + Tk + 16 * S->max_tiles;
-  S->max_items1 = (kLtPlanes * (S->E_pad128 / 128) + Ish / 64) * n_sh_max;
-  S->max_items2 = S->max_tiles * (I / 64);
-  S->max_items3 = S->max_tiles * (H / 128);
   size_t off = 0;
   auto take = [&](size_t b) {
     const size_t o = off;
@@ -502,9 +489,6 @@ cudaError_t large_t_alloc(moe_layer* L) {
   const size_t o_perm = take((size_t)Tk * 4);
   const size_t o_offs = take((size_t)(E + 1) * 4);
   const size_t o_tiles = take((size_t)S->max_tiles * sizeof(LtTile));
-  const size_t o_i1 = take((size_t)S->max_items1 * sizeof(LtItem));
-  const size_t o_i2 = take((size_t)S->max_items2 * sizeof(LtItem));
-  const size_t o_i3 = take((size_t)S->max_items3 * sizeof(LtItem));
   const size_t o_xg = take((size_t)S->max_rows * H * 2);
   const size_t o_h = take((size_t)S->max_rows * S->Imax * 2);
   const size_t o_z = take((size_t)(Tk + Tm) * H * 2);
@@ -521,13 +505,10 @@ cudaError_t large_t_alloc(moe_layer* L) {
   S->perm = reinterpret_cast<int*>(w + o_perm);
   S->offsets = reinterpret_cast<int*>(w + o_offs);
   S->tiles = reinterpret_cast<LtTile*>(w + o_tiles);
-  S->items1 = reinterpret_cast<LtItem*>(w + o_i1);
-  S->items2 = reinterpret_cast<LtItem*>(w + o_i2);
-  S->items3 = reinterpret_cast<LtItem*>(w + o_i3);
   S->xg = w + o_xg;
   S->h = w + o_h;
   S->z = reinterpret_cast<__nv_bfloat16*>(w + o_z);
-  S->perm_smem = (3 * E + 32 * E) * 4;
+  S->perm_smem = (3 * E + 2 * E * (kPermChunk / 32)) * 4;
   LT_CK(cudaFuncSetAttribute(lt_perm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S->perm_smem));
   LT_CK(lt_gemm_configure());
   return cudaSuccess;
@@ -568,13 +549,16 @@ int* large_t_counters(const moe_layer* L) { return L->lt ? L->lt->counters : nul
 
 cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st) {
   LtState* S = L->lt;
-  const int H = L->H, E = L->E, k = L->k, Tk = T * k;
-  const int n_sh = (T + 127) / 128;
-  const int prow_sh = 128 * (n_sh - 1) + round16(T - 128 * (n_sh - 1));
+  const int H = L->H, E = L->E, k = L->k;
+  const int n_sh = (T + kLtMaxN - 1) / kLtMaxN;
+  const int prow_sh = kLtMaxN * (n_sh - 1) + round16(T - kLtMaxN * (n_sh - 1));
+  const int n_rt_r = S->E_pad128 / 128;
+  const int n_rt_items = kLtPlanes * n_rt_r * n_sh;
+  const int n_gu_sh = L->Ish / 64;
 
-  PrepParams pp{static_cast<const __nv_bfloat16*>(x), T, H, k, L->Ish, S->E_pad128, n_sh, S->tiles, S->items1,
-                S->items3, S->counters, S->xg};
-  lt_prep_kernel<<<n_sh, 256, 0, st>>>(pp);
+  PrepParams pp{static_cast<const __nv_bfloat16*>(x), T, H, k, n_sh, n_rt_items + n_gu_sh * n_sh, S->tiles,
+                S->counters, S->xg};
+  lt_prep_kernel<<<dim3(n_sh, kColSlices), 256, 0, st>>>(pp);
   LT_CK(cudaGetLastError());
 
   LtGemmParams g{};
@@ -586,9 +570,13 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStr
   g.H = H; g.I = L->I; g.Ish = L->Ish; g.Imax = S->Imax; g.E_pad128 = S->E_pad128; g.T = T; g.k = k;
   g.xg = S->xg; g.h = S->h; g.z = S->z; g.logits = S->logits;
   g.timeout_ns = 2000000000ull;
+  g.n_rt_router = n_rt_r;
+  g.n_router_tiles = n_sh;
   const int grid = L->num_sms;
 
-  g.items = S->items1; g.n_items = S->counters + 6; g.queue = S->counters + 0; g.exit_cnt = S->counters + 3;
+  // router logits + shared-expert gate/up (plain token tiles)
+  g.n_items = S->counters + 6; g.queue = S->counters + 0; g.exit_cnt = S->counters + 3;
+  g.n_rt_items = n_rt_items; g.tile_kind = kItemGU; g.tile0 = 0; g.n_rt_tile = n_gu_sh > 0 ? n_gu_sh : 1;
   LT_CK(lt_gemm_launch(g, grid, st));
 
   const int warps = 8;
@@ -604,25 +592,27 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStr
 #undef LT_TOPK
   LT_CK(cudaGetLastError());
 
-  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, S->offsets, S->perm, S->pos,
-               S->tiles, S->items2, S->items3, S->counters};
+  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, S->offsets, S->perm, S->pos, S->tiles, S->counters};
   lt_perm_kernel<<<1, kPermThreads, S->perm_smem, st>>>(P);
   LT_CK(cudaGetLastError());
 
-  const int max_routed = S->max_tiles - (L->T_max + 127) / 128;
-  lt_gather_kernel<<<max_routed, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), S->perm, S->tiles, S->counters,
-                                                n_sh, k, H, S->xg);
+  const int max_routed = S->max_tiles - (L->T_max + kLtMaxN - 1) / kLtMaxN;
+  lt_gather_kernel<<<dim3(max_routed, kColSlices), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), S->perm,
+                                                                  S->tiles, S->counters, n_sh, k, H, S->xg);
   LT_CK(cudaGetLastError());
 
-  g.items = S->items2; g.n_items = S->counters + 7; g.queue = S->counters + 1; g.exit_cnt = S->counters + 4;
+  // routed gate/up
+  g.n_items = S->counters + 7; g.queue = S->counters + 1; g.exit_cnt = S->counters + 4;
+  g.n_rt_items = 0; g.tile_kind = kItemGU; g.tile0 = n_sh; g.n_rt_tile = L->I / 64;
   LT_CK(lt_gemm_launch(g, grid, st));
-  g.items = S->items3; g.n_items = S->counters + 8; g.queue = S->counters + 2; g.exit_cnt = S->counters + 5;
+  // down projections: shared tiles (if any) then routed tiles
+  g.n_items = S->counters + 8; g.queue = S->counters + 2; g.exit_cnt = S->counters + 5;
+  g.n_rt_items = 0; g.tile_kind = kItemDN; g.tile0 = L->Ish > 0 ? 0 : n_sh; g.n_rt_tile = H / 128;
   LT_CK(lt_gemm_launch(g, grid, st));
 
   lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, T, k, H, L->Ish > 0,
                                        static_cast<__nv_bfloat16*>(y));
   LT_CK(cudaGetLastError());
-  (void)Tk;
   return cudaSuccess;
 }
 

@@ -28,7 +28,7 @@ namespace moe {
 
 constexpr int kLtRows = 128;       // MMA M: weight rows per tile
 constexpr int kLtKb = 64;          // K columns per pipeline stage
-constexpr int kLtMaxN = 128;       // tokens per token tile
+constexpr int kLtMaxN = 64;        // tokens per token tile
 constexpr int kLtQ8Chunk = 8704;   // 128 rows x 64 columns of Q8_0
 constexpr int kLtQ4Super = 18432;  // 128 rows x 256 columns of Q4KS
 constexpr int kLtQ4Hdr = 2048;
@@ -38,7 +38,7 @@ constexpr int kLtPlanes = 3;       // router: W = W1 + W2 + W3, each bf16
 
 enum { kItemGU = 0, kItemDN = 1, kItemRT = 2 };
 
-// A token tile: up to 128 slots of one group (an expert, or e = -1 for the
+// A token tile: up to 64 slots of one group (an expert, or e = -1 for the
 // shared expert) that share the weights of every work item on the tile.
 struct LtTile {
   int e;      // routed expert, or -1 (shared expert / plain token tile)
@@ -49,21 +49,18 @@ struct LtTile {
   int pad[3];
 };
 
-// A work item of the grouped GEMM: one 128-row weight tile against one token tile.
-struct LtItem {
-  int kind;   // kItemGU / kItemDN / kItemRT
-  int rt;     // row tile
-  int tile;   // index into the tile array
-  int plane;  // router plane (kItemRT)
-};
-
 __host__ __device__ inline int64_t lt_tile_bytes(int fmt, int K) {
   return fmt == MOE_Q8_0 ? (int64_t)136 * K : fmt == MOE_Q4KS ? (int64_t)72 * K : (int64_t)256 * K;
 }
 
+// A work item of the grouped GEMM is one 128-row weight tile against one
+// token tile.  A launch's items are numbered: first n_rt_items router items
+// (plane-major, then token tile, then row tile), then tile items (token tile
+// tile0 + i / n_rt_tile, row tile i % n_rt_tile, of kind tile_kind).
 struct LtGemmParams {
-  const LtItem* items;
-  const int* n_items;
+  const int* n_items;  // device: item count of the launch
+  int n_rt_items, n_rt_router, n_router_tiles;
+  int tile_kind, tile0, n_rt_tile;
   int* queue;
   int* exit_cnt;
   int* status;
