@@ -19,6 +19,7 @@ cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int 
 size_t accept_static_bytes();
 cudaError_t accept_static_scratch(void** out);
 int small_t_smem_bytes(const SmallParams& P);
+int finalize_misc_bytes(int T, int E, int k);
 cudaError_t small_t_configure(int L, int smem_bytes);
 cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st);
 bool large_t_enabled(const moe_layer* L);
@@ -238,7 +239,9 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
       L->sdn_ch = choose_chunking(sfmt, d->I_shared, shift);
       if (L->sgu_ch.n == 0 || L->sdn_ch.n == 0) return fail(MOE_EFORMAT, "no chunking for shared format %d", sfmt);
     }
-    stage = chunk_bytes(MOE_F32, kRouterCc) + (int64_t)std::min(d->T_max, kMaxSmallT) * kRouterCc * (L_limbs == 2 ? 2 : 4);
+    // a router stage: room for one tile's weights (512 columns) and its x slice
+    stage = kRouterTileChunks * chunk_bytes(MOE_F32, kRouterCc) +
+            (int64_t)std::min(d->T_max, kMaxSmallT) * kRouterTileChunks * kRouterCc * (L_limbs == 2 ? 2 : 4);
     stage = std::max(stage, stage_need(fmt, L->gu_ch));
     stage = std::max(stage, stage_need(fmt, L->dn_ch));
     if (has_sh) {
@@ -372,9 +375,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.z = reinterpret_cast<float*>(w + o_z);
   (void)counters_end;
 
-  const int Tk = Tm * k;
-  const size_t fin = align_up((size_t)Tm * d->E * 4, 16) + 4 * (align_up(d->E, 4) + 3 * align_up(Tk, 4));
-  sp.misc_bytes = (int)align_up(fin, 16);
+  sp.misc_bytes = (int)align_up((size_t)finalize_misc_bytes(Tm, d->E, k), 16);
   // every byte not needed elsewhere goes to the stage ring; it must hold at
   // least two of the largest stages
   sp.n_stages = kMaxSlots;

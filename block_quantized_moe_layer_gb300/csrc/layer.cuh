@@ -26,7 +26,8 @@ struct Sync {
   int routing_ready;  // routing published
   int exit_cnt;       // CTAs that left
   int n_rent;         // routed entries (written with the routing)
-  int pad[2];
+  int routing_aux;    // ids, gates, offsets, perm, pos written (after routing_ready)
+  int pad;
 };
 
 struct SmallParams {

@@ -168,12 +168,14 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     const Entry* ep = nullptr;
     bool shared_e = false;
     if (t < NR) {
+      // a router tile is one stage holding the tile's x slice; the consumers
+      // load the tile's router weights themselves
       kind = kRouter;
       rgk = (t / P.n_kt) << 16;
       rbt = t % P.n_kt;  // router: index of the 512-column slice
-      nch = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);
+      nch = 1;
       fmt = MOE_F32;
-      nbc = kRouterCc / 32;
+      nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);  // 128-column chunks in the slice
       M = P.T;
     } else if (t < NR + NSG) {
       kind = kGateUp;
@@ -210,8 +212,8 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     int64_t cbytes;
     int e_id = -1;
     if (kind == kRouter) {
-      cbytes = chunk_bytes(MOE_F32, kRouterCc);
-      wbase = P.router + ((int64_t)(rgk >> 16) * P.n_rc + kRouterTileChunks * rbt) * cbytes;
+      cbytes = 0;
+      wbase = nullptr;
     } else {
       shared_e = entry < P.n_sh;
       if (shared_e) {
@@ -241,14 +243,17 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         wbase = (shared_e ? P.sdn : P.dn + (int64_t)e_id * P.dn_stride) + (int64_t)(4 * rbt) * nch * cbytes;
       }
     }
-    const uint32_t per = kind == kRouter ? (uint32_t)(kRouterCc * XEL) : (uint32_t)(nbc * RB);
+    const uint32_t per = kind == kRouter ? (uint32_t)(nbc * kRouterCc * XEL) : (uint32_t)(nbc * RB);
     const uint32_t wb = (uint32_t)cbytes;
-    const int need = (int)((wb + (uint32_t)M * per + 127u) & ~127u);
+    // a router stage reserves room for the tile's weights, which the
+    // consumers copy in themselves (cp.async), ahead of the x slice
+    const uint32_t resv = kind == kRouter ? (uint32_t)nbc * (uint32_t)chunk_bytes(MOE_F32, kRouterCc) : wb;
+    const int need = (int)((resv + (uint32_t)M * per + 127u) & ~127u);
     // activation sources of this tile at chunk 0, and their step per chunk
     const uint8_t* asrc[kMaxSmallT];
     int64_t astep;
     if (kind == kRouter) {
-      astep = (int64_t)kRouterCc * XEL;
+      astep = 0;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
         asrc[m] = static_cast<const uint8_t*>(P.x) + ((int64_t)m * P.H + (int64_t)kRouterTileChunks * rbt * kRouterCc) * XEL;
@@ -288,7 +293,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       dd[3] = h3;
       uint8_t* stage = smem + plan.ring + pos;
       mbar_arrive_expect_tx(&full[s], wb + (uint32_t)M * per);
-      bulk_g2s(stage, wbase + (int64_t)q * cbytes, wb, &full[s]);
+      if (wb) bulk_g2s(stage, wbase + (int64_t)q * cbytes, wb, &full[s]);
       if (!dep_ok) {
         if (kind == kGateUp) {
           // shared gate/up needs the x records; routed ones were gated by the routing flag
@@ -303,11 +308,11 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         if (dep_ok) fence_proxy_async_global();
         else ok = false;  // the consumers see the status word; the stage is still completed below
       }
-      uint8_t* adst = stage + wb;
+      uint8_t* adst = stage + resv;
       const int64_t aoff = (int64_t)(kind == kRouter ? c : c) * astep;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
-        if (m < M) bulk_g2s(adst + m * per, dep_ok ? asrc[m] + aoff : wbase, per, &full[s]);
+        if (m < M) bulk_g2s(adst + m * per, dep_ok ? asrc[m] + aoff : asrc[0], per, &full[s]);
       ++issued;
     }
     t = t_next;
@@ -469,9 +474,20 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fm
 // ---------------------------------------------------------------------------
 // consumer: routing (last router tile)
 // ---------------------------------------------------------------------------
+// fp32 -> unsigned key with the same order (no NaNs; -0 is mapped to +0 first).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // The k largest of row[0..E) by (value desc, index asc), one warp; lane l
-// holds experts l, l+32, ... (NPER of them) in registers.  Writes ids and
-// values in slot order.
+// holds experts l, l+32, ... (NPER of them) in registers.  Each round takes
+// the exact maximum value over the lanes' current bests (a warp max of the
+// order-preserving keys), then the lowest expert index among the lanes that
+// hold it.  Writes ids and values in slot order (lane 0).
 template <int NPER>
 __device__ __forceinline__ void topk_token(const float* row, int E, int k, int* ids, float* vals_out) {
   const int lane = threadIdx.x & 31;
@@ -479,37 +495,98 @@ __device__ __forceinline__ void topk_token(const float* row, int E, int k, int* 
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : -INFINITY;
+    const float x = e < E ? row[e] : -INFINITY;
+    v[i] = x == x ? x : -INFINITY;
   }
+  uint32_t taken = 0;
   for (int j = 0; j < k; ++j) {
     float best = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && v[i] > best) { best = v[i]; bi = e; }  // ascending e: the first wins ties
+      // ascending e: a later equal value never replaces an earlier one
+      if (e < E && !((taken >> i) & 1u) && (v[i] > best || bi == 0x7fffffff)) {
+        best = v[i];
+        bi = e;
+      }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    const uint32_t key = bi == 0x7fffffff ? 0u : order_key(best);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t wi = __reduce_min_sync(0xffffffffu, key == m ? (uint32_t)bi : 0x7fffffffu);
+    if ((int)(wi & 31u) == lane) taken |= 1u << (wi >> 5);
+    if (lane == 0) {
+      ids[j] = (int)wi;
+      vals_out[j] = key_value(m);
     }
-#pragma unroll
-    for (int i = 0; i < NPER; ++i)
-      if (lane + 32 * i == bi) v[i] = -INFINITY;
-    if (lane == 0) { ids[j] = bi; vals_out[j] = best; }
   }
 }
 
+// Scratch of finalize_routing in the misc region (bytes, see finalize_misc_bytes).
+struct FinLayout {
+  int lg, cnt, off, sid, sl, sg, sperm, spos, wtot;
+};
+__host__ __device__ inline FinLayout fin_layout(int T, int E, int k) {
+  const int Tk = T * k, e4 = (E + 3) & ~3, t4 = (Tk + 3) & ~3;
+  FinLayout f;
+  f.lg = 0;
+  f.cnt = ((T * E * 4 + 15) & ~15);
+  f.off = f.cnt + 4 * e4;
+  f.sid = f.off + 4 * e4;
+  f.sl = f.sid + 4 * t4;
+  f.sg = f.sl + 4 * t4;
+  f.sperm = f.sg + 4 * t4;
+  f.spos = f.sperm + 4 * t4;
+  f.wtot = f.spos + 4 * t4;
+  return f;
+}
+int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).wtot + 4 * 2 * kConsumerWarps + 16; }
+
+// Exclusive scan over the consumer threads of two ints at once.
+__device__ __forceinline__ void consumer_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* wtot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, ia, o);
+    const int y = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += x; ib += y; }
+  }
+  if (lane == 31) {
+    wtot[2 * warp] = ia;
+    wtot[2 * warp + 1] = ib;
+  }
+  consumer_sync();
+  int ba = 0, bb = 0;
+  ta = 0;
+  tb = 0;
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    if (w < warp) { ba += wtot[2 * w]; bb += wtot[2 * w + 1]; }
+    ta += wtot[2 * w];
+    tb += wtot[2 * w + 1];
+  }
+  ea = ba + ia - a;
+  eb = bb + ib - b;
+}
+
+// Runs on the consumer threads of the CTA that finished the last router
+// tile: logits, top-k and gates, then the permutation and the routed work
+// entries.  The entries and their count are published first (routing_ready);
+// ids, gates, offsets, perm and pos follow (routing_aux), since only the
+// combine and moe_get_routing read them.
 __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
-  float* lg = reinterpret_cast<float*>(misc);                       // [T*E]
-  int* cnt = reinterpret_cast<int*>(misc + ((T * E * 4 + 15) & ~15)); // [E]
-  int* sid = cnt + ((E + 3) & ~3);                                   // [Tk]
-  float* sl = reinterpret_cast<float*>(sid + ((Tk + 3) & ~3));       // [Tk]
-  int* sperm = reinterpret_cast<int*>(sl + ((Tk + 3) & ~3));         // [Tk]
+  const FinLayout f = fin_layout(T, E, k);
+  float* lg = reinterpret_cast<float*>(misc + f.lg);       // [T*E]
+  int* cnt = reinterpret_cast<int*>(misc + f.cnt);         // [E]
+  int* off = reinterpret_cast<int*>(misc + f.off);         // [E]
+  int* sid = reinterpret_cast<int*>(misc + f.sid);         // [Tk]
+  float* sl = reinterpret_cast<float*>(misc + f.sl);       // [Tk]
+  float* sg = reinterpret_cast<float*>(misc + f.sg);       // [Tk]
+  int* sperm = reinterpret_cast<int*>(misc + f.sperm);     // [Tk]
+  int* spos = reinterpret_cast<int*>(misc + f.spos);       // [Tk]
+  int* wtot = reinterpret_cast<int*>(misc + f.wtot);       // [2 * warps]
 
   __threadfence();
   // logits: thread i sums, in slice order, the partials of experts e = i,
@@ -534,13 +611,11 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
       for (int c = 0; c < 4; ++c)
         if (4 * q + c < T) lg[(4 * q + c) * E + e] = vv[c] + bias;
     }
+    cnt[e] = 0;
   }
-  for (int e = tid; e < E; e += kConsumerWarps * 32) cnt[e] = 0;
   consumer_sync();
 
-  // top-k per token (one warp per token): (value desc, index asc).  Each lane
-  // keeps its experts' logits (e = lane + 32 i) in registers.
-  const int lane = tid & 31, warp = tid >> 5;
+  // top-k and gates per token (one warp per token)
   const int nper = (E + 31) / 32;
   for (int t = warp; t < T; t += kConsumerWarps) {
     if (nper <= 4) topk_token<4>(lg + t * E, E, k, sid + t * k, sl + t * k);
@@ -553,83 +628,87 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
       const float l0 = sl[t * k];
       float sum = 0.f;
       for (int j = 0; j < k; ++j) sum += expf(sl[t * k + j] - l0);
-      const float g = expf(sl[t * k + lane] - l0) / sum;
-      P.gates[t * k + lane] = g;
-      P.ids[t * k + lane] = sid[t * k + lane];
+      sg[t * k + lane] = expf(sl[t * k + lane] - l0) / sum;
     }
   }
   consumer_sync();
 
+  // stable rank of each pair among the earlier pairs of its expert, and the
+  // histogram (warp 0, 32 pairs at a time, equal experts found with match_any)
+  int rank[4], ep[4];
   if (warp == 0) {
-    // rank of each pair among the earlier pairs of its expert (stable), and
-    // the histogram: 32 pairs at a time, equal experts found with match_any
-    int rank[4], ep[4];
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < (Tk + 31) / 32; ++r) {
       const int p = lane + 32 * r;
       const int e = p < Tk ? sid[p] : -1 - lane;
       const unsigned mask = __match_any_sync(0xffffffffu, e);
-      rank[r] = 0;
-      ep[r] = -1;
-      if (p < Tk) {
-        ep[r] = e;
-        rank[r] = cnt[e] + __popc(mask & ((1u << lane) - 1u));
-      }
+      ep[r] = p < Tk ? e : -1;
+      rank[r] = p < Tk ? cnt[e] + __popc(mask & ((1u << lane) - 1u)) : 0;
       __syncwarp();
       if (p < Tk && (mask & ((1u << lane) - 1u)) == 0) cnt[e] += __popc(mask);  // one lane per expert
       __syncwarp();
     }
-    // exclusive scans over experts: pair offsets, entry counts
-    const int nper = (E + 31) / 32;
-    const int e0 = lane * nper, e1 = min(E, e0 + nper);
-    int sum_p = 0, sum_w = 0;
-    for (int e = e0; e < e1; ++e) { sum_p += cnt[e]; sum_w += (cnt[e] + kGroup - 1) / kGroup; }
-    int inc_p = sum_p, inc_w = sum_w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, inc_p, o);
-      const int b = __shfl_up_sync(0xffffffffu, inc_w, o);
-      if (lane >= o) { inc_p += a; inc_w += b; }
+  }
+  consumer_sync();
+
+  // pair offsets and routed entries: thread i owns a contiguous run of experts
+  const int ept = (E + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
+  int np = 0, nw = 0;
+  for (int e = e0; e < e1; ++e) {
+    np += cnt[e];
+    nw += (cnt[e] + kGroup - 1) / kGroup;
+  }
+  int po, wo, ptot, wtot_all;
+  consumer_scan2(np, nw, po, wo, ptot, wtot_all, wtot);
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt[e];
+    off[e] = po;
+    for (int g = 0; g * kGroup < c; ++g) {
+      int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + wo);
+      dst[0] = e;
+      dst[1] = po + g * kGroup;
+      dst[2] = min(kGroup, c - g * kGroup);
+      ++wo;
     }
-    int off = inc_p - sum_p, went = inc_w - sum_w;
-    const int total_w = __shfl_sync(0xffffffffu, inc_w, 31);
-    // offsets: reuse cnt[] as the running offset table
-    for (int e = e0; e < e1; ++e) {
-      const int c = cnt[e];
-      P.offsets[e] = off;
-      cnt[e] = off;  // now: start of expert e in perm
-      if (c > 0) {
-        for (int g = 0; g * kGroup < c; ++g) {
-          int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + went);
-          dst[0] = e;
-          dst[1] = off + g * kGroup;
-          dst[2] = min(kGroup, c - g * kGroup);
-          ++went;
-        }
-      }
-      off += c;
-    }
-    if (lane == 31) P.offsets[E] = off;
-    __syncwarp();
-    for (int r = 0; r < 4; ++r) {
+    po += c;
+  }
+  consumer_sync();
+  if (warp == 0) {
+    for (int r = 0; r < (Tk + 31) / 32; ++r) {
       const int p = lane + 32 * r;
       if (p < Tk) {
-        const int slot = cnt[ep[r]] + rank[r];
+        const int slot = off[ep[r]] + rank[r];
         sperm[slot] = p;
-        P.perm[slot] = p;
-        P.pos[p] = slot;
+        spos[p] = slot;
       }
     }
-    __syncwarp();
-    // tokens of each routed entry
-    for (int w = lane; w < total_w; w += 32) {
-      int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + w);
-      const int slot0 = dst[1], M = dst[2];
-      for (int m = 0; m < kGroup; ++m) dst[3 + m] = m < M ? sperm[slot0 + m] / k : 0;
-    }
-    if (lane == 0) P.sync->n_rent = total_w;
+  }
+  consumer_sync();
+  // tokens of each routed entry
+  for (int w = tid; w < wtot_all; w += kConsumerWarps * 32) {
+    int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + w);
+    const int slot0 = __ldcg(dst + 1), M = __ldcg(dst + 2);
+    for (int m = 0; m < kGroup; ++m) dst[3 + m] = m < M ? sperm[slot0 + m] / k : 0;
+  }
+  consumer_sync();
+  if (tid == 0) {
+    P.sync->n_rent = wtot_all;
     __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release(&P.sync->routing_ready, 1);
+    st_release(&P.sync->routing_ready, 1);
+  }
+  // what only the combine and moe_get_routing read
+  for (int q = tid; q < Tk; q += kConsumerWarps * 32) {
+    P.ids[q] = sid[q];
+    P.gates[q] = sg[q];
+    P.perm[q] = sperm[q];
+    P.pos[q] = spos[q];
+  }
+  for (int e = tid; e < E; e += kConsumerWarps * 32) P.offsets[e] = off[e];
+  if (tid == 0) P.offsets[E] = ptot;
+  consumer_sync();
+  if (tid == 0) {
+    __threadfence();
+    st_release(&P.sync->routing_aux, 1);
   }
 }
 
@@ -683,62 +762,94 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     const int d_rg = d.rgks >> 16, d_ks = d.rgks & 0xFFFF;  // router tiles
 
     if (d.kind == kRouter) {
-      const uint8_t* xs = stage + chunk_bytes(MOE_F32, kRouterCc);  // [T][128] x slice
+      // One router tile: 32 experts (lane = expert row) x a slice of ncc
+      // 128-column chunks.  The stage holds the slice of x ([T][cols]); the
+      // router weights are loaded straight from global memory, all of a
+      // thread's loads in flight at once (warp w takes float4 columns w,
+      // w + 8, ...; one warp load is 512 contiguous bytes).
+      const int kt = d_ks / kRouterTileChunks, ncc = d.nbc, cols = ncc * kRouterCc;
+      const float4* wsrc = reinterpret_cast<const float4*>(P.router) + (int64_t)d_rg * P.n_ks * 64 * 32;
+      float4* wst = reinterpret_cast<float4*>(const_cast<uint8_t*>(stage));  // [cols/4][32 rows]
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int k4 = warp + kConsumerWarps * i;
+        if (k4 < cols / 4) cp_async16(wst + k4 * 32 + lane, wsrc + (int64_t)(kt * 128 + k4) * 32 + lane);
+      }
+      const uint8_t* xs = stage + cols * kRows * 4;
       auto xval = [&](int t, int c) -> float {
-        if constexpr (L == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xs)[t * kRouterCc + c]);
-        else return reinterpret_cast<const float*>(xs)[t * kRouterCc + c];
+        if constexpr (L == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xs)[t * cols + c]);
+        else return reinterpret_cast<const float*>(xs)[t * cols + c];
       };
-      if (d_rg < T && warp < kRouterCc / 32) {
-        // x slice -> activation records for tokens t = rg, rg + n_rg, ... (warp w: block 4*ks + w)
+      if (d_rg < T) {
+        // x slice -> activation records of tokens t = rg, rg + n_rg, ... (warp w: blocks w, w + 8)
         for (int t = d_rg; t < T; t += P.n_rg)
-          write_record<L>(xval(t, warp * 32 + lane),
-                          P.xrec + ((int64_t)t * (P.H / 32) + d_ks * (kRouterCc / 32) + warp) * RB);
+          for (int b = warp; b < cols / 32; b += kConsumerWarps)
+            write_record<L>(xval(t, b * 32 + lane),
+                            P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
         __threadfence();
         fence_proxy_async_global();
       }
-      if (d.chunk == 0)
-        for (int t = 0; t < kMaxSmallT; ++t) racc[t] = 0.f;
-      for (int k4 = warp * 4; k4 < warp * 4 + 4; ++k4) {
-        const float4 w = *reinterpret_cast<const float4*>(stage + (k4 * 32 + lane) * 16);
+      // four independent accumulators per token (one per float4 component)
+      float ra[kMaxSmallT][4];
 #pragma unroll
-        for (int t = 0; t < kMaxSmallT; ++t) {
-          if (t < T) {
-            float4 xv;
-            if constexpr (L == 2) {
-              const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * kRouterCc + k4 * 4) * 2);
-              xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                               __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-            } else {
-              xv = *reinterpret_cast<const float4*>(xs + (t * kRouterCc + k4 * 4) * 4);
+      for (int t = 0; t < kMaxSmallT; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ra[t][c] = 0.f;
+      cp_async_wait_all();  // a thread reads back only the weights it copied
+      const int ncol4 = cols / 4;
+      // rolled loops: this code runs once per launch, so its instruction
+      // fetches are cold and code size, not issue rate, decides its time
+#pragma unroll 1
+      for (int i = 0; i < 16; ++i) {
+        const int k4 = warp + kConsumerWarps * i;
+        if (k4 < ncol4) {
+          const float4 w = wst[k4 * 32 + lane];
+#pragma unroll
+          for (int t = 0; t < kMaxSmallT; ++t) {
+            if (t < T) {
+              float4 xv;
+              if constexpr (L == 2) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * cols + k4 * 4) * 2);
+                xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                                 __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+              } else {
+                xv = *reinterpret_cast<const float4*>(xs + (t * cols + k4 * 4) * 4);
+              }
+              ra[t][0] = fmaf(w.x, xv.x, ra[t][0]);
+              ra[t][1] = fmaf(w.y, xv.y, ra[t][1]);
+              ra[t][2] = fmaf(w.z, xv.z, ra[t][2]);
+              ra[t][3] = fmaf(w.w, xv.w, ra[t][3]);
             }
-            racc[t] = fmaf(w.x, xv.x, fmaf(w.y, xv.y, fmaf(w.z, xv.z, fmaf(w.w, xv.w, racc[t]))));
           }
         }
       }
+#pragma unroll
+      for (int t = 0; t < kMaxSmallT; ++t) racc[t] = (ra[t][0] + ra[t][1]) + (ra[t][2] + ra[t][3]);
+      // the stage's weights were written through the generic proxy; the next
+      // user of these bytes may be a bulk copy
+      tc_fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (d.chunk == d.nch - 1) {
 #pragma unroll
-        for (int t = 0; t < kMaxSmallT; ++t)
-          if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
-        consumer_sync();
-        if (tid < T * 32) {
-          const int t = tid >> 5, r = tid & 31;
-          float v = 0.f;
-          for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
-          P.partials[((int64_t)(d_ks / kRouterTileChunks) * P.E_pad + d_rg * 32 + r) * P.Tp + t] = v;
-        }
-        __threadfence();
-        consumer_sync();
-        if (tid == 0) {
-          if (d_rg < T) atomicAdd(&P.sync->x_done, d.nch * ((T - 1 - d_rg) / P.n_rg + 1));
-          const int old = atomicAdd(&P.sync->router_done, 1);
-          flags[0] = (old == P.n_rg * P.n_kt - 1);
-        }
-        consumer_sync();
-        if (flags[0]) finalize_routing(P, misc);
-        consumer_sync();
+      for (int t = 0; t < kMaxSmallT; ++t)
+        if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
+      consumer_sync();
+      if (tid < T * 32) {
+        const int t = tid >> 5, r = tid & 31;
+        float v = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
+        P.partials[((int64_t)kt * P.E_pad + d_rg * 32 + r) * P.Tp + t] = v;
       }
+      __threadfence();
+      consumer_sync();
+      if (tid == 0) {
+        if (d_rg < T) atomicAdd(&P.sync->x_done, ncc * ((T - 1 - d_rg) / P.n_rg + 1));
+        const int old = atomicAdd(&P.sync->router_done, 1);
+        flags[0] = (old == P.n_rg * P.n_kt - 1);
+      }
+      consumer_sync();
+      if (flags[0]) finalize_routing(P, misc);
+      consumer_sync();
     } else {
       if (d.chunk == 0) {
 #pragma unroll
@@ -865,7 +976,12 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
   float* sg = reinterpret_cast<float*>(smem + plan.escr);                       // [T*k] gates
   int* sp = reinterpret_cast<int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);  // [T*k] slots
   const int T = P.T, k = P.k;
+  int* flags = reinterpret_cast<int*>(smem + plan.flags);
   __threadfence();
+  if (threadIdx.x == 0)  // set right after the routing; long done by now
+    flags[2] = wait_flag_geq(&P.sync->routing_aux, 1, P.timeout_ns, P.status, kSiteRouting, -1);
+  __syncthreads();
+  if (!flags[2]) return;
   for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
     sg[q] = __ldcg(&P.gates[q]);
     sp[q] = __ldcg(&P.pos[q]);
@@ -945,6 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.sync->router_done = 0;
       P.sync->x_done = 0;
       P.sync->routing_ready = 0;
+      P.sync->routing_aux = 0;
       P.sync->n_rent = 0;
       P.sync->exit_cnt = 0;
     }
