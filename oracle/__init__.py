@@ -6,7 +6,9 @@ legs of ``bench.py`` may use it.  It shares no code with the CUDA path.
 
 Everything here is plain numpy.  Block formats are decoded to fp32 exactly as
 defined in :mod:`oracle.formats`; routing, the expert FFNs and the combine run
-in fp64 (:mod:`oracle.moe`); acceptance is :mod:`oracle.accept`.
+in fp64 (:mod:`oracle.moe`); acceptance is :mod:`oracle.accept`; one MTP
+draft/verify round (target stack, output norm, LM head, draft heads,
+acceptance) is :mod:`oracle.mtp`.
 
 Sources (page title, section):
   * "Step-5 Preview GGUF" (smalinin/Step-5-Preview-GGUF), "Model background"
@@ -31,4 +33,4 @@ acceptance example).  The end-to-end layer values themselves have no printed
 counterpart on the pages: they are pinned only through those parts.
 """
 
-from . import formats, moe, accept  # noqa: F401
+from . import formats, moe, accept, mtp  # noqa: F401
