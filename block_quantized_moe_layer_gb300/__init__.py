@@ -21,7 +21,8 @@ EXPORTS = (
     "moe_layer_create", "moe_forward", "moe_get_routing", "moe_layer_status",
     "moe_layer_weight_bytes", "moe_layer_workspace_bytes", "moe_layer_destroy",
     "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
-    "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_last_error",
+    "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
+    "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
 )
 
 
@@ -69,6 +70,13 @@ def lib():
             "mtp_verify_accept_workspace_bytes": (sz, [i32, i32]),
             "mtp_verify_accept": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp, sz, vp]),
             "mtp_verify_accept_noalloc": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp]),
+            "moe_forward_residual": (_c.c_int, [vp, vp, i32, vp, vp]),
+            "moe_lm_head_create": (_c.c_int, [_c.POINTER(MoeTensor), i32, i32, vp, _c.POINTER(vp)]),
+            "moe_lm_head_forward": (_c.c_int, [vp, vp, i32, _c.c_float, vp, vp]),
+            "moe_lm_head_destroy": (None, [vp]),
+            "mtp_round_workspace_bytes": (sz, [i32, i32, i32, i32]),
+            "mtp_round": (_c.c_int, [_c.POINTER(vp), i32, _c.POINTER(vp), i32, vp, vp, vp, _c.c_float, vp, sz,
+                                     vp, vp, vp, vp, vp, vp]),
             "moe_last_error": (_c.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -156,13 +164,14 @@ class Layer:
     def workspace_bytes(self):
         return lib().moe_layer_workspace_bytes(self.handle)
 
-    def forward(self, x, y=None, stream=None):
+    def forward(self, x, y=None, stream=None, residual=False):
+        """y = MoE(x), or x + MoE(x) with ``residual``."""
         import torch
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
-        _check(lib().moe_forward(self.handle, x.data_ptr() if T else None, T,
-                                 y.data_ptr() if T else None, _stream(stream)))
+        f = lib().moe_forward_residual if residual else lib().moe_forward
+        _check(f(self.handle, x.data_ptr() if T else None, T, y.data_ptr() if T else None, _stream(stream)))
         return y
 
     def routing(self, T, stream=None):
@@ -230,3 +239,72 @@ def verify_accept_noalloc(draft_ids, logits, out=None, stream=None):
     _check(lib().mtp_verify_accept_noalloc(draft_ids.data_ptr() if k else None, k, logits.data_ptr(), V,
                                            out.data_ptr(), out.data_ptr() + 4, _stream(stream)))
     return out
+
+
+class LmHead:
+    """Output norm + Q8_0 LM head [V, H] on the current CUDA device; ``w`` is
+    the serialised Q8_0 byte tensor (host or device)."""
+
+    def __init__(self, w, V, H, T_max, act, stream=None):
+        self.V, self.H, self.T_max, self.act = V, H, T_max, act
+        t = _tensor(FMT_Q8_0, V, H, w)
+        h = _c.c_void_p()
+        _check(lib().moe_lm_head_create(_c.byref(t), T_max, act, _stream(stream), _c.byref(h)))
+        self.handle = h
+
+    def forward(self, x, eps=1e-6, out=None, stream=None):
+        """fp32 logits [T, V] of rmsnorm(x)."""
+        import torch
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.V, dtype=torch.float32, device=x.device)
+        _check(lib().moe_lm_head_forward(self.handle, x.data_ptr() if T else None, T, eps,
+                                         out.data_ptr() if T else None, _stream(stream)))
+        return out
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().moe_lm_head_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def round_workspace(H, k, V, act, device="cuda"):
+    import torch
+    n = lib().mtp_round_workspace_bytes(H, k, V, act)
+    if n == 0:
+        raise MoEError(MOE_EINVAL, "mtp_round_workspace_bytes: arguments out of range")
+    return torch.zeros(n + 256, dtype=torch.uint8, device=device)
+
+
+def _aligned(buf, a=256):
+    off = (-buf.data_ptr()) % a
+    return buf.data_ptr() + off, buf.numel() - off
+
+
+def mtp_round(layers, heads, lm, x, noise, eps=1e-6, workspace=None, head_out=True, stream=None):
+    """One MTP draft/verify round (see ``mtp_round`` in moe_layer.h).  Returns
+    a dict of device tensors: logits [k+1, V], drafts [k], accept [n, next],
+    head_out [k, k, H] (if requested)."""
+    import torch
+    k = len(heads)
+    H, V = lm.H, lm.V
+    dev = x.device
+    if workspace is None:
+        workspace = round_workspace(H, k, V, lm.act, dev)
+    wp, wn = _aligned(workspace)
+    logits = torch.empty(k + 1, V, dtype=torch.float32, device=dev)
+    drafts = torch.empty(k, dtype=torch.int32, device=dev)
+    acc = torch.empty(2, dtype=torch.int32, device=dev)
+    hout = torch.empty(k, k, H, dtype=x.dtype, device=dev) if head_out else None
+    tl = (_c.c_void_p * max(1, len(layers)))(*[L.handle.value for L in layers])
+    hl = (_c.c_void_p * k)(*[L.handle.value for L in heads])
+    _check(lib().mtp_round(tl, len(layers), hl, k, lm.handle, x.data_ptr(), noise.data_ptr(), eps, wp, wn,
+                           logits.data_ptr(), hout.data_ptr() if hout is not None else None, drafts.data_ptr(),
+                           acc.data_ptr(), acc.data_ptr() + 4, _stream(stream)))
+    return dict(logits=logits, drafts=drafts, accept=acc, head_out=hout)

@@ -30,7 +30,7 @@ size_t large_t_weight_bytes(const moe_layer* L);
 size_t large_t_workspace_bytes(const moe_layer* L);
 int* large_t_status_word(const moe_layer* L);
 int* large_t_counters(const moe_layer* L);
-cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st);
+cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool residual, cudaStream_t st);
 cudaError_t large_t_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm,
                                 cudaStream_t st);
 void large_t_release(moe_layer* L);
@@ -51,6 +51,20 @@ int fail(int code, const char* fmt, ...) {
   g_err = buf;
   return code;
 }
+
+}  // namespace
+
+int moe::set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+namespace {
 
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -385,7 +399,9 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if (sp.ring_bytes < 2 * stage)
     return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has (stage %lld B)", (long long)stage);
   L->smem_bytes = small_t_smem_bytes(sp);
-  CK(small_t_configure(L_limbs, L->smem_bytes), "configure small-T kernel");
+  // the attribute belongs to the kernel, not to this layer: set it to the
+  // device limit, which bounds every layer's plan
+  CK(small_t_configure(L_limbs, max_optin), "configure small-T kernel");
 
   CK(cudaStreamSynchronize(st), "create sync");
   guard.keep = true;
@@ -394,7 +410,10 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   return MOE_OK;
 }
 
-int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
+}  // extern "C"
+
+namespace {
+int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, bool residual) {
   if (!L) return fail(MOE_EINVAL, "moe_forward: NULL layer");
   if (T < 0 || T > L->T_max) return fail(MOE_EINVAL, "moe_forward: T=%d outside 0..%d", T, L->T_max);
   if (T == 0) return MOE_OK;
@@ -408,7 +427,7 @@ int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   L->last_T = T;
   if (T > kMaxSmallT) {
-    CK(large_t_forward(L, x, T, y, st), "moe_forward (tensor-core path)");
+    CK(large_t_forward(L, x, T, y, residual, st), "moe_forward (tensor-core path)");
     return MOE_OK;
   }
   SmallParams P = L->sp;
@@ -417,8 +436,20 @@ int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
   P.n_sh = L->Ish > 0 ? (T + kGroup - 1) / kGroup : 0;
   P.x = x;
   P.y = y;
+  P.residual = residual ? 1 : 0;
   CK(small_t_launch(P, L->act == MOE_ACT_BF16 ? 2 : 4, L->num_sms, L->smem_bytes, st), "moe_forward launch");
   return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
+  return forward_impl(L, x, T, y, stream, false);
+}
+
+int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
+  return forward_impl(L, x, T, y, stream, true);
 }
 
 int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, void* stream) {

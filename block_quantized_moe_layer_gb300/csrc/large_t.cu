@@ -394,7 +394,7 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
 // y[t] = sum_j g[t,j] z[pos[t,j]] + z[T k + t]; one block per token, 8 columns per thread step.
 __global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const float* __restrict__ gates,
                                   const int* __restrict__ pos, int T, int k, int H, bool shared,
-                                  __nv_bfloat16* __restrict__ y) {
+                                  const __nv_bfloat16* __restrict__ xres, __nv_bfloat16* __restrict__ y) {
   const int t = blockIdx.x;
   __shared__ float g[kMaxTopK];
   __shared__ int ps[kMaxTopK];
@@ -415,6 +415,12 @@ __global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const flo
     }
     if (shared) {
       const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)(T * k + t) * H + 8 * c);
+      const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] += __bfloat162float(b[m]);
+    }
+    if (xres) {
+      const uint4 u = *reinterpret_cast<const uint4*>(xres + (int64_t)t * H + 8 * c);
       const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
 #pragma unroll
       for (int m = 0; m < 8; ++m) acc[m] += __bfloat162float(b[m]);
@@ -547,7 +553,7 @@ size_t large_t_workspace_bytes(const moe_layer* L) { return L->lt ? L->lt->ws_by
 int* large_t_status_word(const moe_layer* L) { return L->lt ? L->lt->status : nullptr; }
 int* large_t_counters(const moe_layer* L) { return L->lt ? L->lt->counters : nullptr; }
 
-cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStream_t st) {
+cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool residual, cudaStream_t st) {
   LtState* S = L->lt;
   const int H = L->H, E = L->E, k = L->k;
   const int n_sh = (T + kLtMaxN - 1) / kLtMaxN;
@@ -611,6 +617,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, cudaStr
   LT_CK(lt_gemm_launch(g, grid, st));
 
   lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, T, k, H, L->Ish > 0,
+                                       residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
                                        static_cast<__nv_bfloat16*>(y));
   LT_CK(cudaGetLastError());
   return cudaSuccess;

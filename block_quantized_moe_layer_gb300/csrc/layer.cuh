@@ -55,6 +55,7 @@ struct SmallParams {
   // activations
   const void* x;  // [T, H] bf16 (L = 2) or fp32 (L = 4)
   void* y;        // [T, H] same type
+  int residual;   // 1: y = x + MoE(x)
   // workspace
   Sync* sync;
   int* status;
@@ -101,3 +102,15 @@ struct moe_layer {
   // prefill-sized path (T > kMaxSmallT), present when T_max > kMaxSmallT
   moe::LtState* lt = nullptr;
 };
+
+// Output norm + LM head of the MTP round (lm_head.cu, mtp.cu).
+struct moe_lm_head {
+  int dev = 0, V = 0, H = 0, T_max = 0, act = 0, num_sms = 0;
+  int8_t* q = nullptr;   // [V][H] int8 codes
+  __half* sc = nullptr;  // [V][H/32] fp16 scales
+};
+
+namespace moe {
+// Records a formatted message for moe_last_error() and returns `code` (api.cu).
+int set_error(int code, const char* fmt, ...);
+}  // namespace moe

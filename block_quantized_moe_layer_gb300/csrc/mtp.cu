@@ -1,0 +1,286 @@
+// mtp.cu -- the output head entry points and one MTP draft/verify round.
+//
+// mtp_round sequences, on the caller's stream: the pre-norm residual target
+// blocks, the output norm + LM head on the verify batch, the noisy draft rows,
+// the draft heads, the LM head on the draft rows, their argmax, and greedy
+// acceptance.  Everything runs in this library's kernels; nothing allocates.
+#include "layer.cuh"
+
+namespace moe {
+cudaError_t lm_repack(const uint8_t* src, int8_t* q, __half* sc, int64_t nblocks, cudaStream_t st);
+cudaError_t lm_configure(int H);
+cudaError_t lm_forward(const moe_lm_head* lm, const void* x, int T, float eps, float* logits, cudaStream_t st);
+size_t accept_workspace_bytes(int k, int V);
+
+namespace {
+
+template <int L>
+__device__ __forceinline__ float ld_act(const void* p, int64_t i) {
+  if constexpr (L == 2) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  else return static_cast<const float*>(p)[i];
+}
+template <int L>
+__device__ __forceinline__ float st_act(void* p, int64_t i, float v) {  // returns the stored value
+  if constexpr (L == 2) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    static_cast<__nv_bfloat16*>(p)[i] = b;
+    return __bfloat162float(b);
+  } else {
+    static_cast<float*>(p)[i] = v;
+    return v;
+  }
+}
+
+// Sum over the block (blockDim.x == 256).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < 8; ++w) s += red[w];
+  __syncthreads();
+  return s;
+}
+
+// One row per block: h_out = h_in + y (stored in the act dtype; skipped when
+// y is NULL, h_in is then the row) and xn = rmsnorm(h_out) (act dtype).
+template <int L>
+__global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict__ h_in, const void* __restrict__ y,
+                                                          void* __restrict__ h_out, void* __restrict__ xn, int H,
+                                                          float eps) {
+  __shared__ float red[8];
+  const int64_t base = (int64_t)blockIdx.x * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    float v = ld_act<L>(h_in, base + c);
+    if (y) v = st_act<L>(h_out, base + c, v + ld_act<L>(y, base + c));
+    ss = fmaf(v, v, ss);
+  }
+  __syncthreads();  // h_out written by this block before it is read back
+  const float inv = 1.f / sqrtf(block_sum(ss, red) / (float)H + eps);
+  const void* src = y ? h_out : h_in;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) st_act<L>(xn, base + c, ld_act<L>(src, base + c) * inv);
+}
+
+// Block (j, i), i <= j: v = h[i] + noise[j][i]; hin[j][i] = rmsnorm(v) (the
+// head's input) and, for i == j, rows[j] = v (the row the draft is read from).
+template <int L>
+__global__ void __launch_bounds__(256) draft_rows_kernel(const void* __restrict__ h, const float* __restrict__ noise,
+                                                         int k, int H, float eps, void* __restrict__ hin,
+                                                         void* __restrict__ rows) {
+  __shared__ float red[8];
+  const int j = blockIdx.x / k, i = blockIdx.x % k;
+  if (i > j) return;
+  const int64_t src = (int64_t)i * H, nz = ((int64_t)j * k + i) * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = ld_act<L>(h, src + c) + noise[nz + c];
+    ss = fmaf(v, v, ss);
+    if (i == j) st_act<L>(rows, (int64_t)j * H + c, v);
+  }
+  const float inv = 1.f / sqrtf(block_sum(ss, red) / (float)H + eps);
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    st_act<L>(hin, nz + c, (ld_act<L>(h, src + c) + noise[nz + c]) * inv);
+}
+
+// ids[r] = argmax of row r (lowest index on ties); one CTA per row.
+__global__ void argmax_rows_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids) {
+  __shared__ float sv[8];
+  __shared__ int si[8];
+  const float* row = logits + (int64_t)blockIdx.x * V;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    const float v = row[c];
+    if (v > bv || bi == 0x7fffffff) { bv = v; bi = c; }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x / 32); ++w)
+      if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
+    ids[blockIdx.x] = bi;
+  }
+}
+
+size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+struct RoundLayout {
+  size_t hA, hB, xn, ytmp, hin, hout, rows, dlog, acc, total;
+};
+RoundLayout round_layout(int H, int k, int V, int act) {
+  const size_t esz = act == MOE_ACT_BF16 ? 2 : 4;
+  RoundLayout r{};
+  size_t off = 0;
+  auto take = [&](size_t b) { const size_t o = off; off = al256(off + b); return o; };
+  r.acc = take(accept_workspace_bytes(k, V));  // must stay zero between calls: first
+  r.hA = take((size_t)(k + 1) * H * esz);
+  r.hB = take((size_t)(k + 1) * H * esz);
+  r.xn = take((size_t)(k + 1) * H * esz);
+  r.ytmp = take((size_t)(k + 1) * H * esz);
+  r.hin = take((size_t)k * k * H * esz);
+  r.hout = take((size_t)k * k * H * esz);
+  r.rows = take((size_t)k * H * esz);
+  r.dlog = take((size_t)k * V * 4);
+  r.total = off;
+  return r;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+#define MCK(call, what)                                                                      \
+  do {                                                                                       \
+    cudaError_t e_ = (call);                                                                 \
+    if (e_ != cudaSuccess) return set_error(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e_)); \
+  } while (0)
+
+extern "C" {
+
+int moe_lm_head_create(const moe_tensor* w, int32_t T_max, int32_t act_dtype, void* stream, moe_lm_head** out) {
+  if (!w || !out) return set_error(MOE_EINVAL, "moe_lm_head_create: NULL argument");
+  if (w->fmt != MOE_Q8_0) return set_error(MOE_EFORMAT, "moe_lm_head_create: the output matrix must be Q8_0");
+  if (w->reserved != 0) return set_error(MOE_EINVAL, "moe_lm_head_create: reserved field must be 0");
+  const int64_t V = w->rows, H = w->cols;
+  if (V < 1 || V > (1 << 24) || H <= 0 || H % 512 || H > 16384)
+    return set_error(MOE_EINVAL, "moe_lm_head_create: shape [V, H] must have 1 <= V <= 2^24, H a multiple of 512 <= 16384");
+  if (T_max < 1 || T_max > 8) return set_error(MOE_EINVAL, "moe_lm_head_create: T_max outside 1..8");
+  if (act_dtype != MOE_ACT_BF16 && act_dtype != MOE_ACT_F32) return set_error(MOE_EINVAL, "moe_lm_head_create: act_dtype");
+  if (!w->data || w->nbytes != (size_t)V * (H / 32) * 34)
+    return set_error(MOE_EINVAL, "moe_lm_head_create: data NULL or nbytes != V * H / 32 * 34");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe_lm_head* lm = new moe_lm_head();
+  lm->V = (int)V;
+  lm->H = (int)H;
+  lm->T_max = T_max;
+  lm->act = act_dtype;
+  uint8_t* staged = nullptr;
+  auto cleanup = [&](int rc) {
+    if (staged) cudaFree(staged);
+    if (rc != MOE_OK) moe_lm_head_destroy(lm);
+    return rc;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&lm->dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&lm->num_sms, cudaDevAttrMultiProcessorCount, lm->dev)) != cudaSuccess)
+    return cleanup(set_error(MOE_ECUDA, "%s", cudaGetErrorString(e)));
+  if ((e = cudaMalloc(&lm->q, (size_t)V * H)) != cudaSuccess ||
+      (e = cudaMalloc(&lm->sc, (size_t)V * (H / 32) * 2)) != cudaSuccess)
+    return cleanup(set_error(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s", cudaGetErrorString(e)));
+  cudaPointerAttributes pa{};
+  const uint8_t* src = static_cast<const uint8_t*>(w->data);
+  if (cudaPointerGetAttributes(&pa, w->data) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    if ((e = cudaMalloc(&staged, w->nbytes)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(staged, w->data, w->nbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+      return cleanup(set_error(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s", cudaGetErrorString(e)));
+    src = staged;
+  }
+  if ((e = lm_repack(src, lm->q, lm->sc, V * (H / 32), st)) != cudaSuccess || (e = lm_configure((int)H)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return cleanup(set_error(MOE_ECUDA, "%s", cudaGetErrorString(e)));
+  *out = lm;
+  return cleanup(MOE_OK);
+}
+
+int moe_lm_head_forward(moe_lm_head* lm, const void* x, int32_t T, float eps, float* logits, void* stream) {
+  if (!lm) return set_error(MOE_EINVAL, "moe_lm_head_forward: NULL head");
+  if (T < 0 || T > lm->T_max) return set_error(MOE_EINVAL, "moe_lm_head_forward: T outside 0..T_max");
+  if (T == 0) return MOE_OK;
+  if (!x || !logits) return set_error(MOE_EINVAL, "moe_lm_head_forward: NULL x or logits");
+  if (reinterpret_cast<uintptr_t>(x) & 15) return set_error(MOE_EINVAL, "moe_lm_head_forward: x must be 16-byte aligned");
+  if (!(eps >= 0.f)) return set_error(MOE_EINVAL, "moe_lm_head_forward: eps must be >= 0");
+  cudaError_t e = lm_forward(lm, x, T, eps, logits, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error(MOE_ECUDA, "moe_lm_head_forward: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+void moe_lm_head_destroy(moe_lm_head* lm) {
+  if (!lm) return;
+  cudaFree(lm->q);
+  cudaFree(lm->sc);
+  delete lm;
+}
+
+size_t mtp_round_workspace_bytes(int32_t H, int32_t k, int32_t V, int32_t act_dtype) {
+  if (H <= 0 || k < 1 || k > 7 || V < 1 || V > (1 << 24) || (act_dtype != MOE_ACT_BF16 && act_dtype != MOE_ACT_F32))
+    return 0;
+  return round_layout(H, k, V, act_dtype).total;
+}
+
+int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* const* draft_heads, int32_t k,
+              moe_lm_head* lm, const void* x, const float* noise, float eps, void* workspace,
+              size_t workspace_bytes, float* target_logits, void* head_out, int32_t* draft_ids,
+              int32_t* out_n_accepted, int32_t* out_next_token, void* stream) {
+  if (k < 1 || k > 7) return set_error(MOE_EINVAL, "mtp_round: k outside 1..7");
+  if (n_target < 0 || (n_target > 0 && !target_layers) || !draft_heads || !lm || !x || !noise || !workspace ||
+      !target_logits || !draft_ids || !out_n_accepted || !out_next_token)
+    return set_error(MOE_EINVAL, "mtp_round: NULL argument");
+  const int H = lm->H, act = lm->act, V = lm->V;
+  if (lm->T_max < k + 1) return set_error(MOE_EINVAL, "mtp_round: the LM head's T_max is below k+1");
+  for (int l = 0; l < n_target; ++l) {
+    const moe_layer* L = target_layers[l];
+    if (!L || L->H != H || L->act != act || L->T_max < k + 1)
+      return set_error(MOE_EINVAL, "mtp_round: target layer %d: NULL, or H / act_dtype / T_max mismatch", l);
+  }
+  for (int j = 0; j < k; ++j) {
+    const moe_layer* L = draft_heads[j];
+    if (!L || L->H != H || L->act != act || L->T_max < j + 1)
+      return set_error(MOE_EINVAL, "mtp_round: draft head %d: NULL, or H / act_dtype / T_max mismatch", j);
+  }
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(head_out)) & 15)
+    return set_error(MOE_EINVAL, "mtp_round: x and head_out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return set_error(MOE_EINVAL, "mtp_round: workspace must be 256-byte aligned");
+  const RoundLayout r = round_layout(H, k, V, act);
+  if (workspace_bytes < r.total) return set_error(MOE_EINVAL, "mtp_round: workspace %zu bytes, need %zu", workspace_bytes, r.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const size_t esz = act == MOE_ACT_BF16 ? 2 : 4;
+  int rc;
+  // target stack: pre-norm residual blocks h <- h + MoE(rmsnorm(h)); the
+  // hidden state ping-pongs between hA and hB, xn holds the normalised rows
+  const void* cur = x;
+  void* xn = w + r.xn;
+  void* yt = w + r.ytmp;
+  if (act == MOE_ACT_BF16) add_rmsnorm_kernel<2><<<k + 1, 256, 0, st>>>(x, nullptr, nullptr, xn, H, eps);
+  else add_rmsnorm_kernel<4><<<k + 1, 256, 0, st>>>(x, nullptr, nullptr, xn, H, eps);
+  MCK(cudaGetLastError(), "mtp_round: norm");
+  for (int l = 0; l < n_target; ++l) {
+    void* out = w + ((l & 1) ? r.hB : r.hA);
+    if ((rc = moe_forward(target_layers[l], xn, k + 1, yt, stream))) return rc;
+    if (act == MOE_ACT_BF16) add_rmsnorm_kernel<2><<<k + 1, 256, 0, st>>>(cur, yt, out, xn, H, eps);
+    else add_rmsnorm_kernel<4><<<k + 1, 256, 0, st>>>(cur, yt, out, xn, H, eps);
+    MCK(cudaGetLastError(), "mtp_round: residual + norm");
+    cur = out;
+  }
+  if ((rc = moe_lm_head_forward(lm, cur, k + 1, eps, target_logits, stream))) return rc;
+  // noisy rows for the heads, and the rows the drafts are read from
+  if (act == MOE_ACT_BF16)
+    draft_rows_kernel<2><<<k * k, 256, 0, st>>>(cur, noise, k, H, eps, w + r.hin, w + r.rows);
+  else
+    draft_rows_kernel<4><<<k * k, 256, 0, st>>>(cur, noise, k, H, eps, w + r.hin, w + r.rows);
+  MCK(cudaGetLastError(), "mtp_round: draft rows");
+  uint8_t* hout = head_out ? static_cast<uint8_t*>(head_out) : w + r.hout;
+  for (int j = 0; j < k; ++j) {
+    const size_t o = (size_t)j * k * H * esz;
+    if ((rc = moe_forward(draft_heads[j], w + r.hin + o, j + 1, hout + o, stream))) return rc;
+  }
+  float* dlog = reinterpret_cast<float*>(w + r.dlog);
+  if ((rc = moe_lm_head_forward(lm, w + r.rows, k, eps, dlog, stream))) return rc;
+  argmax_rows_kernel<<<k, 256, 0, st>>>(dlog, V, draft_ids);
+  MCK(cudaGetLastError(), "mtp_round: draft argmax");
+  return mtp_verify_accept(draft_ids, k, target_logits, V, out_n_accepted, out_next_token, w + r.acc,
+                           accept_workspace_bytes(k, V), stream);
+}
+
+}  // extern "C"

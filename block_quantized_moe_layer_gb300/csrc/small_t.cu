@@ -1001,6 +1001,10 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
     for (int j = 0; j < kMaxTopK; ++j)
       if (j < k) acc = fmaf(sg[t * k + j], zv[j], acc);
     acc += zs;
+    if (P.residual) {
+      if constexpr (L == 2) acc += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + r]);
+      else acc += reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + r];
+    }
     if constexpr (L == 2) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + r] = __float2bfloat16_rn(acc);
     else reinterpret_cast<float*>(P.y)[(int64_t)t * P.H + r] = acc;
   }

@@ -133,3 +133,53 @@ def noise(seed: int, head: int, shape, std, device="cpu") -> torch.Tensor:
 
 def with_T(w: Workload, T: int) -> Workload:
     return replace(w, T=T)
+
+
+@dataclass(frozen=True)
+class RoundWorkload:
+    """One MTP draft/verify round: k drafts (verify batch k + 1), target
+    layers, k draft heads (head j runs at T = j + 1), a Q8_0 LM head [V, H]
+    and the draft noise std ("Support Step3.5/3.7 flash mtp3", "Overview":
+    three chained heads, a four-row verify batch)."""
+    name: str
+    seed: int
+    k: int
+    V: int
+    layers: Tuple[Workload, ...]
+    heads: Tuple[Workload, ...]
+    lm_std: float = 0.02
+    noise_std: float = 0.05
+
+
+def round_workload(name, seed, H, E, top_k, I, I_sh, k=3, n_layers=8, V=32768, bias_std=0.5, q8_layers=(0, 7),
+                   noise_std=0.05) -> RoundWorkload:
+    """Target layers in the mixed recipe (routed Q4KS, shared Q8_0) except
+    ``q8_layers`` (all Q8_0); draft heads in the mixed recipe."""
+    layers = tuple(Workload(f"{name}_L{l}", seed * 100 + l, T=k + 1, H=H, E=E, top_k=top_k, I=I, I_shared=I_sh,
+                            bias_std=bias_std, routed_fmt=FMT_Q8_0 if l in q8_layers else FMT_Q4KS)
+                   for l in range(n_layers))
+    heads = tuple(Workload(f"{name}_D{j}", seed * 100 + 50 + j, T=j + 1, H=H, E=E, top_k=top_k, I=I, I_shared=I_sh,
+                           bias_std=bias_std, routed_fmt=FMT_Q4KS) for j in range(k))
+    return RoundWorkload(name, seed, k, V, layers, heads, noise_std=noise_std)
+
+
+ROUNDS = {
+    # the Step-5-shaped round: 8 target layers, 3 heads, vocab 32768
+    "mtp_round": round_workload("mtp_round", 4, 4096, 352, 8, 1280, 1280),
+    # a small round for full comparisons
+    "tiny_round": round_workload("tiny_round", 5, 512, 16, 2, 256, 256, n_layers=3, V=1000, q8_layers=(0,)),
+}
+
+
+def lm_weight(r: RoundWorkload, device="cpu") -> torch.Tensor:
+    """fp32 [V, H] LM head weights N(0, lm_std^2)."""
+    return normal((r.V, r.layers[0].H), r.lm_std, device, (r.seed * 1_000_003 + _LM * 65_537 + 12_345) & 0x7FFF_FFFF_FFFF)
+
+
+def round_inputs(r: RoundWorkload, device="cpu", variant: int = 0):
+    """(x bf16 [k+1, H], noise fp32 [k, k, H]): the verify batch and, for head j,
+    rows 0..j of noise[j]."""
+    x = activations(r.layers[0], device, T=r.k + 1, variant=variant)
+    H = r.layers[0].H
+    nz = torch.stack([noise(r.seed + 1000 * variant, j, (r.k, H), r.noise_std, device) for j in range(r.k)])
+    return x, nz

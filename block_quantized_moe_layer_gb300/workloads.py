@@ -6,7 +6,7 @@ are freed afterwards.
 """
 import torch
 
-from . import FMT_F32, Layer, quantize, synth
+from . import FMT_F32, FMT_Q8_0, Layer, LmHead, quantize, synth
 
 
 def synthetic_layer(w: synth.Workload, act, T_max=None, device="cuda", keep_serialised=False):
@@ -34,3 +34,21 @@ def synthetic_layer(w: synth.Workload, act, T_max=None, device="cuda", keep_seri
     del experts, shared
     torch.cuda.synchronize()
     return L, None
+
+
+def synthetic_lm_head(r: synth.RoundWorkload, act, T_max=8, device="cuda"):
+    """LmHead for round workload ``r`` (weights drawn on the device, Q8_0)."""
+    w = synth.lm_weight(r, device)
+    q = quantize(FMT_Q8_0, w)
+    del w
+    lm = LmHead(q, r.V, r.layers[0].H, T_max, act)
+    del q
+    torch.cuda.synchronize()
+    return lm
+
+
+def synthetic_round(r: synth.RoundWorkload, act, device="cuda"):
+    """(target layers, draft heads, LM head) for round workload ``r``."""
+    layers = [synthetic_layer(w, act, T_max=r.k + 1, device=device)[0] for w in r.layers]
+    heads = [synthetic_layer(w, act, T_max=j + 1, device=device)[0] for j, w in enumerate(r.heads)]
+    return layers, heads, synthetic_lm_head(r, act, T_max=r.k + 1, device=device)

@@ -111,6 +111,12 @@ int moe_layer_create(const moe_layer_desc* desc, void* stream, moe_layer** out);
  * Device-side wait failures are reported by moe_layer_status(). */
 int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
 
+/* y = x + MoE(x): a residual layer (the target stack of an MTP round,
+ * "Support Step3.5/3.7 flash mtp3", "Overview" step 2).  Same arguments,
+ * rules and errors as moe_forward; the sum is formed in fp32 and rounded
+ * once to the act_dtype. */
+int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
+
 /* Copies the routing of the last moe_forward (device-to-device, async on
  * `stream`): ids int32 [T, k] and gates fp32 [T, k] in slot order, offsets
  * int32 [E+1], perm int32 [T*k] (pair ids t*k+j grouped by expert, ascending
@@ -179,6 +185,48 @@ int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, 
  *   e.g. by issuing them on one stream. */
 int mtp_verify_accept_noalloc(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V,
                               int32_t* out_n_accepted, int32_t* out_next_token, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Output head and one MTP draft/verify round.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_lm_head moe_lm_head;
+
+/* Uploads a Q8_0 output matrix w [V, H] ("Step-5 Preview GGUF", "Precision
+ * distribution" table: the main output matrix is Q8_0); `w.data` may be a
+ * host or device pointer and is read only during the call (which
+ * synchronises `stream`).  1 <= V <= 2^24, H a positive multiple of 512 and
+ * at most 16384, 1 <= T_max <= 8.  act_dtype (moe_act) is the type of the
+ * rows forward() is given.  Errors: MOE_EINVAL, MOE_EFORMAT (w not Q8_0 or
+ * wrong shape), MOE_ENOMEM, MOE_ECUDA. */
+int moe_lm_head_create(const moe_tensor* w, int32_t T_max, int32_t act_dtype, void* stream, moe_lm_head** out);
+
+/* logits fp32 [T, V] = w . rmsnorm(x) for x [T, H] in the head's act_dtype,
+ * rmsnorm(v) = v / sqrt(mean(v^2) + eps) (weight 1; the output norm before
+ * the LM head).  0 <= T <= T_max; x 16-byte aligned; asynchronous. */
+int moe_lm_head_forward(moe_lm_head* lm, const void* x, int32_t T, float eps, float* logits, void* stream);
+void moe_lm_head_destroy(moe_lm_head* lm);
+
+/* One MTP draft/verify round on synthetic weights, the reading of
+ * "Support Step3.5/3.7 flash mtp3", "Overview" steps 1-6 used by this
+ * library (the pages give the data flow, not a synthetic model):
+ *   h_0 = x (the verify batch [k+1, H]); h_{l+1} = h_l + MoE_l(rmsnorm(h_l))
+ *   for the n_target layers (pre-norm residual blocks); logits = lm(h_n)
+ *   (output norm + LM head), written to target_logits fp32 [k+1, V];
+ *   head j (j < k) runs on rmsnorm of the j+1 rows h~_j = h_n[0..j] +
+ *   noise[j][0..j] (the noise stands in for an imperfect draft model) and
+ *   writes head_out[j] ([k][k][H], rows 0..j used; may be NULL to discard);
+ *   draft_ids[j] = argmax (lowest id on ties) of lm(h~_j[j]);
+ *   then greedy acceptance as mtp_verify_accept.
+ * Every layer and the head must share act_dtype; all layers have hidden H,
+ * T_max >= k+1.  noise fp32 [k][k][H] (device).  1 <= k <= 7.
+ * workspace: device scratch of mtp_round_workspace_bytes(H, k, V, act)
+ * bytes, 256-byte aligned, zero-filled before its first use and left so.
+ * Asynchronous; no allocation.  Errors: MOE_EINVAL on any mismatch. */
+size_t mtp_round_workspace_bytes(int32_t H, int32_t k, int32_t V, int32_t act_dtype);
+int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* const* draft_heads, int32_t k,
+              moe_lm_head* lm, const void* x, const float* noise, float eps, void* workspace,
+              size_t workspace_bytes, float* target_logits, void* head_out, int32_t* draft_ids,
+              int32_t* out_n_accepted, int32_t* out_next_token, void* stream);
 
 /* Message for the last error on the calling thread; valid until the next
  * call on that thread.  Never NULL. */

@@ -12,15 +12,17 @@ GGUF", "Precision distribution" table: the main output matrix is Q8_0.
 
 The pages give the data flow but no synthetic model, so the round here is a
 reading of it, with every step a plain definition:
-  target      h_0 = x (the [k+1, H] verify batch); h_{l+1} = h_l + MoE_l(h_l)
-              for the L target layers (residual layers, no inner norm);
-              h_tgt = h_L
+  target      h_0 = x (the [k+1, H] verify batch); h_{l+1} = h_l +
+              MoE_l(rmsnorm(h_l)) for the L target layers (pre-norm residual
+              blocks: without the norm the SwiGLU, quadratic in its input,
+              makes the synthetic stack's hidden state grow by orders of
+              magnitude per layer); h_tgt = h_L
   logits      logits = W_lm . rmsnorm(h) with rmsnorm(v) = v / sqrt(mean(v^2) + eps)
               (weight 1), W_lm a Q8_0 matrix [V, H]
-  drafts      head j (j = 0..k-1) is one MoE layer run on the j+1 rows
-              h~_j = h_tgt[0..j] + noise[j][0..j] (the noise stands in for an
-              imperfect draft model: it is what makes drafts differ from the
-              target); its output is computed and compared as a layer output;
+  drafts      head j (j = 0..k-1) is one MoE layer run on rmsnorm of the j+1
+              rows h~_j = h_tgt[0..j] + noise[j][0..j] (the noise stands in
+              for an imperfect draft model: it is what makes drafts differ from
+              the target); its output is computed and compared as a layer output;
               draft token d_{j+1} = argmax W_lm . rmsnorm(h~_j[j])
   acceptance  greedy: oracle.accept.greedy_accept(d_1..d_k, logits)
 Since drafts are a function of the target's hidden states here, the target
@@ -46,11 +48,11 @@ def lm_logits(h, lm: moe.QTensor, eps=1e-6):
     return rmsnorm(h, eps) @ lm.dense().T
 
 
-def target_stack(x, layers):
-    """h_tgt for the verify batch x [T, H] through residual MoE layers."""
+def target_stack(x, layers, eps=1e-6):
+    """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers."""
     h = np.asarray(x, F64)
     for L in layers:
-        y, _ = moe.forward(h, L)
+        y, _ = moe.forward(rmsnorm(h, eps), L)
         h = h + y
     return h
 
@@ -63,12 +65,12 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6):
     k = len(heads)
     x = np.asarray(x, F64)
     assert x.shape[0] == k + 1
-    h_tgt = target_stack(x, layers)
+    h_tgt = target_stack(x, layers, eps)
     logits = lm_logits(h_tgt, lm, eps)
     head_out, rows = [], []
     for j, head in enumerate(heads):
         ht = h_tgt[: j + 1] + np.asarray(noise[j][: j + 1], F64)
-        y, _ = moe.forward(ht, head)
+        y, _ = moe.forward(rmsnorm(ht, eps), head)
         head_out.append(y)
         rows.append(ht[j])
     rows = np.stack(rows) if rows else np.zeros((0, x.shape[1]))

@@ -55,10 +55,14 @@ def test_target_stack_residual():
     zero = _layer(3, zero=True)
     assert np.array_equal(mtp.target_stack(x, [zero, zero]), x)  # zero experts: h stays x
     L = _layer(4)
-    y, _ = moe.forward(x, L)
+    y, _ = moe.forward(mtp.rmsnorm(x), L)
     assert np.allclose(mtp.target_stack(x, [L]), x + y, rtol=0, atol=0)
-    y2, _ = moe.forward(x + y, L)
+    y2, _ = moe.forward(mtp.rmsnorm(x + y), L)
     assert np.allclose(mtp.target_stack(x, [L, L]), x + y + y2, rtol=0, atol=0)
+    # the blocks see normalised inputs: scaling x by 4 (exact in binary, eps 0)
+    # scales the skip path only
+    y0, _ = moe.forward(mtp.rmsnorm(x, eps=0.0), L)
+    assert np.allclose(mtp.target_stack(4.0 * x, [L], eps=0.0) - 4.0 * x, y0, rtol=1e-12, atol=1e-12)
 
 
 def _round(noise_scale, k=3, seed=5):
@@ -91,7 +95,7 @@ def test_round_draft_rows_are_normalised():
 def test_round_head_outputs_and_acceptance():
     r, x, layers, heads, lm, noise = _round(3.0)
     for j in range(3):
-        y, _ = moe.forward(r["h_tgt"][: j + 1] + noise[j][: j + 1], heads[j])
+        y, _ = moe.forward(mtp.rmsnorm(r["h_tgt"][: j + 1] + noise[j][: j + 1]), heads[j])
         assert np.allclose(r["head_out"][j], y, rtol=0, atol=0)
     # the acceptance is the greedy rule on the drafts and the target logits
     n = 0
