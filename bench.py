@@ -39,7 +39,9 @@ def parse():
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--workload", default="verify_q8")
-    p.add_argument("--copies", type=int, default=4)
+    p.add_argument("--copies", type=int, default=None,
+                   help="weight copies rotated in the timed loop (default 4 for T <= 8, 1 above: one layer then "
+                        "touches every expert, far more than L2)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=2000)
@@ -164,11 +166,14 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    if args.workload in synth.ROUNDS:
+        return run_round(args)
     w = synth.WORKLOADS[args.workload]
     if args.experts:
         import dataclasses
         w = dataclasses.replace(w, E=args.experts)
-    layers = [synthetic_layer(w, pkg.ACT_BF16, T_max=w.T)[0] for _ in range(args.copies)]
+    copies = args.copies if args.copies is not None else (4 if w.T <= 8 else 1)
+    layers = [synthetic_layer(w, pkg.ACT_BF16, T_max=w.T)[0] for _ in range(copies)]
     x = synth.activations(w, "cuda")
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -237,8 +242,9 @@ def run_ours(args):
 
     peak, peak_src = measured_peaks()
     achieved = alg / (kern_us * 1e-6) / 1e9
-    src = os.path.join(ROOT, "block_quantized_moe_layer_gb300", "csrc", "small_t.cu")
+    src = os.path.join(ROOT, "block_quantized_moe_layer_gb300", "csrc", "small_t.cu" if w.T <= 8 else "gemm_tc.cu")
     tr = traffic_record(src)
+    kname = "moe_small_t_kernel" if w.T <= 8 else "moe_forward (8 launches; the grouped tcgen05 GEMMs dominate)"
     out = {
         "metric": METRIC,
         "value": round(us_per_layer, 3),
@@ -264,12 +270,16 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": tr["bytes_per_launch"] if tr else None,
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "moe_small_t_kernel", "kernel_us": round(kern_us, 3)},
+                     "kernel": kname, "kernel_us": round(kern_us, 3)},
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (1 if w.T <= 8 else 8),
     }
+    if w.T > 8:
+        flops = 2.0 * w.T * (w.top_k * 3 * w.H * w.I + 3 * w.H * w.I_shared + w.H * w.E)
+        out["tensor"] = {"useful_tflops": round(flops / (us_per_layer * 1e-6) / 1e12, 1),
+                         "note": "useful FLOPs (routed + shared + router) / layer time"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, n = cpu_baseline_sample(w)
         out["cpu_baseline"] = {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(),
@@ -284,12 +294,117 @@ def run_ours(args):
         print(json.dumps(out))
 
 
+def run_round(args):
+    """One MTP draft/verify round per step (8 target layers, 3 draft heads, two
+    LM-head passes, acceptance) through the mtp_round C call."""
+    import ctypes
+    import torch
+    import block_quantized_moe_layer_gb300 as pkg
+    from block_quantized_moe_layer_gb300 import synth
+    from block_quantized_moe_layer_gb300.workloads import synthetic_round
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    r = synth.ROUNDS[args.workload]
+    layers, heads, lm = synthetic_round(r, pkg.ACT_BF16)
+    x, noise = synth.round_inputs(r, "cuda")
+    H, V, k = lm.H, lm.V, r.k
+    ws = pkg.round_workspace(H, k, V, pkg.ACT_BF16)
+    wp, wn = pkg._aligned(ws)
+    logits = torch.empty(k + 1, V, dtype=torch.float32, device="cuda")
+    drafts = torch.empty(k, dtype=torch.int32, device="cuda")
+    acc = torch.empty(2, dtype=torch.int32, device="cuda")
+    tl = (ctypes.c_void_p * len(layers))(*[L.handle.value for L in layers])
+    hl = (ctypes.c_void_p * k)(*[L.handle.value for L in heads])
+    stream = torch.cuda.current_stream()
+    lib = pkg.lib()
+
+    def step(xd, nd):
+        rc = lib.mtp_round(tl, len(layers), hl, k, lm.handle, xd.data_ptr(), nd.data_ptr(), 1e-6, wp, wn,
+                           logits.data_ptr(), None, drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4,
+                           stream.cuda_stream)
+        if rc:
+            raise RuntimeError(lib.moe_last_error().decode())
+    for _ in range(max(args.warmup, 3)):
+        step(x, noise)
+    torch.cuda.synchronize()
+    for L in layers + heads:
+        L.status()
+    # algorithmic bytes of one round: each layer's router, unique experts and
+    # shared expert at its batch size, plus two LM-head passes
+    alg = 0
+    for L, wl in list(zip(layers, r.layers)) + list(zip(heads, r.heads)):
+        offs = L.routing(wl.T)[2]
+        alg += algorithmic_bytes(wl, int((offs[1:] > offs[:-1]).sum().item()))
+    alg += 2 * V * (H // 32) * 34
+    steps = min(args.steps, 500)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        step(x, noise)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    us = t0.elapsed_time(t1) * 1e3 / steps
+    xh, nh = x.cpu().pin_memory(), noise.cpu().pin_memory()
+    ah = torch.empty(2, dtype=torch.int32).pin_memory()
+    dh = torch.empty(k, dtype=torch.int32).pin_memory()
+    xd, nd = torch.empty_like(x), torch.empty_like(noise)
+    e2e_steps = min(args.e2e_steps, steps)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        nd.copy_(nh, non_blocking=True)
+        step(xd, nd)
+        ah.copy_(acc, non_blocking=True)
+        dh.copy_(drafts, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e = t0.elapsed_time(t1) * 1e3 / e2e_steps
+    peak, peak_src = measured_peaks()
+    out = {
+        "metric": "µs per MTP draft/verify round (8 target layers T=4, draft heads T=1,2,3, 2 LM-head passes, "
+                  "acceptance) and effective HBM GB/s",
+        "value": round(us, 2), "unit": "us/round", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "q8_0/q4ks weights x bf16 activations (int dp4a, fp32 accumulate)",
+        "data": "synthetic (seeded, random-init weights of the workload's shapes)",
+        "config": {"workload": r.name, "k": k, "V": V, "H": H, "target_layers": len(layers),
+                   "algorithmic_bytes": alg, "n_accepted_last": int(acc[0].item())},
+        "effective_gbs": round(alg / (us * 1e-6) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(alg / (us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4),
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "mtp_round (whole round)"},
+        "clocks": clk,
+        "e2e": {"value": round(e2e, 2), "unit": "us/round",
+                "h2d_bytes_per_step": x.numel() * x.element_size() + noise.numel() * noise.element_size(),
+                "d2h_bytes_per_step": 4 * (2 + k), "steps": e2e_steps},
+        # per round: a layer launch and a residual/norm launch per target layer, the
+        # first norm, two LM-head launches, draft rows, the heads, argmax, acceptance
+        "gpu_launches": steps * (2 * len(layers) + len(heads) + 6),
+    }
+    for L in layers + heads:
+        L.close()
+    lm.close()
+    if rank == 0:
+        print(json.dumps(out))
+
+
 def run_reference(args):
     """The oracle on bounded samples of the workload: each step runs the
     oracle's routing for the batch plus the FFN of a slice of the touched
     row blocks; µs/layer is extrapolated from time per row block."""
     rank, world, _ = dist_env()
     if rank != 0:
+        return
+    from block_quantized_moe_layer_gb300 import synth as _synth
+    if args.workload in _synth.ROUNDS:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-layer workloads only"}))
         return
     import torch
     from oracle import moe as omoe
