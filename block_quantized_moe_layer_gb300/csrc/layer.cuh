@@ -15,7 +15,9 @@ struct Entry {
   int slot0;
   int M;
   int tok[kGroup];
+  int pad;  // 32 bytes: copied with 16-byte loads
 };
+static_assert(sizeof(Entry) == 32, "Entry is copied as two 16-byte vectors");
 
 // Cross-CTA counters of the fused kernel.  All zero between launches: the
 // last CTA to leave resets them.

@@ -190,9 +190,19 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         if (!wait_flag_geq(&P.sync->routing_ready, 1, P.timeout_ns, P.status, kSiteRouting, t)) { ok = false; break; }
         fence_proxy_async_global();
         n_rent = __ldcg(&P.sync->n_rent);
-        const int* src = reinterpret_cast<const int*>(P.entries + P.n_sh);
-        int* dst = reinterpret_cast<int*>(ecache + P.n_sh);
-        for (int i = 0; i < n_rent * (int)(sizeof(Entry) / 4); ++i) dst[i] = __ldcg(src + i);
+        // 16-byte loads, eight in flight at a time
+        const int4* src = reinterpret_cast<const int4*>(P.entries + P.n_sh);
+        int4* dst = reinterpret_cast<int4*>(ecache + P.n_sh);
+        const int nv = n_rent * (int)(sizeof(Entry) / 16);
+        for (int i = 0; i < nv; i += 8) {
+          int4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (i + u < nv) v[u] = __ldcg(src + i + u);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (i + u < nv) dst[i + u] = v[u];
+        }
       }
       const int A = NR + NSG + NSD;
       const int NG = n_rent * P.n_gu, ND = n_rent * P.n_dt;
@@ -413,9 +423,9 @@ __device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float
 // plus one record read per warp.  acc[r][m] collects this lane's share of
 // row r's dot product with vector m; the lanes are summed when the row group
 // is complete.
-template <int L>
-__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M,
-                                           float (&acc)[kRowsPerWarp][kGroup]) {
+template <int L, int M>
+__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int fmt,
+                                             float (&acc)[kRowsPerWarp][kGroup]) {
   constexpr int RB = rec_bytes(L);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r0 = warp * kRowsPerWarp;
@@ -432,8 +442,8 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fm
         dq[r] = __half2float(sc[(r0 + r) * nbc + b]);
       }
 #pragma unroll
-      for (int m = 0; m < kGroup; ++m) {
-        if (m < M) {
+      for (int m = 0; m < M; ++m) {
+        {
           const uint8_t* rec = A + (m * nbc + b) * RB;
           const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
 #pragma unroll
@@ -442,7 +452,7 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fm
       }
     }
   } else {  // MOE_Q4KS
-    const uint8_t* hdr = stage + nbc * 512;
+    const uint8_t* hdr = stage + nbc * 512;  // (M is a compile-time count: the token loops unroll fully)
     const int nsup = nbc / 8;
     for (int b = lane; b < nbc; b += 32) {
       uint4 qv[kRowsPerWarp];
@@ -454,8 +464,8 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fm
         q4_scales(hd, b & 7, sa[r], sb[r]);
       }
 #pragma unroll
-      for (int m = 0; m < kGroup; ++m) {
-        if (m < M) {
+      for (int m = 0; m < M; ++m) {
+        {
           const uint8_t* rec = A + (m * nbc + b) * RB;
           const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
           const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
@@ -468,6 +478,20 @@ __device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fm
         }
       }
     }
+  }
+}
+
+// The token count of a stage as a compile-time constant, so the loops over
+// tokens unroll without predicates (a runtime bound there keeps the loads of
+// different tokens from being scheduled together).
+template <int L>
+__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M,
+                                           float (&acc)[kRowsPerWarp][kGroup]) {
+  switch (M) {
+    case 1: gemv_chunk_m<L, 1>(stage, nbc, fmt, acc); break;
+    case 2: gemv_chunk_m<L, 2>(stage, nbc, fmt, acc); break;
+    case 3: gemv_chunk_m<L, 3>(stage, nbc, fmt, acc); break;
+    default: gemv_chunk_m<L, kGroup>(stage, nbc, fmt, acc); break;
   }
 }
 
@@ -712,6 +736,44 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   }
 }
 
+// Router tile dot products: lane = expert row, warp w takes float4 columns
+// w, w + 8, ... of the slice; T tokens (compile time), four independent
+// accumulators per token (one per float4 component).
+template <int L, int T>
+__device__ __forceinline__ void router_dot(const float4* wst, const uint8_t* xs, int cols, float (&racc)[kMaxSmallT]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float ra[T][4];
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) ra[t][c] = 0.f;
+  const int ncol4 = cols / 4;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int k4 = warp + kConsumerWarps * i;
+    if (k4 < ncol4) {
+      const float4 w = wst[k4 * 32 + lane];
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float4 xv;
+        if constexpr (L == 2) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * cols + k4 * 4) * 2);
+          xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+        } else {
+          xv = *reinterpret_cast<const float4*>(xs + (t * cols + k4 * 4) * 4);
+        }
+        ra[t][0] = fmaf(w.x, xv.x, ra[t][0]);
+        ra[t][1] = fmaf(w.y, xv.y, ra[t][1]);
+        ra[t][2] = fmaf(w.z, xv.z, ra[t][2]);
+        ra[t][3] = fmaf(w.w, xv.w, ra[t][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxSmallT; ++t) racc[t] = t < T ? (ra[t][0] + ra[t][1]) + (ra[t][2] + ra[t][3]) : 0.f;
+}
+
 // ---------------------------------------------------------------------------
 // consumers
 // ---------------------------------------------------------------------------
@@ -789,42 +851,17 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         __threadfence();
         fence_proxy_async_global();
       }
-      // four independent accumulators per token (one per float4 component)
-      float ra[kMaxSmallT][4];
-#pragma unroll
-      for (int t = 0; t < kMaxSmallT; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ra[t][c] = 0.f;
       cp_async_wait_all();  // a thread reads back only the weights it copied
-      const int ncol4 = cols / 4;
-      // rolled loops: this code runs once per launch, so its instruction
-      // fetches are cold and code size, not issue rate, decides its time
-#pragma unroll 1
-      for (int i = 0; i < 16; ++i) {
-        const int k4 = warp + kConsumerWarps * i;
-        if (k4 < ncol4) {
-          const float4 w = wst[k4 * 32 + lane];
-#pragma unroll
-          for (int t = 0; t < kMaxSmallT; ++t) {
-            if (t < T) {
-              float4 xv;
-              if constexpr (L == 2) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * cols + k4 * 4) * 2);
-                xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                                 __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-              } else {
-                xv = *reinterpret_cast<const float4*>(xs + (t * cols + k4 * 4) * 4);
-              }
-              ra[t][0] = fmaf(w.x, xv.x, ra[t][0]);
-              ra[t][1] = fmaf(w.y, xv.y, ra[t][1]);
-              ra[t][2] = fmaf(w.z, xv.z, ra[t][2]);
-              ra[t][3] = fmaf(w.w, xv.w, ra[t][3]);
-            }
-          }
-        }
+      switch (T) {
+        case 1: router_dot<L, 1>(wst, xs, cols, racc); break;
+        case 2: router_dot<L, 2>(wst, xs, cols, racc); break;
+        case 3: router_dot<L, 3>(wst, xs, cols, racc); break;
+        case 4: router_dot<L, 4>(wst, xs, cols, racc); break;
+        case 5: router_dot<L, 5>(wst, xs, cols, racc); break;
+        case 6: router_dot<L, 6>(wst, xs, cols, racc); break;
+        case 7: router_dot<L, 7>(wst, xs, cols, racc); break;
+        default: router_dot<L, 8>(wst, xs, cols, racc); break;
       }
-#pragma unroll
-      for (int t = 0; t < kMaxSmallT; ++t) racc[t] = (ra[t][0] + ra[t][1]) + (ra[t][2] + ra[t][3]);
       // the stage's weights were written through the generic proxy; the next
       // user of these bytes may be a bulk copy
       tc_fence_async_smem();
