@@ -22,7 +22,7 @@ constexpr int kProducerWarp = 8;    // issues the bulk copies (one thread)
 constexpr int kEpilogueWarp = 9;    // reduces finished row groups, does the bookkeeping
 constexpr int kThreads = 10 * 32;
 constexpr int kGroup = 4;           // activation vectors per tile (token group)
-constexpr int kRowsPerWarp = kRows / kConsumerWarps;  // 4 rows of a chunk per consumer warp
+constexpr int kBlocksPerStep = kConsumerWarps;        // consumer warp w takes blocks w, w + 8, ...
 constexpr int kRouterKc = 256;      // router repack block columns
 constexpr int kRouterCc = 128;      // router chunk columns (half a repack block)
 constexpr int kRouterTileChunks = 4;  // router chunks per router tile (512 columns)
@@ -42,11 +42,11 @@ constexpr int kMaxSlots = 8;        // stage descriptor slots of the small-T rin
 __host__ __device__ constexpr int rec_bytes(int L) { return 32 * L + 16; }
 
 // Bytes of one weight chunk: 32 rows x Kc columns (nbc = Kc/32 blocks).
-//   Q8_0 : quants [32 rows][2 halves][nbc][16 B], then scales [32 rows][nbc] fp16
-//   Q4KS : quants [32 rows][nbc sub-blocks][16 B] (nibbles permuted so that
+//   Q8_0 : quants [nbc][2 halves][32 rows][16 B], then scales [nbc][32 rows] fp16
+//   Q4KS : quants [nbc sub-blocks][32 rows][16 B] (nibbles permuted so that
 //          (word & 0x0F0F0F0F) holds weights 8w..8w+3 and
 //          ((word >> 4) & 0x0F0F0F0F) weights 8w+4..8w+7), then the
-//          serialised 16-byte superblock headers [32 rows][nbc/8][16 B]
+//          serialised 16-byte superblock headers [nbc/8][32 rows][16 B]
 //   F32  : [Kc/4][32 rows][4 floats]   (router; lane = row)
 __host__ __device__ inline int64_t chunk_bytes(int fmt, int Kc) {
   if (fmt == MOE_Q8_0) return (int64_t)(Kc / 32) * 1088;

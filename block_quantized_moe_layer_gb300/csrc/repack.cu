@@ -5,9 +5,9 @@
 // (gate rows at chunk rows 0-15 and up rows at 16-31 of the same gate/up
 // tile, so that one tile yields complete SwiGLU outputs).  Each (tile, chunk)
 // is contiguous: chunk_bytes(fmt, Kc) at offset (tile * nch + c) * chunk_bytes.
-// Within a chunk the 16-byte pieces of consecutive blocks of one row are
-// adjacent, so the 32 lanes of a warp (one block each) read one row with
-// conflict-free 128-bit loads.
+// Within a chunk the 16-byte pieces of the 32 rows of one block are adjacent,
+// so the 32 lanes of a warp (one row each) read one block with conflict-free
+// 128-bit loads.
 #include "common.cuh"
 
 namespace moe {
@@ -24,14 +24,14 @@ __global__ void repack_q8_kernel(const uint8_t* __restrict__ src, uint8_t* __res
   const int64_t cb = chunk_bytes(MOE_Q8_0, Kc);
   uint8_t* chunk = dst + ((int64_t)tile * nch + c) * cb;
   const uint8_t* s = src + i * 34;
-  uint8_t* q0 = chunk + ((int64_t)(lr * 2 + 0) * nbc + lb) * 16;
-  uint8_t* q1 = chunk + ((int64_t)(lr * 2 + 1) * nbc + lb) * 16;
+  uint8_t* q0 = chunk + ((int64_t)(lb * 2 + 0) * kRows + lr) * 16;
+  uint8_t* q1 = chunk + ((int64_t)(lb * 2 + 1) * kRows + lr) * 16;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     q0[j] = s[2 + j];
     q1[j] = s[18 + j];
   }
-  uint8_t* sc = chunk + nbc * 1024 + (lr * nbc + lb) * 2;
+  uint8_t* sc = chunk + nbc * 1024 + (lb * kRows + lr) * 2;
   sc[0] = s[0];
   sc[1] = s[1];
 }
@@ -49,7 +49,7 @@ __global__ void repack_q4ks_kernel(const uint8_t* __restrict__ src, uint8_t* __r
   const int64_t cb = chunk_bytes(MOE_Q4KS, Kc);
   uint8_t* chunk = dst + ((int64_t)tile * nch + c) * cb;
   const uint8_t* s = src + i * 144;
-  uint8_t* hdr = chunk + nbc * 512 + (lr * (nbc / 8) + lsb0 / 8) * 16;
+  uint8_t* hdr = chunk + nbc * 512 + ((lsb0 / 8) * kRows + lr) * 16;
 #pragma unroll
   for (int j = 0; j < 16; ++j) hdr[j] = s[j];
   for (int j = 0; j < 8; ++j) {
@@ -61,7 +61,7 @@ __global__ void repack_q4ks_kernel(const uint8_t* __restrict__ src, uint8_t* __r
       q[2 * l] = v & 0x0F;
       q[2 * l + 1] = v >> 4;
     }
-    uint8_t* out = chunk + ((int64_t)lr * nbc + lsb0 + j) * 16;
+    uint8_t* out = chunk + ((int64_t)(lsb0 + j) * kRows + lr) * 16;
 #pragma unroll
     for (int w = 0; w < 4; ++w)
 #pragma unroll

@@ -51,8 +51,8 @@ struct SmemPlan {
   int ring, bars, rbars, descs, metas, rred, red, misc, ecache, escr, pend, flags, total;
 };
 
-constexpr int kRedSlots = 8;
-constexpr int kRedSlotBytes = 32 * kGroup * 4;  // sums of one 32-row group: [32 rows][kGroup]
+constexpr int kRedSlots = 4;
+constexpr int kRedSlotBytes = kConsumerWarps * kRows * kGroup * 4;  // one 32-row group: [warp][row][token]
 
 // The ring holds variable-size stages back to back (ring_bytes); n_slots
 // descriptor slots, each with a full / empty barrier pair.
@@ -417,65 +417,46 @@ __device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float
   b = dmin * (float)field6(hd.y, hd.z, hd.w, 8 + s);
 }
 
-// One chunk.  Warp w owns rows 4w..4w+3 of the chunk; lane l owns blocks l,
-// l+32, ...  Per block a lane loads its activation record once and reuses it
-// for the warp's four rows, so the shared-memory traffic is the weights once
-// plus one record read per warp.  acc[r][m] collects this lane's share of
-// row r's dot product with vector m; the lanes are summed when the row group
-// is complete.
+// One chunk.  Lane l owns row l of the chunk; warp w owns blocks w, w + 8,
+// ... (a warp load of one block's 16-byte pieces covers the 32 rows in 512
+// contiguous bytes; the block's activation records are a broadcast read, one
+// per warp).  acc[m] collects this warp's share of the lane's row against
+// vector m; the 8 warps' shares are summed by the epilogue warp.
 template <int L, int M>
-__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int fmt,
-                                             float (&acc)[kRowsPerWarp][kGroup]) {
+__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int fmt, float (&acc)[kGroup]) {
   constexpr int RB = rec_bytes(L);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r0 = warp * kRowsPerWarp;
   const uint8_t* A = stage + chunk_bytes(fmt, nbc * 32);
   if (fmt == MOE_Q8_0) {
     const __half* sc = reinterpret_cast<const __half*>(stage + nbc * 1024);
-    for (int b = lane; b < nbc; b += 32) {
-      uint4 q0[kRowsPerWarp], q1[kRowsPerWarp];
-      float dq[kRowsPerWarp];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        q0[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)((r0 + r) * 2 + 0) * nbc + b) * 16);
-        q1[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)((r0 + r) * 2 + 1) * nbc + b) * 16);
-        dq[r] = __half2float(sc[(r0 + r) * nbc + b]);
-      }
+#pragma unroll 2
+    for (int b = warp; b < nbc; b += kBlocksPerStep) {
+      const uint4 q0 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 0) * kRows + lane) * 16);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 1) * kRows + lane) * 16);
+      const float dq = __half2float(sc[b * kRows + lane]);
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        {
-          const uint8_t* rec = A + (m * nbc + b) * RB;
-          const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
-#pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) acc[r][m] = fmaf(dq[r] * asc, q8_block<L>(q0[r], q1[r], rec), acc[r][m]);
-        }
+        const uint8_t* rec = A + (m * nbc + b) * RB;
+        const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
+        acc[m] = fmaf(dq * asc, q8_block<L>(q0, q1, rec), acc[m]);
       }
     }
   } else {  // MOE_Q4KS
-    const uint8_t* hdr = stage + nbc * 512;  // (M is a compile-time count: the token loops unroll fully)
-    const int nsup = nbc / 8;
-    for (int b = lane; b < nbc; b += 32) {
-      uint4 qv[kRowsPerWarp];
-      float sa[kRowsPerWarp], sb[kRowsPerWarp];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        qv[r] = *reinterpret_cast<const uint4*>(stage + ((int64_t)(r0 + r) * nbc + b) * 16);
-        const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((r0 + r) * nsup + (b >> 3)) * 16);
-        q4_scales(hd, b & 7, sa[r], sb[r]);
-      }
+    const uint8_t* hdr = stage + nbc * 512;
+#pragma unroll 2
+    for (int b = warp; b < nbc; b += kBlocksPerStep) {
+      const uint4 qv = *reinterpret_cast<const uint4*>(stage + ((int64_t)b * kRows + lane) * 16);
+      const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((b >> 3) * kRows + lane) * 16);
+      float sa, sb;
+      q4_scales(hd, b & 7, sa, sb);
+      uint32_t w[8];
+      q4_unpack(qv, w);
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        {
-          const uint8_t* rec = A + (m * nbc + b) * RB;
-          const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
-          const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
-#pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) {
-            uint32_t w[8];
-            q4_unpack(qv[r], w);
-            acc[r][m] = fmaf(sa[r] * asc, q4_block<L>(w, rec), fmaf(-sb[r], sx, acc[r][m]));
-          }
-        }
+        const uint8_t* rec = A + (m * nbc + b) * RB;
+        const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
+        const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
+        acc[m] = fmaf(sa * asc, q4_block<L>(w, rec), fmaf(-sb, sx, acc[m]));
       }
     }
   }
@@ -485,8 +466,7 @@ __device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int 
 // tokens unroll without predicates (a runtime bound there keeps the loads of
 // different tokens from being scheduled together).
 template <int L>
-__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M,
-                                           float (&acc)[kRowsPerWarp][kGroup]) {
+__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M, float (&acc)[kGroup]) {
   switch (M) {
     case 1: gemv_chunk_m<L, 1>(stage, nbc, fmt, acc); break;
     case 2: gemv_chunk_m<L, 2>(stage, nbc, fmt, acc); break;
@@ -794,7 +774,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   const int T = P.T;
   int s = 0, rs = 0;
   uint32_t ph = 0, rph = 0;
-  float acc[kRowsPerWarp][kGroup];
+  float acc[kGroup];
   float racc[kMaxSmallT];
 
   while (true) {
@@ -890,32 +870,18 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     } else {
       if (d.chunk == 0) {
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-          for (int m = 0; m < kGroup; ++m) acc[r][m] = 0.f;
+        for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
       }
       gemv_chunk<L>(stage, d.nbc, d.fmt, d.M, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (d.chunk == d.nch - 1) {
-        // a 32-row group is complete: sum the lanes and hand the group's
-        // results to the epilogue warp (the descriptor is copied before the
-        // stage is released, since the producer reuses it)
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-          for (int m = 0; m < kGroup; ++m)
-#pragma unroll
-            for (int o = 16; o; o >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], o);
+        // a 32-row group is complete: hand this warp's share of every row to
+        // the epilogue warp (the descriptor is copied before the stage is
+        // released, since the producer reuses it)
         if (!mbar_wait_bounded(&rempty[rs], rph ^ 1u, P.timeout_ns, P.status, kSiteRedEmpty, rs)) break;
-        float mine = 0.f;
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-          for (int m = 0; m < kGroup; ++m)
-            if (lane == r * kGroup + m) mine = acc[r][m];
-        float* slot = red + rs * (kRedSlotBytes / 4);
-        if (lane < kRowsPerWarp * kGroup) slot[warp * kRowsPerWarp * kGroup + lane] = mine;
+        float4* slot = reinterpret_cast<float4*>(red + rs * (kRedSlotBytes / 4));  // [warp][row][token]
+        slot[warp * kRows + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         if (tid == 0) metas[rs] = d;
         __syncwarp();
         if (lane == 0) mbar_arrive(&rfull[rs]);
@@ -945,8 +911,14 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     if (!mbar_wait_bounded(&rfull[rs], rph, P.timeout_ns, P.status, kSiteRedFull, rs)) break;
     const Desc d = metas[rs];
     if (d.kind == kEnd) break;
-    const float4 vv = reinterpret_cast<const float4*>(red + rs * (kRedSlotBytes / 4))[lane];  // row = lane
-    const float v[kGroup] = {vv.x, vv.y, vv.z, vv.w};
+    // row = lane: sum the consumer warps' shares in warp order
+    const float4* slot = reinterpret_cast<const float4*>(red + rs * (kRedSlotBytes / 4));
+    float v[kGroup] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float4 x = slot[w * kRows + lane];
+      v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&rempty[rs]);
     if (++rs == kRedSlots) { rs = 0; rph ^= 1u; }
