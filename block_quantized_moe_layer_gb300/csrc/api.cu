@@ -356,9 +356,9 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_gucnt = take((size_t)w_max * 4);
   const size_t o_ready = take((size_t)w_max * 4);
   const size_t o_dcnt = take((size_t)n_dt * 4);
+  const size_t o_lfx = take((size_t)E_pad * 8 * 8);  // zero between launches, like the counters
   const size_t counters_end = off;
   const size_t o_status = take(16);
-  const size_t o_part = take((size_t)((d->H / kRouterCc + kRouterTileChunks - 1) / kRouterTileChunks) * E_pad * 8 * 4);
   const size_t o_ids = take((size_t)Tm * k * 4);
   const size_t o_gates = take((size_t)Tm * k * 4);
   const size_t o_pos = take((size_t)Tm * k * 4);
@@ -377,7 +377,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.entry_ready = reinterpret_cast<int*>(w + o_ready);
   sp.d_cnt = reinterpret_cast<int*>(w + o_dcnt);
   sp.status = reinterpret_cast<int*>(w + o_status);
-  sp.partials = reinterpret_cast<float*>(w + o_part);
+  sp.lfx = reinterpret_cast<long long*>(w + o_lfx);
   sp.ids = reinterpret_cast<int*>(w + o_ids);
   sp.gates = reinterpret_cast<float*>(w + o_gates);
   sp.pos = reinterpret_cast<int*>(w + o_pos);

@@ -156,6 +156,13 @@ __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Fetch-and-add with acquire and release semantics at GPU scope.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Orders this thread's generic-proxy global accesses with its async-proxy
 // (bulk copy) accesses: records written with st.global by one CTA and read
 // with cp.async.bulk by another need it on both sides of the flag hand-off.
@@ -195,11 +202,11 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
+
+// Scale of the block sum in a record: sum(X) * 2^-s in fp32, rounded once.
+// The integer sum is exact; for L = 2 it fits fp32's mantissa (|sum| < 2^20),
+// and the scaling by a power of two is exact (no subnormal results: s <= 120).
+__device__ __forceinline__ float record_sumx(long long sx, int s) { return ldexpf(__ll2float_rn(sx), -s); }
 
 // One warp converts 32 values (lane i holds v) into an activation record.
 template <int L>
@@ -214,14 +221,70 @@ __device__ __forceinline__ void write_record(float v, uint8_t* rec) {
   const int X = __float2int_rn(ldexpf(v, s));
 #pragma unroll
   for (int l = 0; l < L; ++l) rec[l * 32 + lane] = (uint8_t)((X >> (8 * l)) & 0xFF);
-  const double sx = warp_sum_d((double)X);
-  if (lane == 0) {
-    float* meta = reinterpret_cast<float*>(rec + 32 * L);
-    meta[0] = ldexpf(1.f, -s);
-    meta[1] = (float)ldexp(sx, -s);
-    meta[2] = 0.f;
-    meta[3] = 0.f;
+  long long sx;
+  if constexpr (L == 2) {
+    sx = __reduce_add_sync(0xffffffffu, X);  // |X| <= 2^14: the sum fits 32 bits
+  } else {
+    sx = X;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
   }
+  if (lane == 0)
+    *reinterpret_cast<float4*>(rec + 32 * L) = make_float4(ldexpf(1.f, -s), record_sumx(sx, s), 0.f, 0.f);
+}
+
+// The same record as write_record, written by one thread for one block of 32
+// values read from shared memory (bf16 for L = 2, fp32 for L = 4).  The
+// arithmetic is the same.
+template <int L>
+__device__ __forceinline__ void write_record_lane(const uint8_t* src, uint8_t* rec) {
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < (L == 2 ? 4 : 8); ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
+    if constexpr (L == 2) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+      v[4 * q] = __uint_as_float(u.x);
+      v[4 * q + 1] = __uint_as_float(u.y);
+      v[4 * q + 2] = __uint_as_float(u.z);
+      v[4 * q + 3] = __uint_as_float(u.w);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int s = 0;
+  if (amax > 0.f) {
+    s = (8 * L - 3) - ilogbf(amax);
+    s = max(-100, min(120, s));
+  }
+  long long sx = 0;
+  uint32_t packed[L][8];
+#pragma unroll
+  for (int l = 0; l < L; ++l)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) packed[l][j] = 0u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int X = __float2int_rn(ldexpf(v[i], s));
+    sx += X;
+#pragma unroll
+    for (int l = 0; l < L; ++l) packed[l][i >> 2] |= (uint32_t)((X >> (8 * l)) & 0xFF) << (8 * (i & 3));
+  }
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    uint4* d = reinterpret_cast<uint4*>(rec + 32 * l);
+    d[0] = make_uint4(packed[l][0], packed[l][1], packed[l][2], packed[l][3]);
+    d[1] = make_uint4(packed[l][4], packed[l][5], packed[l][6], packed[l][7]);
+  }
+  *reinterpret_cast<float4*>(rec + 32 * L) =
+      make_float4(ldexpf(1.f, -s), record_sumx(sx, s), 0.f, 0.f);
 }
 
 // Status bits written into the layer's status word.

@@ -64,7 +64,7 @@ struct SmallParams {
   int* gu_cnt;       // [w_max]
   int* entry_ready;  // [w_max]
   int* d_cnt;        // [n_dt]
-  float* partials;   // [n_kt][E_pad][Tp]
+  long long* lfx;    // [E_pad][Tp] router logits in units of 2^-32, summed with integer atomics
   int* ids;          // [T*k]
   float* gates;      // [T*k]
   int* pos;          // [T*k]

@@ -14,10 +14,14 @@
 //
 // Tile order in the queue (each kind only waits on kinds before it, so every
 // tile another tile waits for has already been claimed by a running CTA):
-//   router tiles     32 experts x 256 columns; partial logits to global.  The
-//                    tiles of row group 0 also turn x into activation records.
-//                    The last router tile to finish computes the routing
-//                    (top-k, gates, permutation, expert work entries).
+//   x records        one per 512-column slice of x: all T tokens' activation
+//                    records (one 32-column block per thread)
+//   router tiles     32 experts x 512 columns; each adds its share of the
+//                    logits to a global sum kept as exact 2^-32 fixed point
+//                    (integer atomics, so the sum does not depend on the
+//                    order of arrival).  The last router tile to finish
+//                    computes the routing (top-k, gates, permutation, expert
+//                    work entries).
 //   shared gate/up   32 outputs (16+16 gate/up rows, twice) x full K
 //   shared down      128 outputs x full I
 //   routed gate/up   per routed work entry (<= 4 tokens of one expert)
@@ -25,7 +29,8 @@
 // Hand-offs use last-arriver counters: the last gate/up tile of an entry
 // publishes it (its activation records are complete); the last down tile of
 // a 128-row block combines that block of y in slot order.  No floating-point
-// atomics: every sum has a fixed order, so results are bit-reproducible.
+// atomics: every floating-point sum has a fixed order (the logits' integer
+// sum has none to keep), so results are bit-reproducible.
 // Every spin-wait is bounded; on timeout the kernel records where in the
 // status word, drains its own copies and leaves.
 //
@@ -38,7 +43,7 @@
 
 namespace moe {
 
-enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3 };
+enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3, kXRec = 4 };
 
 struct Desc {
   int kind, chunk, nch, M;         // read by every consumer thread
@@ -149,6 +154,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   uint32_t* readybits = reinterpret_cast<uint32_t*>(smem + plan.flags) + 4;  // [8] entries seen published
   constexpr int RB = rec_bytes(L);
   constexpr int XEL = L == 2 ? 2 : 4;  // bytes of one x element
+  const int NX = P.n_kt;  // x-record items (one per 512-column slice of x) come first
   const int NR = P.n_rg * P.n_kt;
   const int NSG = P.n_sh * P.n_gu_sh, NSD = P.n_sh * P.n_dt;
   const int NS = P.n_stages;
@@ -161,15 +167,22 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   int n_rent = -1;
   for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
-  int t = atomicAdd(&P.sync->queue, 1);
+  int t = atomicAdd(&P.sync->queue, 1) - NX;
   while (ok) {
-    const int t_next = atomicAdd(&P.sync->queue, 1);  // claim one ahead: its latency overlaps this tile
+    const int t_next = atomicAdd(&P.sync->queue, 1) - NX;  // claim one ahead: its latency overlaps this tile
     int kind, rgk = 0, rbt, entry = 0, ngroups = 1, nch = 1, nbc, fmt, M, slot0 = 0, n_tiles = 0;
     const Entry* ep = nullptr;
     bool shared_e = false;
-    if (t < NR) {
-      // a router tile is one stage holding the tile's x slice; the consumers
-      // load the tile's router weights themselves
+    if (t < 0) {
+      // an x-record item: the slice of x for all T tokens, no weights
+      kind = kXRec;
+      rbt = t + NX;
+      fmt = MOE_F32;
+      nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);
+      M = P.T;
+    } else if (t < NR) {
+      // a router tile is one stage: the tile's router weights (one contiguous
+      // range of the repacked router) and its x slice
       kind = kRouter;
       rgk = (t / P.n_kt) << 16;
       rbt = t % P.n_kt;  // router: index of the 512-column slice
@@ -221,9 +234,12 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     const uint8_t* wbase;
     int64_t cbytes;
     int e_id = -1;
-    if (kind == kRouter) {
+    if (kind == kXRec) {
       cbytes = 0;
       wbase = nullptr;
+    } else if (kind == kRouter) {
+      cbytes = (int64_t)nbc * chunk_bytes(MOE_F32, kRouterCc);
+      wbase = P.router + ((int64_t)(rgk >> 16) * P.n_ks * 64 + kRouterTileChunks * 32 * rbt) * kRows * 16;
     } else {
       shared_e = entry < P.n_sh;
       if (shared_e) {
@@ -253,16 +269,15 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         wbase = (shared_e ? P.sdn : P.dn + (int64_t)e_id * P.dn_stride) + (int64_t)(4 * rbt) * nch * cbytes;
       }
     }
-    const uint32_t per = kind == kRouter ? (uint32_t)(nbc * kRouterCc * XEL) : (uint32_t)(nbc * RB);
+    const bool xslice = kind == kRouter || kind == kXRec;  // the stage holds a slice of x
+    const uint32_t per = xslice ? (uint32_t)(nbc * kRouterCc * XEL) : (uint32_t)(nbc * RB);
     const uint32_t wb = (uint32_t)cbytes;
-    // a router stage reserves room for the tile's weights, which the
-    // consumers copy in themselves (cp.async), ahead of the x slice
-    const uint32_t resv = kind == kRouter ? (uint32_t)nbc * (uint32_t)chunk_bytes(MOE_F32, kRouterCc) : wb;
+    const uint32_t resv = wb;
     const int need = (int)((resv + (uint32_t)M * per + 127u) & ~127u);
     // activation sources of this tile at chunk 0, and their step per chunk
     const uint8_t* asrc[kMaxSmallT];
     int64_t astep;
-    if (kind == kRouter) {
+    if (xslice) {
       astep = 0;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
@@ -278,7 +293,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       }
     }
     const int4 h3 = make_int4(slot0, P.n_sh + max(n_rent, 0), n_tiles, 0);
-    bool dep_ok = kind == kRouter;
+    bool dep_ok = xslice;
     const int nstages = ngroups * nch;
     for (int q = 0; q < nstages && ok; ++q) {
       const int g = q / nch, c = q - g * nch;
@@ -295,7 +310,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       if (!ok) break;
       head = pos + need;
       const int s = issued & (NS - 1);
-      const int kch = kind == kRouter ? kRouterTileChunks * rbt + c : 0;
+      const int kch = xslice ? kRouterTileChunks * rbt + c : 0;
       int4* dd = reinterpret_cast<int4*>(descs + s);
       dd[0] = make_int4(kind, c, nch, M);
       dd[1] = make_int4(nbc, fmt, rgk | kch, pos);
@@ -319,7 +334,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         else ok = false;  // the consumers see the status word; the stage is still completed below
       }
       uint8_t* adst = stage + resv;
-      const int64_t aoff = (int64_t)(kind == kRouter ? c : c) * astep;
+      const int64_t aoff = (int64_t)c * astep;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
         if (m < M) bulk_g2s(adst + m * per, dep_ok ? asrc[m] + aoff : asrc[0], per, &full[s]);
@@ -487,140 +502,146 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// The k largest of row[0..E) by (value desc, index asc), one warp; lane l
-// holds experts l, l+32, ... (NPER of them) in registers.  Each round takes
-// the exact maximum value over the lanes' current bests (a warp max of the
-// order-preserving keys), then the lowest expert index among the lanes that
-// hold it.  Writes ids and values in slot order (lane 0).
+// Largest of N values by a pairwise tree (depth log2 N).
+template <int N>
+__device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
+  uint64_t t[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) t[i] = c[i];
+#pragma unroll
+  for (int w = 1; w < N; w <<= 1)
+#pragma unroll
+    for (int i = 0; i + w < N; i += 2 * w) t[i] = t[i] > t[i + w] ? t[i] : t[i + w];
+  return t[0];
+}
+
+// The k largest of row[0..E) by (value desc, index asc), one warp.  Lane l
+// holds experts l, l + 32, ... (NPER of them) in registers as 64-bit
+// composites (order-preserving key of the value, then the complemented index,
+// so a larger composite is a larger value or, on equal values, a lower
+// index; 0 = none) and keeps its largest.  Each round takes the exact maximum
+// key over the lanes (a warp max); if several lanes hold it, the lowest
+// expert index among them wins (a second warp min, only then).  The winning
+// lane writes the slot, clears that expert and takes the tree maximum of what
+// it has left.  NaN counts as -inf.  Writes ids and values in slot order.
 template <int NPER>
 __device__ __forceinline__ void topk_token(const float* row, int E, int k, int* ids, float* vals_out) {
   const int lane = threadIdx.x & 31;
-  float v[NPER];
+  uint64_t c[NPER];
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    const float x = e < E ? row[e] : -INFINITY;
-    v[i] = x == x ? x : -INFINITY;
+    const float x = e < E ? row[e] : 0.f;
+    c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
   }
-  uint32_t taken = 0;
+  uint64_t best = tree_max(c);
+#pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    float best = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NPER; ++i) {
-      const int e = lane + 32 * i;
-      // ascending e: a later equal value never replaces an earlier one
-      if (e < E && !((taken >> i) & 1u) && (v[i] > best || bi == 0x7fffffff)) {
-        best = v[i];
-        bi = e;
-      }
-    }
-    const uint32_t key = bi == 0x7fffffff ? 0u : order_key(best);
+    const uint32_t key = (uint32_t)(best >> 32);
     const uint32_t m = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t wi = __reduce_min_sync(0xffffffffu, key == m ? (uint32_t)bi : 0x7fffffffu);
-    if ((int)(wi & 31u) == lane) taken |= 1u << (wi >> 5);
-    if (lane == 0) {
+    const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
+    int wl = __ffs(holders) - 1;
+    if (holders & (holders - 1u))
+      wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
+    if (lane == wl) {
+      const uint32_t wi = ~(uint32_t)best;
       ids[j] = (int)wi;
       vals_out[j] = key_value(m);
+      const int slot = (int)(wi >> 5);
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (i == slot) c[i] = 0ull;
+      best = tree_max(c);
     }
   }
 }
 
 // Scratch of finalize_routing in the misc region (bytes, see finalize_misc_bytes).
 struct FinLayout {
-  int lg, cnt, off, sid, sl, sg, sperm, spos, wtot;
+  int lg, sid, sl, sg, sperm, spos, slt, srank, sent, end;
 };
 __host__ __device__ inline FinLayout fin_layout(int T, int E, int k) {
-  const int Tk = T * k, e4 = (E + 3) & ~3, t4 = (Tk + 3) & ~3;
+  const int t4 = (T * k + 3) & ~3;
   FinLayout f;
   f.lg = 0;
-  f.cnt = ((T * E * 4 + 15) & ~15);
-  f.off = f.cnt + 4 * e4;
-  f.sid = f.off + 4 * e4;
+  f.sid = ((T * E * 4 + 15) & ~15);
   f.sl = f.sid + 4 * t4;
   f.sg = f.sl + 4 * t4;
   f.sperm = f.sg + 4 * t4;
   f.spos = f.sperm + 4 * t4;
-  f.wtot = f.spos + 4 * t4;
+  f.slt = f.spos + 4 * t4;
+  f.srank = f.slt + 4 * t4;
+  f.sent = f.srank + 4 * t4;
+  f.end = f.sent + 4 * t4;
   return f;
 }
-int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).wtot + 4 * 2 * kConsumerWarps + 16; }
-
-// Exclusive scan over the consumer threads of two ints at once.
-__device__ __forceinline__ void consumer_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* wtot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int ia = a, ib = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, ia, o);
-    const int y = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) { ia += x; ib += y; }
-  }
-  if (lane == 31) {
-    wtot[2 * warp] = ia;
-    wtot[2 * warp + 1] = ib;
-  }
-  consumer_sync();
-  int ba = 0, bb = 0;
-  ta = 0;
-  tb = 0;
-  for (int w = 0; w < kConsumerWarps; ++w) {
-    if (w < warp) { ba += wtot[2 * w]; bb += wtot[2 * w + 1]; }
-    ta += wtot[2 * w];
-    tb += wtot[2 * w + 1];
-  }
-  ea = ba + ia - a;
-  eb = bb + ib - b;
-}
+int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).end + 16; }
 
 // Runs on the consumer threads of the CTA that finished the last router
 // tile: logits, top-k and gates, then the permutation and the routed work
 // entries.  The entries and their count are published first (routing_ready);
 // ids, gates, offsets, perm and pos follow (routing_aux), since only the
 // combine and moe_get_routing read them.
+//
+// With Tk = T * k <= 128 pairs, pair p finds its place by counting: lt = the
+// pairs of lower experts, rank = the earlier pairs of its own expert, so its
+// slot is lt + rank (experts ascending, tokens ascending within an expert).
+// The first pair of an expert owns that expert's entries: its entry index is
+// the number of entries of all lower experts.
 __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NT = kConsumerWarps * 32;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
   const FinLayout f = fin_layout(T, E, k);
-  float* lg = reinterpret_cast<float*>(misc + f.lg);       // [T*E]
-  int* cnt = reinterpret_cast<int*>(misc + f.cnt);         // [E]
-  int* off = reinterpret_cast<int*>(misc + f.off);         // [E]
-  int* sid = reinterpret_cast<int*>(misc + f.sid);         // [Tk]
-  float* sl = reinterpret_cast<float*>(misc + f.sl);       // [Tk]
-  float* sg = reinterpret_cast<float*>(misc + f.sg);       // [Tk]
-  int* sperm = reinterpret_cast<int*>(misc + f.sperm);     // [Tk]
-  int* spos = reinterpret_cast<int*>(misc + f.spos);       // [Tk]
-  int* wtot = reinterpret_cast<int*>(misc + f.wtot);       // [2 * warps]
+  float* lg = reinterpret_cast<float*>(misc + f.lg);    // [T*E]
+  int* sid = reinterpret_cast<int*>(misc + f.sid);      // [Tk]
+  float* sl = reinterpret_cast<float*>(misc + f.sl);    // [Tk]
+  float* sg = reinterpret_cast<float*>(misc + f.sg);    // [Tk]
+  int* sperm = reinterpret_cast<int*>(misc + f.sperm);  // [Tk]
+  int* spos = reinterpret_cast<int*>(misc + f.spos);    // [Tk]
+  int* slt = reinterpret_cast<int*>(misc + f.slt);      // [Tk] pairs of lower experts
+  int* srank = reinterpret_cast<int*>(misc + f.srank);  // [Tk] earlier pairs of the same expert
+  int* sent = reinterpret_cast<int*>(misc + f.sent);    // [Tk] entries owned (first pair of an expert)
 
-  __threadfence();
-  // logits: thread i sums, in slice order, the partials of experts e = i,
-  // i + 256, ... (the loads of one expert are all in flight before the adds)
-  for (int e = tid; e < E; e += kConsumerWarps * 32) {
-    const float bias = P.router_b ? P.router_b[e] : 0.f;
-    for (int q = 0; q < P.Tp / 4; ++q) {
-      float4 a[8];
+  // (the router counter was taken with acquire semantics)
+  // logits: thread i converts the fixed-point sums of experts e = i, i + 256
+  // (all loads in flight before the conversions), then any further experts
+  {
+    const int nq = P.Tp / 2;  // 16-byte pairs per expert (Tp <= 8)
+    const longlong2* lp = reinterpret_cast<const longlong2*>(P.lfx);
+    auto put = [&](int e, const longlong2* a) {
+      const float bias = P.router_b ? P.router_b[e] : 0.f;
 #pragma unroll
-      for (int kt = 0; kt < 8; ++kt)
-        if (kt < P.n_kt)
-          a[kt] = __ldcg(reinterpret_cast<const float4*>(P.partials + ((int64_t)kt * P.E_pad + e) * P.Tp) + q);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < 4; ++q)
+        if (q < nq) {
+          // one rounding to fp32, then an exact power-of-two scale
+          if (2 * q < T) lg[(2 * q) * E + e] = __ll2float_rn(a[q].x) * 0x1p-32f + bias;
+          if (2 * q + 1 < T) lg[(2 * q + 1) * E + e] = __ll2float_rn(a[q].y) * 0x1p-32f + bias;
+        }
+    };
+    longlong2 a[2][4];
 #pragma unroll
-      for (int kt = 0; kt < 8; ++kt)
-        if (kt < P.n_kt) { v.x += a[kt].x; v.y += a[kt].y; v.z += a[kt].z; v.w += a[kt].w; }
-      for (int kt = 8; kt < P.n_kt; ++kt) {  // H > 4096: further slices, one at a time
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(P.partials + ((int64_t)kt * P.E_pad + e) * P.Tp) + q);
-        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
-      }
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-      for (int c = 0; c < 4; ++c)
-        if (4 * q + c < T) lg[(4 * q + c) * E + e] = vv[c] + bias;
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (tid + u * NT < E && q < nq) a[u][q] = __ldcg(lp + (int64_t)(tid + u * NT) * nq + q);
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (tid + u * NT < E) put(tid + u * NT, a[u]);
+#pragma unroll 1
+    for (int e = tid + 2 * NT; e < E; e += NT) {  // E > 512
+      longlong2 c[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nq) c[q] = __ldcg(lp + (int64_t)e * nq + q);
+      put(e, c);
     }
-    cnt[e] = 0;
   }
   consumer_sync();
 
   // top-k and gates per token (one warp per token)
   const int nper = (E + 31) / 32;
+#pragma unroll 1
   for (int t = warp; t < T; t += kConsumerWarps) {
     if (nper <= 4) topk_token<4>(lg + t * E, E, k, sid + t * k, sl + t * k);
     else if (nper <= 8) topk_token<8>(lg + t * E, E, k, sid + t * k, sl + t * k);
@@ -628,92 +649,153 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
     else if (nper <= 16) topk_token<16>(lg + t * E, E, k, sid + t * k, sl + t * k);
     else topk_token<kMaxE / 32>(lg + t * E, E, k, sid + t * k, sl + t * k);
     __syncwarp();
-    if (lane < k) {
-      const float l0 = sl[t * k];
-      float sum = 0.f;
-      for (int j = 0; j < k; ++j) sum += expf(sl[t * k + j] - l0);
-      sg[t * k + lane] = expf(sl[t * k + lane] - l0) / sum;
-    }
+    // gates: softmax over the k selected logits (lane j: slot j), the sum by
+    // a fixed shuffle tree
+    const float l0 = sl[t * k];
+    const float ex = lane < k ? expf(sl[t * k + lane] - l0) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) sg[t * k + lane] = ex / sum;
   }
   consumer_sync();
 
-  // stable rank of each pair among the earlier pairs of its expert, and the
-  // histogram (warp 0, 32 pairs at a time, equal experts found with match_any)
-  int rank[4], ep[4];
-  if (warp == 0) {
-    for (int r = 0; r < (Tk + 31) / 32; ++r) {
-      const int p = lane + 32 * r;
-      const int e = p < Tk ? sid[p] : -1 - lane;
-      const unsigned mask = __match_any_sync(0xffffffffu, e);
-      ep[r] = p < Tk ? e : -1;
-      rank[r] = p < Tk ? cnt[e] + __popc(mask & ((1u << lane) - 1u)) : 0;
+  // slot of each pair (experts ascending, tokens ascending within an
+  // expert) and the routed entries (up to kGroup consecutive slots of one
+  // expert each, in slot order)
+  int n_rent = 0;
+  if (Tk <= 32) {
+    // one warp, lane p = pair p.  lt = pairs of lower experts, by a radix
+    // over the bits of the expert index (lanes past Tk get expert 1024,
+    // above every real one); eq ends as the lanes with my expert.
+    if (warp == 0) {
+      const bool act = lane < Tk;
+      const int ekey = act ? sid[lane] : 1024;
+      int lt = 0;
+      uint32_t eq = 0xffffffffu;
+#pragma unroll
+      for (int b = 10; b >= 0; --b) {
+        const bool bit = (ekey >> b) & 1;
+        const uint32_t ones = __ballot_sync(0xffffffffu, bit);
+        if (bit) lt += __popc(eq & ~ones);
+        eq &= bit ? ones : ~ones;
+      }
+      const uint32_t below = (1u << lane) - 1u;
+      const int rank = __popc(eq & below), cnt = __popc(eq);
+      if (act) {
+        sperm[lt + rank] = lane;
+        spos[lane] = lt + rank;
+      }
       __syncwarp();
-      if (p < Tk && (mask & ((1u << lane) - 1u)) == 0) cnt[e] += __popc(mask);  // one lane per expert
-      __syncwarp();
+      // slot view: lane i holds the pair at slot i
+      const int q = act ? sperm[lane] : 0;
+      const int e_i = __shfl_sync(0xffffffffu, ekey, q);
+      const int r_i = __shfl_sync(0xffffffffu, rank, q);
+      const int c_i = __shfl_sync(0xffffffffu, cnt, q);
+      const int tok = q / k;
+      const uint32_t starts = __ballot_sync(0xffffffffu, act && r_i % kGroup == 0);
+      int tk[kGroup];
+      tk[0] = tok;
+#pragma unroll
+      for (int m = 1; m < kGroup; ++m) tk[m] = __shfl_down_sync(0xffffffffu, tok, m);
+      if ((starts >> lane) & 1u) {
+        const int M = min(kGroup, c_i - r_i);
+        int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + __popc(starts & below));
+        dst[0] = make_int4(e_i, lane, M, tk[0]);
+        dst[1] = make_int4(M > 1 ? tk[1] : 0, M > 2 ? tk[2] : 0, M > 3 ? tk[3] : 0, 0);
+      }
+      n_rent = __popc(starts);
     }
-  }
-  consumer_sync();
-
-  // pair offsets and routed entries: thread i owns a contiguous run of experts
-  const int ept = (E + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
-  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
-  int np = 0, nw = 0;
-  for (int e = e0; e < e1; ++e) {
-    np += cnt[e];
-    nw += (cnt[e] + kGroup - 1) / kGroup;
-  }
-  int po, wo, ptot, wtot_all;
-  consumer_scan2(np, nw, po, wo, ptot, wtot_all, wtot);
-  for (int e = e0; e < e1; ++e) {
-    const int c = cnt[e];
-    off[e] = po;
-    for (int g = 0; g * kGroup < c; ++g) {
-      int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + wo);
-      dst[0] = e;
-      dst[1] = po + g * kGroup;
-      dst[2] = min(kGroup, c - g * kGroup);
-      ++wo;
+  } else {
+    // general case: pair p counts over all pairs
+    const int4* sid4 = reinterpret_cast<const int4*>(sid);
+    const int4* sent4 = reinterpret_cast<const int4*>(sent);
+    const int nq4 = (Tk + 3) / 4;
+    if (tid < Tk) {
+      const int p = tid, e = sid[p];
+      int lt = 0, rank = 0, c = 0;
+#pragma unroll 4
+      for (int q4 = 0; q4 < nq4; ++q4) {
+        const int4 v = sid4[q4];
+        const int ev[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = 4 * q4 + u;
+          if (q < Tk) {
+            lt += ev[u] < e;
+            rank += (ev[u] == e) & (q < p);
+            c += ev[u] == e;
+          }
+        }
+      }
+      const int slot = lt + rank;
+      sperm[slot] = p;
+      spos[p] = slot;
+      slt[p] = lt;
+      srank[p] = rank;
+      sent[p] = rank == 0 ? (c + kGroup - 1) / kGroup : 0;
     }
-    po += c;
-  }
-  consumer_sync();
-  if (warp == 0) {
-    for (int r = 0; r < (Tk + 31) / 32; ++r) {
-      const int p = lane + 32 * r;
-      if (p < Tk) {
-        const int slot = off[ep[r]] + rank[r];
-        sperm[slot] = p;
-        spos[p] = slot;
+    consumer_sync();
+    // entries: the first pair of each expert writes them (tokens from the
+    // permutation); its entry index is the entry count of the lower experts
+    if (tid < Tk && srank[tid] == 0) {
+      const int e = sid[tid], lt = slt[tid], ne = sent[tid];
+      int w0 = 0, c = 0;
+#pragma unroll 4
+      for (int q4 = 0; q4 < nq4; ++q4) {
+        const int4 v = sid4[q4], n = sent4[q4];
+        const int ev[4] = {v.x, v.y, v.z, v.w}, nv[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (4 * q4 + u < Tk) {
+            w0 += ev[u] < e ? nv[u] : 0;
+            c += ev[u] == e;
+          }
+      }
+#pragma unroll 1
+      for (int g = 0; g < ne; ++g) {
+        const int slot0 = lt + g * kGroup, M = min(kGroup, c - g * kGroup);
+        int tok[kGroup];
+#pragma unroll
+        for (int m = 0; m < kGroup; ++m) tok[m] = m < M ? sperm[slot0 + m] / k : 0;
+        int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + w0 + g);
+        dst[0] = make_int4(e, slot0, M, tok[0]);
+        dst[1] = make_int4(tok[1], tok[2], tok[3], 0);
+      }
+    }
+    if (tid == 0) {
+#pragma unroll 4
+      for (int q4 = 0; q4 < nq4; ++q4) {
+        const int4 n = sent4[q4];
+        const int nv[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (4 * q4 + u < Tk) n_rent += nv[u];
       }
     }
   }
   consumer_sync();
-  // tokens of each routed entry
-  for (int w = tid; w < wtot_all; w += kConsumerWarps * 32) {
-    int* dst = reinterpret_cast<int*>(P.entries + P.n_sh + w);
-    const int slot0 = __ldcg(dst + 1), M = __ldcg(dst + 2);
-    for (int m = 0; m < kGroup; ++m) dst[3 + m] = m < M ? sperm[slot0 + m] / k : 0;
-  }
-  consumer_sync();
+  // the barrier orders every thread's entry writes before thread 0's release
   if (tid == 0) {
-    P.sync->n_rent = wtot_all;
-    __threadfence();
+    P.sync->n_rent = n_rent;
     st_release(&P.sync->routing_ready, 1);
   }
   // what only the combine and moe_get_routing read
-  for (int q = tid; q < Tk; q += kConsumerWarps * 32) {
-    P.ids[q] = sid[q];
-    P.gates[q] = sg[q];
-    P.perm[q] = sperm[q];
-    P.pos[q] = spos[q];
+  if (tid < Tk) {
+    P.ids[tid] = sid[tid];
+    P.gates[tid] = sg[tid];
+    P.perm[tid] = sperm[tid];
+    P.pos[tid] = spos[tid];
   }
-  for (int e = tid; e < E; e += kConsumerWarps * 32) P.offsets[e] = off[e];
-  if (tid == 0) P.offsets[E] = ptot;
+#pragma unroll 1
+  for (int e = tid; e <= E; e += NT) {
+    int o = 0;
+#pragma unroll 4
+    for (int q = 0; q < Tk; ++q) o += sid[q] < e;
+    P.offsets[e] = o;
+  }
   consumer_sync();
-  if (tid == 0) {
-    __threadfence();
-    st_release(&P.sync->routing_aux, 1);
-  }
+  if (tid == 0) st_release(&P.sync->routing_aux, 1);
 }
 
 // Router tile dot products: lane = expert row, warp w takes float4 columns
@@ -803,35 +885,29 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     const uint8_t* stage = smem + plan.ring + d.off;
     const int d_rg = d.rgks >> 16, d_ks = d.rgks & 0xFFFF;  // router tiles
 
-    if (d.kind == kRouter) {
-      // One router tile: 32 experts (lane = expert row) x a slice of ncc
-      // 128-column chunks.  The stage holds the slice of x ([T][cols]); the
-      // router weights are loaded straight from global memory, all of a
-      // thread's loads in flight at once (warp w takes float4 columns w,
-      // w + 8, ...; one warp load is 512 contiguous bytes).
-      const int kt = d_ks / kRouterTileChunks, ncc = d.nbc, cols = ncc * kRouterCc;
-      const float4* wsrc = reinterpret_cast<const float4*>(P.router) + (int64_t)d_rg * P.n_ks * 64 * 32;
-      float4* wst = reinterpret_cast<float4*>(const_cast<uint8_t*>(stage));  // [cols/4][32 rows]
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int k4 = warp + kConsumerWarps * i;
-        if (k4 < cols / 4) cp_async16(wst + k4 * 32 + lane, wsrc + (int64_t)(kt * 128 + k4) * 32 + lane);
-      }
-      const uint8_t* xs = stage + cols * kRows * 4;
-      auto xval = [&](int t, int c) -> float {
-        if constexpr (L == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xs)[t * cols + c]);
-        else return reinterpret_cast<const float*>(xs)[t * cols + c];
-      };
-      if (d_rg < T) {
-        // x slice -> activation records of tokens t = rg, rg + n_rg, ... (warp w: blocks w, w + 8)
-        for (int t = d_rg; t < T; t += P.n_rg)
-          for (int b = warp; b < cols / 32; b += kConsumerWarps)
-            write_record<L>(xval(t, b * 32 + lane),
-                            P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
-        __threadfence();
+    if (d.kind == kXRec) {
+      // x slice ([T][cols] in the stage) -> activation records, one 32-column
+      // block per thread; the proxy fence makes them visible to the bulk
+      // copies that read them after x_done
+      const int kt = d_ks / kRouterTileChunks, cols = d.nbc * kRouterCc, nb = cols / 32;
+      constexpr int XEL = L == 2 ? 2 : 4;
+      if (tid < T * nb) {
+        const int t = tid / nb, b = tid - (tid / nb) * nb;
+        write_record_lane<L>(stage + (t * cols + b * 32) * XEL,
+                             P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
         fence_proxy_async_global();
       }
-      cp_async_wait_all();  // a thread reads back only the weights it copied
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      consumer_sync();  // orders every thread's record writes before thread 0's release
+      if (tid == 0) atom_add_acq_rel(&P.sync->x_done, T * d.nbc);
+    } else if (d.kind == kRouter) {
+      // One router tile: 32 experts (lane = expert row) x a slice of ncc
+      // 128-column chunks.  The stage holds the tile's router weights
+      // ([cols/4][32 rows][4]) and then the slice of x ([T][cols]).
+      const int ncc = d.nbc, cols = ncc * kRouterCc;
+      const float4* wst = reinterpret_cast<const float4*>(stage);
+      const uint8_t* xs = stage + cols * kRows * 4;
       switch (T) {
         case 1: router_dot<L, 1>(wst, xs, cols, racc); break;
         case 2: router_dot<L, 2>(wst, xs, cols, racc); break;
@@ -842,9 +918,6 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         case 7: router_dot<L, 7>(wst, xs, cols, racc); break;
         default: router_dot<L, 8>(wst, xs, cols, racc); break;
       }
-      // the stage's weights were written through the generic proxy; the next
-      // user of these bytes may be a bulk copy
-      tc_fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
@@ -852,16 +925,20 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
       consumer_sync();
       if (tid < T * 32) {
+        // this slice's share of logit (t, expert 32 rg + r), added as an
+        // exact integer multiple of 2^-32: the total does not depend on the
+        // order in which the slices arrive
         const int t = tid >> 5, r = tid & 31;
         float v = 0.f;
         for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
-        P.partials[((int64_t)kt * P.E_pad + d_rg * 32 + r) * P.Tp + t] = v;
+        atomicAdd(reinterpret_cast<unsigned long long*>(P.lfx) + (int64_t)(d_rg * 32 + r) * P.Tp + t,
+                  (unsigned long long)__float2ll_rn(v * 4294967296.f));
       }
-      __threadfence();
+      // the barrier orders every thread's additions before thread 0's
+      // release (acquire-release) count
       consumer_sync();
       if (tid == 0) {
-        if (d_rg < T) atomicAdd(&P.sync->x_done, ncc * ((T - 1 - d_rg) / P.n_rg + 1));
-        const int old = atomicAdd(&P.sync->router_done, 1);
+        const int old = atom_add_acq_rel(&P.sync->router_done, 1);
         flags[0] = (old == P.n_rg * P.n_kt - 1);
       }
       consumer_sync();
@@ -903,7 +980,6 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   const float* red = reinterpret_cast<const float*>(smem + plan.red);
   constexpr int RB = rec_bytes(L);
   const int lane = threadIdx.x & 31;
-  const int T = P.T, k = P.k;
   int rs = 0;
   uint32_t rph = 0;
   float keep[kGroup] = {0.f, 0.f, 0.f, 0.f};
@@ -939,26 +1015,22 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         }
       }
       if (d.group == d.ngroups - 1) {
-        __threadfence();
+        // the records are read by bulk copies; __syncwarp orders the lanes'
+        // writes before lane 0's acquire-release count, whose release covers
+        // them and, for the last tile, those of the tiles counted before it
         fence_proxy_async_global();
         __syncwarp();
-        int last = 0;
-        if (lane == 0) last = (atomicAdd(&P.gu_cnt[d.entry], 1) == d.n_tiles_entry - 1);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && lane == 0) {
-          __threadfence();
+        if (lane == 0 && atom_add_acq_rel(&P.gu_cnt[d.entry], 1) == d.n_tiles_entry - 1)
           st_release(&P.entry_ready[d.entry], 1);
-        }
       }
     } else {  // kDown
       const int row = d.rbt * 128 + d.group * 32 + lane;
       for (int m = 0; m < d.M; ++m) P.z[(int64_t)(d.slot0 + m) * P.H + row] = v[m];
       if (d.group == d.ngroups - 1) {
-        __threadfence();
-        __syncwarp();
+        __syncwarp();  // orders the lanes' z writes before lane 0's release
         int last = 0;
         if (lane == 0) {
-          const int old = atomicAdd(&P.d_cnt[d.rbt], 1);
+          const int old = atom_add_acq_rel(&P.d_cnt[d.rbt], 1);
           // a shared down tile may finish before the routing is published; the
           // routed down tiles only run after it, so it cannot be last then
           int n_ent = d.n_ent;
@@ -1069,6 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.entry_ready[i] = 0;
     }
     for (int i = threadIdx.x; i < P.n_dt; i += blockDim.x) P.d_cnt[i] = 0;
+    for (int i = threadIdx.x; i < P.E_pad * P.Tp; i += blockDim.x) P.lfx[i] = 0;
     if (threadIdx.x == 0) {
       P.sync->queue = 0;
       P.sync->router_done = 0;
