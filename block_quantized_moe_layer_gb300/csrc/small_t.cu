@@ -167,6 +167,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   int n_rent = -1;
   for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
+  const uint64_t wpol = l2_evict_first_policy();  // weights are read once per launch
   int t = atomicAdd(&P.sync->queue, 1) - NX;
   while (ok) {
     const int t_next = atomicAdd(&P.sync->queue, 1) - NX;  // claim one ahead: its latency overlaps this tile
@@ -318,7 +319,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       dd[3] = h3;
       uint8_t* stage = smem + plan.ring + pos;
       mbar_arrive_expect_tx(&full[s], wb + (uint32_t)M * per);
-      if (wb) bulk_g2s(stage, wbase + (int64_t)q * cbytes, wb, &full[s]);
+      if (wb) bulk_g2s_hint(stage, wbase + (int64_t)q * cbytes, wb, &full[s], wpol);
       if (!dep_ok) {
         if (kind == kGateUp) {
           // shared gate/up needs the x records; routed ones were gated by the routing flag
