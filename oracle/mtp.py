@@ -48,11 +48,14 @@ def lm_logits(h, lm: moe.QTensor, eps=1e-6):
     return rmsnorm(h, eps) @ lm.dense().T
 
 
-def target_stack(x, layers, eps=1e-6):
-    """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers."""
+def target_stack(x, layers, eps=1e-6, routes=None):
+    """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers.
+    If `routes` is a list, each layer's routing dict is appended to it."""
     h = np.asarray(x, F64)
     for L in layers:
-        y, _ = moe.forward(rmsnorm(h, eps), L)
+        y, r = moe.forward(rmsnorm(h, eps), L)
+        if routes is not None:
+            routes.append(r)
         h = h + y
     return h
 
@@ -61,16 +64,19 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6):
     """One round.  x [k+1, H]; heads: k layers; noise [k][k][H] (head j uses
     rows 0..j of noise[j]).  Returns a dict with h_tgt, logits, head_out
     (list of [j+1, H]), draft_rows [k, H], draft_logits [k, V], drafts [k],
-    n_accepted, next_token and argmax (the target's per-row argmax)."""
+    n_accepted, next_token, argmax (the target's per-row argmax) and the routing
+    dicts of every target layer (target_routes) and head (head_routes)."""
     k = len(heads)
     x = np.asarray(x, F64)
     assert x.shape[0] == k + 1
-    h_tgt = target_stack(x, layers, eps)
+    target_routes, head_routes = [], []
+    h_tgt = target_stack(x, layers, eps, target_routes)
     logits = lm_logits(h_tgt, lm, eps)
     head_out, rows = [], []
     for j, head in enumerate(heads):
         ht = h_tgt[: j + 1] + np.asarray(noise[j][: j + 1], F64)
-        y, _ = moe.forward(rmsnorm(ht, eps), head)
+        y, hr = moe.forward(rmsnorm(ht, eps), head)
+        head_routes.append(hr)
         head_out.append(y)
         rows.append(ht[j])
     rows = np.stack(rows) if rows else np.zeros((0, x.shape[1]))
@@ -79,4 +85,4 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6):
     n, nxt, amax = accept.greedy_accept(drafts, logits)
     return dict(h_tgt=h_tgt, logits=logits, head_out=head_out, draft_rows=rows,
                 draft_logits=draft_logits, drafts=drafts, n_accepted=n, next_token=nxt,
-                argmax=amax)
+                argmax=amax, target_routes=target_routes, head_routes=head_routes)

@@ -15,6 +15,14 @@ pytestmark = pytest.mark.gpu
 
 XDT = {pkg.ACT_BF16: torch.bfloat16, pkg.ACT_F32: torch.float32}
 TOL = {pkg.ACT_BF16: 2e-2, pkg.ACT_F32: 1e-3}
+# Router margin below which a layer's expert choice for a token may differ
+# between the GPU chain and the fp64 oracle chain: the GPU's hidden state
+# carries the rounding of every earlier layer (bf16: ~2^-8 relative per
+# element), so its router logits differ from the oracle's by far more than
+# within one layer.  A token whose top-k boundary margin is below this in any
+# layer is reported and left out of the value comparisons (the per-layer
+# near-tie rule, widened to the chain's input perturbation).
+CHAIN_TIE = {pkg.ACT_BF16: 5e-2, pkg.ACT_F32: 1e-3}
 
 
 def _oracle_lm(r):
@@ -79,24 +87,38 @@ def _check_round(r, act, report):
         # the oracle round on the same inputs
         ref = omtp.mtp_round(to_np(x), [synth_oracle_layer(w, "cuda") for w in r.layers],
                              [synth_oracle_layer(w, "cuda") for w in r.heads], _oracle_lm(r), to_np(noise))
+        # rows whose routing in some target layer sits within the chain's perturbation
+        T = r.k + 1
+        chain = np.zeros(T, bool)
+        for rt, w in zip(ref["target_routes"], r.layers):
+            chain |= omoe.near_tie_tokens(rt["logits"], w.top_k, CHAIN_TIE[act])
+        ok = ~chain
+        assert ok.sum() >= 1, "every verify row has a routing near tie: nothing left to compare"
         lerr = np.abs(logits - ref["logits"]).max(axis=1)
         scale = np.abs(ref["logits"]).max()
-        assert lerr.max() / scale <= TOL[act], f"target logits rel err {lerr.max() / scale:.2e}"
+        assert lerr[ok].max() / scale <= TOL[act], f"target logits rel err {lerr[ok].max() / scale:.2e}"
         hout = to_np(out["head_out"])
+        head_ok = []
         for j in range(r.k):
-            e = omoe.max_rel_err(hout[j, : j + 1], ref["head_out"][j])
-            assert e <= TOL[act], f"head {j}: max rel err {e:.2e}"
+            rows = ok[: j + 1] & ~omoe.near_tie_tokens(ref["head_routes"][j]["logits"], r.heads[j].top_k,
+                                                        CHAIN_TIE[act])
+            head_ok.append(rows)
+            if rows.any():
+                e = omoe.max_rel_err(hout[j, : j + 1][rows], ref["head_out"][j][rows])
+                assert e <= TOL[act], f"head {j}: max rel err {e:.2e}"
         # drafts: the LM head on the noisy rows, checked where the decision is unique
         d_err = [np.abs(lm.forward(torch.from_numpy(ref["draft_rows"][j:j + 1]).to(XDT[act]).cuda())
                         .cpu().numpy()[0] - ref["draft_logits"][j]).max() for j in range(r.k)]
-        near = []
+        near = [f"chain-row{i}" for i in range(T) if chain[i]]
         for j in range(r.k):
-            if _decided(ref["draft_logits"][j], 4 * max(d_err[j], lerr.max())):
+            if not ok[j]:
+                near.append(f"draft{j}")
+            elif _decided(ref["draft_logits"][j], 4 * max(d_err[j], lerr[ok].max())):
                 assert drafts[j] == ref["drafts"][j], f"draft {j}"
             else:
                 near.append(f"draft{j}")
         for i in range(r.k + 1):
-            if _decided(ref["logits"][i], lerr[i]):
+            if ok[i] and _decided(ref["logits"][i], lerr[i]):
                 assert amax_gpu[i] == ref["argmax"][i], f"target argmax row {i}"
             else:
                 near.append(f"row{i}")
@@ -104,7 +126,8 @@ def _check_round(r, act, report):
         if not any(f"row{i}" in near or f"draft{i}" in near for i in rows):
             assert (n_gpu, next_gpu) == (ref["n_accepted"], ref["next_token"])
         report(f"{r.name} act={act}: n_accepted gpu {n_gpu} oracle {ref['n_accepted']}, next {next_gpu}/"
-               f"{ref['next_token']}, logits rel err {lerr.max() / scale:.2e}, near ties {near}")
+               f"{ref['next_token']}, logits rel err {lerr[ok].max() / scale:.2e} over {ok.sum()}/{T} rows, "
+               f"near ties {near}")
     finally:
         for L in layers + heads:
             L.close()
