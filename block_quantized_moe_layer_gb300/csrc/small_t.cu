@@ -47,13 +47,14 @@ enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3, kXRec = 4 }
 
 struct Desc {
   int kind, chunk, nch, M;         // read by every consumer thread
-  int nbc, fmt, rgks, off;         //   " (rgks = router row group << 16 | chunk; off = ring offset)
+  int nbc, fmt, rgks, off;         //   " (off = ring offset; rgks: router and x-record items: row
+                                   //   group << 16 | chunk; gate/up and down: groups in the stage)
   int entry, rbt, group, ngroups;  // read by the epilogue warp
   int slot0, n_ent, n_tiles_entry, pad;
 };
 
 struct SmemPlan {
-  int ring, bars, rbars, descs, metas, rred, red, misc, ecache, escr, pend, flags, total;
+  int ring, bars, rbars, ebar, descs, metas, rred, red, misc, ecache, escr, pend, flags, total;
 };
 
 constexpr int kRedSlots = 4;
@@ -66,7 +67,8 @@ __host__ __device__ inline SmemPlan smem_plan(int n_stages, int ring_bytes, int 
   p.ring = 0;
   p.bars = ring_bytes;
   p.rbars = p.bars + 2 * n_stages * 8;
-  p.descs = p.rbars + 2 * kRedSlots * 8;
+  p.ebar = p.rbars + 2 * kRedSlots * 8;  // the producer's work-entry copy
+  p.descs = p.ebar + 16;
   p.metas = p.descs + n_stages * (int)sizeof(Desc);
   // the router's scratch (rred, misc) shares bytes with the epilogue ring: a
   // CTA's router tiles and the routing come before any of its gate/up or down
@@ -204,18 +206,14 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         if (!wait_flag_geq(&P.sync->routing_ready, 1, P.timeout_ns, P.status, kSiteRouting, t)) { ok = false; break; }
         fence_proxy_async_global();
         n_rent = __ldcg(&P.sync->n_rent);
-        // 16-byte loads, eight in flight at a time
-        const int4* src = reinterpret_cast<const int4*>(P.entries + P.n_sh);
-        int4* dst = reinterpret_cast<int4*>(ecache + P.n_sh);
-        const int nv = n_rent * (int)(sizeof(Entry) / 16);
-        for (int i = 0; i < nv; i += 8) {
-          int4 v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (i + u < nv) v[u] = __ldcg(src + i + u);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (i + u < nv) dst[i + u] = v[u];
+        // the routed entries, in one bulk copy (their writers fenced them for
+        // the async proxy before the routing flag)
+        if (n_rent > 0) {
+          uint64_t* ebar = reinterpret_cast<uint64_t*>(smem + plan.ebar);
+          const uint32_t eb = (uint32_t)n_rent * (uint32_t)sizeof(Entry);
+          mbar_arrive_expect_tx(ebar, eb);
+          bulk_g2s(ecache + P.n_sh, P.entries + P.n_sh, eb, ebar);
+          if (!mbar_wait_bounded(ebar, 0, P.timeout_ns, P.status, kSiteEntry, -1)) { ok = false; break; }
         }
       }
       const int A = NR + NSG + NSD;
@@ -272,7 +270,15 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     }
     const bool xslice = kind == kRouter || kind == kXRec;  // the stage holds a slice of x
     const uint32_t per = xslice ? (uint32_t)(nbc * kRouterCc * XEL) : (uint32_t)(nbc * RB);
-    const uint32_t wb = (uint32_t)cbytes;
+    // A group that is one chunk may share its stage with the next groups of
+    // the tile (contiguous in memory, same records): fewer, larger stages,
+    // as long as two of them fit the ring.
+    int gps = 1;
+    if (!xslice && nch == 1)
+      while (2 * gps <= 4 && ngroups % (2 * gps) == 0 &&
+             (int64_t)2 * gps * cbytes + (int64_t)M * per <= (int64_t)(P.ring_bytes / 2))
+        gps *= 2;
+    const uint32_t wb = (uint32_t)(gps * cbytes);
     const uint32_t resv = wb;
     const int need = (int)((resv + (uint32_t)M * per + 127u) & ~127u);
     // activation sources of this tile at chunk 0, and their step per chunk
@@ -295,9 +301,9 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     }
     const int4 h3 = make_int4(slot0, P.n_sh + max(n_rent, 0), n_tiles, 0);
     bool dep_ok = xslice;
-    const int nstages = ngroups * nch;
+    const int nstages = ngroups * nch / gps;
     for (int q = 0; q < nstages && ok; ++q) {
-      const int g = q / nch, c = q - g * nch;
+      const int g = q * gps / nch, c = q * gps - g * nch;
       // ring space: a free slot, then free bytes
       while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
       int pos = 0;
@@ -314,12 +320,12 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       const int kch = xslice ? kRouterTileChunks * rbt + c : 0;
       int4* dd = reinterpret_cast<int4*>(descs + s);
       dd[0] = make_int4(kind, c, nch, M);
-      dd[1] = make_int4(nbc, fmt, rgk | kch, pos);
+      dd[1] = make_int4(nbc, fmt, xslice ? rgk | kch : gps, pos);
       dd[2] = make_int4(entry, rbt, g, ngroups);
       dd[3] = h3;
       uint8_t* stage = smem + plan.ring + pos;
       mbar_arrive_expect_tx(&full[s], wb + (uint32_t)M * per);
-      if (wb) bulk_g2s_hint(stage, wbase + (int64_t)q * cbytes, wb, &full[s], wpol);
+      if (wb) bulk_g2s_hint(stage, wbase + (int64_t)q * wb, wb, &full[s], wpol);
       if (!dep_ok) {
         if (kind == kGateUp) {
           // shared gate/up needs the x records; routed ones were gated by the routing flag
@@ -439,10 +445,10 @@ __device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float
 // per warp).  acc[m] collects this warp's share of the lane's row against
 // vector m; the 8 warps' shares are summed by the epilogue warp.
 template <int L, int M>
-__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int fmt, float (&acc)[kGroup]) {
+__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, const uint8_t* A, int nbc, int fmt,
+                                             float (&acc)[kGroup]) {
   constexpr int RB = rec_bytes(L);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint8_t* A = stage + chunk_bytes(fmt, nbc * 32);
   if (fmt == MOE_Q8_0) {
     const __half* sc = reinterpret_cast<const __half*>(stage + nbc * 1024);
 #pragma unroll 2
@@ -482,12 +488,13 @@ __device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, int nbc, int 
 // tokens unroll without predicates (a runtime bound there keeps the loads of
 // different tokens from being scheduled together).
 template <int L>
-__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, int nbc, int fmt, int M, float (&acc)[kGroup]) {
+__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, const uint8_t* A, int nbc, int fmt, int M,
+                                           float (&acc)[kGroup]) {
   switch (M) {
-    case 1: gemv_chunk_m<L, 1>(stage, nbc, fmt, acc); break;
-    case 2: gemv_chunk_m<L, 2>(stage, nbc, fmt, acc); break;
-    case 3: gemv_chunk_m<L, 3>(stage, nbc, fmt, acc); break;
-    default: gemv_chunk_m<L, kGroup>(stage, nbc, fmt, acc); break;
+    case 1: gemv_chunk_m<L, 1>(stage, A, nbc, fmt, acc); break;
+    case 2: gemv_chunk_m<L, 2>(stage, A, nbc, fmt, acc); break;
+    case 3: gemv_chunk_m<L, 3>(stage, A, nbc, fmt, acc); break;
+    default: gemv_chunk_m<L, kGroup>(stage, A, nbc, fmt, acc); break;
   }
 }
 
@@ -704,6 +711,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
         int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + __popc(starts & below));
         dst[0] = make_int4(e_i, lane, M, tk[0]);
         dst[1] = make_int4(M > 1 ? tk[1] : 0, M > 2 ? tk[2] : 0, M > 3 ? tk[3] : 0, 0);
+        fence_proxy_async_global();  // the producers fetch the entries with a bulk copy
       }
       n_rent = __popc(starts);
     }
@@ -763,6 +771,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
         dst[0] = make_int4(e, slot0, M, tok[0]);
         dst[1] = make_int4(tok[1], tok[2], tok[3], 0);
       }
+      fence_proxy_async_global();  // the producers fetch the entries with a bulk copy
     }
     if (tid == 0) {
 #pragma unroll 4
@@ -946,25 +955,43 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       if (flags[0]) finalize_routing(P, misc);
       consumer_sync();
     } else {
-      if (d.chunk == 0) {
+      // gate/up or down: one chunk of a group, or gps whole groups of one
+      // chunk each (their weights back to back, then the shared records)
+      const int gps = d.rgks;
+      const int cb = (int)chunk_bytes(d.fmt, d.nbc * 32);
+      const uint8_t* recs = stage + gps * cb;
+      bool failed = false;
+      for (int j = 0; j < gps; ++j) {
+        if (d.chunk == 0) {
 #pragma unroll
-        for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
+          for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
+        }
+        gemv_chunk<L>(stage + j * cb, recs, d.nbc, d.fmt, d.M, acc);
+        if (j == gps - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (d.chunk == d.nch - 1) {
+          // a 32-row group is complete: hand this warp's share of every row to
+          // the epilogue warp (the descriptor is copied before the stage is
+          // released, since the producer reuses it)
+          if (!mbar_wait_bounded(&rempty[rs], rph ^ 1u, P.timeout_ns, P.status, kSiteRedEmpty, rs)) {
+            failed = true;
+            break;
+          }
+          float4* slot = reinterpret_cast<float4*>(red + rs * (kRedSlotBytes / 4));  // [warp][row][token]
+          slot[warp * kRows + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          if (tid == 0) {
+            Desc dj = d;
+            dj.group = d.group + j;
+            metas[rs] = dj;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rfull[rs]);
+          if (++rs == kRedSlots) { rs = 0; rph ^= 1u; }
+        }
       }
-      gemv_chunk<L>(stage, d.nbc, d.fmt, d.M, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (d.chunk == d.nch - 1) {
-        // a 32-row group is complete: hand this warp's share of every row to
-        // the epilogue warp (the descriptor is copied before the stage is
-        // released, since the producer reuses it)
-        if (!mbar_wait_bounded(&rempty[rs], rph ^ 1u, P.timeout_ns, P.status, kSiteRedEmpty, rs)) break;
-        float4* slot = reinterpret_cast<float4*>(red + rs * (kRedSlotBytes / 4));  // [warp][row][token]
-        slot[warp * kRows + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        if (tid == 0) metas[rs] = d;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rfull[rs]);
-        if (++rs == kRedSlots) { rs = 0; rph ^= 1u; }
-      }
+      if (failed) break;
     }
     if (++s == P.n_stages) { s = 0; ph ^= 1u; }
   }
@@ -1112,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       mbar_init(&rfull[i], kConsumerWarps);
       mbar_init(&rempty[i], 1);
     }
+    mbar_init(reinterpret_cast<uint64_t*>(smem + plan.ebar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
