@@ -149,6 +149,19 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (launched
+// with programmatic stream serialization) start its CTAs early, and wait for
+// the previous kernel's completion and memory before reading what it wrote.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Prefetch of a global range into L2 (a hint; 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // bulk_g2s with an L2 cache policy.
 __device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t policy) {

@@ -112,7 +112,7 @@ __device__ inline bool wait_flag_geq(const int* p, int v, uint64_t limit_ns, int
       return false;
     }
     __nanosleep(ns);
-    ns = min(ns * 2, 512);
+    ns = min(ns * 2, 128);
   }
 }
 
@@ -301,6 +301,14 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     }
     const int4 h3 = make_int4(slot0, P.n_sh + max(n_rent, 0), n_tiles, 0);
     bool dep_ok = xslice;
+    if (kind == kGateUp && shared_e) {
+      // the shared expert's loads start once the x records exist: in the
+      // launch's first microseconds the router tiles, which the routing waits
+      // for, get the memory bandwidth
+      dep_ok = wait_flag_geq(&P.sync->x_done, P.T * P.n_rc, P.timeout_ns, P.status, kSiteX, t);
+      if (dep_ok) fence_proxy_async_global();
+      else ok = false;
+    }
     const int nstages = ngroups * nch / gps;
     for (int q = 0; q < nstages && ok; ++q) {
       const int g = q * gps / nch, c = q * gps - g * nch;
@@ -328,8 +336,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       if (wb) bulk_g2s_hint(stage, wbase + (int64_t)q * wb, wb, &full[s], wpol);
       if (!dep_ok) {
         if (kind == kGateUp) {
-          // shared gate/up needs the x records; routed ones were gated by the routing flag
-          dep_ok = !shared_e || wait_flag_geq(&P.sync->x_done, P.T * P.n_rc, P.timeout_ns, P.status, kSiteX, t);
+          dep_ok = true;  // routed gate/up: gated by the routing flag (shared: waited above)
         } else if (readybits[entry >> 5] & (1u << (entry & 31))) {
           dep_ok = true;
         } else {
@@ -1129,7 +1136,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   uint64_t* rempty = rfull + kRedSlots;
   int* flags = reinterpret_cast<int*>(smem + plan.flags);
   int* pend = reinterpret_cast<int*>(smem + plan.pend);
+  // The next launch in the stream may start as this one's CTAs leave; until
+  // griddep_wait it touches nothing this launch (or an earlier one) writes.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
+    // constant data only: warm L2 with one router tile's weights (tile = CTA)
+    if ((int)blockIdx.x < P.n_rg * P.n_kt) {
+      const int rg = blockIdx.x / P.n_kt, kt = blockIdx.x % P.n_kt;
+      const int nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * kt);
+      prefetch_l2(P.router + ((int64_t)rg * P.n_ks * 64 + kRouterTileChunks * 32 * kt) * kRows * 16,
+                  (uint32_t)(nbc * chunk_bytes(MOE_F32, kRouterCc)));
+    }
     pend[0] = 0;
     for (int i = 0; i < P.n_stages; ++i) {
       mbar_init(&full[i], 1);
@@ -1142,6 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     mbar_init(reinterpret_cast<uint64_t*>(smem + plan.ebar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  griddep_wait();  // x, the workspace and its counters are the previous launches' to finish with
   __syncthreads();
 
   const int warp = threadIdx.x >> 5;
@@ -1197,10 +1215,22 @@ cudaError_t small_t_configure(int L, int smem_bytes) {
   return cudaFuncSetAttribute(moe_small_t_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
+// Launched with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes (it waits for it before reading
+// anything that kernel could have written).
 cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st) {
-  if (L == 2) moe_small_t_kernel<2><<<grid, kThreads, smem_bytes, st>>>(P);
-  else moe_small_t_kernel<4><<<grid, kThreads, smem_bytes, st>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L == 2) return cudaLaunchKernelEx(&cfg, moe_small_t_kernel<2>, P);
+  return cudaLaunchKernelEx(&cfg, moe_small_t_kernel<4>, P);
 }
 
 }  // namespace moe
