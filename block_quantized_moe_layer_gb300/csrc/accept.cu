@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const int32_t* _
   __shared__ float sv[kAcceptThreads / 32];
   __shared__ int si[kAcceptThreads / 32];
   __shared__ int last;
+  griddep_launch_dependents();
+  griddep_wait();  // the logits and drafts may come from the previous kernel in the stream
   const int row = blockIdx.x / S, sp = blockIdx.x % S;
   const int per = (V + S - 1) / S;
   const int c0 = sp * per, c1 = min(V, c0 + per);
@@ -101,8 +103,8 @@ cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int 
   const int S = accept_splits(V);
   int* counter = static_cast<int*>(ws);
   ArgPart* parts = reinterpret_cast<ArgPart*>(static_cast<uint8_t*>(ws) + 16);
-  accept_kernel<<<(k + 1) * S, kAcceptThreads, 0, st>>>(draft, k, logits, V, S, out_n, out_next, counter, parts);
-  return cudaGetLastError();
+  return launch_pdl(accept_kernel, (k + 1) * S, kAcceptThreads, 0, st, draft, k, logits, V, S, out_n, out_next,
+                    counter, parts);
 }
 
 // Scratch of the allocation-free entry point (mtp_verify_accept_noalloc).

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 lm_head_kernel(const int8_t* __restrict__ q, const __half* __restrict__ sc, int V, int H, const void* x, int T,
                float eps, float* __restrict__ logits) {
   extern __shared__ __align__(16) uint8_t lsm[];
+  griddep_launch_dependents();
+  griddep_wait();  // x may come from the previous kernel in the stream
   uint8_t* lo = lsm;                                          // [T][H]
   int8_t* hi = reinterpret_cast<int8_t*>(lsm + kLmTokens * H);  // [T][H]
   float* asc = reinterpret_cast<float*>(lsm + 2 * kLmTokens * H);  // [T][H/32]
@@ -154,13 +156,13 @@ cudaError_t lm_forward(const moe_lm_head* lm, const void* x, int T, float eps, f
     const int n = min(kLmTokens, T - t0);
     const void* xg = static_cast<const uint8_t*>(x) + (size_t)t0 * lm->H * esz;
     float* lg = logits + (int64_t)t0 * lm->V;
+    cudaError_t e;
     if (lm->act == MOE_ACT_BF16)
-      lm_head_kernel<2><<<lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st>>>(lm->q, lm->sc, lm->V, lm->H, xg, n,
-                                                                               eps, lg);
+      e = launch_pdl(lm_head_kernel<2>, lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st, (const int8_t*)lm->q,
+                     (const __half*)lm->sc, lm->V, lm->H, xg, n, eps, lg);
     else
-      lm_head_kernel<4><<<lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st>>>(lm->q, lm->sc, lm->V, lm->H, xg, n,
-                                                                               eps, lg);
-    cudaError_t e = cudaGetLastError();
+      e = launch_pdl(lm_head_kernel<4>, lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st, (const int8_t*)lm->q,
+                     (const __half*)lm->sc, lm->V, lm->H, xg, n, eps, lg);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict
                                                           void* __restrict__ h_out, void* __restrict__ xn, int H,
                                                           float eps) {
   __shared__ float red[8];
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t base = (int64_t)blockIdx.x * H;
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(256) draft_rows_kernel(const void* __restrict_
                                                          int k, int H, float eps, void* __restrict__ hin,
                                                          void* __restrict__ rows) {
   __shared__ float red[8];
+  griddep_launch_dependents();
+  griddep_wait();
   const int j = blockIdx.x / k, i = blockIdx.x % k;
   if (i > j) return;
   const int64_t src = (int64_t)i * H, nz = ((int64_t)j * k + i) * H;
@@ -84,16 +88,43 @@ __global__ void __launch_bounds__(256) draft_rows_kernel(const void* __restrict_
     st_act<L>(hin, nz + c, (ld_act<L>(h, src + c) + noise[nz + c]) * inv);
 }
 
-// ids[r] = argmax of row r (lowest index on ties); one CTA per row.
-__global__ void argmax_rows_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids) {
-  __shared__ float sv[8];
-  __shared__ int si[8];
+// ids[r] = argmax of row r (lowest index on ties); one CTA of kArgThreads per
+// row.  With V % 4 == 0 each thread reads float4 c4 = t, t + kArgThreads, ...
+// eight loads at a time, all in flight before the compares.
+constexpr int kArgThreads = 1024;
+__global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const float* __restrict__ logits, int V,
+                                                                  int32_t* __restrict__ ids) {
+  __shared__ float sv[kArgThreads / 32];
+  __shared__ int si[kArgThreads / 32];
+  griddep_launch_dependents();
+  griddep_wait();
   const float* row = logits + (int64_t)blockIdx.x * V;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
-  for (int c = threadIdx.x; c < V; c += blockDim.x) {
-    const float v = row[c];
+  // per thread the indices visited increase, so strict > keeps the lowest
+  auto take = [&](float v, int c) {
     if (v > bv || bi == 0x7fffffff) { bv = v; bi = c; }
+  };
+  if ((V & 3) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = V / 4;
+    for (int c0 = threadIdx.x; c0 < n4; c0 += 8 * kArgThreads) {
+      float4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + u * kArgThreads < n4) a[u] = __ldg(r4 + c0 + u * kArgThreads);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + u * kArgThreads < n4) {
+          const int c = 4 * (c0 + u * kArgThreads);
+          take(a[u].x, c);
+          take(a[u].y, c + 1);
+          take(a[u].z, c + 2);
+          take(a[u].w, c + 3);
+        }
+    }
+  } else {
+    for (int c = threadIdx.x; c < V; c += kArgThreads) take(row[c], c);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -105,7 +136,7 @@ __global__ void argmax_rows_kernel(const float* __restrict__ logits, int V, int3
   if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < (int)(blockDim.x / 32); ++w)
+    for (int w = 1; w < kArgThreads / 32; ++w)
       if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
     ids[blockIdx.x] = bi;
   }
@@ -247,29 +278,34 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   uint8_t* w = static_cast<uint8_t*>(workspace);
   const size_t esz = act == MOE_ACT_BF16 ? 2 : 4;
   int rc;
+  cudaError_t e = cudaSuccess;
   // target stack: pre-norm residual blocks h <- h + MoE(rmsnorm(h)); the
   // hidden state ping-pongs between hA and hB, xn holds the normalised rows
   const void* cur = x;
   void* xn = w + r.xn;
   void* yt = w + r.ytmp;
-  if (act == MOE_ACT_BF16) add_rmsnorm_kernel<2><<<k + 1, 256, 0, st>>>(x, nullptr, nullptr, xn, H, eps);
-  else add_rmsnorm_kernel<4><<<k + 1, 256, 0, st>>>(x, nullptr, nullptr, xn, H, eps);
-  MCK(cudaGetLastError(), "mtp_round: norm");
+  if (act == MOE_ACT_BF16)
+    e = launch_pdl(add_rmsnorm_kernel<2>, k + 1, 256, 0, st, x, (const void*)nullptr, (void*)nullptr, xn, H, eps);
+  else
+    e = launch_pdl(add_rmsnorm_kernel<4>, k + 1, 256, 0, st, x, (const void*)nullptr, (void*)nullptr, xn, H, eps);
+  MCK(e, "mtp_round: norm");
   for (int l = 0; l < n_target; ++l) {
     void* out = w + ((l & 1) ? r.hB : r.hA);
     if ((rc = moe_forward(target_layers[l], xn, k + 1, yt, stream))) return rc;
-    if (act == MOE_ACT_BF16) add_rmsnorm_kernel<2><<<k + 1, 256, 0, st>>>(cur, yt, out, xn, H, eps);
-    else add_rmsnorm_kernel<4><<<k + 1, 256, 0, st>>>(cur, yt, out, xn, H, eps);
-    MCK(cudaGetLastError(), "mtp_round: residual + norm");
+    if (act == MOE_ACT_BF16) e = launch_pdl(add_rmsnorm_kernel<2>, k + 1, 256, 0, st, cur, yt, out, xn, H, eps);
+    else e = launch_pdl(add_rmsnorm_kernel<4>, k + 1, 256, 0, st, cur, yt, out, xn, H, eps);
+    MCK(e, "mtp_round: residual + norm");
     cur = out;
   }
   if ((rc = moe_lm_head_forward(lm, cur, k + 1, eps, target_logits, stream))) return rc;
   // noisy rows for the heads, and the rows the drafts are read from
   if (act == MOE_ACT_BF16)
-    draft_rows_kernel<2><<<k * k, 256, 0, st>>>(cur, noise, k, H, eps, w + r.hin, w + r.rows);
+    e = launch_pdl(draft_rows_kernel<2>, k * k, 256, 0, st, cur, noise, k, H, eps, (void*)(w + r.hin),
+                   (void*)(w + r.rows));
   else
-    draft_rows_kernel<4><<<k * k, 256, 0, st>>>(cur, noise, k, H, eps, w + r.hin, w + r.rows);
-  MCK(cudaGetLastError(), "mtp_round: draft rows");
+    e = launch_pdl(draft_rows_kernel<4>, k * k, 256, 0, st, cur, noise, k, H, eps, (void*)(w + r.hin),
+                   (void*)(w + r.rows));
+  MCK(e, "mtp_round: draft rows");
   uint8_t* hout = head_out ? static_cast<uint8_t*>(head_out) : w + r.hout;
   for (int j = 0; j < k; ++j) {
     const size_t o = (size_t)j * k * H * esz;
@@ -277,8 +313,8 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   }
   float* dlog = reinterpret_cast<float*>(w + r.dlog);
   if ((rc = moe_lm_head_forward(lm, w + r.rows, k, eps, dlog, stream))) return rc;
-  argmax_rows_kernel<<<k, 256, 0, st>>>(dlog, V, draft_ids);
-  MCK(cudaGetLastError(), "mtp_round: draft argmax");
+  e = launch_pdl(argmax_rows_kernel, k, kArgThreads, 0, st, (const float*)dlog, V, draft_ids);
+  MCK(e, "mtp_round: draft argmax");
   return mtp_verify_accept(draft_ids, k, target_logits, V, out_n_accepted, out_next_token, w + r.acc,
                            accept_workspace_bytes(k, V), stream);
 }
