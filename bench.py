@@ -55,6 +55,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def replica_max_ms(total_ms, device):
+    """The job's time: the longest rank's timed region (every rank ran the same
+    steps on its own replica; no data-path exchange)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(total_ms)
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def per_unit_us(total_ms, steps, world):
+    """Whole-job µs per unit (layer or round): the job's time over the units
+    that all ranks processed."""
+    return total_ms * 1e3 / (steps * world)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -228,11 +246,8 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_stop)
     launch_us = [a.elapsed_time(b) * 1e3 for (a, b) in evs[: (args.steps + sample_every - 1) // sample_every]]
     kern_us = statistics.mean(launch_us)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = t.item()
-    us_per_layer = total_ms * 1e3 / (args.steps * world)
+    total_ms = replica_max_ms(total_ms, "cuda")
+    us_per_layer = per_unit_us(total_ms, args.steps, world)
 
     # end to end: pinned host x -> device, forward, device -> pinned host y, every step
     xh = x.cpu().pin_memory()
@@ -286,6 +301,10 @@ def run_ours(args):
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "steps": e2e_steps},
         "gpu_launches": args.steps * (1 if w.T <= 8 else 8),
+        # event-bracketed launches (every 8th of the timed loop)
+        "launch_us": {"p10": round(float(np.percentile(launch_us, 10)), 3),
+                      "p50": round(float(np.percentile(launch_us, 50)), 3),
+                      "p90": round(float(np.percentile(launch_us, 90)), 3), "samples": len(launch_us)},
     }
     if w.T > 8:
         # a contraction: the roofline is the tensor pipe's (bf16 MMA), the unit
@@ -360,14 +379,18 @@ def run_round(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for _ in range(steps):
         step(x, noise)
     t1.record(stream)
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     clk = clocks.stop()
-    us = t0.elapsed_time(t1) * 1e3 / steps
+    us = per_unit_us(replica_max_ms(t0.elapsed_time(t1), "cuda"), steps, world)
     xh, nh = x.cpu().pin_memory(), noise.cpu().pin_memory()
     ah = torch.empty(2, dtype=torch.int32).pin_memory()
     dh = torch.empty(k, dtype=torch.int32).pin_memory()
@@ -388,7 +411,7 @@ def run_round(args):
     out = {
         "metric": "µs per MTP draft/verify round (8 target layers T=4, draft heads T=1,2,3, 2 LM-head passes, "
                   "acceptance) and effective HBM GB/s",
-        "value": round(us, 2), "unit": "us/round", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "value": round(us, 2), "unit": "us/round", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "q8_0/q4ks weights x bf16 activations (int dp4a, fp32 accumulate)",
         "data": "synthetic (seeded, random-init weights of the workload's shapes)",
@@ -410,6 +433,8 @@ def run_round(args):
     for L in layers + heads:
         L.close()
     lm.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(out))
 
