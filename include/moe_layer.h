@@ -108,7 +108,14 @@ int moe_layer_create(const moe_layer_desc* desc, void* stream, moe_layer** out);
  * x and y must be 16-byte aligned and must not overlap.  T == 0 returns
  * MOE_OK and launches nothing.  No allocation happens here.  Calls on one
  * layer must not run concurrently (they share the layer's workspace).
- * Device-side wait failures are reported by moe_layer_status(). */
+ * Device-side wait failures are reported by moe_layer_status().
+ * Launch overlap (T <= 8): the kernel is launched with programmatic stream
+ * serialization.  Its blocks may start while the previous kernel in the
+ * stream is still running; before that kernel completes they only read the
+ * layer's own constant weights, and they wait for it (and for its memory
+ * operations) before reading x or the workspace.  Stream order is therefore
+ * kept for every kernel, whether or not the previous kernel triggers early.
+ * The kernel lets the next kernel in the stream launch early too. */
 int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
 
 /* y = x + MoE(x): a residual layer (the target stack of an MTP round,
@@ -161,7 +168,9 @@ int moe_quantize(int32_t fmt, const float* w, int64_t rows, int64_t cols, void* 
  *   workspace: device scratch of mtp_verify_accept_workspace_bytes(k, V)
  *   bytes, 16-byte aligned, owned by the caller; it must be zero-filled
  *   before its first use and is left zero-filled by every call that
- *   completes.  Calls sharing one workspace must not overlap on the GPU. */
+ *   completes.  Calls sharing one workspace must not overlap on the GPU.
+ *   Launched with programmatic stream serialization like moe_forward: it
+ *   waits for the previous kernel in the stream before reading anything. */
 size_t mtp_verify_accept_workspace_bytes(int32_t k, int32_t V);
 int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, int32_t V,
                       int32_t* out_n_accepted, int32_t* out_next_token, void* workspace,
