@@ -147,6 +147,60 @@ def measured_tensor_peak():
     return 1700.0, "fallback sustained bf16 figure"
 
 
+def run_e2e(stream, steps, host_in, dev_in, run, dev_out, host_out):
+    """End-to-end steps: each step copies its inputs host -> device (pinned),
+    runs, and copies its result device -> host (pinned).  The copies have their
+    own streams and the buffers are doubled, so step i+1's input copy and step
+    i's result copy overlap the neighbouring steps' kernels, as a serving loop
+    would run them.  dev_in[b] / dev_out[b] / host_out[b]: lists of tensors of
+    buffer b; run(i, b) launches step i on `stream` reading dev_in[b] and
+    writing dev_out[b].  Returns µs per step: events on `stream` from before
+    the first input copy to after the last result copy."""
+    import torch
+    nb = len(dev_in)
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    x_ready = [torch.cuda.Event() for _ in range(nb)]
+    ran = [torch.cuda.Event() for _ in range(nb)]
+    y_read = [torch.cuda.Event() for _ in range(nb)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    h2d.wait_event(e0)
+
+    def copy_in(i):
+        b = i % nb
+        with torch.cuda.stream(h2d):
+            if i >= nb:
+                h2d.wait_event(ran[b])  # step i - nb has read buffer b
+            for d, h in zip(dev_in[b], host_in):
+                d.copy_(h, non_blocking=True)
+            x_ready[b].record(h2d)
+
+    copy_in(0)
+    for i in range(steps):
+        b = i % nb
+        if i + 1 < steps:
+            copy_in(i + 1)
+        stream.wait_event(x_ready[b])
+        if i >= nb:
+            stream.wait_event(y_read[b])  # step i - nb's result has been copied out
+        run(i, b)
+        ran[b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ran[b])
+            for h, d in zip(host_out[b], dev_out[b]):
+                h.copy_(d, non_blocking=True)
+            y_read[b].record(d2h)
+    stream.wait_event(y_read[(steps - 1) % nb])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps
+
+
+E2E_NOTE = ("every step: inputs host->device from pinned memory, the step, result device->host to pinned "
+            "memory; copies on their own streams, buffers doubled, so copies overlap neighbouring steps")
+
+
 def traffic_record(kernel_src):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -249,22 +303,17 @@ def run_ours(args):
     total_ms = replica_max_ms(total_ms, "cuda")
     us_per_layer = per_unit_us(total_ms, args.steps, world)
 
-    # end to end: pinned host x -> device, forward, device -> pinned host y, every step
+    # end to end through the public call: pinned host x -> device, forward,
+    # device -> pinned host y, every step
     xh = x.cpu().pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    xd = torch.empty_like(x)
-    e2e_steps = min(args.e2e_steps, args.steps)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        layers[i % len(layers)].forward(xd, y)
-        yh.copy_(y, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1e3 / e2e_steps
-    assert torch.equal(yh.cuda(), y)
+    xd = [torch.empty_like(x) for _ in range(2)]
+    yd = [torch.empty_like(x) for _ in range(2)]
+    yh = [torch.empty_like(xh).pin_memory() for _ in range(2)]
+    e2e_steps = max(2, min(args.e2e_steps, args.steps))
+    e2e_us = run_e2e(stream, e2e_steps, [xh], [[a] for a in xd],
+                     lambda i, b: layers[i % len(layers)].forward(xd[b], yd[b]), [[a] for a in yd],
+                     [[a] for a in yh])
+    assert torch.equal(yh[(e2e_steps - 1) % 2].cuda(), y)
 
     peak, peak_src = measured_peaks()
     achieved = alg / (kern_us * 1e-6) / 1e9
@@ -299,7 +348,8 @@ def run_ours(args):
                      "kernel": kname, "kernel_us": round(kern_us, 3)},
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": xh.numel() * xh.element_size(),
-                "d2h_bytes_per_step": yh.numel() * yh.element_size(), "steps": e2e_steps},
+                "d2h_bytes_per_step": yh[0].numel() * yh[0].element_size(), "steps": e2e_steps,
+                "copies": E2E_NOTE},
         "gpu_launches": args.steps * (1 if w.T <= 8 else 8),
         # event-bracketed launches (every 8th of the timed loop)
         "launch_us": {"p10": round(float(np.percentile(launch_us, 10)), 3),
@@ -356,7 +406,7 @@ def run_round(args):
     stream = torch.cuda.current_stream()
     lib = pkg.lib()
 
-    def step(xd, nd):
+    def step(xd, nd, acc=acc, drafts=drafts):
         rc = lib.mtp_round(tl, len(layers), hl, k, lm.handle, xd.data_ptr(), nd.data_ptr(), 1e-6, wp, wn,
                            logits.data_ptr(), None, drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4,
                            stream.cuda_stream)
@@ -392,21 +442,17 @@ def run_round(args):
     clk = clocks.stop()
     us = per_unit_us(replica_max_ms(t0.elapsed_time(t1), "cuda"), steps, world)
     xh, nh = x.cpu().pin_memory(), noise.cpu().pin_memory()
-    ah = torch.empty(2, dtype=torch.int32).pin_memory()
-    dh = torch.empty(k, dtype=torch.int32).pin_memory()
-    xd, nd = torch.empty_like(x), torch.empty_like(noise)
-    e2e_steps = min(args.e2e_steps, steps)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for _ in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        nd.copy_(nh, non_blocking=True)
-        step(xd, nd)
-        ah.copy_(acc, non_blocking=True)
-        dh.copy_(drafts, non_blocking=True)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    e2e = t0.elapsed_time(t1) * 1e3 / e2e_steps
+    xd = [torch.empty_like(x) for _ in range(2)]
+    nd = [torch.empty_like(noise) for _ in range(2)]
+    ad = [torch.empty(2, dtype=torch.int32, device="cuda") for _ in range(2)]
+    dd = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(2)]
+    ah = [torch.empty(2, dtype=torch.int32).pin_memory() for _ in range(2)]
+    dh = [torch.empty(k, dtype=torch.int32).pin_memory() for _ in range(2)]
+    e2e_steps = max(2, min(args.e2e_steps, steps))
+    e2e = run_e2e(stream, e2e_steps, [xh, nh], [[xd[b], nd[b]] for b in range(2)],
+                  lambda i, b: step(xd[b], nd[b], ad[b], dd[b]), [[ad[b], dd[b]] for b in range(2)],
+                  [[ah[b], dh[b]] for b in range(2)])
+    assert ah[(e2e_steps - 1) % 2].tolist() == acc.cpu().tolist()
     peak, peak_src = measured_peaks()
     out = {
         "metric": "µs per MTP draft/verify round (8 target layers T=4, draft heads T=1,2,3, 2 LM-head passes, "
@@ -425,7 +471,7 @@ def run_round(args):
         "clocks": clk,
         "e2e": {"value": round(e2e, 2), "unit": "us/round",
                 "h2d_bytes_per_step": x.numel() * x.element_size() + noise.numel() * noise.element_size(),
-                "d2h_bytes_per_step": 4 * (2 + k), "steps": e2e_steps},
+                "d2h_bytes_per_step": 4 * (2 + k), "steps": e2e_steps, "copies": E2E_NOTE},
         # per round: a layer launch and a residual/norm launch per target layer, the
         # first norm, two LM-head launches, draft rows, the heads, argmax, acceptance
         "gpu_launches": steps * (2 * len(layers) + len(heads) + 6),
