@@ -36,6 +36,15 @@ lm_head_kernel(const int8_t* __restrict__ q, const __half* __restrict__ sc, int 
                float eps, float* __restrict__ logits) {
   extern __shared__ __align__(16) uint8_t lsm[];
   griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    // constant data: start this CTA's first rows on their way to L2 while the
+    // previous kernel in the stream finishes
+    const int64_t r0 = (int64_t)blockIdx.x * (kLmThreads / 32) * kLmRows;
+    if (r0 < V) {
+      const int64_t nr = min((int64_t)(kLmThreads / 32) * kLmRows, (int64_t)V - r0);
+      prefetch_l2(q + r0 * H, (uint32_t)(nr * H));
+    }
+  }
   griddep_wait();  // x may come from the previous kernel in the stream
   uint8_t* lo = lsm;                                          // [T][H]
   int8_t* hi = reinterpret_cast<int8_t*>(lsm + kLmTokens * H);  // [T][H]
