@@ -64,3 +64,34 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.moe_quantize(7, None, 1, 32, None, None) == pkg.MOE_EFORMAT
     assert lib.moe_quantize(pkg.FMT_Q8_0, None, 1, 32, None, None) == pkg.MOE_EINVAL
     assert out.value is None
+
+
+def test_mtp_entry_points_reject_bad_arguments_on_host(lib):
+    # workspace sizing: k outside 1..7, V outside 1..2^24, unknown act dtype
+    assert lib.mtp_round_workspace_bytes(4096, 3, 32768, pkg.ACT_BF16) > 0
+    assert lib.mtp_round_workspace_bytes(4096, 0, 32768, pkg.ACT_BF16) == 0
+    assert lib.mtp_round_workspace_bytes(4096, 8, 32768, pkg.ACT_BF16) == 0
+    assert lib.mtp_round_workspace_bytes(4096, 3, 0, pkg.ACT_BF16) == 0
+    assert lib.mtp_round_workspace_bytes(4096, 3, 32768, 7) == 0
+    # the round: k outside 1..7, then NULL arguments, before any device work
+    assert lib.mtp_round(None, 0, None, 0, None, None, None, 1e-6, None, 0, None, None, None, None, None,
+                         None) == pkg.MOE_EINVAL
+    assert b"k outside" in lib.moe_last_error()
+    assert lib.mtp_round(None, 0, None, 3, None, None, None, 1e-6, None, 0, None, None, None, None, None,
+                         None) == pkg.MOE_EINVAL
+    assert b"NULL" in lib.moe_last_error()
+    # the LM head: NULL, wrong format, shape and T_max checks
+    out = ctypes.c_void_p()
+    assert lib.moe_lm_head_create(None, 4, pkg.ACT_BF16, None, ctypes.byref(out)) == pkg.MOE_EINVAL
+    t = pkg.MoeTensor()
+    t.fmt, t.rows, t.cols = pkg.FMT_Q4KS, 1000, 4096
+    assert lib.moe_lm_head_create(ctypes.byref(t), 4, pkg.ACT_BF16, None, ctypes.byref(out)) == pkg.MOE_EFORMAT
+    t.fmt, t.cols = pkg.FMT_Q8_0, 4000  # H not a multiple of 512
+    assert lib.moe_lm_head_create(ctypes.byref(t), 4, pkg.ACT_BF16, None, ctypes.byref(out)) == pkg.MOE_EINVAL
+    t.cols = 4096
+    assert lib.moe_lm_head_create(ctypes.byref(t), 9, pkg.ACT_BF16, None, ctypes.byref(out)) == pkg.MOE_EINVAL
+    assert lib.moe_lm_head_create(ctypes.byref(t), 4, pkg.ACT_BF16, None, ctypes.byref(out)) == pkg.MOE_EINVAL
+    assert b"nbytes" in lib.moe_last_error()  # data NULL
+    assert out.value is None
+    assert lib.moe_lm_head_forward(None, None, 4, 1e-6, None, None) == pkg.MOE_EINVAL
+    assert lib.moe_forward_residual(None, None, 4, None, None) == pkg.MOE_EINVAL
