@@ -147,6 +147,21 @@ def measured_tensor_peak():
     return 1700.0, "fallback sustained bf16 figure"
 
 
+def expert_load_summary(offsets):
+    """Tokens per expert (M_e) from the routing offsets [E+1]: how many experts
+    got work, and the spread of their loads (a histogram over power-of-two
+    bins: bin b counts experts with 2^b <= M_e < 2^(b+1))."""
+    off = np.asarray(offsets, dtype=np.int64)
+    m = off[1:] - off[:-1]
+    used = m[m > 0]
+    if used.size == 0:
+        return {"experts_used": 0}
+    bins = np.bincount(np.floor(np.log2(used)).astype(np.int64))
+    return {"experts_used": int(used.size), "pairs": int(m.sum()), "min": int(used.min()),
+            "median": float(np.median(used)), "max": int(used.max()),
+            "pow2_hist": [int(b) for b in bins]}
+
+
 def run_e2e(stream, steps, host_in, dev_in, run, dev_out, host_out):
     """End-to-end steps: each step copies its inputs host -> device (pinned),
     runs, and copies its result device -> host (pinned).  The copies have their
@@ -267,6 +282,7 @@ def run_ours(args):
         L.status()
     offs = layers[0].routing(w.T)[2]
     n_unique = int((offs[1:] > offs[:-1]).sum().item())
+    load = expert_load_summary(offs.cpu().numpy())
     alg = algorithmic_bytes(w, n_unique)
 
     # timed region: exactly K steps; every 8th launch is bracketed by events
@@ -335,7 +351,7 @@ def run_ours(args):
         "data": "synthetic (seeded, random-init weights of the workload's shapes)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.top_k, "I": w.I,
                    "I_shared": w.I_shared, "routed_fmt": ["f32", "bf16", "q8_0", "q4ks"][w.routed_fmt],
-                   "unique_experts": n_unique, "algorithmic_bytes": alg,
+                   "unique_experts": n_unique, "algorithmic_bytes": alg, "tokens_per_expert": load,
                    "l2": f"rotating {len(layers)} weight copies of {layers[0].weight_bytes / 1e9:.2f} GB (> L2)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(w.T / (us_per_layer * 1e-6), 1),

@@ -55,3 +55,4 @@ def test_single_process_is_its_own_job():
     assert not dist.is_initialized()
     assert bench.replica_max_ms(7.25, "cpu") == 7.25
     assert bench.per_unit_us(7.25, 10, 1) == pytest.approx(725.0)
+
