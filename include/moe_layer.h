@@ -19,6 +19,17 @@
  *   FFN_e(v) = Wd_e (silu(Wg_e v) * (Wu_e v)),  silu(u) = u / (1 + e^-u);
  *   y[t] = sum_j g[t,j] FFN_ids[t,j](x[t]) + FFN_shared(x[t]).
  *
+ * Arithmetic:
+ *   - T <= 8: weights enter as their integer codes; x and the SwiGLU outputs
+ *     as 32-value block fixed point (16-bit limbs in bf16 mode, 32-bit in
+ *     fp32 mode).  Every block product is therefore exact, and block sums are
+ *     scaled and accumulated in fp32.
+ *   - The router logits are fp32 sums over 512-column slices, added across
+ *     slices exactly (as integer multiples of 2^-32) and rounded once.
+ *   - The same inputs give the same output bits on every call.
+ *   - T > 8: weights are dequantised to bf16; bf16 tensor-core products with
+ *     fp32 accumulation.
+ *
  * Conventions for every call:
  *   - Pointers are DEVICE pointers unless a comment says "host".
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
