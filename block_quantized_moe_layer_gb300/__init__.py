@@ -93,6 +93,12 @@ def _check(rc):
     return rc
 
 
+def _require(cond, msg):
+    """Argument checks that survive python -O (unlike assert)."""
+    if not cond:
+        raise MoEError(MOE_EINVAL, msg)
+
+
 def _stream(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -106,7 +112,8 @@ def quantized_bytes(fmt, rows, cols):
 def quantize(fmt, w, out=None, stream=None):
     """fp32 [rows, cols] CUDA tensor -> serialised uint8 CUDA tensor."""
     import torch
-    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous()
+    _require(w.is_cuda and w.dtype == torch.float32 and w.is_contiguous() and w.dim() == 2,
+             "quantize: w must be a contiguous 2-D fp32 CUDA tensor")
     rows, cols = w.shape
     n = quantized_bytes(fmt, rows, cols)
     if n == 0:
@@ -215,7 +222,10 @@ def verify_accept(draft_ids, logits, workspace=None, out=None, stream=None):
     import torch
     k = draft_ids.numel()
     V = logits.shape[1]
-    assert logits.shape[0] == k + 1 and logits.dtype == torch.float32 and logits.is_contiguous()
+    _require(logits.dim() == 2 and logits.shape[0] == k + 1 and logits.dtype == torch.float32
+             and logits.is_contiguous() and logits.is_cuda, "verify_accept: logits must be fp32 [k+1, V] on the GPU")
+    _require(k == 0 or (draft_ids.dtype == torch.int32 and draft_ids.is_contiguous() and draft_ids.is_cuda),
+             "verify_accept: draft_ids must be contiguous int32 on the GPU")
     if workspace is None:
         workspace = accept_workspace(k, V, logits.device)
     if out is None:
@@ -233,7 +243,10 @@ def verify_accept_noalloc(draft_ids, logits, out=None, stream=None):
     import torch
     k = draft_ids.numel()
     V = logits.shape[1]
-    assert logits.shape[0] == k + 1 and logits.dtype == torch.float32 and logits.is_contiguous()
+    _require(logits.dim() == 2 and logits.shape[0] == k + 1 and logits.dtype == torch.float32
+             and logits.is_contiguous() and logits.is_cuda, "verify_accept: logits must be fp32 [k+1, V] on the GPU")
+    _require(k == 0 or (draft_ids.dtype == torch.int32 and draft_ids.is_contiguous() and draft_ids.is_cuda),
+             "verify_accept: draft_ids must be contiguous int32 on the GPU")
     if out is None:
         out = torch.empty(2, dtype=torch.int32, device=logits.device)
     _check(lib().mtp_verify_accept_noalloc(draft_ids.data_ptr() if k else None, k, logits.data_ptr(), V,

@@ -95,3 +95,13 @@ def test_mtp_entry_points_reject_bad_arguments_on_host(lib):
     assert out.value is None
     assert lib.moe_lm_head_forward(None, None, 4, 1e-6, None, None) == pkg.MOE_EINVAL
     assert lib.moe_forward_residual(None, None, 4, None, None) == pkg.MOE_EINVAL
+
+
+def test_binding_rejects_bad_tensors_before_any_launch():
+    import torch
+    with pytest.raises(pkg.MoEError):  # logits on the host
+        pkg.verify_accept(torch.zeros(3, dtype=torch.int32), torch.zeros(4, 10))
+    with pytest.raises(pkg.MoEError):  # [k+1, V] mismatch
+        pkg.verify_accept_noalloc(torch.zeros(3, dtype=torch.int32), torch.zeros(3, 10))
+    with pytest.raises(pkg.MoEError):  # not a CUDA fp32 matrix
+        pkg.quantize(pkg.FMT_Q8_0, torch.zeros(4, 32))
