@@ -111,3 +111,13 @@ def test_permutation_invariants(T, E, k):
 def test_near_tie_rule():
     l = np.array([[3.0, 2.0, 1.0, 1.00005], [3.0, 2.0, 1.0, 0.5]])
     assert moe.near_tie_tokens(l, 3).tolist() == [True, False]
+
+
+def test_max_rel_err_is_per_row_then_max():
+    # row 0: max |diff| 0.5 over max |y*| 10 -> 0.05; row 1: 0.3 / 1 -> 0.3
+    y_ref = np.array([[10.0, -2.0, 0.0], [1.0, 0.5, -1.0]])
+    y = y_ref + np.array([[0.5, -0.1, 0.0], [0.0, 0.3, 0.0]])
+    assert moe.max_rel_err(y, y_ref) == pytest.approx(0.3, rel=1e-15)
+    # a row's error is relative to that row's own scale, not the tensor's
+    assert moe.max_rel_err(y[:1], y_ref[:1]) == pytest.approx(0.05, rel=1e-15)
+    assert moe.max_rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
