@@ -81,6 +81,26 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo, else lscpu), for the
+    cpu_baseline record."""
+    import platform
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
 def algorithmic_bytes(w, n_unique):
     """Router weight + bias + unique routed experts + shared expert + x + y,
     at the serialised sizes of their formats."""
@@ -315,9 +335,15 @@ def run_ours(args):
         L.status()
     total_ms = t_start.elapsed_time(t_stop)
     launch_us = [a.elapsed_time(b) * 1e3 for (a, b) in evs[: (args.steps + sample_every - 1) // sample_every]]
-    kern_us = statistics.mean(launch_us)
     total_ms = replica_max_ms(total_ms, "cuda")
     us_per_layer = per_unit_us(total_ms, args.steps, world)
+    # The roofline's launch duration: a T <= 8 step is one launch, so the
+    # average launch duration over the timed region is the step time (events
+    # on the launching stream around all K steps).  The event-bracketed
+    # launches below are a diagnostic only: an event between two launches
+    # removes their programmatic-launch overlap.  A T > 8 forward is eight
+    # launches whose grouped GEMMs dominate; its unit is the whole forward.
+    kern_us = total_ms * 1e3 / args.steps
 
     # end to end through the public call: pinned host x -> device, forward,
     # device -> pinned host y, every step
@@ -367,27 +393,27 @@ def run_ours(args):
                 "d2h_bytes_per_step": yh[0].numel() * yh[0].element_size(), "steps": e2e_steps,
                 "copies": E2E_NOTE},
         "gpu_launches": args.steps * (1 if w.T <= 8 else 8),
-        # event-bracketed launches (every 8th of the timed loop)
+        # diagnostic: event-bracketed launches (every 8th of the timed loop;
+        # the events remove those launches' overlap with their neighbours)
         "launch_us": {"p10": round(float(np.percentile(launch_us, 10)), 3),
                       "p50": round(float(np.percentile(launch_us, 50)), 3),
                       "p90": round(float(np.percentile(launch_us, 90)), 3), "samples": len(launch_us)},
     }
     if w.T > 8:
-        # a contraction: the roofline is the tensor pipe's (bf16 MMA), the unit
-        # one forward (its grouped GEMM launches dominate), timed like the T<=8 path
+        # HBM-bound like the T <= 8 path (about 49 flop/B against a ridge of
+        # ~257 flop/B at the measured peaks): the roofline is HBM over the
+        # forward's algorithmic bytes; the tensor pipe's share is secondary
         flops = 2.0 * w.T * (w.top_k * 3 * w.H * w.I + 3 * w.H * w.I_shared + w.H * w.E)
         tpk, tsrc = measured_tensor_peak()
         got = flops / (kern_us * 1e-6) / 1e12
-        out["roofline"] = {"bound": "tensor", "achieved": round(got, 1), "peak": tpk, "unit": "TFLOP/s",
-                           "frac": round(got / tpk, 4), "traffic": None, "peak_source": tsrc,
-                           "kernel": kname, "kernel_us": round(kern_us, 3),
-                           "flops_per_launch": flops, "hbm_gbs_achieved": round(achieved, 1)}
-        out["tensor"] = {"useful_tflops": round(flops / (us_per_layer * 1e-6) / 1e12, 1),
-                         "note": "useful FLOPs (routed + shared + router) / layer time"}
+        out["roofline"]["kernel_us"] = round(kern_us, 3)
+        out["tensor"] = {"useful_tflops": round(got, 1), "peak": tpk, "frac": round(got / tpk, 4),
+                         "peak_source": tsrc, "flops_per_forward": flops,
+                         "note": "useful FLOPs (routed + shared + router) / forward time; secondary to the HBM bound"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, n = cpu_baseline_sample(w)
         out["cpu_baseline"] = {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(),
-                               "kind": "oracle",
+                               "cpu": cpu_model(), "kind": "oracle",
                                "sample": f"{n} full layer forwards (T={w.T}, distinct x), median; numpy fp64, "
                                          f"BLAS on up to {os.cpu_count()} threads"}
     for L in layers:
@@ -569,8 +595,8 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp64 (numpy oracle)", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.top_k, "I": w.I},
-        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"routing of the batch once + {per_step} of the layer's {n_blocks} "
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer", "cores": os.cpu_count(), "cpu": cpu_model(),
+                         "kind": "oracle", "sample": f"routing of the batch once + {per_step} of the layer's {n_blocks} "
                                    f"32-row weight blocks (dequantise + multiply) per step; "
                                    f"time per block x blocks per layer"},
         "e2e": {"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -9,7 +9,6 @@
 // (max, argmax) to the caller's workspace, and the last CTA to finish (a
 // counter in the workspace) reduces the partials in split order, counts the
 // matching prefix and writes the two outputs.  The counter is left at zero.
-#include <mutex>
 
 #include "common.cuh"
 
@@ -121,25 +120,20 @@ static __device__ __align__(256) uint8_t g_accept_scratch[kAcceptStaticBytes];
 
 size_t accept_static_bytes() { return kAcceptStaticBytes; }
 
-// Device address of g_accept_scratch on the current device, looked up once
-// per device (the lookup loads the module on that device, so the first call
-// on a device belongs before any stream capture on it).
+// Device address of g_accept_scratch in the current device's context.  The
+// host-side name of the array is only a stand-in, so the address is asked of
+// the runtime with that device current.  It is looked up on every call
+// rather than cached: a cached address would outlive the context it belongs
+// to (cudaDeviceReset tears the context down and the module is loaded again,
+// possibly elsewhere, in the next one), while the lookup itself is a host-side
+// table read once the module is loaded.  The first lookup on a device loads
+// the library's module there, so the first call on a device belongs before
+// any stream capture on it.
 cudaError_t accept_static_scratch(void** out) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t rc = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t rc = cudaGetSymbolAddress(&p, g_accept_scratch);
   if (rc != cudaSuccess) return rc;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    rc = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (rc != cudaSuccess) return rc;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

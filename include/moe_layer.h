@@ -197,9 +197,13 @@ int mtp_verify_accept(const int32_t* draft_ids, int32_t k, const float* logits, 
  *   the call accepts only 16 + 8 * (k+1) * ceil(V / 16384) <= 4096 (every
  *   V <= 507904 for every k <= 15) and returns MOE_EINVAL, with a message
  *   naming the sizes, beyond that.  It allocates nothing and calls no
- *   allocating library.  The first call on a device looks the array's
- *   address up (this loads the library's module on that device), so make
- *   it before any stream capture on that device.  All calls on a device
+ *   allocating library.  Every call looks the array's device address up in
+ *   the current context (so a call after cudaDeviceReset finds the array of
+ *   the new context); the first call on a device also loads the library's
+ *   module there, so make it before any stream capture on that device.
+ *   The array keeps the last call's contents: its first 16 bytes (a
+ *   counter) are zero at module load and every completed call leaves them
+ *   zero; the rest is written before it is read.  All calls on a device
  *   share the array: calls whose kernels overlap on the GPU (different
  *   streams, other host threads) race and must be ordered by the caller,
  *   e.g. by issuing them on one stream. */

@@ -181,3 +181,17 @@ def max_rel_err(y, y_ref):
     y_ref = np.asarray(y_ref, F64)
     den = np.maximum(np.abs(y_ref).max(axis=1), 1e-30)
     return float((np.abs(y - y_ref).max(axis=1) / den).max()) if y.size else 0.0
+
+
+def max_rel_err_elementwise(y, y_ref, floor=1e-3):
+    """Element-wise relative error, the second figure of the "max relative
+    error" reading: |y - y*| / max(|y*|, floor * max_h |y*|) per element (the
+    floor is taken per token row, so near-zero outputs do not dominate);
+    returns the max over all elements."""
+    y = np.asarray(y, F64)
+    y_ref = np.asarray(y_ref, F64)
+    if not y.size:
+        return 0.0
+    den = np.maximum(np.abs(y_ref), floor * np.abs(y_ref).max(axis=1, keepdims=True))
+    den = np.maximum(den, 1e-30)
+    return float((np.abs(y - y_ref) / den).max())

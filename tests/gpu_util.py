@@ -63,4 +63,7 @@ def check_layer(layer, x, oracle_layer, k, E, tol, label=""):
     assert np.isfinite(yn).all()
     err = omoe.max_rel_err(yn[keep], y_ref[keep])
     assert err <= tol, f"{label}: max rel err {err:.3e} > {tol}"
+    r["elementwise_err"] = omoe.max_rel_err_elementwise(yn[keep], y_ref[keep])
+    print(f"{label}: max rel err {err:.3e} (element-wise, 1e-3 floor: {r['elementwise_err']:.3e}), "
+          f"excluded {int((~keep).sum())} of {T} tokens")
     return err, int((~keep).sum()), r

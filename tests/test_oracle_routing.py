@@ -121,3 +121,20 @@ def test_max_rel_err_is_per_row_then_max():
     # a row's error is relative to that row's own scale, not the tensor's
     assert moe.max_rel_err(y[:1], y_ref[:1]) == pytest.approx(0.05, rel=1e-15)
     assert moe.max_rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
+
+
+def test_max_rel_err_elementwise_floor():
+    # element-wise ratios against max(|y*|, 1e-3 * row max):
+    #   row 0: 0.1/10 = 0.01; 0.02/2 = 0.01; 1e-6 against the floor 1e-2 -> 1e-4
+    #   row 1: 0.5 / 0.5 = 1.0 (the largest)
+    y_ref = np.array([[10.0, -2.0, 0.0], [1.0, 0.5, -1.0]])
+    y = y_ref + np.array([[0.1, -0.02, 1e-6], [0.0, 0.5, 0.0]])
+    assert moe.max_rel_err_elementwise(y, y_ref) == pytest.approx(1.0, rel=1e-12)
+    assert moe.max_rel_err_elementwise(y[:1], y_ref[:1]) == pytest.approx(0.01, rel=1e-12)
+    # a near-zero reference element is measured against the row's floor, not itself
+    y_ref = np.array([[1.0, 1e-9]])
+    y = np.array([[1.0, 1e-9 + 5e-4]])
+    assert moe.max_rel_err_elementwise(y, y_ref) == pytest.approx(0.5, rel=1e-9)
+    assert moe.max_rel_err_elementwise(y, y_ref, floor=1e-2) == pytest.approx(0.05, rel=1e-9)
+    # never below the row-max metric
+    assert moe.max_rel_err_elementwise(y, y_ref) >= moe.max_rel_err(y, y_ref)

@@ -1,12 +1,18 @@
 """The allocation-free acceptance entry point (static scratch inside the
-library) against the workspace entry point, and its size limit.
+library), its size limit, and its results against the oracle's greedy
+acceptance and against the workspace entry point.
 
-Named to be collected last, so that it also runs after every other test has
-used the library on the same device."""
+Some callers cannot allocate device memory: a C runtime that drives the
+draft/verify loop with no device allocator of its own, for which cudaMalloc /
+cudaFree would also synchronise the device between verify rounds.  This file
+checks the entry point made for them.  It is named to be collected last, so
+that it also runs after every other test has used the library on the same
+device."""
 import numpy as np
 import pytest
 
 import block_quantized_moe_layer_gb300 as pkg
+from oracle import accept as oacc
 
 
 def test_noalloc_rejects_sizes_beyond_static_scratch():
@@ -33,10 +39,15 @@ def _case(rng, k, V, reject_at):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("k,V", [(0, 1), (3, 32768), (7, 151_936), (15, 507_904), (4, 1_000)])
-def test_noalloc_matches_workspace_entry_two_calls_in_a_row(k, V):
+def test_noalloc_matches_oracle_and_workspace_entry_two_calls_in_a_row(k, V):
     import torch
     rng = np.random.default_rng(k * 1009 + V)
     cases = [_case(rng, k, V, None), _case(rng, k, V, (k // 2) if k else None)]
+    # the oracle's greedy acceptance on the same host arrays
+    want = []
+    for draft, logits in cases:
+        n, nxt, _ = oacc.greedy_accept(draft.tolist(), logits)
+        want.append([n, nxt])
     dev = []
     for draft, logits in cases:
         dev.append((torch.tensor(draft, dtype=torch.int32, device="cuda"),
@@ -46,12 +57,15 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row(k, V):
     for (d, lg), o in zip(dev, outs):
         pkg.verify_accept_noalloc(d, lg, out=o)
     torch.cuda.synchronize()
-    for (d, lg), o in zip(dev, outs):
-        ref = pkg.verify_accept(d, lg).cpu().tolist()
-        assert o.cpu().tolist() == ref
-    # and again, interleaved with the workspace entry point
-    for (d, lg), o in zip(dev, outs):
+    for (d, lg), o, w in zip(dev, outs, want):
+        got = o.cpu().tolist()
+        assert got == w, (got, w)
+        assert got == pkg.verify_accept(d, lg).cpu().tolist()
+    # and again, each call interleaved with the workspace entry point
+    for (d, lg), o, w in zip(dev, outs, want):
         o.fill_(-7)
         pkg.verify_accept_noalloc(d, lg, out=o)
         ref = pkg.verify_accept(d, lg)
-        assert o.cpu().tolist() == ref.cpu().tolist()
+        got = o.cpu().tolist()
+        assert got == w, (got, w)
+        assert got == ref.cpu().tolist()
