@@ -333,6 +333,8 @@ def run_ours(args):
     clk = clocks.stop()
     for L in layers:
         L.status()
+    # phase timeline of the timed loop's last launch (T <= 8 kernel)
+    phases = layers[(args.steps - 1) % len(layers)].timeline() if w.T <= 8 else None
     total_ms = t_start.elapsed_time(t_stop)
     launch_us = [a.elapsed_time(b) * 1e3 for (a, b) in evs[: (args.steps + sample_every - 1) // sample_every]]
     total_ms = replica_max_ms(total_ms, "cuda")
@@ -393,6 +395,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": yh[0].numel() * yh[0].element_size(), "steps": e2e_steps,
                 "copies": E2E_NOTE},
         "gpu_launches": args.steps * (1 if w.T <= 8 else 8),
+        # µs after the first block passed its dependency wait, last timed launch
+        "phases_us": ({k: (None if v is None else round(v, 2)) for k, v in phases.items()} if phases else None),
         # diagnostic: event-bracketed launches (every 8th of the timed loop;
         # the events remove those launches' overlap with their neighbours)
         "launch_us": {"p10": round(float(np.percentile(launch_us, 10)), 3),

@@ -23,7 +23,13 @@ EXPORTS = (
     "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
     "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
     "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
+    "moe_layer_timeline",
 )
+
+# event names of moe_layer_timeline, in order
+TIMELINE = ("entry", "start", "x_records", "router_done", "routing_ready", "first_routed_issue",
+            "first_routed_compute", "shared_gate_up_done", "last_gate_up_done", "first_down_issue",
+            "queue_exhausted", "last_down_block", "last_combine", "first_exit", "last_exit")
 
 
 class MoeTensor(_c.Structure):
@@ -78,6 +84,7 @@ def lib():
             "mtp_round": (_c.c_int, [_c.POINTER(vp), i32, _c.POINTER(vp), i32, vp, vp, vp, _c.c_float, vp, sz,
                                      vp, vp, vp, vp, vp, vp]),
             "moe_last_error": (_c.c_char_p, []),
+            "moe_layer_timeline": (_c.c_int, [vp, _c.POINTER(i64), i32, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -192,6 +199,15 @@ class Layer:
         _check(lib().moe_get_routing(self.handle, ids.data_ptr(), gates.data_ptr(), offs.data_ptr(),
                                      perm.data_ptr(), _stream(stream)))
         return ids, gates, offs, perm
+
+    def timeline(self, stream=None):
+        """Phase timeline of the last completed T <= 8 launch: {event: µs
+        after the first block passed its dependency wait, or None}."""
+        n = len(TIMELINE)
+        buf = (_c.c_int64 * n)()
+        _check(lib().moe_layer_timeline(self.handle, buf, n, _stream(stream)))
+        return {name: (None if buf[i] < 0 and name != "entry" else buf[i] / 1e3)
+                for i, name in enumerate(TIMELINE)}
 
     def status(self, stream=None):
         """Raises MoEError(MOE_ETIMEOUT) if a device-side wait gave up."""

@@ -359,6 +359,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_lfx = take((size_t)E_pad * 8 * 8);  // zero between launches, like the counters
   const size_t counters_end = off;
   const size_t o_status = take(16);
+  const size_t o_stamps = take(2 * kNumStamps * 8);
   const size_t o_ids = take((size_t)Tm * k * 4);
   const size_t o_gates = take((size_t)Tm * k * 4);
   const size_t o_pos = take((size_t)Tm * k * 4);
@@ -377,6 +378,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.entry_ready = reinterpret_cast<int*>(w + o_ready);
   sp.d_cnt = reinterpret_cast<int*>(w + o_dcnt);
   sp.status = reinterpret_cast<int*>(w + o_status);
+  sp.stamps = reinterpret_cast<unsigned long long*>(w + o_stamps);
   sp.lfx = reinterpret_cast<long long*>(w + o_lfx);
   sp.ids = reinterpret_cast<int*>(w + o_ids);
   sp.gates = reinterpret_cast<float*>(w + o_gates);
@@ -496,6 +498,23 @@ int moe_layer_status(moe_layer* L, void* stream) {
       return fail(MOE_ETIMEOUT, "a device-side wait of the tensor-core path timed out: %s (detail %d, block %d)",
                   sites[site], word[2], word[3]);
     }
+  }
+  return MOE_OK;
+}
+
+int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream) {
+  if (!L || !out_ns || n < 1) return fail(MOE_EINVAL, "moe_layer_timeline: NULL argument or n < 1");
+  CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "timeline sync");
+  unsigned long long w[kNumStamps];
+  CK(cudaMemcpy(w, L->sp.stamps + kNumStamps, sizeof w, cudaMemcpyDeviceToHost), "timeline read");
+  auto at = [&](int i) -> int64_t {
+    if (w[i] == 0ull) return -1;
+    return (int64_t)(((kStampFirstMask >> i) & 1u) ? ~w[i] : w[i]);
+  };
+  const int64_t t0 = at(kTsStart);
+  for (int i = 0; i < n; ++i) {
+    const int64_t v = i < kNumStamps ? at(i) : -1;
+    out_ns[i] = (v < 0 || t0 < 0) ? -1 : v - t0;
   }
   return MOE_OK;
 }

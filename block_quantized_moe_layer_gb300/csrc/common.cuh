@@ -185,6 +185,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Phase stamp: word w keeps the maximum of t ("last" events) or of ~t
+// ("first" events).
+__device__ __forceinline__ void stamp_last(unsigned long long* st, int w) {
+  atomicMax(st + w, (unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void stamp_first(unsigned long long* st, int w) {
+  atomicMax(st + w, ~(unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void stamp_first_at(unsigned long long* st, int w, uint64_t t) {
+  atomicMax(st + w, ~(unsigned long long)t);
+}
+
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

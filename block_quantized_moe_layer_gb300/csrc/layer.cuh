@@ -32,6 +32,35 @@ struct Sync {
   int pad;
 };
 
+// Phase stamps of one small-T launch (globaltimer, ns).  Each kind is kept
+// in one 64-bit word of the workspace: "first" events as the maximum of the
+// complemented time (so every word is an atomic maximum and starts at 0),
+// "last" and single events as the maximum of the time.  The last CTA to
+// leave copies the words to a second array (the last completed launch) and
+// zeroes them; a launch's CTAs only write them after their dependency wait,
+// so consecutive launches never mix.
+enum Stamp : int {
+  kTsEntry = 0,          // first: a CTA entered the kernel (before its dependency wait)
+  kTsStart,              // first: a CTA passed the dependency wait
+  kTsXDone,              // the x records are complete
+  kTsRouterDone,         // the last router tile finished (the routing starts)
+  kTsRoutingReady,       // the routing is published
+  kTsFirstRoutedIssue,   // first: a routed gate/up weight copy is issued
+  kTsFirstRoutedCompute, // first: a consumer starts a routed gate/up stage
+  kTsSharedGateUp,       // last: the shared expert's gate/up outputs are complete
+  kTsLastGateUp,         // last: a routed entry's gate/up outputs are complete
+  kTsFirstDownIssue,     // first: a routed down weight copy is issued
+  kTsLastIssue,          // last: a producer found the queue exhausted
+  kTsLastDownDone,       // last: a 128-row block of z is complete
+  kTsLastCombine,        // last: a combine finished
+  kTsFirstExit,          // first: a CTA is leaving
+  kTsLastExit,           // the last CTA is leaving
+  kNumStamps
+};
+constexpr uint32_t kStampFirstMask = (1u << kTsEntry) | (1u << kTsStart) | (1u << kTsFirstRoutedIssue) |
+                                     (1u << kTsFirstRoutedCompute) | (1u << kTsFirstDownIssue) |
+                                     (1u << kTsFirstExit);
+
 struct SmallParams {
   // shapes
   int H, E, k, I, Ish, T;
@@ -61,6 +90,7 @@ struct SmallParams {
   // workspace
   Sync* sync;
   int* status;
+  unsigned long long* stamps;  // [2][kNumStamps]: this launch, then the last completed launch
   int* gu_cnt;       // [w_max]
   int* entry_ready;  // [w_max]
   int* d_cnt;        // [n_dt]

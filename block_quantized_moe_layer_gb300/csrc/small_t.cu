@@ -170,6 +170,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
   const uint64_t wpol = l2_evict_first_policy();  // weights are read once per launch
+  bool st_gu = false, st_dn = false;               // first routed gate/up / down copy stamped
   int t = atomicAdd(&P.sync->queue, 1) - NX;
   while (ok) {
     const int t_next = atomicAdd(&P.sync->queue, 1) - NX;  // claim one ahead: its latency overlaps this tile
@@ -227,6 +228,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         entry = P.n_sh + (t - A - NG) / P.n_dt;
         rbt = (t - A - NG) % P.n_dt;
       } else {
+        stamp_last(P.stamps, kTsLastIssue);
         break;  // queue exhausted
       }
     }
@@ -310,6 +312,15 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       else ok = false;
     }
     const int nstages = ngroups * nch / gps;
+    if (e_id >= 0) {
+      if (kind == kGateUp && !st_gu) {
+        stamp_first(P.stamps, kTsFirstRoutedIssue);
+        st_gu = true;
+      } else if (kind == kDown && !st_dn) {
+        stamp_first(P.stamps, kTsFirstDownIssue);
+        st_dn = true;
+      }
+    }
     for (int q = 0; q < nstages && ok; ++q) {
       const int g = q * gps / nch, c = q * gps - g * nch;
       // ring space: a free slot, then free bytes
@@ -796,6 +807,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   if (tid == 0) {
     P.sync->n_rent = n_rent;
     st_release(&P.sync->routing_ready, 1);
+    stamp_last(P.stamps, kTsRoutingReady);
   }
   // what only the combine and moe_get_routing read
   if (tid < Tk) {
@@ -875,6 +887,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   uint32_t ph = 0, rph = 0;
   float acc[kGroup];
   float racc[kMaxSmallT];
+  bool st_routed = false;  // (thread 0) first routed gate/up stage stamped
 
   while (true) {
     if (!mbar_wait_bounded(&full[s], ph, P.timeout_ns, P.status, kSiteFull, s)) break;
@@ -917,7 +930,8 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       consumer_sync();  // orders every thread's record writes before thread 0's release
-      if (tid == 0) atom_add_acq_rel(&P.sync->x_done, T * d.nbc);
+      if (tid == 0 && atom_add_acq_rel(&P.sync->x_done, T * d.nbc) + T * d.nbc == T * P.n_rc)
+        stamp_last(P.stamps, kTsXDone);
     } else if (d.kind == kRouter) {
       // One router tile: 32 experts (lane = expert row) x a slice of ncc
       // 128-column chunks.  The stage holds the tile's router weights
@@ -959,13 +973,20 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         flags[0] = (old == P.n_rg * P.n_kt - 1);
       }
       consumer_sync();
-      if (flags[0]) finalize_routing(P, misc);
+      if (flags[0]) {
+        if (tid == 0) stamp_last(P.stamps, kTsRouterDone);
+        finalize_routing(P, misc);
+      }
       consumer_sync();
     } else {
       // gate/up or down: one chunk of a group, or gps whole groups of one
       // chunk each (their weights back to back, then the shared records)
       const int gps = d.rgks;
       const int cb = (int)chunk_bytes(d.fmt, d.nbc * 32);
+      if (tid == 0 && !st_routed && d.kind == kGateUp && d.entry >= P.n_sh) {
+        stamp_first(P.stamps, kTsFirstRoutedCompute);
+        st_routed = true;
+      }
       const uint8_t* recs = stage + gps * cb;
       bool failed = false;
       for (int j = 0; j < gps; ++j) {
@@ -1055,8 +1076,10 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         // them and, for the last tile, those of the tiles counted before it
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0 && atom_add_acq_rel(&P.gu_cnt[d.entry], 1) == d.n_tiles_entry - 1)
+        if (lane == 0 && atom_add_acq_rel(&P.gu_cnt[d.entry], 1) == d.n_tiles_entry - 1) {
           st_release(&P.entry_ready[d.entry], 1);
+          stamp_last(P.stamps, d.entry < P.n_sh ? kTsSharedGateUp : kTsLastGateUp);
+        }
       }
     } else {  // kDown
       const int row = d.rbt * 128 + d.group * 32 + lane;
@@ -1075,6 +1098,7 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last && lane == 0) {
+          stamp_last(P.stamps, kTsLastDownDone);
           // this CTA combines the block when it leaves (with all its threads)
           int* pend = reinterpret_cast<int*>(smem + plan.pend);
           pend[1 + pend[0]] = d.rbt;
@@ -1139,6 +1163,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   // The next launch in the stream may start as this one's CTAs leave; until
   // griddep_wait it touches nothing this launch (or an earlier one) writes.
   griddep_launch_dependents();
+  const uint64_t t_entry = globaltimer_ns();
   if (threadIdx.x == 0) {
     // constant data only: warm L2 with one router tile's weights (tile = CTA)
     if ((int)blockIdx.x < P.n_rg * P.n_kt) {
@@ -1160,6 +1185,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   griddep_wait();  // x, the workspace and its counters are the previous launches' to finish with
+  if (threadIdx.x == 0) {
+    stamp_first_at(P.stamps, kTsEntry, t_entry);
+    stamp_first(P.stamps, kTsStart);
+  }
   __syncthreads();
 
   const int warp = threadIdx.x >> 5;
@@ -1172,10 +1201,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   }
 
   __syncthreads();
-  if (pend[0] > 0) combine_blocks<L>(P, smem, plan, pend);
+  if (pend[0] > 0) {
+    combine_blocks<L>(P, smem, plan, pend);
+    __syncthreads();
+    if (threadIdx.x == 0) stamp_last(P.stamps, kTsLastCombine);
+  }
   // the last CTA out resets the cross-CTA counters for the next launch
   __syncthreads();
   if (threadIdx.x == 0) {
+    stamp_first(P.stamps, kTsFirstExit);
     __threadfence();
     const int old = atomicAdd(&P.sync->exit_cnt, 1);
     flags[1] = (old == (int)gridDim.x - 1);
@@ -1189,6 +1223,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     }
     for (int i = threadIdx.x; i < P.n_dt; i += blockDim.x) P.d_cnt[i] = 0;
     for (int i = threadIdx.x; i < P.E_pad * P.Tp; i += blockDim.x) P.lfx[i] = 0;
+    // this launch's phase stamps become the last completed launch's
+    if (threadIdx.x < kNumStamps) {
+      const unsigned long long v =
+          threadIdx.x == kTsLastExit ? (unsigned long long)globaltimer_ns() : __ldcg(P.stamps + threadIdx.x);
+      P.stamps[kNumStamps + threadIdx.x] = v;
+      P.stamps[threadIdx.x] = 0ull;
+    }
     if (threadIdx.x == 0) {
       P.sync->queue = 0;
       P.sync->router_done = 0;

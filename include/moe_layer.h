@@ -147,6 +147,30 @@ int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, 
  * (the word is then cleared and the workspace re-zeroed). */
 int moe_layer_status(moe_layer* L, void* stream);
 
+/* Phase timeline of the layer's last completed T <= 8 launch, for
+ * profiling: synchronises `stream`, then writes n (>= 1) int64 values to the
+ * HOST array out_ns, in nanoseconds of the GPU's global timer relative to
+ * the first of the launch's blocks to pass its dependency wait, -1 where the
+ * event did not happen (or i >= 15).  The events, in order:
+ *   0 first block entered the kernel (before its dependency wait; negative
+ *     when it started during the previous kernel)
+ *   1 first block passed its dependency wait (0 by definition)
+ *   2 the activation records of x were complete
+ *   3 the last router tile finished (the routing starts)
+ *   4 the routing was published
+ *   5 first routed gate/up weight copy issued
+ *   6 first routed gate/up stage computed
+ *   7 the shared expert's gate/up outputs were complete
+ *   8 the last routed entry's gate/up outputs were complete
+ *   9 first routed down weight copy issued
+ *  10 the last block found the work queue exhausted
+ *  11 the last 128-row block of the down outputs was complete
+ *  12 the last combine finished
+ *  13 first block leaving
+ *  14 last block leaving
+ * The stamps cost a few atomic writes per block and are always recorded. */
+int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream);
+
 /* Bytes of weights resident on the device (repacked), and of workspace. */
 size_t moe_layer_weight_bytes(const moe_layer* L);
 size_t moe_layer_workspace_bytes(const moe_layer* L);
