@@ -453,8 +453,8 @@ def run_round(args):
     lib = pkg.lib()
 
     def step(xd, nd, acc=acc, drafts=drafts):
-        rc = lib.mtp_round(tl, len(layers), hl, k, lm.handle, xd.data_ptr(), nd.data_ptr(), 1e-6, wp, wn,
-                           logits.data_ptr(), None, drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4,
+        rc = lib.mtp_round(tl, len(layers), hl, k, lm.handle, xd.data_ptr(), nd.data_ptr(), 1e-6, 0.0, wp, wn,
+                           logits.data_ptr(), None, None, drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4,
                            stream.cuda_stream)
         if rc:
             raise RuntimeError(lib.moe_last_error().decode())

@@ -23,7 +23,7 @@ EXPORTS = (
     "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
     "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
     "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
-    "moe_layer_timeline",
+    "moe_layer_timeline", "moe_layer_inject_timeout",
 )
 
 # event names of moe_layer_timeline, in order
@@ -40,10 +40,10 @@ class MoeTensor(_c.Structure):
 class MoeLayerDesc(_c.Structure):
     _fields_ = [("H", _c.c_int32), ("E", _c.c_int32), ("top_k", _c.c_int32), ("I", _c.c_int32),
                 ("I_shared", _c.c_int32), ("T_max", _c.c_int32), ("act_dtype", _c.c_int32),
-                ("reserved", _c.c_int32), ("router_w", MoeTensor), ("router_b", MoeTensor),
+                ("wait_limit_us", _c.c_uint32), ("router_w", MoeTensor), ("router_b", MoeTensor),
                 ("gate", _c.POINTER(MoeTensor)), ("up", _c.POINTER(MoeTensor)),
                 ("down", _c.POINTER(MoeTensor)), ("sh_gate", MoeTensor), ("sh_up", MoeTensor),
-                ("sh_down", MoeTensor)]
+                ("sh_down", MoeTensor), ("expert_begin", _c.c_int32), ("expert_count", _c.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -81,10 +81,11 @@ def lib():
             "moe_lm_head_forward": (_c.c_int, [vp, vp, i32, _c.c_float, vp, vp]),
             "moe_lm_head_destroy": (None, [vp]),
             "mtp_round_workspace_bytes": (sz, [i32, i32, i32, i32]),
-            "mtp_round": (_c.c_int, [_c.POINTER(vp), i32, _c.POINTER(vp), i32, vp, vp, vp, _c.c_float, vp, sz,
-                                     vp, vp, vp, vp, vp, vp]),
+            "mtp_round": (_c.c_int, [_c.POINTER(vp), i32, _c.POINTER(vp), i32, vp, vp, vp, _c.c_float, _c.c_float,
+                                     vp, sz, vp, vp, vp, vp, vp, vp, vp]),
             "moe_last_error": (_c.c_char_p, []),
             "moe_layer_timeline": (_c.c_int, [vp, _c.POINTER(i64), i32, vp]),
+            "moe_layer_inject_timeout": (_c.c_int, [vp, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -140,24 +141,31 @@ def _tensor(fmt, rows, cols, t):
 class Layer:
     """One MoE layer resident on the current CUDA device.
 
-    experts: list of E tuples (fmt, gate, up, down) of serialised byte
-    tensors (host or device); shared: one such tuple or None.
+    experts: list of tuples (fmt, gate, up, down) of serialised byte tensors
+    (host or device), one per routed expert held: all E, or the n experts
+    from ``expert_begin`` on (one shard of an expert-parallel split); shared:
+    one such tuple or None.  ``wait_limit_us`` bounds every device-side wait
+    (0: the library's default).
     """
 
     def __init__(self, H, E, top_k, I, I_shared, T_max, act, router_w, router_b, experts, shared,
-                 stream=None):
+                 stream=None, expert_begin=0, wait_limit_us=0):
         self.H, self.E, self.top_k, self.I, self.I_shared = H, E, top_k, I, I_shared
         self.T_max, self.act = T_max, act
-        gate = (MoeTensor * E)()
-        up = (MoeTensor * E)()
-        down = (MoeTensor * E)()
+        n = len(experts)
+        _require(n >= 1, "Layer: at least one routed expert must be held")
+        self.expert_begin, self.expert_count = expert_begin, n
+        gate = (MoeTensor * n)()
+        up = (MoeTensor * n)()
+        down = (MoeTensor * n)()
         for e, (fmt, g, u, d) in enumerate(experts):
             gate[e] = _tensor(fmt, I, H, g)
             up[e] = _tensor(fmt, I, H, u)
             down[e] = _tensor(fmt, H, I, d)
         desc = MoeLayerDesc()
         desc.H, desc.E, desc.top_k, desc.I, desc.I_shared = H, E, top_k, I, I_shared
-        desc.T_max, desc.act_dtype, desc.reserved = T_max, act, 0
+        desc.T_max, desc.act_dtype, desc.wait_limit_us = T_max, act, wait_limit_us
+        desc.expert_begin, desc.expert_count = expert_begin, (0 if (expert_begin == 0 and n == E) else n)
         desc.router_w = _tensor(FMT_F32, E, H, router_w)
         desc.router_b = _tensor(FMT_F32, 1, E, router_b)
         desc.gate, desc.up, desc.down = gate, up, down
@@ -208,6 +216,11 @@ class Layer:
         _check(lib().moe_layer_timeline(self.handle, buf, n, _stream(stream)))
         return {name: (None if buf[i] < 0 and name != "entry" else buf[i] / 1e3)
                 for i, name in enumerate(TIMELINE)}
+
+    def inject_timeout(self, site=1):
+        """Test hook: the next T <= 8 forward's routing wait runs out (see
+        moe_layer_inject_timeout)."""
+        _check(lib().moe_layer_inject_timeout(self.handle, site))
 
     def status(self, stream=None):
         """Raises MoEError(MOE_ETIMEOUT) if a device-side wait gave up."""
@@ -316,10 +329,11 @@ def _aligned(buf, a=256):
     return buf.data_ptr() + off, buf.numel() - off
 
 
-def mtp_round(layers, heads, lm, x, noise, eps=1e-6, workspace=None, head_out=True, stream=None):
+def mtp_round(layers, heads, lm, x, noise, eps=1e-6, p_min=0.0, workspace=None, head_out=True, stream=None):
     """One MTP draft/verify round (see ``mtp_round`` in moe_layer.h).  Returns
-    a dict of device tensors: logits [k+1, V], drafts [k], accept [n, next],
-    head_out [k, k, H] (if requested)."""
+    a dict of device tensors: logits [k+1, V], draft_logits [k, V], drafts
+    [k] (-1 past the confidence cut p_min), accept [n, next], head_out
+    [k, k, H] (if requested)."""
     import torch
     k = len(heads)
     H, V = lm.H, lm.V
@@ -328,12 +342,13 @@ def mtp_round(layers, heads, lm, x, noise, eps=1e-6, workspace=None, head_out=Tr
         workspace = round_workspace(H, k, V, lm.act, dev)
     wp, wn = _aligned(workspace)
     logits = torch.empty(k + 1, V, dtype=torch.float32, device=dev)
+    dlogits = torch.empty(k, V, dtype=torch.float32, device=dev)
     drafts = torch.empty(k, dtype=torch.int32, device=dev)
     acc = torch.empty(2, dtype=torch.int32, device=dev)
     hout = torch.empty(k, k, H, dtype=x.dtype, device=dev) if head_out else None
     tl = (_c.c_void_p * max(1, len(layers)))(*[L.handle.value for L in layers])
     hl = (_c.c_void_p * k)(*[L.handle.value for L in heads])
-    _check(lib().mtp_round(tl, len(layers), hl, k, lm.handle, x.data_ptr(), noise.data_ptr(), eps, wp, wn,
-                           logits.data_ptr(), hout.data_ptr() if hout is not None else None, drafts.data_ptr(),
-                           acc.data_ptr(), acc.data_ptr() + 4, _stream(stream)))
-    return dict(logits=logits, drafts=drafts, accept=acc, head_out=hout)
+    _check(lib().mtp_round(tl, len(layers), hl, k, lm.handle, x.data_ptr(), noise.data_ptr(), eps, p_min, wp, wn,
+                           logits.data_ptr(), dlogits.data_ptr(), hout.data_ptr() if hout is not None else None,
+                           drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4, _stream(stream)))
+    return dict(logits=logits, draft_logits=dlogits, drafts=drafts, accept=acc, head_out=hout)

@@ -9,6 +9,12 @@
 // (max, argmax) to the caller's workspace, and the last CTA to finish (a
 // counter in the workspace) reduces the partials in split order, counts the
 // matching prefix and writes the two outputs.  The counter is left at zero.
+//
+// Inside an MTP round the last CTA also applies the draft confidence cut
+// ("Step-3.5-Flash MTP GGUF", "Usage": --spec-draft-p-min): given each
+// draft's probability under its own logits, drafting stopped at the first
+// draft below p_min, so that draft and every later one become -1 (they match
+// no token, which ends the accepted prefix there).
 
 #include "common.cuh"
 
@@ -34,7 +40,9 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const int32_t* __restrict__ draft, int k,
                                                                 const float* __restrict__ logits, int V, int S,
                                                                 int32_t* out_n, int32_t* out_next,
-                                                                int* counter, ArgPart* parts) {
+                                                                int* counter, ArgPart* parts,
+                                                                const float* __restrict__ dprob, float p_min,
+                                                                int32_t* draft_cut) {
   __shared__ float sv[kAcceptThreads / 32];
   __shared__ int si[kAcceptThreads / 32];
   __shared__ int last;
@@ -69,10 +77,19 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const int32_t* _
   __syncthreads();
   if (!last || threadIdx.x != 0) return;
   __threadfence();
+  int kk = k;  // drafts kept by the confidence cut
+  if (dprob) {
+    for (int j = 0; j < k; ++j)
+      if (!(dprob[j] >= p_min)) {
+        kk = j;
+        break;
+      }
+    for (int j = kk; j < k; ++j) draft_cut[j] = -1;
+  }
   int n = 0;
   bool run = true;
   int a_n = 0;
-  for (int r = 0; r <= k; ++r) {
+  for (int r = 0; r <= kk; ++r) {
     float rv = -INFINITY;
     int ri = 0x7fffffff;
     for (int s = 0; s < S; ++s) {
@@ -81,7 +98,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const int32_t* _
       if (better(v, i, rv, ri)) { rv = v; ri = i; }
     }
     if (run) {
-      if (r < k && ri == draft[r]) {
+      if (r < kk && ri == draft[r]) {
         ++n;
       } else {
         a_n = ri;
@@ -103,7 +120,18 @@ cudaError_t accept_launch(const int32_t* draft, int k, const float* logits, int 
   int* counter = static_cast<int*>(ws);
   ArgPart* parts = reinterpret_cast<ArgPart*>(static_cast<uint8_t*>(ws) + 16);
   return launch_pdl(accept_kernel, (k + 1) * S, kAcceptThreads, 0, st, draft, k, logits, V, S, out_n, out_next,
-                    counter, parts);
+                    counter, parts, (const float*)nullptr, 0.f, (int32_t*)nullptr);
+}
+
+// The same with the draft confidence cut: dprob[k] the drafts' probabilities;
+// drafts from the first one below p_min on are set to -1 in `draft`.
+cudaError_t accept_launch_cut(int32_t* draft, int k, const float* logits, int V, const float* dprob, float p_min,
+                              int32_t* out_n, int32_t* out_next, void* ws, cudaStream_t st) {
+  const int S = accept_splits(V);
+  int* counter = static_cast<int*>(ws);
+  ArgPart* parts = reinterpret_cast<ArgPart*>(static_cast<uint8_t*>(ws) + 16);
+  return launch_pdl(accept_kernel, (k + 1) * S, kAcceptThreads, 0, st, (const int32_t*)draft, k, logits, V, S, out_n,
+                    out_next, counter, parts, dprob, p_min, draft);
 }
 
 // Scratch of the allocation-free entry point (mtp_verify_accept_noalloc).

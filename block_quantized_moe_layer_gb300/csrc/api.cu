@@ -175,7 +175,6 @@ int moe_quantize(int32_t fmt, const float* w, int64_t rows, int64_t cols, void* 
 int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if (!d || !out) return fail(MOE_EINVAL, "moe_layer_create: NULL argument");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d->reserved != 0) return fail(MOE_EINVAL, "reserved must be 0");
   if (d->H <= 0 || d->H % 256 || d->H > 128 * kMaxDownTiles)
     return fail(MOE_EINVAL, "H=%d must be a positive multiple of 256, at most %d", d->H, 128 * kMaxDownTiles);
   if (d->E < 1 || d->E > 1024) return fail(MOE_EINVAL, "E=%d out of range 1..1024", d->E);
@@ -186,6 +185,11 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   if (d->act_dtype != MOE_ACT_BF16 && d->act_dtype != MOE_ACT_F32)
     return fail(MOE_EINVAL, "act_dtype=%d", d->act_dtype);
   if (!d->gate || !d->up || !d->down) return fail(MOE_EINVAL, "gate/up/down descriptor arrays are NULL");
+  // the routed experts held (expert parallelism)
+  const int e0 = d->expert_begin, n_e = d->expert_count == 0 ? d->E : d->expert_count;
+  if (d->expert_count < 0 || e0 < 0 || (d->expert_count == 0 && e0 != 0) || n_e < 1 || e0 + n_e > d->E)
+    return fail(MOE_EINVAL, "expert range [%d, %d + %d) outside 0..E=%d (expert_count 0 means all E from 0)", e0, e0,
+                d->expert_count, d->E);
   if (d->T_max > kMaxSmallT) {
     // the tensor-core path: 128-row weight tiles, 64-column K-blocks, bf16 operands
     if (d->act_dtype != MOE_ACT_BF16)
@@ -200,7 +204,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const bool has_bias = d->router_b.data != nullptr;
   if (has_bias && (rc = check_tensor(d->router_b, 1, d->E, false, "router_b"))) return rc;
   const int fmt = d->gate[0].fmt;
-  for (int e = 0; e < d->E; ++e) {
+  for (int e = 0; e < n_e; ++e) {
     char nm[64];
     snprintf(nm, sizeof nm, "gate[%d]", e);
     if ((rc = check_tensor(d->gate[e], d->I, d->H, true, nm))) return rc;
@@ -225,6 +229,8 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   moe_layer* L = new moe_layer();
   L->H = d->H; L->E = d->E; L->k = d->top_k; L->I = d->I; L->Ish = d->I_shared;
   L->T_max = d->T_max; L->act = d->act_dtype; L->fmt = fmt; L->sfmt = sfmt;
+  L->e0 = e0; L->n_e = n_e;
+  L->timeout_ns = d->wait_limit_us ? (uint64_t)d->wait_limit_us * 1000ull : 2000000000ull;
   struct Guard {
     moe_layer* L;
     bool keep = false;
@@ -272,8 +278,8 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t router_bytes = (size_t)E_pad * d->H * 4;
   CK(cudaMalloc(&L->router, router_bytes), "alloc router");
   if (has_bias) CK(cudaMalloc(&L->router_b, (size_t)d->E * 4), "alloc bias");
-  CK(cudaMalloc(&L->gu, (size_t)L->gu_stride * d->E), "alloc gate/up");
-  CK(cudaMalloc(&L->dn, (size_t)L->dn_stride * d->E), "alloc down");
+  CK(cudaMalloc(&L->gu, (size_t)L->gu_stride * n_e), "alloc gate/up");
+  CK(cudaMalloc(&L->dn, (size_t)L->dn_stride * n_e), "alloc down");
   size_t sgu_b = 0, sdn_b = 0;
   if (has_sh) {
     sgu_b = tile_bytes_total(sfmt, d->I_shared / 16, L->sgu_ch);
@@ -281,7 +287,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
     CK(cudaMalloc(&L->sgu, sgu_b), "alloc shared gate/up");
     CK(cudaMalloc(&L->sdn, sdn_b), "alloc shared down");
   }
-  L->weight_bytes = router_bytes + (has_bias ? d->E * 4 : 0) + (size_t)(L->gu_stride + L->dn_stride) * d->E +
+  L->weight_bytes = router_bytes + (has_bias ? d->E * 4 : 0) + (size_t)(L->gu_stride + L->dn_stride) * n_e +
                     sgu_b + sdn_b;
   if (large_t_enabled(L)) {
     CK(large_t_alloc(L), "allocate the prefill-sized path");
@@ -300,7 +306,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
     const cudaMemcpyKind kind = is_device_ptr(d->router_b.data) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
     CK(cudaMemcpyAsync(L->router_b, d->router_b.data, (size_t)d->E * 4, kind, st), "copy bias");
   }
-  for (int e = 0; e < d->E; ++e) {
+  for (int e = 0; e < n_e; ++e) {
     uint8_t* gu = L->gu + (int64_t)e * L->gu_stride;
     uint8_t* dn = L->dn + (int64_t)e * L->dn_stride;
     if ((rc = stg.get(d->gate[e].data, d->gate[e].nbytes, st, &src))) return rc;
@@ -335,6 +341,8 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   SmallParams& sp = L->sp;
   sp = SmallParams{};
   sp.H = d->H; sp.E = d->E; sp.k = k; sp.I = d->I; sp.Ish = d->I_shared;
+  sp.e0 = e0; sp.n_e = n_e;
+  sp.act_f32 = d->act_dtype == MOE_ACT_F32 ? 1 : 0;
   sp.n_rg = n_rg; sp.n_ks = n_ks; sp.n_rc = d->H / kRouterCc;
   sp.n_kt = (sp.n_rc + kRouterTileChunks - 1) / kRouterTileChunks; sp.n_gu = d->I / 32; sp.n_gu_sh = d->I_shared / 32; sp.n_dt = n_dt;
   sp.Imax = Imax; sp.E_pad = E_pad; sp.w_max = w_max;
@@ -344,7 +352,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.fmt = fmt; sp.sfmt = sfmt;
   sp.gu_nch = L->gu_ch.n; sp.gu_kc = L->gu_ch.Kc; sp.dn_nch = L->dn_ch.n; sp.dn_kc = L->dn_ch.Kc;
   sp.sgu_nch = L->sgu_ch.n; sp.sgu_kc = L->sgu_ch.Kc; sp.sdn_nch = L->sdn_ch.n; sp.sdn_kc = L->sdn_ch.Kc;
-  sp.timeout_ns = 2000000000ull;
+  sp.timeout_ns = L->timeout_ns;
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -439,6 +447,11 @@ int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, 
   P.x = x;
   P.y = y;
   P.residual = residual ? 1 : 0;
+  P.ready_target = 1;
+  if (L->inject == 1) {
+    P.ready_target = 2;  // published as 1: the routed tiles' wait runs out
+    L->inject = 0;
+  }
   CK(small_t_launch(P, L->act == MOE_ACT_BF16 ? 2 : 4, L->num_sms, L->smem_bytes, st), "moe_forward launch");
   return MOE_OK;
 }
@@ -516,6 +529,13 @@ int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream) {
     const int64_t v = i < kNumStamps ? at(i) : -1;
     out_ns[i] = (v < 0 || t0 < 0) ? -1 : v - t0;
   }
+  return MOE_OK;
+}
+
+int moe_layer_inject_timeout(moe_layer* L, int32_t site) {
+  if (!L) return fail(MOE_EINVAL, "moe_layer_inject_timeout: NULL layer");
+  if (site != 1) return fail(MOE_EINVAL, "moe_layer_inject_timeout: site %d (only 1 is defined)", site);
+  L->inject = site;
   return MOE_OK;
 }
 

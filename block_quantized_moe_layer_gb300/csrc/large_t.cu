@@ -279,6 +279,7 @@ __device__ int block_excl_scan(int v, int* warp_tot, int* total) {
 struct PermParams {
   const int* ids;
   int T, E, k, H, I, Ish, n_sh, prow_sh;
+  int e0, n_e;  // routed experts held: token tiles only for [e0, e0 + n_e), by local index
   int* offsets;
   int* perm;
   int* pos;
@@ -350,9 +351,10 @@ __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermPara
     }
     __syncthreads();
   }
-  // routed token tiles (E <= 1024: thread e handles expert e)
+  // routed token tiles (E <= 1024: thread e handles expert e), for the
+  // experts this layer holds; a tile names its expert by local index
   const int e = tid;
-  const int M = e < E ? cnt[e] : 0;
+  const int M = e < E && e >= P.e0 && e < P.e0 + P.n_e ? cnt[e] : 0;
   const int ntt = (M + kLtMaxN - 1) / kLtMaxN;
   const int rows = M > 0 ? kLtMaxN * (ntt - 1) + round16(M - kLtMaxN * (ntt - 1)) : 0;
   int n_tiles, n_rows;
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermPara
   for (int i = 0; i < ntt; ++i) {
     const int ni = min(kLtMaxN, M - kLtMaxN * i);
     P.tiles[P.n_sh + tb + i] =
-        LtTile{e, off[e] + kLtMaxN * i, ni, round16(ni), P.prow_sh + pb + kLtMaxN * i, {0, 0, 0}};
+        LtTile{e - P.e0, off[e] + kLtMaxN * i, ni, round16(ni), P.prow_sh + pb + kLtMaxN * i, {0, 0, 0}};
   }
   if (tid == 0) {
     const int n_gu = P.I / 64, n_dn = P.H / 128;
@@ -392,22 +394,36 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
 }
 
 // y[t] = sum_j g[t,j] z[pos[t,j]] + z[T k + t]; one block per token, 8 columns per thread step.
+// Pairs whose expert the layer does not hold (an expert-parallel shard) are
+// left out of the sum.
 __global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const float* __restrict__ gates,
-                                  const int* __restrict__ pos, int T, int k, int H, bool shared,
-                                  const __nv_bfloat16* __restrict__ xres, __nv_bfloat16* __restrict__ y) {
+                                  const int* __restrict__ pos, const int* __restrict__ ids, int e0, int n_e, int T,
+                                  int k, int H, bool shared, const __nv_bfloat16* __restrict__ xres,
+                                  __nv_bfloat16* __restrict__ y) {
   const int t = blockIdx.x;
   __shared__ float g[kMaxTopK];
   __shared__ int ps[kMaxTopK];
-  if (threadIdx.x < k) {
-    g[threadIdx.x] = gates[t * k + threadIdx.x];
-    ps[threadIdx.x] = pos[t * k + threadIdx.x];
+  __shared__ int nk;
+  if (threadIdx.x == 0) {
+    // the held pairs, in slot order
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[t * k + j];
+      if (e >= e0 && e < e0 + n_e) {
+        g[n] = gates[t * k + j];
+        ps[n] = pos[t * k + j];
+        ++n;
+      }
+    }
+    nk = n;
   }
   __syncthreads();
+  const int kh = nk;
   for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) acc[m] = 0.f;
-    for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < kh; ++j) {
       const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)ps[j] * H + 8 * c);
       const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
 #pragma unroll
@@ -463,10 +479,10 @@ cudaError_t large_t_alloc(moe_layer* L) {
   S->gu_stride = (int64_t)(I / 64) * lt_tile_bytes(L->fmt, H);
   S->dn_stride = (int64_t)(H / 128) * lt_tile_bytes(L->fmt, I);
   S->router_plane = (int64_t)(S->E_pad128 / 128) * lt_tile_bytes(MOE_BF16, H);
-  LT_CK(cudaMalloc(&S->gu, (size_t)S->gu_stride * E));
-  LT_CK(cudaMalloc(&S->dn, (size_t)S->dn_stride * E));
+  LT_CK(cudaMalloc(&S->gu, (size_t)S->gu_stride * L->n_e));
+  LT_CK(cudaMalloc(&S->dn, (size_t)S->dn_stride * L->n_e));
   LT_CK(cudaMalloc(&S->router, (size_t)S->router_plane * kLtPlanes));
-  size_t wb = (size_t)(S->gu_stride + S->dn_stride) * E + (size_t)S->router_plane * kLtPlanes;
+  size_t wb = (size_t)(S->gu_stride + S->dn_stride) * L->n_e + (size_t)S->router_plane * kLtPlanes;
   if (Ish > 0) {
     const size_t a = (size_t)(Ish / 64) * lt_tile_bytes(L->sfmt, H), b = (size_t)(H / 128) * lt_tile_bytes(L->sfmt, Ish);
     LT_CK(cudaMalloc(&S->sgu, a));
@@ -575,7 +591,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   g.fmt = L->fmt; g.sfmt = L->sfmt;
   g.H = H; g.I = L->I; g.Ish = L->Ish; g.Imax = S->Imax; g.E_pad128 = S->E_pad128; g.T = T; g.k = k;
   g.xg = S->xg; g.h = S->h; g.z = S->z; g.logits = S->logits;
-  g.timeout_ns = 2000000000ull;
+  g.timeout_ns = L->timeout_ns;
   g.n_rt_router = n_rt_r;
   g.n_router_tiles = n_sh;
   const int grid = L->num_sms;
@@ -598,7 +614,8 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
 #undef LT_TOPK
   LT_CK(cudaGetLastError());
 
-  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, S->offsets, S->perm, S->pos, S->tiles, S->counters};
+  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, L->e0, L->n_e, S->offsets, S->perm, S->pos,
+               S->tiles, S->counters};
   lt_perm_kernel<<<1, kPermThreads, S->perm_smem, st>>>(P);
   LT_CK(cudaGetLastError());
 
@@ -616,7 +633,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   g.n_rt_items = 0; g.tile_kind = kItemDN; g.tile0 = L->Ish > 0 ? 0 : n_sh; g.n_rt_tile = H / 128;
   LT_CK(lt_gemm_launch(g, grid, st));
 
-  lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, T, k, H, L->Ish > 0,
+  lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, S->ids, L->e0, L->n_e, T, k, H, L->Ish > 0,
                                        residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
                                        static_cast<__nv_bfloat16*>(y));
   LT_CK(cudaGetLastError());

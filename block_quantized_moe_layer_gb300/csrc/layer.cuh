@@ -64,6 +64,7 @@ constexpr uint32_t kStampFirstMask = (1u << kTsEntry) | (1u << kTsStart) | (1u <
 struct SmallParams {
   // shapes
   int H, E, k, I, Ish, T;
+  int e0, n_e;            // routed experts held by this layer: [e0, e0 + n_e) (all E unless sharded)
   int n_rg, n_ks, n_kt;   // router: row groups of 32 experts, 256-column repack blocks, 512-column tiles
   int n_rc;               // router: 128-column chunks (H / 128)
   int Tp;                 // T rounded up to 4 (partial-logit row stride)
@@ -87,6 +88,7 @@ struct SmallParams {
   const void* x;  // [T, H] bf16 (L = 2) or fp32 (L = 4)
   void* y;        // [T, H] same type
   int residual;   // 1: y = x + MoE(x)
+  int act_f32;    // 1: x and y are fp32 (check mode), else bf16
   // workspace
   Sync* sync;
   int* status;
@@ -107,6 +109,7 @@ struct SmallParams {
   // shared-memory plan
   int n_stages, ring_bytes, misc_bytes;  // descriptor slots, bytes of the stage ring, router scratch
   uint64_t timeout_ns;
+  int ready_target;  // value of routing_ready the producers wait for: 1 (2 only under moe_layer_inject_timeout)
 };
 
 }  // namespace moe
@@ -114,6 +117,9 @@ struct SmallParams {
 struct moe_layer {
   int dev = 0;
   int H = 0, E = 0, k = 0, I = 0, Ish = 0, T_max = 0, act = 0;
+  int e0 = 0, n_e = 0;          // routed experts held: [e0, e0 + n_e) of the E the router scores
+  uint64_t timeout_ns = 0;      // bound of every device-side wait
+  int inject = 0;               // one-shot wait-timeout test hook (moe_layer_inject_timeout)
   int fmt = 0, sfmt = 0;
   uint8_t* router = nullptr;
   float* router_b = nullptr;

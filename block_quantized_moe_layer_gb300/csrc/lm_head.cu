@@ -158,15 +158,18 @@ cudaError_t lm_configure(int H) {
   return cudaFuncSetAttribute(lm_head_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lm_smem_bytes(H));
 }
 
-// Rows are processed in groups of kLmTokens (one launch per group).
-cudaError_t lm_forward(const moe_lm_head* lm, const void* x, int T, float eps, float* logits, cudaStream_t st) {
-  const size_t esz = lm->act == MOE_ACT_BF16 ? 2 : 4;
+// Rows are processed in groups of kLmTokens (one launch per group); x is
+// fp32 (x_f32) or bf16.  The arithmetic after the norm (16-bit block fixed
+// point of the normalised rows, exact dp4a sums) is the same for both.
+cudaError_t lm_forward(const moe_lm_head* lm, const void* x, bool x_f32, int T, float eps, float* logits,
+                       cudaStream_t st) {
+  const size_t esz = x_f32 ? 4 : 2;
   for (int t0 = 0; t0 < T; t0 += kLmTokens) {
     const int n = min(kLmTokens, T - t0);
     const void* xg = static_cast<const uint8_t*>(x) + (size_t)t0 * lm->H * esz;
     float* lg = logits + (int64_t)t0 * lm->V;
     cudaError_t e;
-    if (lm->act == MOE_ACT_BF16)
+    if (!x_f32)
       e = launch_pdl(lm_head_kernel<2>, lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st, (const int8_t*)lm->q,
                      (const __half*)lm->sc, lm->V, lm->H, xg, n, eps, lg);
     else

@@ -4,13 +4,20 @@
 // blocks, the output norm + LM head on the verify batch, the noisy draft rows,
 // the draft heads, the LM head on the draft rows, their argmax, and greedy
 // acceptance.  Everything runs in this library's kernels; nothing allocates.
+// The residual stream (the hidden state h between blocks, and the noisy draft
+// rows) is kept in fp32 whatever the activation type; only the inputs and
+// outputs of the MoE layers are in the act dtype (as in the pages' runtime,
+// whose hidden states between operations are F32 tensors).
 #include "layer.cuh"
 
 namespace moe {
 cudaError_t lm_repack(const uint8_t* src, int8_t* q, __half* sc, int64_t nblocks, cudaStream_t st);
 cudaError_t lm_configure(int H);
-cudaError_t lm_forward(const moe_lm_head* lm, const void* x, int T, float eps, float* logits, cudaStream_t st);
+cudaError_t lm_forward(const moe_lm_head* lm, const void* x, bool x_f32, int T, float eps, float* logits,
+                       cudaStream_t st);
 size_t accept_workspace_bytes(int k, int V);
+cudaError_t accept_launch_cut(int32_t* draft, int k, const float* logits, int V, const float* dprob, float p_min,
+                              int32_t* out_n, int32_t* out_next, void* ws, cudaStream_t st);
 
 namespace {
 
@@ -43,11 +50,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-// One row per block: h_out = h_in + y (stored in the act dtype; skipped when
-// y is NULL, h_in is then the row) and xn = rmsnorm(h_out) (act dtype).
-template <int L>
+// One row per block: h_out = h_in + y (fp32; y is in the act dtype; without
+// y, h_out = h_in) and xn = rmsnorm(h_out) (act dtype).  h_in is fp32 (LIN =
+// 4) or the act dtype (LIN = L: the round's input batch).
+template <int L, int LIN>
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict__ h_in, const void* __restrict__ y,
-                                                          void* __restrict__ h_out, void* __restrict__ xn, int H,
+                                                          float* __restrict__ h_out, void* __restrict__ xn, int H,
                                                           float eps) {
   __shared__ float red[8];
   griddep_launch_dependents();
@@ -55,22 +63,23 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict
   const int64_t base = (int64_t)blockIdx.x * H;
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    float v = ld_act<L>(h_in, base + c);
-    if (y) v = st_act<L>(h_out, base + c, v + ld_act<L>(y, base + c));
+    float v = ld_act<LIN>(h_in, base + c);
+    if (y) v += ld_act<L>(y, base + c);
+    h_out[base + c] = v;
     ss = fmaf(v, v, ss);
   }
   __syncthreads();  // h_out written by this block before it is read back
   const float inv = 1.f / sqrtf(block_sum(ss, red) / (float)H + eps);
-  const void* src = y ? h_out : h_in;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) st_act<L>(xn, base + c, ld_act<L>(src, base + c) * inv);
+  for (int c = threadIdx.x; c < H; c += blockDim.x) st_act<L>(xn, base + c, h_out[base + c] * inv);
 }
 
-// Block (j, i), i <= j: v = h[i] + noise[j][i]; hin[j][i] = rmsnorm(v) (the
-// head's input) and, for i == j, rows[j] = v (the row the draft is read from).
+// Block (j, i), i <= j: v = h[i] + noise[j][i] (fp32); hin[j][i] =
+// rmsnorm(v) (the head's input, act dtype) and, for i == j, rows[j] = v
+// (fp32: the row the draft is read from).
 template <int L>
-__global__ void __launch_bounds__(256) draft_rows_kernel(const void* __restrict__ h, const float* __restrict__ noise,
+__global__ void __launch_bounds__(256) draft_rows_kernel(const float* __restrict__ h, const float* __restrict__ noise,
                                                          int k, int H, float eps, void* __restrict__ hin,
-                                                         void* __restrict__ rows) {
+                                                         float* __restrict__ rows) {
   __shared__ float red[8];
   griddep_launch_dependents();
   griddep_wait();
@@ -79,31 +88,57 @@ __global__ void __launch_bounds__(256) draft_rows_kernel(const void* __restrict_
   const int64_t src = (int64_t)i * H, nz = ((int64_t)j * k + i) * H;
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = ld_act<L>(h, src + c) + noise[nz + c];
+    const float v = h[src + c] + noise[nz + c];
     ss = fmaf(v, v, ss);
-    if (i == j) st_act<L>(rows, (int64_t)j * H + c, v);
+    if (i == j) rows[(int64_t)j * H + c] = v;
   }
   const float inv = 1.f / sqrtf(block_sum(ss, red) / (float)H + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    st_act<L>(hin, nz + c, (ld_act<L>(h, src + c) + noise[nz + c]) * inv);
+  for (int c = threadIdx.x; c < H; c += blockDim.x) st_act<L>(hin, nz + c, (h[src + c] + noise[nz + c]) * inv);
 }
 
-// ids[r] = argmax of row r (lowest index on ties); one CTA of kArgThreads per
+// ids[r] = argmax of row r (lowest index on ties) and probs[r] = the softmax
+// probability of that token, 1 / sum_v exp(l_v - max l) (the draft's
+// confidence, for the --spec-draft-p-min cut); one CTA of kArgThreads per
 // row.  With V % 4 == 0 each thread reads float4 c4 = t, t + kArgThreads, ...
-// eight loads at a time, all in flight before the compares.
+// eight loads at a time, all in flight before the compares.  The sum is an
+// online one: each thread keeps sum exp(v - m) for its running maximum m and
+// rescales it when m grows; partial sums merge as s1 e^(m1 - m) + s2 e^(m2 - m)
+// in a fixed order, so the result is deterministic.
 constexpr int kArgThreads = 1024;
+
+__device__ __forceinline__ void merge_sum(float& m, float& s, float om, float os) {
+  if (om == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = om;
+    s = os;
+    return;
+  }
+  const float nm = fmaxf(m, om);
+  s = s * expf(m - nm) + os * expf(om - nm);
+  m = nm;
+}
+
 __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const float* __restrict__ logits, int V,
-                                                                  int32_t* __restrict__ ids) {
+                                                                  int32_t* __restrict__ ids,
+                                                                  float* __restrict__ probs) {
   __shared__ float sv[kArgThreads / 32];
   __shared__ int si[kArgThreads / 32];
+  __shared__ float ss[kArgThreads / 32];
   griddep_launch_dependents();
   griddep_wait();
   const float* row = logits + (int64_t)blockIdx.x * V;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
+  float sum = 0.f;  // sum of exp(v - bv) over the values seen
   // per thread the indices visited increase, so strict > keeps the lowest
   auto take = [&](float v, int c) {
-    if (v > bv || bi == 0x7fffffff) { bv = v; bi = c; }
+    if (v > bv || bi == 0x7fffffff) {
+      sum = bi == 0x7fffffff ? 1.f : fmaf(sum, expf(bv - v), 1.f);
+      bv = v;
+      bi = c;
+    } else {
+      sum += expf(v - bv);
+    }
   };
   if ((V & 3) == 0) {
     const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -126,26 +161,34 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const float* _
   } else {
     for (int c = threadIdx.x; c < V; c += kArgThreads) take(row[c], c);
   }
+  float sm = bi == 0x7fffffff ? -INFINITY : bv;  // the maximum the sum refers to
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
     const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    const float om = __shfl_xor_sync(0xffffffffu, sm, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sum, o);
     if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    merge_sum(sm, sum, om, os);
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; ss[warp] = sum; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kArgThreads / 32; ++w)
+    sm = sv[0];
+    for (int w = 1; w < kArgThreads / 32; ++w) {
+      merge_sum(sm, sum, sv[w], ss[w]);
       if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
+    }
     ids[blockIdx.x] = bi;
+    if (probs) probs[blockIdx.x] = 1.f / sum;
   }
 }
 
 size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct RoundLayout {
-  size_t hA, hB, xn, ytmp, hin, hout, rows, dlog, acc, total;
+  size_t hA, hB, xn, ytmp, hin, hout, rows, dlog, dprob, acc, total;
 };
 RoundLayout round_layout(int H, int k, int V, int act) {
   const size_t esz = act == MOE_ACT_BF16 ? 2 : 4;
@@ -153,14 +196,15 @@ RoundLayout round_layout(int H, int k, int V, int act) {
   size_t off = 0;
   auto take = [&](size_t b) { const size_t o = off; off = al256(off + b); return o; };
   r.acc = take(accept_workspace_bytes(k, V));  // must stay zero between calls: first
-  r.hA = take((size_t)(k + 1) * H * esz);
-  r.hB = take((size_t)(k + 1) * H * esz);
+  r.hA = take((size_t)(k + 1) * H * 4);  // residual stream: fp32
+  r.hB = take((size_t)(k + 1) * H * 4);
   r.xn = take((size_t)(k + 1) * H * esz);
   r.ytmp = take((size_t)(k + 1) * H * esz);
   r.hin = take((size_t)k * k * H * esz);
   r.hout = take((size_t)k * k * H * esz);
-  r.rows = take((size_t)k * H * esz);
+  r.rows = take((size_t)k * H * 4);
   r.dlog = take((size_t)k * V * 4);
+  r.dprob = take((size_t)k * 4);
   r.total = off;
   return r;
 }
@@ -231,7 +275,7 @@ int moe_lm_head_forward(moe_lm_head* lm, const void* x, int32_t T, float eps, fl
   if (!x || !logits) return set_error(MOE_EINVAL, "moe_lm_head_forward: NULL x or logits");
   if (reinterpret_cast<uintptr_t>(x) & 15) return set_error(MOE_EINVAL, "moe_lm_head_forward: x must be 16-byte aligned");
   if (!(eps >= 0.f)) return set_error(MOE_EINVAL, "moe_lm_head_forward: eps must be >= 0");
-  cudaError_t e = lm_forward(lm, x, T, eps, logits, static_cast<cudaStream_t>(stream));
+  cudaError_t e = lm_forward(lm, x, lm->act == MOE_ACT_F32, T, eps, logits, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return set_error(MOE_ECUDA, "moe_lm_head_forward: %s", cudaGetErrorString(e));
   return MOE_OK;
 }
@@ -250,13 +294,14 @@ size_t mtp_round_workspace_bytes(int32_t H, int32_t k, int32_t V, int32_t act_dt
 }
 
 int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* const* draft_heads, int32_t k,
-              moe_lm_head* lm, const void* x, const float* noise, float eps, void* workspace,
-              size_t workspace_bytes, float* target_logits, void* head_out, int32_t* draft_ids,
+              moe_lm_head* lm, const void* x, const float* noise, float eps, float p_min, void* workspace,
+              size_t workspace_bytes, float* target_logits, float* draft_logits, void* head_out, int32_t* draft_ids,
               int32_t* out_n_accepted, int32_t* out_next_token, void* stream) {
   if (k < 1 || k > 7) return set_error(MOE_EINVAL, "mtp_round: k outside 1..7");
   if (n_target < 0 || (n_target > 0 && !target_layers) || !draft_heads || !lm || !x || !noise || !workspace ||
       !target_logits || !draft_ids || !out_n_accepted || !out_next_token)
     return set_error(MOE_EINVAL, "mtp_round: NULL argument");
+  if (!(p_min >= 0.f)) return set_error(MOE_EINVAL, "mtp_round: p_min must be >= 0 (0 keeps every draft)");
   const int H = lm->H, act = lm->act, V = lm->V;
   if (lm->T_max < k + 1) return set_error(MOE_EINVAL, "mtp_round: the LM head's T_max is below k+1");
   for (int l = 0; l < n_target; ++l) {
@@ -281,42 +326,52 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   cudaError_t e = cudaSuccess;
   // target stack: pre-norm residual blocks h <- h + MoE(rmsnorm(h)); the
   // hidden state ping-pongs between hA and hB, xn holds the normalised rows
-  const void* cur = x;
   void* xn = w + r.xn;
   void* yt = w + r.ytmp;
+  float* hA = reinterpret_cast<float*>(w + r.hA);
+  float* hB = reinterpret_cast<float*>(w + r.hB);
+  // h_0 = x (to fp32), xn = rmsnorm(h_0)
   if (act == MOE_ACT_BF16)
-    e = launch_pdl(add_rmsnorm_kernel<2>, k + 1, 256, 0, st, x, (const void*)nullptr, (void*)nullptr, xn, H, eps);
+    e = launch_pdl(add_rmsnorm_kernel<2, 2>, k + 1, 256, 0, st, x, (const void*)nullptr, hA, xn, H, eps);
   else
-    e = launch_pdl(add_rmsnorm_kernel<4>, k + 1, 256, 0, st, x, (const void*)nullptr, (void*)nullptr, xn, H, eps);
+    e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, x, (const void*)nullptr, hA, xn, H, eps);
   MCK(e, "mtp_round: norm");
+  float* cur = hA;
   for (int l = 0; l < n_target; ++l) {
-    void* out = w + ((l & 1) ? r.hB : r.hA);
+    float* out = cur == hA ? hB : hA;
     if ((rc = moe_forward(target_layers[l], xn, k + 1, yt, stream))) return rc;
-    if (act == MOE_ACT_BF16) e = launch_pdl(add_rmsnorm_kernel<2>, k + 1, 256, 0, st, cur, yt, out, xn, H, eps);
-    else e = launch_pdl(add_rmsnorm_kernel<4>, k + 1, 256, 0, st, cur, yt, out, xn, H, eps);
+    if (act == MOE_ACT_BF16)
+      e = launch_pdl(add_rmsnorm_kernel<2, 4>, k + 1, 256, 0, st, (const void*)cur, (const void*)yt, out, xn, H, eps);
+    else
+      e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, (const void*)cur, (const void*)yt, out, xn, H, eps);
     MCK(e, "mtp_round: residual + norm");
     cur = out;
   }
-  if ((rc = moe_lm_head_forward(lm, cur, k + 1, eps, target_logits, stream))) return rc;
+  e = lm_forward(lm, cur, true, k + 1, eps, target_logits, st);
+  MCK(e, "mtp_round: LM head (verify rows)");
   // noisy rows for the heads, and the rows the drafts are read from
+  float* rows = reinterpret_cast<float*>(w + r.rows);
   if (act == MOE_ACT_BF16)
-    e = launch_pdl(draft_rows_kernel<2>, k * k, 256, 0, st, cur, noise, k, H, eps, (void*)(w + r.hin),
-                   (void*)(w + r.rows));
+    e = launch_pdl(draft_rows_kernel<2>, k * k, 256, 0, st, (const float*)cur, noise, k, H, eps, (void*)(w + r.hin),
+                   rows);
   else
-    e = launch_pdl(draft_rows_kernel<4>, k * k, 256, 0, st, cur, noise, k, H, eps, (void*)(w + r.hin),
-                   (void*)(w + r.rows));
+    e = launch_pdl(draft_rows_kernel<4>, k * k, 256, 0, st, (const float*)cur, noise, k, H, eps, (void*)(w + r.hin),
+                   rows);
   MCK(e, "mtp_round: draft rows");
   uint8_t* hout = head_out ? static_cast<uint8_t*>(head_out) : w + r.hout;
   for (int j = 0; j < k; ++j) {
     const size_t o = (size_t)j * k * H * esz;
     if ((rc = moe_forward(draft_heads[j], w + r.hin + o, j + 1, hout + o, stream))) return rc;
   }
-  float* dlog = reinterpret_cast<float*>(w + r.dlog);
-  if ((rc = moe_lm_head_forward(lm, w + r.rows, k, eps, dlog, stream))) return rc;
-  e = launch_pdl(argmax_rows_kernel, k, kArgThreads, 0, st, (const float*)dlog, V, draft_ids);
+  float* dlog = draft_logits ? draft_logits : reinterpret_cast<float*>(w + r.dlog);
+  e = lm_forward(lm, rows, true, k, eps, dlog, st);
+  MCK(e, "mtp_round: LM head (draft rows)");
+  float* dprob = reinterpret_cast<float*>(w + r.dprob);
+  e = launch_pdl(argmax_rows_kernel, k, kArgThreads, 0, st, (const float*)dlog, V, draft_ids, dprob);
   MCK(e, "mtp_round: draft argmax");
-  return mtp_verify_accept(draft_ids, k, target_logits, V, out_n_accepted, out_next_token, w + r.acc,
-                           accept_workspace_bytes(k, V), stream);
+  e = accept_launch_cut(draft_ids, k, target_logits, V, dprob, p_min, out_n_accepted, out_next_token, w + r.acc, st);
+  MCK(e, "mtp_round: acceptance");
+  return MOE_OK;
 }
 
 }  // extern "C"

@@ -204,7 +204,10 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       rbt = (t - NR - NSG) % P.n_dt;
     } else {
       if (n_rent < 0) {
-        if (!wait_flag_geq(&P.sync->routing_ready, 1, P.timeout_ns, P.status, kSiteRouting, t)) { ok = false; break; }
+        if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t)) {
+          ok = false;
+          break;
+        }
         fence_proxy_async_global();
         n_rent = __ldcg(&P.sync->n_rent);
         // the routed entries, in one bulk copy (their writers fenced them for
@@ -607,14 +610,17 @@ int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).end + 
 // tile: logits, top-k and gates, then the permutation and the routed work
 // entries.  The entries and their count are published first (routing_ready);
 // ids, gates, offsets, perm and pos follow (routing_aux), since only the
-// combine and moe_get_routing read them.
+// combine and moe_get_routing read them.  A layer that holds only the routed
+// experts [e0, e0 + n_e) (one shard of an expert-parallel split) routes over
+// all E experts but makes entries for its own only; their expert field is the
+// local index e - e0.
 //
 // With Tk = T * k <= 128 pairs, pair p finds its place by counting: lt = the
 // pairs of lower experts, rank = the earlier pairs of its own expert, so its
 // slot is lt + rank (experts ascending, tokens ascending within an expert).
 // The first pair of an expert owns that expert's entries: its entry index is
 // the number of entries of all lower experts.
-__device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
+__device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NT = kConsumerWarps * 32;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
@@ -719,7 +725,8 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
       const int r_i = __shfl_sync(0xffffffffu, rank, q);
       const int c_i = __shfl_sync(0xffffffffu, cnt, q);
       const int tok = q / k;
-      const uint32_t starts = __ballot_sync(0xffffffffu, act && r_i % kGroup == 0);
+      const bool own = e_i >= P.e0 && e_i < P.e0 + P.n_e;
+      const uint32_t starts = __ballot_sync(0xffffffffu, act && own && r_i % kGroup == 0);
       int tk[kGroup];
       tk[0] = tok;
 #pragma unroll
@@ -727,7 +734,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
       if ((starts >> lane) & 1u) {
         const int M = min(kGroup, c_i - r_i);
         int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + __popc(starts & below));
-        dst[0] = make_int4(e_i, lane, M, tk[0]);
+        dst[0] = make_int4(e_i - P.e0, lane, M, tk[0]);
         dst[1] = make_int4(M > 1 ? tk[1] : 0, M > 2 ? tk[2] : 0, M > 3 ? tk[3] : 0, 0);
         fence_proxy_async_global();  // the producers fetch the entries with a bulk copy
       }
@@ -760,7 +767,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
       spos[p] = slot;
       slt[p] = lt;
       srank[p] = rank;
-      sent[p] = rank == 0 ? (c + kGroup - 1) / kGroup : 0;
+      sent[p] = rank == 0 && e >= P.e0 && e < P.e0 + P.n_e ? (c + kGroup - 1) / kGroup : 0;
     }
     consumer_sync();
     // entries: the first pair of each expert writes them (tokens from the
@@ -786,7 +793,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
 #pragma unroll
         for (int m = 0; m < kGroup; ++m) tok[m] = m < M ? sperm[slot0 + m] / k : 0;
         int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + w0 + g);
-        dst[0] = make_int4(e, slot0, M, tok[0]);
+        dst[0] = make_int4(e - P.e0, slot0, M, tok[0]);
         dst[1] = make_int4(tok[1], tok[2], tok[3], 0);
       }
       fence_proxy_async_global();  // the producers fetch the entries with a bulk copy
@@ -804,10 +811,24 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc) {
   }
   consumer_sync();
   // the barrier orders every thread's entry writes before thread 0's release
+  int* nrent_s = reinterpret_cast<int*>(misc + f.end);
   if (tid == 0) {
     P.sync->n_rent = n_rent;
     st_release(&P.sync->routing_ready, 1);
     stamp_last(P.stamps, kTsRoutingReady);
+    *nrent_s = n_rent;
+  }
+  consumer_sync();
+  // One arrival of the routing on every 128-row block of z: a block is
+  // complete after n_sh + n_rent down tiles and this arrival, and whoever
+  // arrives last combines it.  A shared down tile that finishes before the
+  // routing is known can therefore never be taken for the last one, and a
+  // layer with no down work for this batch (a shard none of whose experts
+  // was chosen, with no shared expert) still gets y from the combine.
+  {
+    const int last = P.n_sh + *nrent_s;
+    for (int b = tid; b < P.n_dt; b += NT)
+      if (atom_add_acq_rel(&P.d_cnt[b], 1) == last) pend[1 + atomicAdd(&pend[0], 1)] = b;
   }
   // what only the combine and moe_get_routing read
   if (tid < Tk) {
@@ -975,7 +996,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       consumer_sync();
       if (flags[0]) {
         if (tid == 0) stamp_last(P.stamps, kTsRouterDone);
-        finalize_routing(P, misc);
+        finalize_routing(P, misc, reinterpret_cast<int*>(smem + plan.pend));
       }
       consumer_sync();
     } else {
@@ -1086,23 +1107,17 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       for (int m = 0; m < d.M; ++m) P.z[(int64_t)(d.slot0 + m) * P.H + row] = v[m];
       if (d.group == d.ngroups - 1) {
         __syncwarp();  // orders the lanes' z writes before lane 0's release
-        int last = 0;
         if (lane == 0) {
+          // the block is complete after every down tile (n_sh + n_rent) and
+          // the routing's own arrival; n_rent is visible whenever the routing
+          // has arrived, and before that no tile can be the last one
           const int old = atom_add_acq_rel(&P.d_cnt[d.rbt], 1);
-          // a shared down tile may finish before the routing is published; the
-          // routed down tiles only run after it, so it cannot be last then
-          int n_ent = d.n_ent;
-          if (d.entry < P.n_sh)
-            n_ent = ld_acquire(&P.sync->routing_ready) ? P.n_sh + __ldcg(&P.sync->n_rent) : 0x7fffffff;
-          last = (old == n_ent - 1);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && lane == 0) {
-          stamp_last(P.stamps, kTsLastDownDone);
-          // this CTA combines the block when it leaves (with all its threads)
-          int* pend = reinterpret_cast<int*>(smem + plan.pend);
-          pend[1 + pend[0]] = d.rbt;
-          pend[0] += 1;
+          if (old == P.n_sh + ld_acquire(&P.sync->n_rent)) {
+            stamp_last(P.stamps, kTsLastDownDone);
+            // this CTA combines the block when it leaves (with all its threads)
+            int* pend = reinterpret_cast<int*>(smem + plan.pend);
+            pend[1 + atomicAdd(&pend[0], 1)] = d.rbt;
+          }
         }
       }
     }
@@ -1123,8 +1138,9 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
   __syncthreads();
   if (!flags[2]) return;
   for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
+    const int e = __ldcg(&P.ids[q]);
     sg[q] = __ldcg(&P.gates[q]);
-    sp[q] = __ldcg(&P.pos[q]);
+    sp[q] = e >= P.e0 && e < P.e0 + P.n_e ? __ldcg(&P.pos[q]) : -1;  // -1: another shard's expert
   }
   __syncthreads();
   const int n = pend[0];
@@ -1134,12 +1150,12 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
     float zv[kMaxTopK];
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) zv[j] = __ldcg(&P.z[(int64_t)sp[t * k + j] * P.H + r]);
+      if (j < k) zv[j] = sp[t * k + j] >= 0 ? __ldcg(&P.z[(int64_t)sp[t * k + j] * P.H + r]) : 0.f;
     const float zs = P.n_sh > 0 ? __ldcg(&P.z[(int64_t)(T * k + t) * P.H + r]) : 0.f;
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) acc = fmaf(sg[t * k + j], zv[j], acc);
+      if (j < k && sp[t * k + j] >= 0) acc = fmaf(sg[t * k + j], zv[j], acc);
     acc += zs;
     if (P.residual) {
       if constexpr (L == 2) acc += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + r]);

@@ -96,14 +96,28 @@ typedef struct {
   int32_t I_shared;  /* shared expert intermediate size; 0 = no shared expert */
   int32_t T_max;     /* largest token count moe_forward will be given, 1..8192 */
   int32_t act_dtype; /* moe_act */
-  int32_t reserved;  /* must be 0 */
+  uint32_t wait_limit_us; /* bound of every device-side wait, in microseconds
+                             (0 = the default, 2 s); a wait that runs out ends
+                             the launch with MOE_ETIMEOUT (moe_layer_status) */
   moe_tensor router_w; /* [E, H], MOE_F32 */
   moe_tensor router_b; /* [1, E], MOE_F32; data == NULL for no bias */
-  const moe_tensor* gate; /* HOST array of E descriptors, each [I, H] */
-  const moe_tensor* up;   /* HOST array of E descriptors, each [I, H] */
-  const moe_tensor* down; /* HOST array of E descriptors, each [H, I] */
+  const moe_tensor* gate; /* HOST array of n descriptors, each [I, H] */
+  const moe_tensor* up;   /* HOST array of n descriptors, each [I, H] */
+  const moe_tensor* down; /* HOST array of n descriptors, each [H, I] */
   moe_tensor sh_gate, sh_up, sh_down; /* [I_shared, H], [I_shared, H], [H, I_shared];
                                          the format may differ from the routed one */
+  /* Expert parallelism: the layer may hold only the routed experts
+   * [expert_begin, expert_begin + n) of the E the router scores, n =
+   * expert_count (0 = all E, with expert_begin 0); gate/up/down then describe
+   * those n experts in order.  Such a layer routes every token over all E
+   * experts (the router is replicated) and its forward returns that shard's
+   * part of y: sum over the token's chosen experts that it holds of
+   * g[t,j] FFN(x[t]), plus the shared expert if it has one (I_shared > 0).
+   * The sum of the parts of shards that cover every expert once, with the
+   * shared expert on exactly one of them, is the layer's y (residual: give
+   * exactly one shard moe_forward_residual). */
+  int32_t expert_begin;
+  int32_t expert_count;
 } moe_layer_desc;
 
 typedef struct moe_layer moe_layer;
@@ -170,6 +184,17 @@ int moe_layer_status(moe_layer* L, void* stream);
  *  14 last block leaving
  * The stamps cost a few atomic writes per block and are always recorded. */
 int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream);
+
+/* Test hook for the bounded device-side waits (no fault is involved).
+ * site 1: the layer's next T <= 8 forward waits for a routing publication
+ * that never comes (its work-claiming threads wait for a flag value the
+ * kernel does not write).  That wait runs out after the layer's
+ * wait_limit_us, every other thread of the launch sees the status word and
+ * stops, all copies in flight are drained, and moe_layer_status() then
+ * returns MOE_ETIMEOUT naming the "routing flag" site and clears the state;
+ * later forwards are unaffected.  The output of the failed forward is
+ * undefined.  Other sites: MOE_EINVAL. */
+int moe_layer_inject_timeout(moe_layer* L, int32_t site);
 
 /* Bytes of weights resident on the device (repacked), and of workspace. */
 size_t moe_layer_weight_bytes(const moe_layer* L);
@@ -263,17 +288,27 @@ void moe_lm_head_destroy(moe_lm_head* lm);
  *   head j (j < k) runs on rmsnorm of the j+1 rows h~_j = h_n[0..j] +
  *   noise[j][0..j] (the noise stands in for an imperfect draft model) and
  *   writes head_out[j] ([k][k][H], rows 0..j used; may be NULL to discard);
- *   draft_ids[j] = argmax (lowest id on ties) of lm(h~_j[j]);
- *   then greedy acceptance as mtp_verify_accept.
+ *   draft_ids[j] = argmax (lowest id on ties) of lm(h~_j[j]), whose logits
+ *   go to draft_logits fp32 [k, V] (may be NULL to discard);
+ *   draft confidence cut ("Step-3.5-Flash MTP GGUF", "Usage":
+ *   --spec-draft-p-min, 0.65 recommended; 0 in the PR's runs): p_j = the
+ *   softmax probability of draft j's token under its logits (fp32,
+ *   1 / sum_v exp(l_v - max l)); drafting stops at the first j with
+ *   p_j < p_min, and draft_ids[j..k-1] are set to -1 (p_min = 0 keeps
+ *   every draft);
+ *   then greedy acceptance as mtp_verify_accept over the kept drafts.
+ * The residual stream h and the noisy rows h~ are kept in fp32 in both
+ * act dtypes (the layers' inputs rmsnorm(h) and outputs are in act_dtype).
  * Every layer and the head must share act_dtype; all layers have hidden H,
  * T_max >= k+1.  noise fp32 [k][k][H] (device).  1 <= k <= 7.
  * workspace: device scratch of mtp_round_workspace_bytes(H, k, V, act)
  * bytes, 256-byte aligned, zero-filled before its first use and left so.
- * Asynchronous; no allocation.  Errors: MOE_EINVAL on any mismatch. */
+ * Asynchronous; no allocation.  Errors: MOE_EINVAL on any mismatch, or
+ * p_min < 0 / NaN. */
 size_t mtp_round_workspace_bytes(int32_t H, int32_t k, int32_t V, int32_t act_dtype);
 int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* const* draft_heads, int32_t k,
-              moe_lm_head* lm, const void* x, const float* noise, float eps, void* workspace,
-              size_t workspace_bytes, float* target_logits, void* head_out, int32_t* draft_ids,
+              moe_lm_head* lm, const void* x, const float* noise, float eps, float p_min, void* workspace,
+              size_t workspace_bytes, float* target_logits, float* draft_logits, void* head_out, int32_t* draft_ids,
               int32_t* out_n_accepted, int32_t* out_next_token, void* stream);
 
 /* Message for the last error on the calling thread; valid until the next

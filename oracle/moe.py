@@ -142,18 +142,25 @@ def route(x, layer: Layer):
                 pos=pos, act=act)
 
 
-def forward(x, layer: Layer, routing=None):
-    """y [T, H] fp64 and the routing dict for x [T, H]."""
+def forward(x, layer: Layer, routing=None, expert_fn=None):
+    """y [T, H] fp64 and the routing dict for x [T, H].
+
+    ``expert_fn(e, xr)``, if given, stands in for ``swiglu_expert(xr,
+    layer.expert(e))`` (the same computation evaluated elsewhere, e.g. by
+    worker processes holding the same weights)."""
     x = np.asarray(x, F64)
     T = x.shape[0]
     r = route(x, layer) if routing is None else routing
     k = layer.top_k
+    if expert_fn is None:
+        def expert_fn(e, xr):
+            return swiglu_expert(xr, layer.expert(e))
     z = np.zeros((T, k, layer.H), F64)
     for e in r["act"]:
         e = int(e)
         sl = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
         toks, slots = sl // k, sl % k
-        z[toks, slots] = swiglu_expert(x[toks], layer.expert(e))
+        z[toks, slots] = expert_fn(e, x[toks])
     y = np.zeros((T, layer.H), F64)
     for j in range(k):
         y += r["gates"][:, j:j + 1] * z[:, j]
@@ -195,3 +202,27 @@ def max_rel_err_elementwise(y, y_ref, floor=1e-3):
     den = np.maximum(np.abs(y_ref), floor * np.abs(y_ref).max(axis=1, keepdims=True))
     den = np.maximum(den, 1e-30)
     return float((np.abs(y - y_ref) / den).max())
+
+
+def forward_shard(x, layer: Layer, begin, count, with_shared, routing=None):
+    """The part of y that one expert-parallel shard computes: the routing over
+    all E experts is the layer's, but only pairs whose expert lies in
+    [begin, begin + count) contribute (with their full gates), plus the shared
+    expert if the shard holds it.  Summed over shards that cover every expert
+    once with the shared expert on one of them, this is forward(x)."""
+    x = np.asarray(x, F64)
+    T = x.shape[0]
+    r = route(x, layer) if routing is None else routing
+    k = layer.top_k
+    y = np.zeros((T, layer.H), F64)
+    for e in r["act"]:
+        e = int(e)
+        if not begin <= e < begin + count:
+            continue
+        sl = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
+        toks, slots = sl // k, sl % k
+        z = swiglu_expert(x[toks], layer.expert(e))
+        y[toks] += r["gates"][toks, slots][:, None] * z
+    if with_shared and layer.shared is not None:
+        y += swiglu_expert(x, layer.shared)
+    return y, r

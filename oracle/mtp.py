@@ -24,7 +24,17 @@ reading of it, with every step a plain definition:
               for an imperfect draft model: it is what makes drafts differ from
               the target); its output is computed and compared as a layer output;
               draft token d_{j+1} = argmax W_lm . rmsnorm(h~_j[j])
-  acceptance  greedy: oracle.accept.greedy_accept(d_1..d_k, logits)
+  draft cut   ("Step-3.5-Flash MTP GGUF", "Usage" and "Notes": the server flag
+              --spec-draft-p-min, 0.65 recommended; "Support Step3.5/3.7 flash
+              mtp3", test settings: 0.0 in the PR's runs.  The pages give the
+              flag and its values only; the reading here is the plain one:)
+              draft j's confidence is the probability of its token under the
+              draft logits, p_j = max_v softmax(draft_logits[j])_v =
+              1 / sum_v exp(l_v - max l); drafting stops at the first j with
+              p_j < p_min, and that draft and every later one are dropped
+              (reported as -1).  p_min = 0 keeps every draft.
+  acceptance  greedy: oracle.accept.greedy_accept(kept drafts, logits of the
+              kept drafts' verify rows)
 Since drafts are a function of the target's hidden states here, the target
 runs first; the work of the round and the acceptance rule are those of the
 trace.
@@ -48,41 +58,68 @@ def lm_logits(h, lm: moe.QTensor, eps=1e-6):
     return rmsnorm(h, eps) @ lm.dense().T
 
 
-def target_stack(x, layers, eps=1e-6, routes=None):
+def target_stack(x, layers, eps=1e-6, routes=None, layer_forward=None):
     """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers.
-    If `routes` is a list, each layer's routing dict is appended to it."""
+    If `routes` is a list, each layer's routing dict is appended to it.
+    ``layer_forward(x, L)``, if given, stands in for ``moe.forward(x, L)``."""
+    fwd = moe.forward if layer_forward is None else layer_forward
     h = np.asarray(x, F64)
     for L in layers:
-        y, r = moe.forward(rmsnorm(h, eps), L)
+        y, r = fwd(rmsnorm(h, eps), L)
         if routes is not None:
             routes.append(r)
         h = h + y
     return h
 
 
-def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6):
+def draft_probability(row):
+    """The largest softmax probability of a logit row, 1 / sum_v exp(l_v - max l),
+    in fp64."""
+    row = np.asarray(row, F64)
+    return float(1.0 / np.exp(row - row.max()).sum())
+
+
+def cut_drafts(drafts, probs, p_min):
+    """The drafts kept under the confidence cut: the longest prefix whose
+    probabilities are all >= p_min.  Returns (kept drafts, n_drafted)."""
+    n = 0
+    while n < len(drafts) and probs[n] >= p_min:
+        n += 1
+    return list(drafts[:n]), n
+
+
+def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, layer_forward=None):
     """One round.  x [k+1, H]; heads: k layers; noise [k][k][H] (head j uses
-    rows 0..j of noise[j]).  Returns a dict with h_tgt, logits, head_out
-    (list of [j+1, H]), draft_rows [k, H], draft_logits [k, V], drafts [k],
-    n_accepted, next_token, argmax (the target's per-row argmax) and the routing
-    dicts of every target layer (target_routes) and head (head_routes)."""
+    rows 0..j of noise[j]); p_min the draft confidence cut.  Returns a dict
+    with h_tgt, logits, head_out (list of [j+1, H]), draft_rows [k, H],
+    draft_logits [k, V], draft_probs [k], drafts [k] (-1 past the cut),
+    n_drafted, n_accepted, next_token, argmax (the target's per-row argmax)
+    and the routing dicts of every target layer (target_routes) and head
+    (head_routes).  ``layer_forward(x, L)``, if given, stands in for
+    ``moe.forward(x, L)``."""
+    fwd = moe.forward if layer_forward is None else layer_forward
     k = len(heads)
     x = np.asarray(x, F64)
     assert x.shape[0] == k + 1
     target_routes, head_routes = [], []
-    h_tgt = target_stack(x, layers, eps, target_routes)
+    h_tgt = target_stack(x, layers, eps, target_routes, layer_forward=fwd)
     logits = lm_logits(h_tgt, lm, eps)
     head_out, rows = [], []
     for j, head in enumerate(heads):
         ht = h_tgt[: j + 1] + np.asarray(noise[j][: j + 1], F64)
-        y, hr = moe.forward(rmsnorm(ht, eps), head)
+        y, hr = fwd(rmsnorm(ht, eps), head)
         head_routes.append(hr)
         head_out.append(y)
         rows.append(ht[j])
     rows = np.stack(rows) if rows else np.zeros((0, x.shape[1]))
     draft_logits = lm_logits(rows, lm, eps)
-    drafts = [accept.argmax_lowest(r) for r in draft_logits]
-    n, nxt, amax = accept.greedy_accept(drafts, logits)
+    tokens = [accept.argmax_lowest(r) for r in draft_logits]
+    probs = [draft_probability(r) for r in draft_logits]
+    kept, n_drafted = cut_drafts(tokens, probs, p_min)
+    n, nxt, _ = accept.greedy_accept(kept, logits[: n_drafted + 1])
+    amax = [accept.argmax_lowest(r) for r in logits]
+    drafts = kept + [-1] * (k - n_drafted)
     return dict(h_tgt=h_tgt, logits=logits, head_out=head_out, draft_rows=rows,
-                draft_logits=draft_logits, drafts=drafts, n_accepted=n, next_token=nxt,
-                argmax=amax, target_routes=target_routes, head_routes=head_routes)
+                draft_logits=draft_logits, draft_probs=probs, drafts=drafts, n_drafted=n_drafted,
+                n_accepted=n, next_token=nxt, argmax=amax, target_routes=target_routes,
+                head_routes=head_routes)

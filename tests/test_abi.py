@@ -74,11 +74,11 @@ def test_mtp_entry_points_reject_bad_arguments_on_host(lib):
     assert lib.mtp_round_workspace_bytes(4096, 3, 0, pkg.ACT_BF16) == 0
     assert lib.mtp_round_workspace_bytes(4096, 3, 32768, 7) == 0
     # the round: k outside 1..7, then NULL arguments, before any device work
-    assert lib.mtp_round(None, 0, None, 0, None, None, None, 1e-6, None, 0, None, None, None, None, None,
-                         None) == pkg.MOE_EINVAL
+    assert lib.mtp_round(None, 0, None, 0, None, None, None, 1e-6, 0.0, None, 0, None, None, None, None, None,
+                         None, None) == pkg.MOE_EINVAL
     assert b"k outside" in lib.moe_last_error()
-    assert lib.mtp_round(None, 0, None, 3, None, None, None, 1e-6, None, 0, None, None, None, None, None,
-                         None) == pkg.MOE_EINVAL
+    assert lib.mtp_round(None, 0, None, 3, None, None, None, 1e-6, 0.0, None, 0, None, None, None, None, None,
+                         None, None) == pkg.MOE_EINVAL
     assert b"NULL" in lib.moe_last_error()
     # the LM head: NULL, wrong format, shape and T_max checks
     out = ctypes.c_void_p()

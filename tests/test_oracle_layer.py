@@ -110,3 +110,28 @@ def test_combine_uses_gates_in_slot_order():
         for j in range(3):
             want += r["gates"][t, j] * moe.swiglu_expert(x[t:t + 1], L.expert(int(r["ids"][t, j])))[0]
         assert np.allclose(y[t], want, rtol=1e-13, atol=1e-15)
+
+
+def test_expert_shards_sum_to_the_layer():
+    # shards covering every expert once, shared expert on one: their parts sum
+    # to the layer's output; each part only holds its own experts' pairs
+    L, ws, sh = _rand_layer(11, E=7, k=3)
+    rng = np.random.default_rng(12)
+    x = rng.normal(size=(5, 64)).astype(np.float32)
+    y, r = moe.forward(x, L)
+    for split in ([(0, 7)], [(0, 3), (3, 4)], [(0, 2), (2, 2), (4, 3)]):
+        parts = [moe.forward_shard(x, L, b, n, i == 0)[0] for i, (b, n) in enumerate(split)]
+        assert np.allclose(sum(parts), y, rtol=1e-12, atol=1e-14)
+    # a shard's part by hand: the gates of its own pairs, and no shared expert
+    part, _ = moe.forward_shard(x, L, 3, 4, False)
+    want = np.zeros_like(part)
+    for t in range(5):
+        for j in range(3):
+            e = int(r["ids"][t, j])
+            if 3 <= e < 7:
+                want[t] += r["gates"][t, j] * moe.swiglu_expert(x[t:t + 1], L.expert(e))[0]
+    assert np.allclose(part, want, rtol=1e-13, atol=1e-15)
+    # a shard none of whose experts is chosen, without the shared expert: zero
+    unused = sorted(set(range(7)) - set(r["ids"][0].tolist()))
+    z, _ = moe.forward_shard(x[:1], L, unused[0], 1, False)
+    assert not z.any()

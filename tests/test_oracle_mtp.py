@@ -2,6 +2,7 @@
 forms, the residual stack against special cases, and the round's acceptance
 against properties that fix how drafts and target rows line up."""
 import numpy as np
+import pytest
 
 from oracle import formats, moe, mtp
 from tests._oracle_layer import layer_from_fp32, qtensor
@@ -102,3 +103,52 @@ def test_round_head_outputs_and_acceptance():
     while n < 3 and r["drafts"][n] == r["argmax"][n]:
         n += 1
     assert r["n_accepted"] == n and r["next_token"] == r["argmax"][n]
+
+
+def test_draft_probability_closed_forms():
+    # two tokens with logits 0 and -ln 3: p = 1 / (1 + 1/3) = 3/4
+    assert mtp.draft_probability([0.0, -np.log(3.0)]) == pytest.approx(0.75, rel=1e-15)
+    # a uniform row: 1 / V, whatever the common value
+    assert mtp.draft_probability(np.full(40, 7.5)) == pytest.approx(1 / 40, rel=1e-15)
+    # shift invariance, and the probability of the argmax, not of index 0
+    row = np.array([0.3, 2.0, -1.0, 1.5])
+    p = np.exp(row) / np.exp(row).sum()
+    assert mtp.draft_probability(row) == pytest.approx(p.max(), rel=1e-14)
+    assert mtp.draft_probability(row + 100.0) == pytest.approx(p.max(), rel=1e-13)
+
+
+def test_cut_drafts_is_a_prefix_rule():
+    d, pr = [11, 22, 33], [0.9, 0.5, 0.95]
+    assert mtp.cut_drafts(d, pr, 0.0) == ([11, 22, 33], 3)
+    assert mtp.cut_drafts(d, pr, 0.5) == ([11, 22, 33], 3)   # p >= p_min is kept
+    assert mtp.cut_drafts(d, pr, 0.6) == ([11], 1)           # a later confident draft is cut too
+    assert mtp.cut_drafts(d, pr, 0.95) == ([], 0)
+    assert mtp.cut_drafts([], [], 0.7) == ([], 0)
+
+
+def test_round_p_min_zero_changes_nothing_and_one_drafts_nothing():
+    r, x, layers, heads, lm, noise = _round(3.0)
+    r0 = mtp.mtp_round(x, layers, heads, lm, noise, p_min=0.0)
+    assert r0["drafts"] == r["drafts"] and r0["n_drafted"] == 3
+    assert (r0["n_accepted"], r0["next_token"]) == (r["n_accepted"], r["next_token"])
+    # p <= 1 always and < 1 for a row of finite logits over V > 1 tokens
+    r1 = mtp.mtp_round(x, layers, heads, lm, noise, p_min=1.0)
+    assert r1["n_drafted"] == 0 and r1["drafts"] == [-1, -1, -1]
+    assert r1["n_accepted"] == 0 and r1["next_token"] == r["argmax"][0]
+
+
+def test_round_p_min_just_above_and_below_a_draft():
+    # no noise: every draft matches the target, so the accepted count equals
+    # the number of drafts the cut keeps
+    r, x, layers, heads, lm, noise = _round(0.0)
+    probs = r["draft_probs"]
+    assert r["n_accepted"] == 3
+    j = int(np.argmin(probs))  # the least confident draft decides the cut
+    below = mtp.mtp_round(x, layers, heads, lm, noise, p_min=probs[j] * (1 - 1e-9))
+    above = mtp.mtp_round(x, layers, heads, lm, noise, p_min=probs[j] * (1 + 1e-9))
+    assert below["n_drafted"] == 3 and below["n_accepted"] == 3
+    want = min(i for i in range(3) if probs[i] < probs[j] * (1 + 1e-9))
+    assert above["n_drafted"] == want == above["n_accepted"]
+    assert above["drafts"][:want] == r["drafts"][:want] and above["drafts"][want:] == [-1] * (3 - want)
+    # the next token is the target's argmax at the first row past the kept drafts
+    assert above["next_token"] == r["argmax"][want]
