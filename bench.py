@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--experts", type=int, default=0,
                    help="override the expert count (smaller resident layer for profiler captures)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override the batch size T (with --experts: the same tokens per expert on a smaller layer)")
     return p.parse_args()
 
 
@@ -287,9 +289,9 @@ def run_ours(args):
     if args.workload in synth.ROUNDS:
         return run_round(args)
     w = synth.WORKLOADS[args.workload]
-    if args.experts:
+    if args.experts or args.tokens:
         import dataclasses
-        w = dataclasses.replace(w, E=args.experts)
+        w = dataclasses.replace(w, E=args.experts or w.E, T=args.tokens or w.T)
     copies = args.copies if args.copies is not None else (4 if w.T <= 8 else 1)
     layers = [synthetic_layer(w, pkg.ACT_BF16, T_max=w.T)[0] for _ in range(copies)]
     x = synth.activations(w, "cuda")

@@ -12,20 +12,23 @@
 //     activation records, down outputs, counters, the combine), so the
 //     consumers never wait on global-memory round trips.
 //
-// Tile order in the queue (each kind only waits on kinds before it, so every
-// tile another tile waits for has already been claimed by a running CTA):
-//   x records        one per 512-column slice of x: all T tokens' activation
-//                    records (one 32-column block per thread)
+// Work items, in order (each kind only waits on kinds before it, so every
+// item another item waits for has already been taken by a running CTA):
 //   router tiles     32 experts x 512 columns; each adds its share of the
 //                    logits to a global sum kept as exact 2^-32 fixed point
 //                    (integer atomics, so the sum does not depend on the
-//                    order of arrival).  The last router tile to finish
-//                    computes the routing (top-k, gates, permutation, expert
-//                    work entries).
+//                    order of arrival).  The tiles of the first 32 experts
+//                    also write the activation records of their slice of x.
+//                    The last router tile to finish computes the routing
+//                    (top-k, gates, permutation, expert work entries).
 //   shared gate/up   32 outputs (16+16 gate/up rows, twice) x full K
 //   shared down      128 outputs x full I
 //   routed gate/up   per routed work entry (<= 4 tokens of one expert)
 //   routed down
+// The router tiles and the shared gate/up tiles go to blocks 0, 1, ... by
+// block index, and each of those blocks starts loading its item's weights
+// before it waits for the previous kernel in the stream; every later item is
+// claimed from a global queue.
 // Hand-offs use last-arriver counters: the last gate/up tile of an entry
 // publishes it (its activation records are complete); the last down tile of
 // a 128-row block combines that block of y in slot order.  No floating-point
@@ -43,11 +46,11 @@
 
 namespace moe {
 
-enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3, kXRec = 4 };
+enum TileKind : int { kRouter = 0, kGateUp = 1, kDown = 2, kEnd = 3 };
 
 struct Desc {
   int kind, chunk, nch, M;         // read by every consumer thread
-  int nbc, fmt, rgks, off;         //   " (off = ring offset; rgks: router and x-record items: row
+  int nbc, fmt, rgks, off;         //   " (off = ring offset; rgks: router tiles: row
                                    //   group << 16 | chunk; gate/up and down: groups in the stage)
   int entry, rbt, group, ngroups;  // read by the epilogue warp
   int slot0, n_ent, n_tiles_entry, pad;
@@ -144,11 +147,146 @@ __device__ __forceinline__ bool wait_released(uint64_t* empty, int NS, int j, co
   return mbar_wait_bounded(&empty[j % NS], (uint32_t)((j / NS) & 1), P.timeout_ns, P.status, kSiteEmpty, j);
 }
 
+// Where a work item's stages come from and how large they are.  Shared by
+// the prefetch before the dependency wait and the main loop, so both place
+// and size the same stages.
+struct Geo {
+  int kind, rgk, rbt, entry, nbc, fmt, M, nch, ngroups, gps, need, nstages, slot0, n_tiles, e_id;
+  uint32_t wb, per;
+  int64_t cbytes;
+  const uint8_t* wbase;
+};
+
+// A router tile: 32 experts (row group rg) x one 512-column slice rbt; one
+// stage holding the tile's weights and then the slice of x.
+template <int L>
+__device__ __forceinline__ Geo geo_router(const SmallParams& P, int rg, int rbt) {
+  constexpr int XEL = L == 2 ? 2 : 4;
+  Geo g;
+  g.kind = kRouter;
+  g.rgk = rg << 16;
+  g.rbt = rbt;
+  g.entry = 0;
+  g.nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);  // 128-column chunks in the slice
+  g.fmt = MOE_F32;
+  g.M = P.T;
+  g.nch = 1;
+  g.ngroups = 1;
+  g.gps = 1;
+  g.nstages = 1;
+  g.slot0 = 0;
+  g.n_tiles = 0;
+  g.e_id = -1;
+  g.cbytes = (int64_t)g.nbc * chunk_bytes(MOE_F32, kRouterCc);
+  g.wbase = P.router + ((int64_t)rg * P.n_ks * 64 + kRouterTileChunks * 32 * rbt) * kRows * 16;
+  g.wb = (uint32_t)g.cbytes;
+  g.per = (uint32_t)(g.nbc * kRouterCc * XEL);
+  g.need = (int)((g.wb + (uint32_t)g.M * g.per + 127u) & ~127u);
+  return g;
+}
+
+// A gate/up tile (32 SwiGLU outputs: 16 gate + 16 up rows, twice) or a down
+// tile (64 output rows: half of one 128-row block of z) of one work entry:
+// the shared expert's (entry < n_sh) or a routed expert's (ep = its entry).
+template <int L>
+__device__ __forceinline__ Geo geo_expert(const SmallParams& P, int kind, int entry, int rbt, const Entry* ep) {
+  constexpr int RB = rec_bytes(L);
+  Geo g;
+  g.kind = kind;
+  g.rgk = 0;
+  g.rbt = rbt;
+  g.entry = entry;
+  const bool shared_e = entry < P.n_sh;
+  if (shared_e) {
+    g.slot0 = P.T * P.k + kGroup * entry;
+    g.M = min(kGroup, P.T - kGroup * entry);
+    g.e_id = -1;
+  } else {
+    g.e_id = ep->e;
+    g.slot0 = ep->slot0;
+    g.M = ep->M;
+  }
+  g.fmt = shared_e ? P.sfmt : P.fmt;
+  int kc;
+  if (kind == kGateUp) {
+    g.ngroups = 2;
+    g.nch = shared_e ? P.sgu_nch : P.gu_nch;
+    kc = shared_e ? P.sgu_kc : P.gu_kc;
+    g.n_tiles = shared_e ? P.n_gu_sh : P.n_gu;
+  } else {
+    g.ngroups = 2;  // 64 output rows
+    g.nch = shared_e ? P.sdn_nch : P.dn_nch;
+    kc = shared_e ? P.sdn_kc : P.dn_kc;
+    g.n_tiles = 0;
+  }
+  g.nbc = kc / 32;
+  g.cbytes = chunk_bytes(g.fmt, kc);
+  g.wbase = kind == kGateUp
+                ? (shared_e ? P.sgu : P.gu + (int64_t)g.e_id * P.gu_stride) + (int64_t)(2 * rbt) * g.nch * g.cbytes
+                : (shared_e ? P.sdn : P.dn + (int64_t)g.e_id * P.dn_stride) + (int64_t)(2 * rbt) * g.nch * g.cbytes;
+  g.per = (uint32_t)(g.nbc * RB);
+  // A group that is one chunk may share its stage with the next groups of
+  // the tile (contiguous in memory, same records): fewer, larger stages,
+  // as long as two of them fit the ring.
+  g.gps = 1;
+  if (g.nch == 1)
+    while (2 * g.gps <= 4 && g.ngroups % (2 * g.gps) == 0 &&
+           (int64_t)2 * g.gps * g.cbytes + (int64_t)g.M * g.per <= (int64_t)(P.ring_bytes / 2))
+      g.gps *= 2;
+  g.wb = (uint32_t)(g.gps * g.cbytes);
+  g.need = (int)((g.wb + (uint32_t)g.M * g.per + 127u) & ~127u);
+  g.nstages = g.ngroups * g.nch / g.gps;
+  return g;
+}
+
+// Descriptor of stage q of an item, placed at ring offset pos.
+__device__ __forceinline__ void write_desc(Desc* d, const Geo& g, int q, int pos) {
+  const int grp = q * g.gps / g.nch, c = q * g.gps - grp * g.nch;
+  const int kch = g.kind == kRouter ? kRouterTileChunks * g.rbt + c : 0;
+  int4* dd = reinterpret_cast<int4*>(d);
+  dd[0] = make_int4(g.kind, c, g.nch, g.M);
+  dd[1] = make_int4(g.nbc, g.fmt, g.kind == kRouter ? g.rgk | kch : g.gps, pos);
+  dd[2] = make_int4(g.entry, g.rbt, grp, g.ngroups);
+  dd[3] = make_int4(g.slot0, 0, g.n_tiles, 0);
+}
+
+// Work items [0, NR + NSG) -- the router tiles, then the shared expert's
+// gate/up tiles -- need nothing computed by this launch to start loading
+// their weights.  Block b < n_static takes item b without claiming it; its
+// producer issues the weights of the item's first stages (as many as fit
+// the ring) before the block waits for the previous kernel in the stream,
+// which overlaps those loads with that kernel's tail.  Weights are constant
+// data, written only when the layer was created.  Returns the stages issued;
+// *head is the ring offset after them.
+template <int L>
+__device__ int producer_prefetch(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, int t, int* head) {
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
+  Desc* descs = reinterpret_cast<Desc*>(smem + plan.descs);
+  const int NR = P.n_rg * P.n_kt;
+  const Geo g = t < NR ? geo_router<L>(P, t / P.n_kt, t % P.n_kt)
+                       : geo_expert<L>(P, kGateUp, (t - NR) / P.n_gu_sh, (t - NR) % P.n_gu_sh, nullptr);
+  const uint64_t wpol = l2_evict_first_policy();
+  int n = 0, pos = 0;
+  while (n < g.nstages && n < P.n_stages && pos + g.need <= P.ring_bytes) {
+    write_desc(descs + n, g, n, pos);
+    mbar_arrive_expect_tx(&full[n], g.wb + (uint32_t)g.M * g.per);
+    bulk_g2s_hint(smem + plan.ring + pos, g.wbase + (int64_t)n * g.wb, g.wb, &full[n], wpol);
+    pos += g.need;
+    ++n;
+  }
+  *head = pos;
+  return n;
+}
+
 // The producer is one thread; everything it keeps per stage lives in
 // registers or shared memory (no local arrays, no captured locals), since a
 // single thread pays the full latency of every dependent access.
+// t0: the block's static item (or -1: claim from the queue), with n_pre of
+// its stages already placed at ring offsets [0, head0) and their weights
+// issued (producer_prefetch).
 template <int L>
-__device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
+__device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, int t0, int n_pre,
+                              int head0) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + P.n_stages;
   Desc* descs = reinterpret_cast<Desc*>(smem + plan.descs);
@@ -156,52 +294,32 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   uint32_t* readybits = reinterpret_cast<uint32_t*>(smem + plan.flags) + 4;  // [8] entries seen published
   constexpr int RB = rec_bytes(L);
   constexpr int XEL = L == 2 ? 2 : 4;  // bytes of one x element
-  const int NX = P.n_kt;  // x-record items (one per 512-column slice of x) come first
   const int NR = P.n_rg * P.n_kt;
-  const int NSG = P.n_sh * P.n_gu_sh, NSD = P.n_sh * P.n_dt;
+  const int NDT = 2 * P.n_dt;  // down tiles per entry (64 output rows each)
+  const int NSG = P.n_sh * P.n_gu_sh, NSD = P.n_sh * NDT;
   const int NS = P.n_stages;
+  const int n_static = min((int)gridDim.x, NR + NSG);  // items taken by block index, not claimed
   // Stage j (in issue order) uses descriptor slot j % NS and `need` bytes of
   // the ring placed right after stage j-1 (or at 0 when the end is reached).
   // Stages [oldest, issued) may still be in flight; their bytes form one arc
   // of the ring that starts at descs[oldest % NS].off and ends at head.
-  int issued = 0, oldest = 0, head = 0;
+  int issued = 0, oldest = 0, head = head0;
   bool ok = true;
   int n_rent = -1;
   for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
   const uint64_t wpol = l2_evict_first_policy();  // weights are read once per launch
   bool st_gu = false, st_dn = false;               // first routed gate/up / down copy stamped
-  int t = atomicAdd(&P.sync->queue, 1) - NX;
+  int t = t0 >= 0 ? t0 : atomicAdd(&P.sync->queue, 1) + n_static;
+  int pre = t0 >= 0 ? n_pre : 0;  // stages of this item placed and loading already
   while (ok) {
-    const int t_next = atomicAdd(&P.sync->queue, 1) - NX;  // claim one ahead: its latency overlaps this tile
-    int kind, rgk = 0, rbt, entry = 0, ngroups = 1, nch = 1, nbc, fmt, M, slot0 = 0, n_tiles = 0;
-    const Entry* ep = nullptr;
-    bool shared_e = false;
-    if (t < 0) {
-      // an x-record item: the slice of x for all T tokens, no weights
-      kind = kXRec;
-      rbt = t + NX;
-      fmt = MOE_F32;
-      nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);
-      M = P.T;
-    } else if (t < NR) {
-      // a router tile is one stage: the tile's router weights (one contiguous
-      // range of the repacked router) and its x slice
-      kind = kRouter;
-      rgk = (t / P.n_kt) << 16;
-      rbt = t % P.n_kt;  // router: index of the 512-column slice
-      nch = 1;
-      fmt = MOE_F32;
-      nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * rbt);  // 128-column chunks in the slice
-      M = P.T;
+    Geo g;
+    if (t < NR) {
+      g = geo_router<L>(P, t / P.n_kt, t % P.n_kt);
     } else if (t < NR + NSG) {
-      kind = kGateUp;
-      entry = (t - NR) / P.n_gu_sh;
-      rbt = (t - NR) % P.n_gu_sh;
+      g = geo_expert<L>(P, kGateUp, (t - NR) / P.n_gu_sh, (t - NR) % P.n_gu_sh, nullptr);
     } else if (t < NR + NSG + NSD) {
-      kind = kDown;
-      entry = (t - NR - NSG) / P.n_dt;
-      rbt = (t - NR - NSG) % P.n_dt;
+      g = geo_expert<L>(P, kDown, (t - NR - NSG) / NDT, (t - NR - NSG) % NDT, nullptr);
     } else {
       if (n_rent < 0) {
         if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t)) {
@@ -221,71 +339,20 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         }
       }
       const int A = NR + NSG + NSD;
-      const int NG = n_rent * P.n_gu, ND = n_rent * P.n_dt;
+      const int NG = n_rent * P.n_gu, ND = n_rent * NDT;
       if (t < A + NG) {
-        kind = kGateUp;
-        entry = P.n_sh + (t - A) / P.n_gu;
-        rbt = (t - A) % P.n_gu;
+        const int entry = P.n_sh + (t - A) / P.n_gu;
+        g = geo_expert<L>(P, kGateUp, entry, (t - A) % P.n_gu, ecache + entry);
       } else if (t < A + NG + ND) {
-        kind = kDown;
-        entry = P.n_sh + (t - A - NG) / P.n_dt;
-        rbt = (t - A - NG) % P.n_dt;
+        const int entry = P.n_sh + (t - A - NG) / NDT;
+        g = geo_expert<L>(P, kDown, entry, (t - A - NG) % NDT, ecache + entry);
       } else {
         stamp_last(P.stamps, kTsLastIssue);
         break;  // queue exhausted
       }
     }
-    const uint8_t* wbase;
-    int64_t cbytes;
-    int e_id = -1;
-    if (kind == kXRec) {
-      cbytes = 0;
-      wbase = nullptr;
-    } else if (kind == kRouter) {
-      cbytes = (int64_t)nbc * chunk_bytes(MOE_F32, kRouterCc);
-      wbase = P.router + ((int64_t)(rgk >> 16) * P.n_ks * 64 + kRouterTileChunks * 32 * rbt) * kRows * 16;
-    } else {
-      shared_e = entry < P.n_sh;
-      if (shared_e) {
-        slot0 = P.T * P.k + kGroup * entry;
-        M = min(kGroup, P.T - kGroup * entry);
-      } else {
-        ep = ecache + entry;
-        e_id = ep->e;
-        slot0 = ep->slot0;
-        M = ep->M;
-      }
-      fmt = shared_e ? P.sfmt : P.fmt;
-      if (kind == kGateUp) {
-        ngroups = 2;
-        nch = shared_e ? P.sgu_nch : P.gu_nch;
-        const int kc = shared_e ? P.sgu_kc : P.gu_kc;
-        nbc = kc / 32;
-        cbytes = chunk_bytes(fmt, kc);
-        wbase = (shared_e ? P.sgu : P.gu + (int64_t)e_id * P.gu_stride) + (int64_t)(2 * rbt) * nch * cbytes;
-        n_tiles = shared_e ? P.n_gu_sh : P.n_gu;
-      } else {
-        ngroups = 4;
-        nch = shared_e ? P.sdn_nch : P.dn_nch;
-        const int kc = shared_e ? P.sdn_kc : P.dn_kc;
-        nbc = kc / 32;
-        cbytes = chunk_bytes(fmt, kc);
-        wbase = (shared_e ? P.sdn : P.dn + (int64_t)e_id * P.dn_stride) + (int64_t)(4 * rbt) * nch * cbytes;
-      }
-    }
-    const bool xslice = kind == kRouter || kind == kXRec;  // the stage holds a slice of x
-    const uint32_t per = xslice ? (uint32_t)(nbc * kRouterCc * XEL) : (uint32_t)(nbc * RB);
-    // A group that is one chunk may share its stage with the next groups of
-    // the tile (contiguous in memory, same records): fewer, larger stages,
-    // as long as two of them fit the ring.
-    int gps = 1;
-    if (!xslice && nch == 1)
-      while (2 * gps <= 4 && ngroups % (2 * gps) == 0 &&
-             (int64_t)2 * gps * cbytes + (int64_t)M * per <= (int64_t)(P.ring_bytes / 2))
-        gps *= 2;
-    const uint32_t wb = (uint32_t)(gps * cbytes);
-    const uint32_t resv = wb;
-    const int need = (int)((resv + (uint32_t)M * per + 127u) & ~127u);
+    const bool xslice = g.kind == kRouter;  // the stage holds a slice of x
+    const bool shared_e = g.kind != kRouter && g.entry < P.n_sh;
     // activation sources of this tile at chunk 0, and their step per chunk
     const uint8_t* asrc[kMaxSmallT];
     int64_t astep;
@@ -293,82 +360,95 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       astep = 0;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
-        asrc[m] = static_cast<const uint8_t*>(P.x) + ((int64_t)m * P.H + (int64_t)kRouterTileChunks * rbt * kRouterCc) * XEL;
+        asrc[m] = static_cast<const uint8_t*>(P.x) +
+                  ((int64_t)m * P.H + (int64_t)kRouterTileChunks * g.rbt * kRouterCc) * XEL;
     } else {
-      astep = (int64_t)nbc * RB;
+      astep = (int64_t)g.nbc * RB;
+      const Entry* ep = ecache + g.entry;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m) {
         const int mm = m < kGroup ? m : 0;
-        asrc[m] = kind == kGateUp
-                      ? P.xrec + (int64_t)(shared_e ? kGroup * entry + mm : ep->tok[mm]) * (P.H / 32) * RB
-                      : P.hrec + (int64_t)(slot0 + mm) * (P.Imax / 32) * RB;
+        asrc[m] = g.kind == kGateUp
+                      ? P.xrec + (int64_t)(shared_e ? kGroup * g.entry + mm : ep->tok[mm]) * (P.H / 32) * RB
+                      : P.hrec + (int64_t)(g.slot0 + mm) * (P.Imax / 32) * RB;
       }
     }
-    const int4 h3 = make_int4(slot0, P.n_sh + max(n_rent, 0), n_tiles, 0);
     bool dep_ok = xslice;
-    if (kind == kGateUp && shared_e) {
-      // the shared expert's loads start once the x records exist: in the
-      // launch's first microseconds the router tiles, which the routing waits
-      // for, get the memory bandwidth
+    if (g.kind == kGateUp && shared_e) {
+      // the shared expert's records are read once they exist (the x records
+      // are written by the first row group's router tiles)
       dep_ok = wait_flag_geq(&P.sync->x_done, P.T * P.n_rc, P.timeout_ns, P.status, kSiteX, t);
       if (dep_ok) fence_proxy_async_global();
       else ok = false;
     }
-    const int nstages = ngroups * nch / gps;
-    if (e_id >= 0) {
-      if (kind == kGateUp && !st_gu) {
+    if (g.e_id >= 0) {
+      if (g.kind == kGateUp && !st_gu) {
         stamp_first(P.stamps, kTsFirstRoutedIssue);
         st_gu = true;
-      } else if (kind == kDown && !st_dn) {
+      } else if (g.kind == kDown && !st_dn) {
         stamp_first(P.stamps, kTsFirstDownIssue);
         st_dn = true;
       }
     }
-    for (int q = 0; q < nstages && ok; ++q) {
-      const int g = q * gps / nch, c = q * gps - g * nch;
-      // ring space: a free slot, then free bytes
-      while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
-      int pos = 0;
-      while (ok) {
-        pos = head + need <= P.ring_bytes ? head : 0;
-        if (oldest == issued) break;
-        const int A = descs[oldest & (NS - 1)].off;
-        if (A < head ? (pos + need <= A || pos >= head) : (pos >= head && pos + need <= A)) break;
-        ok = wait_released(empty, NS, oldest++, P);
-      }
-      if (!ok) break;
-      head = pos + need;
+    for (int q = 0; q < g.nstages && ok; ++q) {
+      const int grp = q * g.gps / g.nch, c = q * g.gps - grp * g.nch;
       const int s = issued & (NS - 1);
-      const int kch = xslice ? kRouterTileChunks * rbt + c : 0;
-      int4* dd = reinterpret_cast<int4*>(descs + s);
-      dd[0] = make_int4(kind, c, nch, M);
-      dd[1] = make_int4(nbc, fmt, xslice ? rgk | kch : gps, pos);
-      dd[2] = make_int4(entry, rbt, g, ngroups);
-      dd[3] = h3;
-      uint8_t* stage = smem + plan.ring + pos;
-      mbar_arrive_expect_tx(&full[s], wb + (uint32_t)M * per);
-      if (wb) bulk_g2s_hint(stage, wbase + (int64_t)q * wb, wb, &full[s], wpol);
+      uint8_t* stage;
+      if (q < pre) {
+        // placed and its weights issued before the dependency wait
+        stage = smem + plan.ring + descs[s].off;
+      } else {
+        // ring space: a free slot, then free bytes
+        while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
+        int pos = 0;
+        while (ok) {
+          pos = head + g.need <= P.ring_bytes ? head : 0;
+          if (oldest == issued) break;
+          const int A = descs[oldest & (NS - 1)].off;
+          if (A < head ? (pos + g.need <= A || pos >= head) : (pos >= head && pos + g.need <= A)) break;
+          ok = wait_released(empty, NS, oldest++, P);
+        }
+        if (!ok) break;
+        head = pos + g.need;
+        write_desc(descs + s, g, q, pos);
+        stage = smem + plan.ring + pos;
+        mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
+        if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
+      }
       if (!dep_ok) {
-        if (kind == kGateUp) {
+        if (g.kind == kGateUp) {
           dep_ok = true;  // routed gate/up: gated by the routing flag (shared: waited above)
-        } else if (readybits[entry >> 5] & (1u << (entry & 31))) {
+        } else if (readybits[g.entry >> 5] & (1u << (g.entry & 31))) {
           dep_ok = true;
         } else {
-          dep_ok = wait_flag_geq(&P.entry_ready[entry], 1, P.timeout_ns, P.status, kSiteEntry,
-                                 entry * 65536 + (t & 0xFFFF));
-          if (dep_ok) readybits[entry >> 5] |= 1u << (entry & 31);
+          dep_ok = wait_flag_geq(&P.entry_ready[g.entry], 1, P.timeout_ns, P.status, kSiteEntry,
+                                 g.entry * 65536 + (t & 0xFFFF));
+          if (dep_ok) readybits[g.entry >> 5] |= 1u << (g.entry & 31);
         }
         if (dep_ok) fence_proxy_async_global();
         else ok = false;  // the consumers see the status word; the stage is still completed below
       }
-      uint8_t* adst = stage + resv;
+      uint8_t* adst = stage + g.wb;
       const int64_t aoff = (int64_t)c * astep;
 #pragma unroll
       for (int m = 0; m < kMaxSmallT; ++m)
-        if (m < M) bulk_g2s(adst + m * per, dep_ok ? asrc[m] + aoff : asrc[0], per, &full[s]);
+        if (m < g.M) bulk_g2s(adst + m * g.per, dep_ok ? asrc[m] + aoff : asrc[0], g.per, &full[s]);
+      (void)grp;
       ++issued;
     }
-    t = t_next;
+    // prefetched stages whose activations were not issued (an error stopped
+    // the loop) still complete: give them their activation bytes
+    for (int q = issued; q < pre; ++q) {
+      const int s = q & (NS - 1);
+      uint8_t* adst = smem + plan.ring + descs[s].off + g.wb;
+      for (int m = 0; m < g.M; ++m) bulk_g2s(adst + m * g.per, asrc[0], g.per, &full[s]);
+      ++issued;
+    }
+    pre = 0;
+    // the next item is claimed once this one's stages are all issued: the
+    // claim's latency overlaps the stages in flight, and when the queue runs
+    // out no block holds a claimed item it has not started
+    t = atomicAdd(&P.sync->queue, 1) + n_static;
   }
   // end marker (or error): hand the consumers an END descriptor in the next slot
   const int n_data = issued;
@@ -531,57 +611,105 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Largest of N values by a pairwise tree (depth log2 N).
+// Descending bitonic sort of N (a power of two) 64-bit keys in registers.
 template <int N>
-__device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
-  uint64_t t[N];
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&a)[N]) {
 #pragma unroll
-  for (int i = 0; i < N; ++i) t[i] = c[i];
+  for (int size = 2; size <= N; size <<= 1)
 #pragma unroll
-  for (int w = 1; w < N; w <<= 1)
+    for (int stride = size / 2; stride > 0; stride >>= 1)
 #pragma unroll
-    for (int i = 0; i + w < N; i += 2 * w) t[i] = t[i] > t[i + w] ? t[i] : t[i + w];
-  return t[0];
+      for (int i = 0; i < N; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const uint64_t x = a[i], y = a[j];
+          const bool sw = desc ? x < y : x > y;
+          a[i] = sw ? y : x;
+          a[j] = sw ? x : y;
+        }
+      }
 }
 
-// The k largest of row[0..E) by (value desc, index asc), one warp.  Lane l
-// holds experts l, l + 32, ... (NPER of them) in registers as 64-bit
-// composites (order-preserving key of the value, then the complemented index,
-// so a larger composite is a larger value or, on equal values, a lower
-// index; 0 = none) and keeps its largest.  Each round takes the exact maximum
-// key over the lanes (a warp max); if several lanes hold it, the lowest
-// expert index among them wins (a second warp min, only then).  The winning
-// lane writes the slot, clears that expert and takes the tree maximum of what
-// it has left.  NaN counts as -inf.  Writes ids and values in slot order.
-template <int NPER>
-__device__ __forceinline__ void topk_token(const float* row, int E, int k, int* ids, float* vals_out) {
-  const int lane = threadIdx.x & 31;
-  uint64_t c[NPER];
+// Keeps the K largest of two descending lists in a: max(a[i], b[K-1-i]) is
+// a bitonic sequence holding the union's K largest, which a bitonic merge
+// sorts.
+template <int K, int N>
+__device__ __forceinline__ void merge_topk(uint64_t (&a)[K], const uint64_t (&b)[N]) {
 #pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    const float x = e < E ? row[e] : 0.f;
-    c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
-  }
-  uint64_t best = tree_max(c);
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const uint32_t key = (uint32_t)(best >> 32);
-    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
-    int wl = __ffs(holders) - 1;
-    if (holders & (holders - 1u))
-      wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
-    if (lane == wl) {
-      const uint32_t wi = ~(uint32_t)best;
-      ids[j] = (int)wi;
-      vals_out[j] = key_value(m);
-      const int slot = (int)(wi >> 5);
+  for (int i = 0; i < K; ++i) a[i] = a[i] > b[K - 1 - i] ? a[i] : b[K - 1 - i];
 #pragma unroll
-      for (int i = 0; i < NPER; ++i)
-        if (i == slot) c[i] = 0ull;
-      best = tree_max(c);
+  for (int stride = K / 2; stride > 0; stride >>= 1)
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const int j = i ^ stride;
+      if (j > i) {
+        const uint64_t x = a[i], y = a[j];
+        a[i] = x > y ? x : y;
+        a[j] = x > y ? y : x;
+      }
     }
+}
+
+// The k (<= K) largest of one token's E logits by (value desc, index asc),
+// one warp.  Logit e is read from its fixed-point sum (one rounding to fp32,
+// an exact power-of-two scale, then + bias, NaN counting as -inf); lane l
+// holds experts l, l + 32, ... (NP of them) as 64-bit composites
+// (order-preserving key of the value, then the complemented index: a larger
+// composite is a larger value or, on equal values, a lower index; 0 = none).
+// Each lane sorts its composites in chunks of up to 16 and keeps its K
+// largest; five merge levels over xor partners then leave every lane with
+// the warp's K largest in order.  The composites are distinct, so the result
+// is exact.  Writes ids, values and gates (softmax over the k selected
+// logits, the sum by a fixed shuffle tree) in slot order.
+template <int NP, int K>
+__device__ __forceinline__ void topk_token_merge(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
+  constexpr int C = NP < 16 ? NP : 16;  // chunk size (>= K)
+  static_assert(C >= K && NP % C == 0, "top-k chunking");
+  const int lane = threadIdx.x & 31;
+  const int E = P.E, k = P.k;
+  uint64_t a[K];
+#pragma unroll
+  for (int ch = 0; ch < NP / C; ++ch) {
+    uint64_t c[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int e = lane + 32 * (ch * C + i);
+      const long long v = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
+      const float b = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
+      const float x = __ll2float_rn(v) * 0x1p-32f + b;
+      c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
+    }
+    bitonic_sort_desc<C>(c);
+    if (ch == 0) {
+#pragma unroll
+      for (int i = 0; i < K; ++i) a[i] = c[i];
+    } else {
+      merge_topk<K, C>(a, c);
+    }
+  }
+#pragma unroll
+  for (int lvl = 1; lvl < 32; lvl <<= 1) {
+    uint64_t o[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) o[i] = __shfl_xor_sync(0xffffffffu, a[i], lvl);
+    merge_topk<K, K>(a, o);
+  }
+  // lane j < k takes slot j (a register select, no dynamic indexing)
+  uint64_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+    if (i == lane) mine = a[i];
+  const float l0 = key_value((uint32_t)(a[0] >> 32));
+  const float lv = key_value((uint32_t)(mine >> 32));
+  const float ex = lane < k ? expf(lv - l0) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    ids[lane] = (int)~(uint32_t)mine;
+    vals[lane] = lv;
+    gates[lane] = ex / sum;
   }
 }
 
@@ -636,59 +764,19 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   int* sent = reinterpret_cast<int*>(misc + f.sent);    // [Tk] entries owned (first pair of an expert)
 
   // (the router counter was taken with acquire semantics)
-  // logits: thread i converts the fixed-point sums of experts e = i, i + 256
-  // (all loads in flight before the conversions), then any further experts
-  {
-    const int nq = P.Tp / 2;  // 16-byte pairs per expert (Tp <= 8)
-    const longlong2* lp = reinterpret_cast<const longlong2*>(P.lfx);
-    auto put = [&](int e, const longlong2* a) {
-      const float bias = P.router_b ? P.router_b[e] : 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < nq) {
-          // one rounding to fp32, then an exact power-of-two scale
-          if (2 * q < T) lg[(2 * q) * E + e] = __ll2float_rn(a[q].x) * 0x1p-32f + bias;
-          if (2 * q + 1 < T) lg[(2 * q + 1) * E + e] = __ll2float_rn(a[q].y) * 0x1p-32f + bias;
-        }
-    };
-    longlong2 a[2][4];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (tid + u * NT < E && q < nq) a[u][q] = __ldcg(lp + (int64_t)(tid + u * NT) * nq + q);
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-      if (tid + u * NT < E) put(tid + u * NT, a[u]);
-#pragma unroll 1
-    for (int e = tid + 2 * NT; e < E; e += NT) {  // E > 512
-      longlong2 c[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < nq) c[q] = __ldcg(lp + (int64_t)e * nq + q);
-      put(e, c);
-    }
-  }
-  consumer_sync();
-
-  // top-k and gates per token (one warp per token)
-  const int nper = (E + 31) / 32;
+  // top-k and gates per token, one warp per token, straight from the
+  // fixed-point logit sums
+  (void)lg;
 #pragma unroll 1
   for (int t = warp; t < T; t += kConsumerWarps) {
-    if (nper <= 4) topk_token<4>(lg + t * E, E, k, sid + t * k, sl + t * k);
-    else if (nper <= 8) topk_token<8>(lg + t * E, E, k, sid + t * k, sl + t * k);
-    else if (nper <= 12) topk_token<12>(lg + t * E, E, k, sid + t * k, sl + t * k);
-    else if (nper <= 16) topk_token<16>(lg + t * E, E, k, sid + t * k, sl + t * k);
-    else topk_token<kMaxE / 32>(lg + t * E, E, k, sid + t * k, sl + t * k);
-    __syncwarp();
-    // gates: softmax over the k selected logits (lane j: slot j), the sum by
-    // a fixed shuffle tree
-    const float l0 = sl[t * k];
-    const float ex = lane < k ? expf(sl[t * k + lane] - l0) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane < k) sg[t * k + lane] = ex / sum;
+    if (k <= 8) {
+      if (E <= 256) topk_token_merge<8, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
+      else if (E <= 512) topk_token_merge<16, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
+      else topk_token_merge<32, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    } else {
+      if (E <= 512) topk_token_merge<16, 16>(P, t, sid + t * k, sl + t * k, sg + t * k);
+      else topk_token_merge<32, 16>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    }
   }
   consumer_sync();
 
@@ -820,13 +908,13 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   }
   consumer_sync();
   // One arrival of the routing on every 128-row block of z: a block is
-  // complete after n_sh + n_rent down tiles and this arrival, and whoever
-  // arrives last combines it.  A shared down tile that finishes before the
+  // complete after its two down tiles of each of the n_sh + n_rent entries
+  // and this arrival, and whoever arrives last combines it.  A shared down tile that finishes before the
   // routing is known can therefore never be taken for the last one, and a
   // layer with no down work for this batch (a shard none of whose experts
   // was chosen, with no shared expert) still gets y from the combine.
   {
-    const int last = P.n_sh + *nrent_s;
+    const int last = 2 * (P.n_sh + *nrent_s);
     for (int b = tid; b < P.n_dt; b += NT)
       if (atom_add_acq_rel(&P.d_cnt[b], 1) == last) pend[1 + atomicAdd(&pend[0], 1)] = b;
   }
@@ -936,24 +1024,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     const uint8_t* stage = smem + plan.ring + d.off;
     const int d_rg = d.rgks >> 16, d_ks = d.rgks & 0xFFFF;  // router tiles
 
-    if (d.kind == kXRec) {
-      // x slice ([T][cols] in the stage) -> activation records, one 32-column
-      // block per thread; the proxy fence makes them visible to the bulk
-      // copies that read them after x_done
-      const int kt = d_ks / kRouterTileChunks, cols = d.nbc * kRouterCc, nb = cols / 32;
-      constexpr int XEL = L == 2 ? 2 : 4;
-      if (tid < T * nb) {
-        const int t = tid / nb, b = tid - (tid / nb) * nb;
-        write_record_lane<L>(stage + (t * cols + b * 32) * XEL,
-                             P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
-        fence_proxy_async_global();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      consumer_sync();  // orders every thread's record writes before thread 0's release
-      if (tid == 0 && atom_add_acq_rel(&P.sync->x_done, T * d.nbc) + T * d.nbc == T * P.n_rc)
-        stamp_last(P.stamps, kTsXDone);
-    } else if (d.kind == kRouter) {
+    if (d.kind == kRouter) {
       // One router tile: 32 experts (lane = expert row) x a slice of ncc
       // 128-column chunks.  The stage holds the tile's router weights
       // ([cols/4][32 rows][4]) and then the slice of x ([T][cols]).
@@ -970,12 +1041,29 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         case 7: router_dot<L, 7>(wst, xs, cols, racc); break;
         default: router_dot<L, 8>(wst, xs, cols, racc); break;
       }
+      if (d_rg == 0) {
+        // the first row group's tiles also turn their slice of x into the
+        // activation records (one 32-column block per thread); the proxy
+        // fence makes them visible to the bulk copies that read them after
+        // x_done
+        const int kt = d_ks / kRouterTileChunks, nb = cols / 32;
+        constexpr int XEL = L == 2 ? 2 : 4;
+        if (tid < T * nb) {
+          const int t = tid / nb, b = tid - (tid / nb) * nb;
+          write_record_lane<L>(xs + (t * cols + b * 32) * XEL,
+                               P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
+          fence_proxy_async_global();
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
       for (int t = 0; t < kMaxSmallT; ++t)
         if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
       consumer_sync();
+      // (the barrier also orders every thread's record writes before thread 0's release)
+      if (d_rg == 0 && tid == 0 && atom_add_acq_rel(&P.sync->x_done, T * d.nbc) + T * d.nbc == T * P.n_rc)
+        stamp_last(P.stamps, kTsXDone);
       if (tid < T * 32) {
         // this slice's share of logit (t, expert 32 rg + r), added as an
         // exact integer multiple of 2^-32: the total does not depend on the
@@ -1046,6 +1134,26 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   }
 }
 
+// The combine's routing arrays in shared memory, by one warp: gates and z
+// positions of the T*k pairs (position -1 for a pair whose expert another
+// shard holds).  Waits (bounded) for the routing arrays to be published;
+// returns false on timeout.
+__device__ bool preload_routing(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
+  float* sg = reinterpret_cast<float*>(smem + plan.escr);                          // [T*k] gates
+  int* sp = reinterpret_cast<int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);  // [T*k] slots
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_flag_geq(&P.sync->routing_aux, 1, P.timeout_ns, P.status, kSiteRouting, -1);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  for (int q = threadIdx.x & 31; q < P.T * P.k; q += 32) {
+    const int e = __ldcg(&P.ids[q]);
+    sg[q] = __ldcg(&P.gates[q]);
+    sp[q] = e >= P.e0 && e < P.e0 + P.n_e ? __ldcg(&P.pos[q]) : -1;
+  }
+  __syncwarp();
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // epilogue warp
 // ---------------------------------------------------------------------------
@@ -1060,6 +1168,7 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   int rs = 0;
   uint32_t rph = 0;
   float keep[kGroup] = {0.f, 0.f, 0.f, 0.f};
+  bool preloaded = false;
   while (true) {
     if (!mbar_wait_bounded(&rfull[rs], rph, P.timeout_ns, P.status, kSiteRedFull, rs)) break;
     const Desc d = metas[rs];
@@ -1103,20 +1212,29 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         }
       }
     } else {  // kDown
-      const int row = d.rbt * 128 + d.group * 32 + lane;
+      if (!preloaded && d.entry >= P.n_sh) {
+        // the first routed down tile: the routing is published (and its
+        // arrays follow right after), so fetch what a combine of this block
+        // needs now rather than when the block completes
+        preloaded = true;
+        if (preload_routing(P, smem, plan) && lane == 0) reinterpret_cast<int*>(smem + plan.flags)[3] = 1;
+      }
+      const int row = d.rbt * 64 + d.group * 32 + lane;
       for (int m = 0; m < d.M; ++m) P.z[(int64_t)(d.slot0 + m) * P.H + row] = v[m];
       if (d.group == d.ngroups - 1) {
         __syncwarp();  // orders the lanes' z writes before lane 0's release
         if (lane == 0) {
-          // the block is complete after every down tile (n_sh + n_rent) and
-          // the routing's own arrival; n_rent is visible whenever the routing
-          // has arrived, and before that no tile can be the last one
-          const int old = atom_add_acq_rel(&P.d_cnt[d.rbt], 1);
-          if (old == P.n_sh + ld_acquire(&P.sync->n_rent)) {
+          // the 128-row block is complete after both halves of every entry's
+          // down tiles (2 (n_sh + n_rent)) and the routing's own arrival;
+          // n_rent is visible whenever the routing has arrived, and before
+          // that no tile can be the last one
+          const int blk = d.rbt >> 1;
+          const int old = atom_add_acq_rel(&P.d_cnt[blk], 1);
+          if (old == 2 * (P.n_sh + ld_acquire(&P.sync->n_rent))) {
             stamp_last(P.stamps, kTsLastDownDone);
             // this CTA combines the block when it leaves (with all its threads)
             int* pend = reinterpret_cast<int*>(smem + plan.pend);
-            pend[1 + atomicAdd(&pend[0], 1)] = d.rbt;
+            pend[1 + atomicAdd(&pend[0], 1)] = blk;
           }
         }
       }
@@ -1126,23 +1244,24 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
 
 // y rows of the 128-row blocks this CTA completed last, in slot order:
 // y[t] = sum_{j<k} g[t,j] z[pos[t,j]] + z_shared[t], all threads of the CTA.
+// The z rows of other blocks' tiles were released by their down-count
+// increments and acquired by this CTA's own; the CTA barrier before this
+// call passes that on to every thread.
 template <int L>
 __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, const int* pend) {
-  float* sg = reinterpret_cast<float*>(smem + plan.escr);                       // [T*k] gates
-  int* sp = reinterpret_cast<int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);  // [T*k] slots
+  const float* sg = reinterpret_cast<const float*>(smem + plan.escr);
+  const int* sp = reinterpret_cast<const int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);
   const int T = P.T, k = P.k;
   int* flags = reinterpret_cast<int*>(smem + plan.flags);
-  __threadfence();
-  if (threadIdx.x == 0)  // set right after the routing; long done by now
-    flags[2] = wait_flag_geq(&P.sync->routing_aux, 1, P.timeout_ns, P.status, kSiteRouting, -1);
-  __syncthreads();
-  if (!flags[2]) return;
-  for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
-    const int e = __ldcg(&P.ids[q]);
-    sg[q] = __ldcg(&P.gates[q]);
-    sp[q] = e >= P.e0 && e < P.e0 + P.n_e ? __ldcg(&P.pos[q]) : -1;  // -1: another shard's expert
+  if (!flags[3]) {
+    // not fetched by the epilogue warp (this CTA saw no routed down tile)
+    if (threadIdx.x < 32) {
+      const bool ok = preload_routing(P, smem, plan);
+      if (threadIdx.x == 0) flags[2] = ok;
+    }
+    __syncthreads();
+    if (!flags[2]) return;
   }
-  __syncthreads();
   const int n = pend[0];
   for (int o = threadIdx.x; o < n * 128 * T; o += blockDim.x) {
     const int b = o / (128 * T), rem = o % (128 * T), t = rem / 128;
@@ -1181,14 +1300,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   griddep_launch_dependents();
   const uint64_t t_entry = globaltimer_ns();
   if (threadIdx.x == 0) {
-    // constant data only: warm L2 with one router tile's weights (tile = CTA)
-    if ((int)blockIdx.x < P.n_rg * P.n_kt) {
-      const int rg = blockIdx.x / P.n_kt, kt = blockIdx.x % P.n_kt;
-      const int nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * kt);
-      prefetch_l2(P.router + ((int64_t)rg * P.n_ks * 64 + kRouterTileChunks * 32 * kt) * kRows * 16,
-                  (uint32_t)(nbc * chunk_bytes(MOE_F32, kRouterCc)));
-    }
     pend[0] = 0;
+    flags[3] = 0;  // the combine's routing arrays are not in shared memory yet
     for (int i = 0; i < P.n_stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -1200,6 +1313,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     mbar_init(reinterpret_cast<uint64_t*>(smem + plan.ebar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();  // barriers initialised before the producer's first copies
+  const int warp = threadIdx.x >> 5;
+  const bool producer = warp == kProducerWarp && (threadIdx.x & 31) == 0;
+  // the block's static first item: its first weight stages start loading
+  // now, while the previous kernel in the stream finishes (constant data only)
+  const int n_static = min((int)gridDim.x, P.n_rg * P.n_kt + P.n_sh * P.n_gu_sh);
+  const int t_static = (int)blockIdx.x < n_static ? (int)blockIdx.x : -1;
+  int n_pre = 0, head0 = 0;
+  if (producer && t_static >= 0) n_pre = producer_prefetch<L>(P, smem, plan, t_static, &head0);
   griddep_wait();  // x, the workspace and its counters are the previous launches' to finish with
   if (threadIdx.x == 0) {
     stamp_first_at(P.stamps, kTsEntry, t_entry);
@@ -1207,9 +1329,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5;
   if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_loop<L>(P, smem, plan);
+    if (producer) producer_loop<L>(P, smem, plan, t_static, n_pre, head0);
   } else if (warp == kEpilogueWarp) {
     epilogue_loop<L>(P, smem, plan);
   } else {

@@ -11,7 +11,9 @@ h_tgt is the target hidden state before the output norm.  "Step-5 Preview
 GGUF", "Precision distribution" table: the main output matrix is Q8_0.
 
 The pages give the data flow but no synthetic model, so the round here is a
-reading of it, with every step a plain definition:
+reading of it, with every step a plain definition (in "bf16" activation mode
+the MoE layers' inputs and outputs are additionally rounded to bf16, as a
+bf16 layer takes and returns them):
   target      h_0 = x (the [k+1, H] verify batch); h_{l+1} = h_l +
               MoE_l(rmsnorm(h_l)) for the L target layers (pre-norm residual
               blocks: without the norm the SwiGLU, quadratic in its input,
@@ -47,6 +49,14 @@ from . import accept, moe
 F64 = np.float64
 
 
+def round_bf16(x):
+    """Round to the nearest bf16 value (8 significant bits, ties to even),
+    directly from fp64; values stay fp64 arrays."""
+    x = np.asarray(x, F64)
+    m, e = np.frexp(x)                  # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)  # np.round: halves to even
+
+
 def rmsnorm(x, eps=1e-6):
     """Row-wise v / sqrt(mean(v^2) + eps), weight 1, fp64."""
     x = np.asarray(x, F64)
@@ -58,17 +68,20 @@ def lm_logits(h, lm: moe.QTensor, eps=1e-6):
     return rmsnorm(h, eps) @ lm.dense().T
 
 
-def target_stack(x, layers, eps=1e-6, routes=None, layer_forward=None):
+def target_stack(x, layers, eps=1e-6, routes=None, layer_forward=None, act="f64"):
     """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers.
     If `routes` is a list, each layer's routing dict is appended to it.
-    ``layer_forward(x, L)``, if given, stands in for ``moe.forward(x, L)``."""
+    ``layer_forward(x, L)``, if given, stands in for ``moe.forward(x, L)``.
+    act = "bf16": the layers' inputs and outputs are bf16 values (rounded
+    to nearest even at the layer boundary; the residual stream stays fp64)."""
     fwd = moe.forward if layer_forward is None else layer_forward
+    io = round_bf16 if act == "bf16" else (lambda v: v)
     h = np.asarray(x, F64)
     for L in layers:
-        y, r = fwd(rmsnorm(h, eps), L)
+        y, r = fwd(io(rmsnorm(h, eps)), L)
         if routes is not None:
             routes.append(r)
-        h = h + y
+        h = h + io(y)
     return h
 
 
@@ -88,7 +101,7 @@ def cut_drafts(drafts, probs, p_min):
     return list(drafts[:n]), n
 
 
-def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, layer_forward=None):
+def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, layer_forward=None, act="f64"):
     """One round.  x [k+1, H]; heads: k layers; noise [k][k][H] (head j uses
     rows 0..j of noise[j]); p_min the draft confidence cut.  Returns a dict
     with h_tgt, logits, head_out (list of [j+1, H]), draft_rows [k, H],
@@ -96,20 +109,23 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, lay
     n_drafted, n_accepted, next_token, argmax (the target's per-row argmax)
     and the routing dicts of every target layer (target_routes) and head
     (head_routes).  ``layer_forward(x, L)``, if given, stands in for
-    ``moe.forward(x, L)``."""
+    ``moe.forward(x, L)``.  act = "bf16": every MoE layer's (and head's)
+    input and output are bf16 values (see target_stack); the residual
+    stream, the draft rows and the logits stay fp64."""
     fwd = moe.forward if layer_forward is None else layer_forward
+    io = round_bf16 if act == "bf16" else (lambda v: v)
     k = len(heads)
     x = np.asarray(x, F64)
     assert x.shape[0] == k + 1
     target_routes, head_routes = [], []
-    h_tgt = target_stack(x, layers, eps, target_routes, layer_forward=fwd)
+    h_tgt = target_stack(x, layers, eps, target_routes, layer_forward=fwd, act=act)
     logits = lm_logits(h_tgt, lm, eps)
     head_out, rows = [], []
     for j, head in enumerate(heads):
         ht = h_tgt[: j + 1] + np.asarray(noise[j][: j + 1], F64)
-        y, hr = fwd(rmsnorm(ht, eps), head)
+        y, hr = fwd(io(rmsnorm(ht, eps)), head)
         head_routes.append(hr)
-        head_out.append(y)
+        head_out.append(io(y))
         rows.append(ht[j])
     rows = np.stack(rows) if rows else np.zeros((0, x.shape[1]))
     draft_logits = lm_logits(rows, lm, eps)

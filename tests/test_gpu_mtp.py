@@ -22,7 +22,11 @@ TOL = {pkg.ACT_BF16: 2e-2, pkg.ACT_F32: 1e-3}
 # within one layer.  A token whose top-k boundary margin is below this in any
 # layer is reported and left out of the value comparisons (the per-layer
 # near-tie rule, widened to the chain's input perturbation).
-CHAIN_TIE = {pkg.ACT_BF16: 5e-2, pkg.ACT_F32: 1e-3}
+CHAIN_TIE = {pkg.ACT_BF16: 5e-2, pkg.ACT_F32: 1e-4}
+# the oracle round in the same precision at the layer boundaries: bf16 layers
+# take and return bf16 values, so in bf16 mode the oracle rounds there too
+# (its routing decisions then see the inputs the kernels see)
+OACT = {pkg.ACT_BF16: "bf16", pkg.ACT_F32: "f64"}
 
 
 def _oracle_lm(r):
@@ -105,7 +109,8 @@ def _check_round(r, act, report, variant=0, pool=None, ol_layers=None, ol_heads=
         fwd = None
         if pool is not None:
             fwd = pool.layer_forward({id(o): w for o, w in zip(ol_layers + ol_heads, r.layers + r.heads)})
-        ref = omtp.mtp_round(to_np(x), ol_layers, ol_heads, ol_lm or _oracle_lm(r), to_np(noise), layer_forward=fwd)
+        ref = omtp.mtp_round(to_np(x), ol_layers, ol_heads, ol_lm or _oracle_lm(r), to_np(noise), layer_forward=fwd,
+                             act=OACT[act])
         # rows whose routing in some target layer sits within the chain's perturbation
         T = r.k + 1
         chain = np.zeros(T, bool)
@@ -191,7 +196,7 @@ def test_mtp_round_full_size_acceptance(full_round_gpu, full_round_oracle):
     r, ol_layers, ol_heads, ol_lm = full_round_oracle
     decided = []
     with OraclePool() as pool:
-        for variant in range(8):
+        for variant in range(6):
             decided.append(_check_round(r, act, print, variant, pool, ol_layers, ol_heads, ol_lm, gpu=gpu))
             if sum(decided) >= 3 and len(decided) >= 4:
                 break
@@ -235,11 +240,14 @@ def test_mtp_round_teacher_forced_layers(full_round_gpu, full_round_oracle):
             check_routing(ids.astype(np.int64), gates, rr, keep, label=f"layer {l}")
             err = omoe.max_rel_err(to_np(y)[keep], y_ref[keep])
             assert err <= TOL[act], f"layer {l}: max rel err {err:.2e}"
-            # the oracle chain, for the drift of the router inputs
-            u_o = omtp.rmsnorm(h_o, eps)
+            # the oracle chain (layer boundaries in the mode's precision),
+            # for the drift of the router inputs
+            io = omtp.round_bf16 if act == pkg.ACT_BF16 else (lambda v: v)
+            u_o = io(omtp.rmsnorm(h_o, eps))
             ro = omoe.route(u_o, ol)
             drift.append(float(np.abs(rr["logits"] - ro["logits"]).max()))
             y_o, _ = pool.forward(u_o, ol, w, routing=ro)
+            y_o = io(y_o)
             print(f"act={act} layer {l}: max rel err {err:.2e}, excluded {(~keep).sum()}, "
                   f"router-logit drift of the chain {drift[-1]:.2e}")
             h = h + y.float()

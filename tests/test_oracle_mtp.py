@@ -152,3 +152,33 @@ def test_round_p_min_just_above_and_below_a_draft():
     assert above["drafts"][:want] == r["drafts"][:want] and above["drafts"][want:] == [-1] * (3 - want)
     # the next token is the target's argmax at the first row past the kept drafts
     assert above["next_token"] == r["argmax"][want]
+
+
+def test_round_bf16_is_nearest_even():
+    import torch
+    # 8 significant bits: halfway cases go to the even neighbour
+    assert mtp.round_bf16(1.0 + 2.0 ** -8) == 1.0
+    assert mtp.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert mtp.round_bf16(-(1.0 + 2.0 ** -8 + 2.0 ** -30)) == -(1.0 + 2.0 ** -7)
+    assert mtp.round_bf16(0.0) == 0.0 and mtp.round_bf16(3.0) == 3.0
+    # on fp32 values it agrees with torch's fp32 -> bf16 conversion (RNE)
+    rng = np.random.default_rng(3)
+    v = (rng.normal(size=20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(mtp.round_bf16(v.astype(np.float64)), want)
+
+
+def test_round_bf16_mode_rounds_the_layer_boundaries():
+    r, x, layers, heads, lm, noise = _round(3.0)
+    rb = mtp.mtp_round(x, layers, heads, lm, noise, act="bf16")
+    # by hand: each layer sees a bf16 input and returns a bf16 output
+    h = np.asarray(x, np.float64)
+    for L in layers:
+        y, _ = moe.forward(mtp.round_bf16(mtp.rmsnorm(h)), L)
+        h = h + mtp.round_bf16(y)
+    assert np.array_equal(rb["h_tgt"], h)
+    for j in range(3):
+        y, _ = moe.forward(mtp.round_bf16(mtp.rmsnorm(h[: j + 1] + noise[j][: j + 1])), heads[j])
+        assert np.array_equal(rb["head_out"][j], mtp.round_bf16(y))
+    # and the f64 mode is the unrounded round
+    assert np.array_equal(mtp.mtp_round(x, layers, heads, lm, noise, act="f64")["h_tgt"], r["h_tgt"])
