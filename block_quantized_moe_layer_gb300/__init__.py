@@ -23,7 +23,7 @@ EXPORTS = (
     "moe_quantized_bytes", "moe_quantize", "mtp_verify_accept_workspace_bytes",
     "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
     "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
-    "moe_layer_timeline", "moe_layer_inject_timeout",
+    "moe_layer_timeline", "moe_layer_inject_timeout", "moe_lm_head_status", "moe_forward_f32",
 )
 
 # event names of moe_layer_timeline, in order
@@ -77,9 +77,11 @@ def lib():
             "mtp_verify_accept": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp, sz, vp]),
             "mtp_verify_accept_noalloc": (_c.c_int, [vp, i32, vp, i32, vp, vp, vp]),
             "moe_forward_residual": (_c.c_int, [vp, vp, i32, vp, vp]),
+            "moe_forward_f32": (_c.c_int, [vp, vp, i32, vp, vp]),
             "moe_lm_head_create": (_c.c_int, [_c.POINTER(MoeTensor), i32, i32, vp, _c.POINTER(vp)]),
             "moe_lm_head_forward": (_c.c_int, [vp, vp, i32, _c.c_float, vp, vp]),
             "moe_lm_head_destroy": (None, [vp]),
+            "moe_lm_head_status": (_c.c_int, [vp, vp]),
             "mtp_round_workspace_bytes": (sz, [i32, i32, i32, i32]),
             "mtp_round": (_c.c_int, [_c.POINTER(vp), i32, _c.POINTER(vp), i32, vp, vp, vp, _c.c_float, _c.c_float,
                                      vp, sz, vp, vp, vp, vp, vp, vp, vp]),
@@ -186,13 +188,15 @@ class Layer:
     def workspace_bytes(self):
         return lib().moe_layer_workspace_bytes(self.handle)
 
-    def forward(self, x, y=None, stream=None, residual=False):
-        """y = MoE(x), or x + MoE(x) with ``residual``."""
+    def forward(self, x, y=None, stream=None, residual=False, out_f32=False):
+        """y = MoE(x), or x + MoE(x) with ``residual``; ``out_f32``: y in fp32
+        whatever the act dtype (T <= 8)."""
         import torch
         T = x.shape[0]
         if y is None:
-            y = torch.empty_like(x)
-        f = lib().moe_forward_residual if residual else lib().moe_forward
+            y = torch.empty(x.shape, dtype=torch.float32, device=x.device) if out_f32 else torch.empty_like(x)
+        _require(not (residual and out_f32), "forward: residual and out_f32 do not combine")
+        f = lib().moe_forward_f32 if out_f32 else (lib().moe_forward_residual if residual else lib().moe_forward)
         _check(f(self.handle, x.data_ptr() if T else None, T, y.data_ptr() if T else None, _stream(stream)))
         return y
 
@@ -303,6 +307,10 @@ class LmHead:
         _check(lib().moe_lm_head_forward(self.handle, x.data_ptr() if T else None, T, eps,
                                          out.data_ptr() if T else None, _stream(stream)))
         return out
+
+    def status(self, stream=None):
+        """Raises MoEError(MOE_ETIMEOUT) if a device-side wait gave up."""
+        _check(lib().moe_lm_head_status(self.handle, _stream(stream)))
 
     def close(self):
         if getattr(self, "handle", None):

@@ -423,17 +423,18 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
 }  // extern "C"
 
 namespace {
-int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, bool residual) {
+int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, bool residual, bool out_f32) {
   if (!L) return fail(MOE_EINVAL, "moe_forward: NULL layer");
   if (T < 0 || T > L->T_max) return fail(MOE_EINVAL, "moe_forward: T=%d outside 0..%d", T, L->T_max);
   if (T == 0) return MOE_OK;
   if (!x || !y) return fail(MOE_EINVAL, "moe_forward: NULL x or y");
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
     return fail(MOE_EINVAL, "moe_forward: x and y must be 16-byte aligned");
+  if (out_f32 && T > kMaxSmallT) return fail(MOE_EINVAL, "moe_forward_f32: T=%d above %d", T, kMaxSmallT);
   const size_t esz = L->act == MOE_ACT_BF16 ? 2 : 4;
   const uintptr_t xb = reinterpret_cast<uintptr_t>(x), yb = reinterpret_cast<uintptr_t>(y);
-  const size_t nb = (size_t)T * L->H * esz;
-  if (xb < yb + nb && yb < xb + nb) return fail(MOE_EINVAL, "moe_forward: x and y overlap");
+  const size_t nbx = (size_t)T * L->H * esz, nby = (size_t)T * L->H * (out_f32 ? 4 : esz);
+  if (xb < yb + nby && yb < xb + nbx) return fail(MOE_EINVAL, "moe_forward: x and y overlap");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   L->last_T = T;
   if (T > kMaxSmallT) {
@@ -447,6 +448,7 @@ int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, 
   P.x = x;
   P.y = y;
   P.residual = residual ? 1 : 0;
+  P.out_f32 = out_f32 ? 1 : 0;
   P.ready_target = 1;
   if (L->inject == 1) {
     P.ready_target = 2;  // published as 1: the routed tiles' wait runs out
@@ -460,11 +462,15 @@ int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, 
 extern "C" {
 
 int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
-  return forward_impl(L, x, T, y, stream, false);
+  return forward_impl(L, x, T, y, stream, false, false);
 }
 
 int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* stream) {
-  return forward_impl(L, x, T, y, stream, true);
+  return forward_impl(L, x, T, y, stream, true, false);
+}
+
+int moe_forward_f32(moe_layer* L, const void* x, int32_t T, float* y, void* stream) {
+  return forward_impl(L, x, T, y, stream, false, true);
 }
 
 int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, void* stream) {

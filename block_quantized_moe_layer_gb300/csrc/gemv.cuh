@@ -1,0 +1,150 @@
+// gemv.cuh -- the integer block dot products of the T <= 8 GEMV (the MoE
+// layer's expert tiles and the LM head).
+//
+// A weight chunk holds 32 rows (lane = row) x Kc columns in the streaming
+// chunk layout (common.cuh, chunk_bytes); the activations of the M vectors
+// are block fixed-point records (common.cuh, write_record), laid out
+// [M][nbc] right after the chunk's data in shared memory or anywhere else.
+// Weights enter as their integer codes, activations as L-limb block fixed
+// point; dp4a gives exact integer block sums, scaled once per block:
+//   Q8_0 : sum_i d q_i v_i       = d * ascale * sum_i q_i X_i
+//   Q4KS : sum_i (a q_i - b) v_i = a * ascale * sum_i q_i X_i - b * sumx
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint32_t field6(uint32_t w0, uint32_t w1, uint32_t w2, int f) {
+  const int p = 6 * f;
+  const int wi = p >> 5, sh = p & 31;
+  const uint32_t lo = wi == 0 ? w0 : (wi == 1 ? w1 : w2);
+  const uint32_t hi = wi == 0 ? w1 : (wi == 1 ? w2 : 0u);
+  return __funnelshift_r(lo, hi, sh) & 63u;
+}
+
+// Integer dot product of one 32-weight Q8_0 block (codes q0 | q1) with one
+// activation record: four independent dp4a chains of four, then the limbs
+// combined exactly (L = 2) or in fp32 (L = 4).
+template <int L>
+__device__ __forceinline__ float q8_block(const uint4 q0, const uint4 q1, const uint8_t* rec) {
+  int c[2 * L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
+    if (l == L - 1) {  // top limb: signed
+      c[2 * l] = dp4a_ss(q0.w, a0.w, dp4a_ss(q0.z, a0.z, dp4a_ss(q0.y, a0.y, dp4a_ss(q0.x, a0.x, 0))));
+      c[2 * l + 1] = dp4a_ss(q1.w, a1.w, dp4a_ss(q1.z, a1.z, dp4a_ss(q1.y, a1.y, dp4a_ss(q1.x, a1.x, 0))));
+    } else {
+      c[2 * l] = dp4a_su(q0.w, a0.w, dp4a_su(q0.z, a0.z, dp4a_su(q0.y, a0.y, dp4a_su(q0.x, a0.x, 0))));
+      c[2 * l + 1] = dp4a_su(q1.w, a1.w, dp4a_su(q1.z, a1.z, dp4a_su(q1.y, a1.y, dp4a_su(q1.x, a1.x, 0))));
+    }
+  }
+  if constexpr (L == 2) {
+    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
+  } else {
+    return fmaf((float)(c[6] + c[7]), 16777216.f,
+                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
+  }
+}
+
+// Same for one 32-weight Q4KS sub-block; w[2j] holds codes 8j..8j+3 and
+// w[2j+1] codes 8j+4..8j+7, one per byte.
+template <int L>
+__device__ __forceinline__ float q4_block(const uint32_t (&w)[8], const uint8_t* rec) {
+  int c[2 * L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
+    if (l == L - 1) {
+      c[2 * l] = dp4a_us(w[3], a0.w, dp4a_us(w[2], a0.z, dp4a_us(w[1], a0.y, dp4a_us(w[0], a0.x, 0))));
+      c[2 * l + 1] = dp4a_us(w[7], a1.w, dp4a_us(w[6], a1.z, dp4a_us(w[5], a1.y, dp4a_us(w[4], a1.x, 0))));
+    } else {
+      c[2 * l] = dp4a_uu(w[3], a0.w, dp4a_uu(w[2], a0.z, dp4a_uu(w[1], a0.y, dp4a_uu(w[0], a0.x, 0))));
+      c[2 * l + 1] = dp4a_uu(w[7], a1.w, dp4a_uu(w[6], a1.z, dp4a_uu(w[5], a1.y, dp4a_uu(w[4], a1.x, 0))));
+    }
+  }
+  if constexpr (L == 2) {
+    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
+  } else {
+    return fmaf((float)(c[6] + c[7]), 16777216.f,
+                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
+  }
+}
+
+__device__ __forceinline__ void q4_unpack(const uint4 qv, uint32_t (&w)[8]) {
+  w[0] = qv.x & 0x0F0F0F0Fu; w[1] = (qv.x >> 4) & 0x0F0F0F0Fu;
+  w[2] = qv.y & 0x0F0F0F0Fu; w[3] = (qv.y >> 4) & 0x0F0F0F0Fu;
+  w[4] = qv.z & 0x0F0F0F0Fu; w[5] = (qv.z >> 4) & 0x0F0F0F0Fu;
+  w[6] = qv.w & 0x0F0F0F0Fu; w[7] = (qv.w >> 4) & 0x0F0F0F0Fu;
+}
+
+// a = d * sc[s], b = dmin * m[s] of sub-block s from a 16-byte superblock header
+__device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float& b) {
+  const float dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+  a = dd * (float)field6(hd.y, hd.z, hd.w, s);
+  b = dmin * (float)field6(hd.y, hd.z, hd.w, 8 + s);
+}
+
+// One chunk.  Lane l owns row l of the chunk; warp w owns blocks w, w + 8,
+// ... (a warp load of one block's 16-byte pieces covers the 32 rows in 512
+// contiguous bytes; the block's activation records are a broadcast read, one
+// per warp).  acc[m] collects this warp's share of the lane's row against
+// vector m; the 8 warps' shares are summed by the epilogue warp.
+template <int L, int M>
+__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, const uint8_t* A, int nbc, int fmt,
+                                             float (&acc)[kGroup]) {
+  constexpr int RB = rec_bytes(L);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (fmt == MOE_Q8_0) {
+    const __half* sc = reinterpret_cast<const __half*>(stage + nbc * 1024);
+#pragma unroll 2
+    for (int b = warp; b < nbc; b += kBlocksPerStep) {
+      const uint4 q0 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 0) * kRows + lane) * 16);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 1) * kRows + lane) * 16);
+      const float dq = __half2float(sc[b * kRows + lane]);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const uint8_t* rec = A + (m * nbc + b) * RB;
+        const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
+        acc[m] = fmaf(dq * asc, q8_block<L>(q0, q1, rec), acc[m]);
+      }
+    }
+  } else {  // MOE_Q4KS
+    const uint8_t* hdr = stage + nbc * 512;
+#pragma unroll 2
+    for (int b = warp; b < nbc; b += kBlocksPerStep) {
+      const uint4 qv = *reinterpret_cast<const uint4*>(stage + ((int64_t)b * kRows + lane) * 16);
+      const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((b >> 3) * kRows + lane) * 16);
+      float sa, sb;
+      q4_scales(hd, b & 7, sa, sb);
+      uint32_t w[8];
+      q4_unpack(qv, w);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const uint8_t* rec = A + (m * nbc + b) * RB;
+        const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
+        const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
+        acc[m] = fmaf(sa * asc, q4_block<L>(w, rec), fmaf(-sb, sx, acc[m]));
+      }
+    }
+  }
+}
+
+// The token count of a stage as a compile-time constant, so the loops over
+// tokens unroll without predicates (a runtime bound there keeps the loads of
+// different tokens from being scheduled together).
+template <int L>
+__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, const uint8_t* A, int nbc, int fmt, int M,
+                                           float (&acc)[kGroup]) {
+  switch (M) {
+    case 1: gemv_chunk_m<L, 1>(stage, A, nbc, fmt, acc); break;
+    case 2: gemv_chunk_m<L, 2>(stage, A, nbc, fmt, acc); break;
+    case 3: gemv_chunk_m<L, 3>(stage, A, nbc, fmt, acc); break;
+    default: gemv_chunk_m<L, kGroup>(stage, A, nbc, fmt, acc); break;
+  }
+}
+
+}  // namespace moe

@@ -90,6 +90,7 @@ struct SmallParams {
   void* y;        // [T, H] same type
   int residual;   // 1: y = x + MoE(x)
   int act_f32;    // 1: x and y are fp32 (check mode), else bf16
+  int out_f32;    // 1: y is fp32 whatever the act dtype (moe_forward_f32)
   // workspace
   Sync* sync;
   int* status;
@@ -144,9 +145,9 @@ struct moe_layer {
 
 // Output norm + LM head of the MTP round (lm_head.cu, mtp.cu).
 struct moe_lm_head {
-  int dev = 0, V = 0, H = 0, T_max = 0, act = 0, num_sms = 0;
-  int8_t* q = nullptr;   // [V][H] int8 codes
-  __half* sc = nullptr;  // [V][H/32] fp16 scales
+  int dev = 0, V = 0, H = 0, T_max = 0, act = 0, num_sms = 0, max_optin = 0;
+  uint8_t* w = nullptr;  // [ceil(V/32)][nch][Q8_0 chunk of 32 rows]
+  int* status = nullptr; // [4]: timeout flag and wait site
 };
 
 namespace moe {

@@ -1,161 +1,225 @@
 // lm_head.cu -- output norm + Q8_0 LM head for the MTP round (T <= 8 rows).
 //
 // logits[t, v] = sum_h w[v, h] * rmsnorm(x[t])[h], rmsnorm(u) = u / sqrt(mean(u^2) + eps).
-// Each CTA first normalises the (up to 4) rows of its token group in fp32
-// and turns them into 16-bit block fixed point: per 32 columns a power-of-two
-// scale 2^-s and integers X with |X| <= 2^14, stored as two byte planes (low
-// byte unsigned, high byte signed).  A warp then takes 2 weight rows at a
-// time; lane l reads 16 consecutive int8 codes of each row per step (one
-// 128-bit load; a warp load covers 512 contiguous bytes of a row) and forms
-// exact integer sums with dp4a against both planes, scaled once per half
-// block by d * 2^-s.  The weights are stored as int8 codes [V][H] plus fp16
-// scales [V][H/32] (the serialised Q8_0 bytes, split).
+//
+// The weights are streamed like an expert's down matrix: repacked at create
+// into 32-row groups of Kc-column chunks (the Q8_0 chunk layout of
+// common.cuh: codes block-major, a warp's 128-bit loads of one block cover
+// the 32 rows), each chunk one 1-D bulk copy into a ring of shared-memory
+// stages.  Each block takes row groups blockIdx.x, blockIdx.x + gridDim.x,
+// ...; its producer thread issues the first stages before the dependency
+// wait (the weights are constant data), so they load while the previous
+// kernel in the stream finishes.  The (up to 4) rows of x are normalised in
+// fp32 and turned into 16-bit block fixed-point records once per block; the
+// 8 consumer warps take the chunk's blocks w, w + 8, ... (lane = row) with
+// exact dp4a sums (gemv.cuh), and their per-row partials are summed in warp
+// order.  Every wait is bounded; a timeout sets the head's status word and
+// the block stops.
+#include "gemv.cuh"
 #include "layer.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kLmThreads = 512;
-constexpr int kLmRows = 2;       // weight rows per warp task
-constexpr int kLmTokens = 4;     // rows of x per launch (token group)
+constexpr int kLmConsumerWarps = kConsumerWarps;                      // 8
+constexpr int kLmThreads = (kLmConsumerWarps + 1) * 32;               // + the producer warp
+constexpr int kLmTokens = 4;                                          // rows of x per launch (token group)
+constexpr int kLmMaxStages = 8;
+constexpr int kLmRecB = rec_bytes(2);                                 // 16-bit block fixed point
 
-__global__ void lm_repack_kernel(const uint8_t* __restrict__ src, int8_t* __restrict__ q, __half* __restrict__ sc,
-                                 int64_t nblocks) {
-  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= nblocks) return;
-  const uint8_t* s = src + b * 34;
-  sc[b] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
-  int8_t* d = q + b * 32;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) d[j] = (int8_t)s[2 + j];
+__global__ void lm_zero_kernel(uint8_t* __restrict__ p, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = 0;
 }
 
-template <int L>
-__global__ void __launch_bounds__(kLmThreads, 1)
-lm_head_kernel(const int8_t* __restrict__ q, const __half* __restrict__ sc, int V, int H, const void* x, int T,
-               float eps, float* __restrict__ logits) {
-  extern __shared__ __align__(16) uint8_t lsm[];
-  griddep_launch_dependents();
-  if (threadIdx.x == 0) {
-    // constant data: start this CTA's first rows on their way to L2 while the
-    // previous kernel in the stream finishes
-    const int64_t r0 = (int64_t)blockIdx.x * (kLmThreads / 32) * kLmRows;
-    if (r0 < V) {
-      const int64_t nr = min((int64_t)(kLmThreads / 32) * kLmRows, (int64_t)V - r0);
-      prefetch_l2(q + r0 * H, (uint32_t)(nr * H));
+struct LmParams {
+  const uint8_t* w;  // [n_rg][nch][chunk]
+  int V, H, nch, Kc, n_rg, T, stages;
+  int64_t chunk;     // bytes of one chunk
+  const void* x;
+  float eps;
+  float* logits;     // [T][V]
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct LmPlan {
+  int ring, recs, red, bars, total;
+};
+__host__ __device__ inline LmPlan lm_plan(int H, int64_t chunk, int stages) {
+  LmPlan p;
+  p.ring = 0;
+  p.recs = (int)(chunk * stages);
+  p.red = p.recs + kLmTokens * (H / 32) * kLmRecB;
+  p.bars = p.red + kLmConsumerWarps * kLmTokens * 32 * 4 + kLmTokens * 8 * 4;
+  p.total = p.bars + 2 * kLmMaxStages * 8 + 16;
+  return p;
+}
+
+__device__ inline bool lm_wait(uint64_t* bar, uint32_t parity, const LmParams& P, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > P.timeout_ns) {
+      if (atomicCAS(P.status, 0, kStatusTimeout) == 0) P.status[1] = site;
+      return false;
     }
   }
-  griddep_wait();  // x may come from the previous kernel in the stream
-  uint8_t* lo = lsm;                                          // [T][H]
-  int8_t* hi = reinterpret_cast<int8_t*>(lsm + kLmTokens * H);  // [T][H]
-  float* asc = reinterpret_cast<float*>(lsm + 2 * kLmTokens * H);  // [T][H/32]
-  __shared__ float red[kLmTokens][kLmThreads / 32];
+  return true;
+}
+
+template <int LIN, int T>
+__device__ void lm_consume(const LmParams& P, uint8_t* smem, const LmPlan& plan, uint64_t* full, uint64_t* empty) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // output norm: sum of squares per row
-  for (int t = 0; t < T; ++t) {
-    float s = 0.f;
-    for (int c = tid; c < H; c += kLmThreads) {
-      float v;
-      if constexpr (L == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[(int64_t)t * H + c]);
-      else v = reinterpret_cast<const float*>(x)[(int64_t)t * H + c];
-      s = fmaf(v, v, s);
-    }
+  const uint8_t* recs = smem + plan.recs;
+  float* red = reinterpret_cast<float*>(smem + plan.red);
+  const int nbc = P.Kc / 32;
+  float acc[kGroup];
+  int i = 0;  // item (row group, chunk) counter of this block
+  for (int g = blockIdx.x; g < P.n_rg; g += gridDim.x) {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) red[t][warp] = s;
+    for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
+    for (int c = 0; c < P.nch; ++c, ++i) {
+      const int s = i % P.stages;
+      if (!lm_wait(&full[s], (uint32_t)((i / P.stages) & 1), P, 2)) return;
+      gemv_chunk_m<2, T>(smem + plan.ring + (int64_t)s * P.chunk, recs + (int64_t)c * T * nbc * kLmRecB, nbc, MOE_Q8_0,
+                         acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // the 8 warps' shares of each row, summed in warp order
+#pragma unroll
+    for (int m = 0; m < T; ++m) red[(warp * kLmTokens + m) * 32 + lane] = acc[m];
+    consumer_sync();
+    if (tid < T * 32) {
+      const int m = tid >> 5, r = g * 32 + (tid & 31);
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kLmConsumerWarps; ++w) v += red[(w * kLmTokens + m) * 32 + (tid & 31)];
+      if (r < P.V) P.logits[(int64_t)m * P.V + r] = v;
+    }
+    consumer_sync();
+  }
+}
+
+template <int LIN>
+__global__ void __launch_bounds__(kLmThreads, 1) lm_stream_kernel(const __grid_constant__ LmParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const LmPlan plan = lm_plan(P.H, P.chunk, P.stages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
+  uint64_t* empty = full + kLmMaxStages;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_items = (P.n_rg - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x * P.nch;
+  griddep_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kLmConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // block fixed point of the normalised rows: warp w converts blocks w, w + 16, ...
-  for (int t = 0; t < T; ++t) {
-    float ss = 0.f;
-    for (int w = 0; w < kLmThreads / 32; ++w) ss += red[t][w];
-    const float inv = 1.f / sqrtf(ss / (float)H + eps);
-    for (int b = warp; b < H / 32; b += kLmThreads / 32) {
-      const int c = b * 32 + lane;
-      float v;
-      if constexpr (L == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[(int64_t)t * H + c]);
-      else v = reinterpret_cast<const float*>(x)[(int64_t)t * H + c];
-      v *= inv;
-      const float amax = warp_max(fabsf(v));
-      int s = 0;
-      if (amax > 0.f) s = max(-100, min(120, 13 - ilogbf(amax)));
-      const int X = __float2int_rn(ldexpf(v, s));
-      lo[t * H + c] = (uint8_t)(X & 0xFF);
-      hi[t * H + c] = (int8_t)(X >> 8);
-      if (lane == 0) asc[t * (H / 32) + b] = ldexpf(1.f, -s);
-    }
-  }
-  __syncthreads();
+  const bool producer = warp == kLmConsumerWarps && lane == 0;
+  const uint64_t wpol = l2_evict_first_policy();
+  // item i of this block: row group blockIdx.x + (i / nch) * gridDim.x, chunk i % nch
+  auto issue = [&](int i) {
+    const int s = i % P.stages;
+    const int g = blockIdx.x + (i / P.nch) * gridDim.x, c = i % P.nch;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)P.chunk);
+    bulk_g2s_hint(smem + plan.ring + (int64_t)s * P.chunk, P.w + ((int64_t)g * P.nch + c) * P.chunk, (uint32_t)P.chunk,
+                  &full[s], wpol);
+  };
+  int issued = 0;
+  if (producer)  // constant data: the first stages load while the previous kernel finishes
+    for (; issued < min(P.stages, n_items); ++issued) issue(issued);
+  griddep_wait();  // x may come from the previous kernel in the stream
 
-  const int nb = H / 32;
-  const int n_tasks = (V + kLmRows - 1) / kLmRows;
-  for (int task = blockIdx.x * (kLmThreads / 32) + warp; task < n_tasks; task += gridDim.x * (kLmThreads / 32)) {
-    const int r0 = task * kLmRows;
-    float acc[kLmRows][kLmTokens];
-#pragma unroll
-    for (int rr = 0; rr < kLmRows; ++rr)
-#pragma unroll
-      for (int t = 0; t < kLmTokens; ++t) acc[rr][t] = 0.f;
-#pragma unroll 4
-    for (int c0 = 0; c0 < H; c0 += 512) {
-      const int col = c0 + 16 * lane, blk = col >> 5;
-      uint4 qv[kLmRows];
-      float d[kLmRows];
-#pragma unroll
-      for (int rr = 0; rr < kLmRows; ++rr) {
-        const int r = min(r0 + rr, V - 1);
-        qv[rr] = __ldg(reinterpret_cast<const uint4*>(q + (int64_t)r * H + col));
-        d[rr] = __half2float(sc[(int64_t)r * nb + blk]);
+  if (producer) {
+    bool ok = true;
+    for (; issued < n_items && ok; ++issued) {
+      ok = lm_wait(&empty[issued % P.stages], (uint32_t)((issued / P.stages - 1) & 1), P, 1);
+      if (ok) issue(issued);
+    }
+    // every copy issued has landed before the block leaves
+    for (int j = max(0, issued - P.stages); j < issued; ++j)
+      lm_wait(&full[j % P.stages], (uint32_t)((j / P.stages) & 1), P, 3);
+  } else if (warp < kLmConsumerWarps) {
+    // records of the normalised rows, [chunk][token][block] (consumers only)
+    float* sq = reinterpret_cast<float*>(smem + plan.red) + kLmConsumerWarps * kLmTokens * 32;  // [T][8]
+    for (int t = 0; t < P.T; ++t) {
+      float ss = 0.f;
+      for (int c = tid; c < P.H; c += kLmConsumerWarps * 32) {
+        float v;
+        if constexpr (LIN == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + c]);
+        else v = reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + c];
+        ss = fmaf(v, v, ss);
       }
 #pragma unroll
-      for (int t = 0; t < kLmTokens; ++t) {
-        if (t < T) {
-          const uint4 xl = *reinterpret_cast<const uint4*>(lo + t * H + col);
-          const uint4 xh = *reinterpret_cast<const uint4*>(hi + t * H + col);
-          const float a = asc[t * nb + blk];
-#pragma unroll
-          for (int rr = 0; rr < kLmRows; ++rr) {
-            int sl = 0, sh = 0;
-            sl = dp4a_su(qv[rr].x, xl.x, sl);
-            sl = dp4a_su(qv[rr].y, xl.y, sl);
-            sl = dp4a_su(qv[rr].z, xl.z, sl);
-            sl = dp4a_su(qv[rr].w, xl.w, sl);
-            sh = dp4a_ss(qv[rr].x, xh.x, sh);
-            sh = dp4a_ss(qv[rr].y, xh.y, sh);
-            sh = dp4a_ss(qv[rr].z, xh.z, sh);
-            sh = dp4a_ss(qv[rr].w, xh.w, sh);
-            acc[rr][t] = fmaf(d[rr] * a, (float)(sl + 256 * sh), acc[rr][t]);
-          }
-        }
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) sq[t * 8 + warp] = ss;
+    }
+    consumer_sync();
+    const int nbc = P.Kc / 32;
+    for (int t = 0; t < P.T; ++t) {
+      float ss = 0.f;
+      for (int w = 0; w < kLmConsumerWarps; ++w) ss += sq[t * 8 + w];
+      const float inv = 1.f / sqrtf(ss / (float)P.H + P.eps);
+      for (int b = warp; b < P.H / 32; b += kLmConsumerWarps) {
+        float v;
+        const int col = b * 32 + lane;
+        if constexpr (LIN == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + col]);
+        else v = reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + col];
+        const int c = b / nbc, lb = b % nbc;
+        write_record<2>(v * inv, smem + plan.recs + (((int64_t)c * P.T + t) * nbc + lb) * kLmRecB);
       }
     }
-#pragma unroll
-    for (int rr = 0; rr < kLmRows; ++rr)
-#pragma unroll
-      for (int t = 0; t < kLmTokens; ++t) {
-        float v = acc[rr][t];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == rr * kLmTokens + t && t < T && r0 + rr < V) logits[(int64_t)t * V + r0 + rr] = v;
-      }
+    consumer_sync();
+    switch (P.T) {
+      case 1: lm_consume<LIN, 1>(P, smem, plan, full, empty); break;
+      case 2: lm_consume<LIN, 2>(P, smem, plan, full, empty); break;
+      case 3: lm_consume<LIN, 3>(P, smem, plan, full, empty); break;
+      default: lm_consume<LIN, 4>(P, smem, plan, full, empty); break;
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t lm_repack(const uint8_t* src, int8_t* q, __half* sc, int64_t nblocks, cudaStream_t st) {
-  lm_repack_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, st>>>(src, q, sc, nblocks);
-  return cudaGetLastError();
+cudaError_t repack_matrix(int fmt, const uint8_t* src, uint8_t* dst, int rows, int K, int rows_per_tile, int lr_off,
+                          Chunking ch, cudaStream_t st);
+
+// Bytes of the repacked head: ceil(V / 32) row groups of nch chunks.
+size_t lm_weight_bytes(int V, int H, Chunking ch) {
+  return (size_t)((V + 31) / 32) * ch.n * (size_t)chunk_bytes(MOE_Q8_0, ch.Kc);
 }
 
-size_t lm_smem_bytes(int H) { return (size_t)2 * kLmTokens * H + (size_t)kLmTokens * (H / 32) * 4; }
+// Chunking of the head's rows: chunks of at most 1024 columns, so that
+// several stages fit the ring beside the records.
+Chunking lm_chunking(int H) { return choose_chunking(MOE_Q8_0, H, 1); }
 
-cudaError_t lm_configure(int H) {
-  cudaError_t e = cudaFuncSetAttribute(lm_head_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)lm_smem_bytes(H));
+cudaError_t lm_repack(const uint8_t* src, uint8_t* dst, int V, int H, cudaStream_t st) {
+  const Chunking ch = lm_chunking(H);
+  const int64_t n = (int64_t)lm_weight_bytes(V, H, ch);
+  lm_zero_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(dst, n);  // rows past V
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(lm_head_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lm_smem_bytes(H));
+  return repack_matrix(MOE_Q8_0, src, dst, V, H, 32, 0, ch, st);
+}
+
+namespace {
+int lm_stages(int H, int64_t chunk, int max_optin) {
+  int s = kLmMaxStages;
+  while (s > 2 && lm_plan(H, chunk, s).total > max_optin) --s;
+  return s;
+}
+}  // namespace
+
+cudaError_t lm_configure(int H, int max_optin) {
+  const Chunking ch = lm_chunking(H);
+  const int64_t chunk = chunk_bytes(MOE_Q8_0, ch.Kc);
+  const int bytes = lm_plan(H, chunk, lm_stages(H, chunk, max_optin)).total;
+  cudaError_t e = cudaFuncSetAttribute(lm_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lm_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // Rows are processed in groups of kLmTokens (one launch per group); x is
@@ -164,17 +228,27 @@ cudaError_t lm_configure(int H) {
 cudaError_t lm_forward(const moe_lm_head* lm, const void* x, bool x_f32, int T, float eps, float* logits,
                        cudaStream_t st) {
   const size_t esz = x_f32 ? 4 : 2;
+  const Chunking ch = lm_chunking(lm->H);
+  LmParams P{};
+  P.w = lm->w;
+  P.V = lm->V;
+  P.H = lm->H;
+  P.nch = ch.n;
+  P.Kc = ch.Kc;
+  P.n_rg = (lm->V + 31) / 32;
+  P.chunk = chunk_bytes(MOE_Q8_0, ch.Kc);
+  P.stages = lm_stages(lm->H, P.chunk, lm->max_optin);
+  P.eps = eps;
+  P.status = lm->status;
+  P.timeout_ns = 2000000000ull;
+  const int smem = lm_plan(lm->H, P.chunk, P.stages).total;
   for (int t0 = 0; t0 < T; t0 += kLmTokens) {
-    const int n = min(kLmTokens, T - t0);
-    const void* xg = static_cast<const uint8_t*>(x) + (size_t)t0 * lm->H * esz;
-    float* lg = logits + (int64_t)t0 * lm->V;
+    P.T = min(kLmTokens, T - t0);
+    P.x = static_cast<const uint8_t*>(x) + (size_t)t0 * lm->H * esz;
+    P.logits = logits + (int64_t)t0 * lm->V;
     cudaError_t e;
-    if (!x_f32)
-      e = launch_pdl(lm_head_kernel<2>, lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st, (const int8_t*)lm->q,
-                     (const __half*)lm->sc, lm->V, lm->H, xg, n, eps, lg);
-    else
-      e = launch_pdl(lm_head_kernel<4>, lm->num_sms, kLmThreads, lm_smem_bytes(lm->H), st, (const int8_t*)lm->q,
-                     (const __half*)lm->sc, lm->V, lm->H, xg, n, eps, lg);
+    if (!x_f32) e = launch_pdl(lm_stream_kernel<2>, lm->num_sms, kLmThreads, smem, st, P);
+    else e = launch_pdl(lm_stream_kernel<4>, lm->num_sms, kLmThreads, smem, st, P);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

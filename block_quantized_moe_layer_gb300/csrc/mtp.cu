@@ -11,8 +11,10 @@
 #include "layer.cuh"
 
 namespace moe {
-cudaError_t lm_repack(const uint8_t* src, int8_t* q, __half* sc, int64_t nblocks, cudaStream_t st);
-cudaError_t lm_configure(int H);
+cudaError_t lm_repack(const uint8_t* src, uint8_t* dst, int V, int H, cudaStream_t st);
+cudaError_t lm_configure(int H, int max_optin);
+Chunking lm_chunking(int H);
+size_t lm_weight_bytes(int V, int H, Chunking ch);
 cudaError_t lm_forward(const moe_lm_head* lm, const void* x, bool x_f32, int T, float eps, float* logits,
                        cudaStream_t st);
 size_t accept_workspace_bytes(int k, int V);
@@ -50,11 +52,11 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-// One row per block: h_out = h_in + y (fp32; y is in the act dtype; without
-// y, h_out = h_in) and xn = rmsnorm(h_out) (act dtype).  h_in is fp32 (LIN =
-// 4) or the act dtype (LIN = L: the round's input batch).
+// One row per block: h_out = h_in + y (fp32; y is the layer's fp32 output;
+// without y, h_out = h_in) and xn = rmsnorm(h_out) (act dtype).  h_in is fp32
+// (LIN = 4) or the act dtype (LIN = L: the round's input batch).
 template <int L, int LIN>
-__global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict__ h_in, const void* __restrict__ y,
+__global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict__ h_in, const float* __restrict__ y,
                                                           float* __restrict__ h_out, void* __restrict__ xn, int H,
                                                           float eps) {
   __shared__ float red[8];
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const void* __restrict
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
     float v = ld_act<LIN>(h_in, base + c);
-    if (y) v += ld_act<L>(y, base + c);
+    if (y) v += y[base + c];
     h_out[base + c] = v;
     ss = fmaf(v, v, ss);
   }
@@ -199,7 +201,7 @@ RoundLayout round_layout(int H, int k, int V, int act) {
   r.hA = take((size_t)(k + 1) * H * 4);  // residual stream: fp32
   r.hB = take((size_t)(k + 1) * H * 4);
   r.xn = take((size_t)(k + 1) * H * esz);
-  r.ytmp = take((size_t)(k + 1) * H * esz);
+  r.ytmp = take((size_t)(k + 1) * H * 4);  // layer outputs: fp32
   r.hin = take((size_t)k * k * H * esz);
   r.hout = take((size_t)k * k * H * esz);
   r.rows = take((size_t)k * H * 4);
@@ -247,10 +249,11 @@ int moe_lm_head_create(const moe_tensor* w, int32_t T_max, int32_t act_dtype, vo
   };
   cudaError_t e;
   if ((e = cudaGetDevice(&lm->dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&lm->num_sms, cudaDevAttrMultiProcessorCount, lm->dev)) != cudaSuccess)
+      (e = cudaDeviceGetAttribute(&lm->num_sms, cudaDevAttrMultiProcessorCount, lm->dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&lm->max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, lm->dev)) != cudaSuccess)
     return cleanup(set_error(MOE_ECUDA, "%s", cudaGetErrorString(e)));
-  if ((e = cudaMalloc(&lm->q, (size_t)V * H)) != cudaSuccess ||
-      (e = cudaMalloc(&lm->sc, (size_t)V * (H / 32) * 2)) != cudaSuccess)
+  if ((e = cudaMalloc(&lm->w, lm_weight_bytes((int)V, (int)H, lm_chunking((int)H)))) != cudaSuccess ||
+      (e = cudaMalloc(&lm->status, 16)) != cudaSuccess || (e = cudaMemsetAsync(lm->status, 0, 16, st)) != cudaSuccess)
     return cleanup(set_error(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s", cudaGetErrorString(e)));
   cudaPointerAttributes pa{};
   const uint8_t* src = static_cast<const uint8_t*>(w->data);
@@ -261,7 +264,7 @@ int moe_lm_head_create(const moe_tensor* w, int32_t T_max, int32_t act_dtype, vo
       return cleanup(set_error(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s", cudaGetErrorString(e)));
     src = staged;
   }
-  if ((e = lm_repack(src, lm->q, lm->sc, V * (H / 32), st)) != cudaSuccess || (e = lm_configure((int)H)) != cudaSuccess ||
+  if ((e = lm_repack(src, lm->w, (int)V, (int)H, st)) != cudaSuccess || (e = lm_configure((int)H, lm->max_optin)) != cudaSuccess ||
       (e = cudaStreamSynchronize(st)) != cudaSuccess)
     return cleanup(set_error(MOE_ECUDA, "%s", cudaGetErrorString(e)));
   *out = lm;
@@ -280,10 +283,26 @@ int moe_lm_head_forward(moe_lm_head* lm, const void* x, int32_t T, float eps, fl
   return MOE_OK;
 }
 
+int moe_lm_head_status(moe_lm_head* lm, void* stream) {
+  if (!lm) return set_error(MOE_EINVAL, "moe_lm_head_status: NULL head");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  int word[4] = {0, 0, 0, 0};
+  if (e == cudaSuccess) e = cudaMemcpy(word, lm->status, 16, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(MOE_ECUDA, "moe_lm_head_status: %s", cudaGetErrorString(e));
+  if (word[0] != 0) {
+    e = cudaMemset(lm->status, 0, 16);
+    if (e != cudaSuccess) return set_error(MOE_ECUDA, "moe_lm_head_status: %s", cudaGetErrorString(e));
+    static const char* sites[] = {"?", "free stage", "full stage", "copy drain"};
+    return set_error(MOE_ETIMEOUT, "a device-side wait of the LM head timed out: %s",
+                     sites[(word[1] >= 0 && word[1] <= 3) ? word[1] : 0]);
+  }
+  return MOE_OK;
+}
+
 void moe_lm_head_destroy(moe_lm_head* lm) {
   if (!lm) return;
-  cudaFree(lm->q);
-  cudaFree(lm->sc);
+  cudaFree(lm->w);
+  cudaFree(lm->status);
   delete lm;
 }
 
@@ -327,23 +346,23 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   // target stack: pre-norm residual blocks h <- h + MoE(rmsnorm(h)); the
   // hidden state ping-pongs between hA and hB, xn holds the normalised rows
   void* xn = w + r.xn;
-  void* yt = w + r.ytmp;
+  float* yt = reinterpret_cast<float*>(w + r.ytmp);
   float* hA = reinterpret_cast<float*>(w + r.hA);
   float* hB = reinterpret_cast<float*>(w + r.hB);
   // h_0 = x (to fp32), xn = rmsnorm(h_0)
   if (act == MOE_ACT_BF16)
-    e = launch_pdl(add_rmsnorm_kernel<2, 2>, k + 1, 256, 0, st, x, (const void*)nullptr, hA, xn, H, eps);
+    e = launch_pdl(add_rmsnorm_kernel<2, 2>, k + 1, 256, 0, st, x, (const float*)nullptr, hA, xn, H, eps);
   else
-    e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, x, (const void*)nullptr, hA, xn, H, eps);
+    e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, x, (const float*)nullptr, hA, xn, H, eps);
   MCK(e, "mtp_round: norm");
   float* cur = hA;
   for (int l = 0; l < n_target; ++l) {
     float* out = cur == hA ? hB : hA;
-    if ((rc = moe_forward(target_layers[l], xn, k + 1, yt, stream))) return rc;
+    if ((rc = moe_forward_f32(target_layers[l], xn, k + 1, yt, stream))) return rc;
     if (act == MOE_ACT_BF16)
-      e = launch_pdl(add_rmsnorm_kernel<2, 4>, k + 1, 256, 0, st, (const void*)cur, (const void*)yt, out, xn, H, eps);
+      e = launch_pdl(add_rmsnorm_kernel<2, 4>, k + 1, 256, 0, st, (const void*)cur, (const float*)yt, out, xn, H, eps);
     else
-      e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, (const void*)cur, (const void*)yt, out, xn, H, eps);
+      e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, (const void*)cur, (const float*)yt, out, xn, H, eps);
     MCK(e, "mtp_round: residual + norm");
     cur = out;
   }

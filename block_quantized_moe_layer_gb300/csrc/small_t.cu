@@ -42,6 +42,7 @@
 // dp4a gives exact integer block dot products, scaled once per block:
 //   Q8_0 : sum_i d q_i v_i       = d * ascale * sum_i q_i X_i
 //   Q4KS : sum_i (a q_i - b) v_i = a * ascale * sum_i q_i X_i - b * sumx
+#include "gemv.cuh"
 #include "layer.cuh"
 
 namespace moe {
@@ -313,13 +314,17 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   int t = t0 >= 0 ? t0 : atomicAdd(&P.sync->queue, 1) + n_static;
   int pre = t0 >= 0 ? n_pre : 0;  // stages of this item placed and loading already
   while (ok) {
-    Geo g;
+    const int t_next = atomicAdd(&P.sync->queue, 1) + n_static;  // claim one ahead: its latency overlaps this item
+    int kind = kGateUp, entry = 0, rbt = 0;
     if (t < NR) {
-      g = geo_router<L>(P, t / P.n_kt, t % P.n_kt);
+      kind = kRouter;
     } else if (t < NR + NSG) {
-      g = geo_expert<L>(P, kGateUp, (t - NR) / P.n_gu_sh, (t - NR) % P.n_gu_sh, nullptr);
+      entry = (t - NR) / P.n_gu_sh;
+      rbt = (t - NR) % P.n_gu_sh;
     } else if (t < NR + NSG + NSD) {
-      g = geo_expert<L>(P, kDown, (t - NR - NSG) / NDT, (t - NR - NSG) % NDT, nullptr);
+      kind = kDown;
+      entry = (t - NR - NSG) / NDT;
+      rbt = (t - NR - NSG) % NDT;
     } else {
       if (n_rent < 0) {
         if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t)) {
@@ -341,16 +346,19 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       const int A = NR + NSG + NSD;
       const int NG = n_rent * P.n_gu, ND = n_rent * NDT;
       if (t < A + NG) {
-        const int entry = P.n_sh + (t - A) / P.n_gu;
-        g = geo_expert<L>(P, kGateUp, entry, (t - A) % P.n_gu, ecache + entry);
+        entry = P.n_sh + (t - A) / P.n_gu;
+        rbt = (t - A) % P.n_gu;
       } else if (t < A + NG + ND) {
-        const int entry = P.n_sh + (t - A - NG) / NDT;
-        g = geo_expert<L>(P, kDown, entry, (t - A - NG) % NDT, ecache + entry);
+        kind = kDown;
+        entry = P.n_sh + (t - A - NG) / NDT;
+        rbt = (t - A - NG) % NDT;
       } else {
         stamp_last(P.stamps, kTsLastIssue);
         break;  // queue exhausted
       }
     }
+    const Geo g = kind == kRouter ? geo_router<L>(P, t / P.n_kt, t % P.n_kt)
+                                  : geo_expert<L>(P, kind, entry, rbt, ecache + entry);
     const bool xslice = g.kind == kRouter;  // the stage holds a slice of x
     const bool shared_e = g.kind != kRouter && g.entry < P.n_sh;
     // activation sources of this tile at chunk 0, and their step per chunk
@@ -445,10 +453,7 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       ++issued;
     }
     pre = 0;
-    // the next item is claimed once this one's stages are all issued: the
-    // claim's latency overlaps the stages in flight, and when the queue runs
-    // out no block holds a claimed item it has not started
-    t = atomicAdd(&P.sync->queue, 1) + n_static;
+    t = t_next;
   }
   // end marker (or error): hand the consumers an END descriptor in the next slot
   const int n_data = issued;
@@ -464,142 +469,6 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
 }
 
 // ---------------------------------------------------------------------------
-// consumer: chunk compute
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t field6(uint32_t w0, uint32_t w1, uint32_t w2, int f) {
-  const int p = 6 * f;
-  const int wi = p >> 5, sh = p & 31;
-  const uint32_t lo = wi == 0 ? w0 : (wi == 1 ? w1 : w2);
-  const uint32_t hi = wi == 0 ? w1 : (wi == 1 ? w2 : 0u);
-  return __funnelshift_r(lo, hi, sh) & 63u;
-}
-
-// Integer dot product of one 32-weight Q8_0 block (codes q0 | q1) with one
-// activation record: four independent dp4a chains of four, then the limbs
-// combined exactly (L = 2) or in fp32 (L = 4).
-template <int L>
-__device__ __forceinline__ float q8_block(const uint4 q0, const uint4 q1, const uint8_t* rec) {
-  int c[2 * L];
-#pragma unroll
-  for (int l = 0; l < L; ++l) {
-    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
-    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
-    if (l == L - 1) {  // top limb: signed
-      c[2 * l] = dp4a_ss(q0.w, a0.w, dp4a_ss(q0.z, a0.z, dp4a_ss(q0.y, a0.y, dp4a_ss(q0.x, a0.x, 0))));
-      c[2 * l + 1] = dp4a_ss(q1.w, a1.w, dp4a_ss(q1.z, a1.z, dp4a_ss(q1.y, a1.y, dp4a_ss(q1.x, a1.x, 0))));
-    } else {
-      c[2 * l] = dp4a_su(q0.w, a0.w, dp4a_su(q0.z, a0.z, dp4a_su(q0.y, a0.y, dp4a_su(q0.x, a0.x, 0))));
-      c[2 * l + 1] = dp4a_su(q1.w, a1.w, dp4a_su(q1.z, a1.z, dp4a_su(q1.y, a1.y, dp4a_su(q1.x, a1.x, 0))));
-    }
-  }
-  if constexpr (L == 2) {
-    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
-  } else {
-    return fmaf((float)(c[6] + c[7]), 16777216.f,
-                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
-  }
-}
-
-// Same for one 32-weight Q4KS sub-block; w[2j] holds codes 8j..8j+3 and
-// w[2j+1] codes 8j+4..8j+7, one per byte.
-template <int L>
-__device__ __forceinline__ float q4_block(const uint32_t (&w)[8], const uint8_t* rec) {
-  int c[2 * L];
-#pragma unroll
-  for (int l = 0; l < L; ++l) {
-    const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 32 * l);
-    const uint4 a1 = *reinterpret_cast<const uint4*>(rec + 32 * l + 16);
-    if (l == L - 1) {
-      c[2 * l] = dp4a_us(w[3], a0.w, dp4a_us(w[2], a0.z, dp4a_us(w[1], a0.y, dp4a_us(w[0], a0.x, 0))));
-      c[2 * l + 1] = dp4a_us(w[7], a1.w, dp4a_us(w[6], a1.z, dp4a_us(w[5], a1.y, dp4a_us(w[4], a1.x, 0))));
-    } else {
-      c[2 * l] = dp4a_uu(w[3], a0.w, dp4a_uu(w[2], a0.z, dp4a_uu(w[1], a0.y, dp4a_uu(w[0], a0.x, 0))));
-      c[2 * l + 1] = dp4a_uu(w[7], a1.w, dp4a_uu(w[6], a1.z, dp4a_uu(w[5], a1.y, dp4a_uu(w[4], a1.x, 0))));
-    }
-  }
-  if constexpr (L == 2) {
-    return (float)((c[2] + c[3]) * 256 + (c[0] + c[1]));
-  } else {
-    return fmaf((float)(c[6] + c[7]), 16777216.f,
-                fmaf((float)(c[4] + c[5]), 65536.f, fmaf((float)(c[2] + c[3]), 256.f, (float)(c[0] + c[1]))));
-  }
-}
-
-__device__ __forceinline__ void q4_unpack(const uint4 qv, uint32_t (&w)[8]) {
-  w[0] = qv.x & 0x0F0F0F0Fu; w[1] = (qv.x >> 4) & 0x0F0F0F0Fu;
-  w[2] = qv.y & 0x0F0F0F0Fu; w[3] = (qv.y >> 4) & 0x0F0F0F0Fu;
-  w[4] = qv.z & 0x0F0F0F0Fu; w[5] = (qv.z >> 4) & 0x0F0F0F0Fu;
-  w[6] = qv.w & 0x0F0F0F0Fu; w[7] = (qv.w >> 4) & 0x0F0F0F0Fu;
-}
-
-// a = d * sc[s], b = dmin * m[s] of sub-block s from a 16-byte superblock header
-__device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float& b) {
-  const float dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-  const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-  a = dd * (float)field6(hd.y, hd.z, hd.w, s);
-  b = dmin * (float)field6(hd.y, hd.z, hd.w, 8 + s);
-}
-
-// One chunk.  Lane l owns row l of the chunk; warp w owns blocks w, w + 8,
-// ... (a warp load of one block's 16-byte pieces covers the 32 rows in 512
-// contiguous bytes; the block's activation records are a broadcast read, one
-// per warp).  acc[m] collects this warp's share of the lane's row against
-// vector m; the 8 warps' shares are summed by the epilogue warp.
-template <int L, int M>
-__device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, const uint8_t* A, int nbc, int fmt,
-                                             float (&acc)[kGroup]) {
-  constexpr int RB = rec_bytes(L);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (fmt == MOE_Q8_0) {
-    const __half* sc = reinterpret_cast<const __half*>(stage + nbc * 1024);
-#pragma unroll 2
-    for (int b = warp; b < nbc; b += kBlocksPerStep) {
-      const uint4 q0 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 0) * kRows + lane) * 16);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(stage + ((int64_t)(b * 2 + 1) * kRows + lane) * 16);
-      const float dq = __half2float(sc[b * kRows + lane]);
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const uint8_t* rec = A + (m * nbc + b) * RB;
-        const float asc = *reinterpret_cast<const float*>(rec + 32 * L);
-        acc[m] = fmaf(dq * asc, q8_block<L>(q0, q1, rec), acc[m]);
-      }
-    }
-  } else {  // MOE_Q4KS
-    const uint8_t* hdr = stage + nbc * 512;
-#pragma unroll 2
-    for (int b = warp; b < nbc; b += kBlocksPerStep) {
-      const uint4 qv = *reinterpret_cast<const uint4*>(stage + ((int64_t)b * kRows + lane) * 16);
-      const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((b >> 3) * kRows + lane) * 16);
-      float sa, sb;
-      q4_scales(hd, b & 7, sa, sb);
-      uint32_t w[8];
-      q4_unpack(qv, w);
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const uint8_t* rec = A + (m * nbc + b) * RB;
-        const float asc = reinterpret_cast<const float*>(rec + 32 * L)[0];
-        const float sx = reinterpret_cast<const float*>(rec + 32 * L)[1];
-        acc[m] = fmaf(sa * asc, q4_block<L>(w, rec), fmaf(-sb, sx, acc[m]));
-      }
-    }
-  }
-}
-
-// The token count of a stage as a compile-time constant, so the loops over
-// tokens unroll without predicates (a runtime bound there keeps the loads of
-// different tokens from being scheduled together).
-template <int L>
-__device__ __forceinline__ void gemv_chunk(const uint8_t* stage, const uint8_t* A, int nbc, int fmt, int M,
-                                           float (&acc)[kGroup]) {
-  switch (M) {
-    case 1: gemv_chunk_m<L, 1>(stage, A, nbc, fmt, acc); break;
-    case 2: gemv_chunk_m<L, 2>(stage, A, nbc, fmt, acc); break;
-    case 3: gemv_chunk_m<L, 3>(stage, A, nbc, fmt, acc); break;
-    default: gemv_chunk_m<L, kGroup>(stage, A, nbc, fmt, acc); break;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // consumer: routing (last router tile)
 // ---------------------------------------------------------------------------
 // fp32 -> unsigned key with the same order (no NaNs; -0 is mapped to +0 first).
@@ -611,103 +480,78 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Descending bitonic sort of N (a power of two) 64-bit keys in registers.
+// Largest of N values by a pairwise tree (depth log2 N).
 template <int N>
-__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&a)[N]) {
+__device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
+  uint64_t t[N];
 #pragma unroll
-  for (int size = 2; size <= N; size <<= 1)
+  for (int i = 0; i < N; ++i) t[i] = c[i];
 #pragma unroll
-    for (int stride = size / 2; stride > 0; stride >>= 1)
+  for (int w = 1; w < N; w <<= 1)
 #pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const uint64_t x = a[i], y = a[j];
-          const bool sw = desc ? x < y : x > y;
-          a[i] = sw ? y : x;
-          a[j] = sw ? x : y;
-        }
-      }
+    for (int i = 0; i + w < N; i += 2 * w) t[i] = t[i] > t[i + w] ? t[i] : t[i + w];
+  return t[0];
 }
 
-// Keeps the K largest of two descending lists in a: max(a[i], b[K-1-i]) is
-// a bitonic sequence holding the union's K largest, which a bitonic merge
-// sorts.
-template <int K, int N>
-__device__ __forceinline__ void merge_topk(uint64_t (&a)[K], const uint64_t (&b)[N]) {
-#pragma unroll
-  for (int i = 0; i < K; ++i) a[i] = a[i] > b[K - 1 - i] ? a[i] : b[K - 1 - i];
-#pragma unroll
-  for (int stride = K / 2; stride > 0; stride >>= 1)
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-      const int j = i ^ stride;
-      if (j > i) {
-        const uint64_t x = a[i], y = a[j];
-        a[i] = x > y ? x : y;
-        a[j] = x > y ? y : x;
-      }
-    }
-}
-
-// The k (<= K) largest of one token's E logits by (value desc, index asc),
-// one warp.  Logit e is read from its fixed-point sum (one rounding to fp32,
-// an exact power-of-two scale, then + bias, NaN counting as -inf); lane l
-// holds experts l, l + 32, ... (NP of them) as 64-bit composites
-// (order-preserving key of the value, then the complemented index: a larger
-// composite is a larger value or, on equal values, a lower index; 0 = none).
-// Each lane sorts its composites in chunks of up to 16 and keeps its K
-// largest; five merge levels over xor partners then leave every lane with
-// the warp's K largest in order.  The composites are distinct, so the result
-// is exact.  Writes ids, values and gates (softmax over the k selected
-// logits, the sum by a fixed shuffle tree) in slot order.
-template <int NP, int K>
-__device__ __forceinline__ void topk_token_merge(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
-  constexpr int C = NP < 16 ? NP : 16;  // chunk size (>= K)
-  static_assert(C >= K && NP % C == 0, "top-k chunking");
+// The k largest of one token's E logits by (value desc, index asc), one
+// warp, with the gates (softmax over the k selected logits, the sum by a
+// fixed shuffle tree), written in slot order.  Logit e is read from its
+// fixed-point sum (one rounding to fp32, an exact power-of-two scale, then
+// + bias; NaN counts as -inf).  Lane l holds experts l, l + 32, ... (NPER of
+// them) as 64-bit composites (order-preserving key of the value, then the
+// complemented index, so a larger composite is a larger value or, on equal
+// values, a lower index; 0 = none) and keeps its largest.  Each round takes
+// the exact maximum key over the lanes (a warp max); if several lanes hold
+// it, the lowest expert index among them wins (a second warp min, only
+// then).  The winning lane clears that expert and takes the tree maximum of
+// what it has left.  The rounds are a loop, not unrolled: this code runs once
+// per launch, so its size (instruction fetch) matters more than its
+// per-round cost.
+template <int NPER>
+__device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
   const int E = P.E, k = P.k;
-  uint64_t a[K];
+  uint64_t c[NPER];
 #pragma unroll
-  for (int ch = 0; ch < NP / C; ++ch) {
-    uint64_t c[C];
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      const int e = lane + 32 * (ch * C + i);
-      const long long v = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
-      const float b = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
-      const float x = __ll2float_rn(v) * 0x1p-32f + b;
-      c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    const long long v = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
+    const float b = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
+    const float x = __ll2float_rn(v) * 0x1p-32f + b;
+    c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
+  }
+  uint64_t best = tree_max(c);
+  float l0 = 0.f, lv = 0.f;
+  int my_id = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const uint32_t key = (uint32_t)(best >> 32);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
+    int wl = __ffs(holders) - 1;
+    if (holders & (holders - 1u))
+      wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
+    const int wi = (int)__shfl_sync(0xffffffffu, ~(uint32_t)best, wl);
+    const float val = key_value(m);
+    if (j == 0) l0 = val;
+    if (lane == j) {
+      my_id = wi;
+      lv = val;
     }
-    bitonic_sort_desc<C>(c);
-    if (ch == 0) {
+    if (lane == wl) {
+      const int slot = wi >> 5;
 #pragma unroll
-      for (int i = 0; i < K; ++i) a[i] = c[i];
-    } else {
-      merge_topk<K, C>(a, c);
+      for (int i = 0; i < NPER; ++i)
+        if (i == slot) c[i] = 0ull;
+      best = tree_max(c);
     }
   }
-#pragma unroll
-  for (int lvl = 1; lvl < 32; lvl <<= 1) {
-    uint64_t o[K];
-#pragma unroll
-    for (int i = 0; i < K; ++i) o[i] = __shfl_xor_sync(0xffffffffu, a[i], lvl);
-    merge_topk<K, K>(a, o);
-  }
-  // lane j < k takes slot j (a register select, no dynamic indexing)
-  uint64_t mine = 0;
-#pragma unroll
-  for (int i = 0; i < K; ++i)
-    if (i == lane) mine = a[i];
-  const float l0 = key_value((uint32_t)(a[0] >> 32));
-  const float lv = key_value((uint32_t)(mine >> 32));
   const float ex = lane < k ? expf(lv - l0) : 0.f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
-    ids[lane] = (int)~(uint32_t)mine;
+    ids[lane] = my_id;
     vals[lane] = lv;
     gates[lane] = ex / sum;
   }
@@ -769,14 +613,9 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   (void)lg;
 #pragma unroll 1
   for (int t = warp; t < T; t += kConsumerWarps) {
-    if (k <= 8) {
-      if (E <= 256) topk_token_merge<8, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
-      else if (E <= 512) topk_token_merge<16, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
-      else topk_token_merge<32, 8>(P, t, sid + t * k, sl + t * k, sg + t * k);
-    } else {
-      if (E <= 512) topk_token_merge<16, 16>(P, t, sid + t * k, sl + t * k, sg + t * k);
-      else topk_token_merge<32, 16>(P, t, sid + t * k, sl + t * k, sg + t * k);
-    }
+    if (E <= 128) topk_token<4>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    else if (E <= 384) topk_token<12>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    else topk_token<kMaxE / 32>(P, t, sid + t * k, sl + t * k, sg + t * k);
   }
   consumer_sync();
 
@@ -1280,7 +1119,7 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
       if constexpr (L == 2) acc += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + r]);
       else acc += reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + r];
     }
-    if constexpr (L == 2) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + r] = __float2bfloat16_rn(acc);
+    if (L == 2 && !P.out_f32) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + r] = __float2bfloat16_rn(acc);
     else reinterpret_cast<float*>(P.y)[(int64_t)t * P.H + r] = acc;
   }
 }

@@ -149,6 +149,14 @@ int moe_forward(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
  * once to the act_dtype. */
 int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* stream);
 
+/* y = MoE(x) as fp32 [T, H] whatever the layer's act_dtype, for callers that
+ * keep the residual stream in fp32 (as the pages' runtime keeps its hidden
+ * states in F32 tensors, "Support Step3.5/3.7 flash mtp3", "Overview"): the
+ * combine's fp32 sum is stored without the rounding to bf16.  T <= 8 only
+ * (MOE_EINVAL above); otherwise the arguments, rules and errors of
+ * moe_forward, with y (4 T H bytes) 16-byte aligned and not overlapping x. */
+int moe_forward_f32(moe_layer* L, const void* x, int32_t T, float* y, void* stream);
+
 /* Copies the routing of the last moe_forward (device-to-device, async on
  * `stream`): ids int32 [T, k] and gates fp32 [T, k] in slot order, offsets
  * int32 [E+1], perm int32 [T*k] (pair ids t*k+j grouped by expert, ascending
@@ -277,6 +285,10 @@ int moe_lm_head_create(const moe_tensor* w, int32_t T_max, int32_t act_dtype, vo
  * rmsnorm(v) = v / sqrt(mean(v^2) + eps) (weight 1; the output norm before
  * the LM head).  0 <= T <= T_max; x 16-byte aligned; asynchronous. */
 int moe_lm_head_forward(moe_lm_head* lm, const void* x, int32_t T, float eps, float* logits, void* stream);
+/* Synchronises `stream` and reports MOE_ETIMEOUT if a bounded device-side
+ * wait of an earlier moe_lm_head_forward (or of an mtp_round's LM-head
+ * passes) gave up (the word is then cleared); MOE_OK otherwise. */
+int moe_lm_head_status(moe_lm_head* lm, void* stream);
 void moe_lm_head_destroy(moe_lm_head* lm);
 
 /* One MTP draft/verify round on synthetic weights, the reading of
@@ -298,7 +310,8 @@ void moe_lm_head_destroy(moe_lm_head* lm);
  *   every draft);
  *   then greedy acceptance as mtp_verify_accept over the kept drafts.
  * The residual stream h and the noisy rows h~ are kept in fp32 in both
- * act dtypes (the layers' inputs rmsnorm(h) and outputs are in act_dtype).
+ * act dtypes: the target layers' inputs rmsnorm(h) are in act_dtype, their
+ * outputs fp32 (moe_forward_f32); head outputs are in act_dtype.
  * Every layer and the head must share act_dtype; all layers have hidden H,
  * T_max >= k+1.  noise fp32 [k][k][H] (device).  1 <= k <= 7.
  * workspace: device scratch of mtp_round_workspace_bytes(H, k, V, act)

@@ -12,8 +12,8 @@ GGUF", "Precision distribution" table: the main output matrix is Q8_0.
 
 The pages give the data flow but no synthetic model, so the round here is a
 reading of it, with every step a plain definition (in "bf16" activation mode
-the MoE layers' inputs and outputs are additionally rounded to bf16, as a
-bf16 layer takes and returns them):
+the MoE layers' inputs are additionally rounded to bf16, as a bf16 layer
+takes them):
   target      h_0 = x (the [k+1, H] verify batch); h_{l+1} = h_l +
               MoE_l(rmsnorm(h_l)) for the L target layers (pre-norm residual
               blocks: without the norm the SwiGLU, quadratic in its input,
@@ -72,8 +72,8 @@ def target_stack(x, layers, eps=1e-6, routes=None, layer_forward=None, act="f64"
     """h_tgt for the verify batch x [T, H] through pre-norm residual MoE layers.
     If `routes` is a list, each layer's routing dict is appended to it.
     ``layer_forward(x, L)``, if given, stands in for ``moe.forward(x, L)``.
-    act = "bf16": the layers' inputs and outputs are bf16 values (rounded
-    to nearest even at the layer boundary; the residual stream stays fp64)."""
+    act = "bf16": the layers' inputs are bf16 values (rmsnorm(h) rounded to
+    nearest even); their outputs and the residual stream keep full precision."""
     fwd = moe.forward if layer_forward is None else layer_forward
     io = round_bf16 if act == "bf16" else (lambda v: v)
     h = np.asarray(x, F64)
@@ -81,7 +81,7 @@ def target_stack(x, layers, eps=1e-6, routes=None, layer_forward=None, act="f64"
         y, r = fwd(io(rmsnorm(h, eps)), L)
         if routes is not None:
             routes.append(r)
-        h = h + io(y)
+        h = h + y
     return h
 
 
@@ -110,8 +110,8 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, lay
     and the routing dicts of every target layer (target_routes) and head
     (head_routes).  ``layer_forward(x, L)``, if given, stands in for
     ``moe.forward(x, L)``.  act = "bf16": every MoE layer's (and head's)
-    input and output are bf16 values (see target_stack); the residual
-    stream, the draft rows and the logits stay fp64."""
+    input is a bf16 value (see target_stack); outputs, the residual stream,
+    the draft rows and the logits keep full precision."""
     fwd = moe.forward if layer_forward is None else layer_forward
     io = round_bf16 if act == "bf16" else (lambda v: v)
     k = len(heads)
@@ -125,7 +125,7 @@ def mtp_round(x, layers, heads, lm: moe.QTensor, noise, eps=1e-6, p_min=0.0, lay
         ht = h_tgt[: j + 1] + np.asarray(noise[j][: j + 1], F64)
         y, hr = fwd(io(rmsnorm(ht, eps)), head)
         head_routes.append(hr)
-        head_out.append(io(y))
+        head_out.append(y)
         rows.append(ht[j])
     rows = np.stack(rows) if rows else np.zeros((0, x.shape[1]))
     draft_logits = lm_logits(rows, lm, eps)

@@ -109,3 +109,20 @@ def test_verify_mixed_full_size(verify_mixed, T):
     x = synth.activations(w, "cuda", T=T)
     err, excl, r = check_layer(L, x, ol, w.top_k, w.E, TOL[pkg.ACT_BF16], f"verify_mixed T={T}")
     print(f"verify_mixed T={T}: max rel err {err:.3e}, excluded {excl}")
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_forward_f32_is_the_unrounded_output(tiny, T):
+    """moe_forward_f32 stores the combine's fp32 sum: in bf16 mode its rounding
+    to bf16 is moe_forward's output bit for bit; in check mode it is that output."""
+    w, L, ol, act = tiny
+    x = synth.activations(w, "cuda", T=T, variant=7).to(XDT[act])
+    y = L.forward(x)
+    y32 = L.forward(x, out_f32=True)
+    torch.cuda.synchronize()
+    L.status()
+    assert y32.dtype == torch.float32
+    assert torch.equal(y32.to(y.dtype), y)
+    ref, r = omoe.forward(to_np(x), ol)
+    keep = ~omoe.near_tie_tokens(r["logits"], w.top_k)
+    assert omoe.max_rel_err(to_np(y32)[keep], ref[keep]) <= TOL[act]
