@@ -55,6 +55,8 @@ enum Stamp : int {
   kTsLastCombine,        // last: a combine finished
   kTsFirstExit,          // first: a CTA is leaving
   kTsLastExit,           // the last CTA is leaving
+  kTsCombineStart,       // last: a combining CTA's roles are done (its combine starts)
+  kTsCombineReady,       // last: a combining CTA has the routing arrays in shared memory
   kNumStamps
 };
 constexpr uint32_t kStampFirstMask = (1u << kTsEntry) | (1u << kTsStart) | (1u << kTsFirstRoutedIssue) |
@@ -69,8 +71,7 @@ struct SmallParams {
   int n_rc;               // router: 128-column chunks (H / 128)
   int Tp;                 // T rounded up to 4 (partial-logit row stride)
   int n_gu, n_gu_sh;      // gate/up tiles per routed / shared entry (32 outputs each)
-  int n_dt;               // 128-row blocks of z (H / 128): the unit of the combine
-                          // (a down tile is half a block, 64 output rows: 2 n_dt tiles per entry)
+  int n_dt;               // down tiles per entry (128 outputs each; the unit of the combine)
   int n_sh;               // shared entries for this T
   int Imax;               // max(I, Ish): row stride of the h records
   int E_pad;              // n_rg * 32

@@ -187,8 +187,8 @@ __device__ __forceinline__ Geo geo_router(const SmallParams& P, int rg, int rbt)
 }
 
 // A gate/up tile (32 SwiGLU outputs: 16 gate + 16 up rows, twice) or a down
-// tile (64 output rows: half of one 128-row block of z) of one work entry:
-// the shared expert's (entry < n_sh) or a routed expert's (ep = its entry).
+// tile (one 128-row block of z) of one work entry: the shared expert's
+// (entry < n_sh) or a routed expert's (ep = its entry).
 template <int L>
 __device__ __forceinline__ Geo geo_expert(const SmallParams& P, int kind, int entry, int rbt, const Entry* ep) {
   constexpr int RB = rec_bytes(L);
@@ -215,7 +215,7 @@ __device__ __forceinline__ Geo geo_expert(const SmallParams& P, int kind, int en
     kc = shared_e ? P.sgu_kc : P.gu_kc;
     g.n_tiles = shared_e ? P.n_gu_sh : P.n_gu;
   } else {
-    g.ngroups = 2;  // 64 output rows
+    g.ngroups = 4;  // 128 output rows
     g.nch = shared_e ? P.sdn_nch : P.dn_nch;
     kc = shared_e ? P.sdn_kc : P.dn_kc;
     g.n_tiles = 0;
@@ -224,7 +224,7 @@ __device__ __forceinline__ Geo geo_expert(const SmallParams& P, int kind, int en
   g.cbytes = chunk_bytes(g.fmt, kc);
   g.wbase = kind == kGateUp
                 ? (shared_e ? P.sgu : P.gu + (int64_t)g.e_id * P.gu_stride) + (int64_t)(2 * rbt) * g.nch * g.cbytes
-                : (shared_e ? P.sdn : P.dn + (int64_t)g.e_id * P.dn_stride) + (int64_t)(2 * rbt) * g.nch * g.cbytes;
+                : (shared_e ? P.sdn : P.dn + (int64_t)g.e_id * P.dn_stride) + (int64_t)(4 * rbt) * g.nch * g.cbytes;
   g.per = (uint32_t)(g.nbc * RB);
   // A group that is one chunk may share its stage with the next groups of
   // the tile (contiguous in memory, same records): fewer, larger stages,
@@ -251,43 +251,11 @@ __device__ __forceinline__ void write_desc(Desc* d, const Geo& g, int q, int pos
   dd[3] = make_int4(g.slot0, 0, g.n_tiles, 0);
 }
 
-// Work items [0, NR + NSG) -- the router tiles, then the shared expert's
-// gate/up tiles -- need nothing computed by this launch to start loading
-// their weights.  Block b < n_static takes item b without claiming it; its
-// producer issues the weights of the item's first stages (as many as fit
-// the ring) before the block waits for the previous kernel in the stream,
-// which overlaps those loads with that kernel's tail.  Weights are constant
-// data, written only when the layer was created.  Returns the stages issued;
-// *head is the ring offset after them.
-template <int L>
-__device__ int producer_prefetch(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, int t, int* head) {
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
-  Desc* descs = reinterpret_cast<Desc*>(smem + plan.descs);
-  const int NR = P.n_rg * P.n_kt;
-  const Geo g = t < NR ? geo_router<L>(P, t / P.n_kt, t % P.n_kt)
-                       : geo_expert<L>(P, kGateUp, (t - NR) / P.n_gu_sh, (t - NR) % P.n_gu_sh, nullptr);
-  const uint64_t wpol = l2_evict_first_policy();
-  int n = 0, pos = 0;
-  while (n < g.nstages && n < P.n_stages && pos + g.need <= P.ring_bytes) {
-    write_desc(descs + n, g, n, pos);
-    mbar_arrive_expect_tx(&full[n], g.wb + (uint32_t)g.M * g.per);
-    bulk_g2s_hint(smem + plan.ring + pos, g.wbase + (int64_t)n * g.wb, g.wb, &full[n], wpol);
-    pos += g.need;
-    ++n;
-  }
-  *head = pos;
-  return n;
-}
-
 // The producer is one thread; everything it keeps per stage lives in
 // registers or shared memory (no local arrays, no captured locals), since a
 // single thread pays the full latency of every dependent access.
-// t0: the block's static item (or -1: claim from the queue), with n_pre of
-// its stages already placed at ring offsets [0, head0) and their weights
-// issued (producer_prefetch).
 template <int L>
-__device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, int t0, int n_pre,
-                              int head0) {
+__device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPlan& plan) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + P.n_stages;
   Desc* descs = reinterpret_cast<Desc*>(smem + plan.descs);
@@ -296,25 +264,23 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   constexpr int RB = rec_bytes(L);
   constexpr int XEL = L == 2 ? 2 : 4;  // bytes of one x element
   const int NR = P.n_rg * P.n_kt;
-  const int NDT = 2 * P.n_dt;  // down tiles per entry (64 output rows each)
+  const int NDT = P.n_dt;  // down tiles per entry (128 output rows each)
   const int NSG = P.n_sh * P.n_gu_sh, NSD = P.n_sh * NDT;
   const int NS = P.n_stages;
-  const int n_static = min((int)gridDim.x, NR + NSG);  // items taken by block index, not claimed
   // Stage j (in issue order) uses descriptor slot j % NS and `need` bytes of
   // the ring placed right after stage j-1 (or at 0 when the end is reached).
   // Stages [oldest, issued) may still be in flight; their bytes form one arc
   // of the ring that starts at descs[oldest % NS].off and ends at head.
-  int issued = 0, oldest = 0, head = head0;
+  int issued = 0, oldest = 0, head = 0;
   bool ok = true;
   int n_rent = -1;
   for (int i = 0; i < 8; ++i) readybits[i] = 0u;
 
   const uint64_t wpol = l2_evict_first_policy();  // weights are read once per launch
   bool st_gu = false, st_dn = false;               // first routed gate/up / down copy stamped
-  int t = t0 >= 0 ? t0 : atomicAdd(&P.sync->queue, 1) + n_static;
-  int pre = t0 >= 0 ? n_pre : 0;  // stages of this item placed and loading already
+  int t = atomicAdd(&P.sync->queue, 1);
   while (ok) {
-    const int t_next = atomicAdd(&P.sync->queue, 1) + n_static;  // claim one ahead: its latency overlaps this item
+    const int t_next = atomicAdd(&P.sync->queue, 1);  // claim one ahead: its latency overlaps this item
     int kind = kGateUp, entry = 0, rbt = 0;
     if (t < NR) {
       kind = kRouter;
@@ -400,29 +366,23 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     }
     for (int q = 0; q < g.nstages && ok; ++q) {
       const int grp = q * g.gps / g.nch, c = q * g.gps - grp * g.nch;
-      const int s = issued & (NS - 1);
-      uint8_t* stage;
-      if (q < pre) {
-        // placed and its weights issued before the dependency wait
-        stage = smem + plan.ring + descs[s].off;
-      } else {
-        // ring space: a free slot, then free bytes
-        while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
-        int pos = 0;
-        while (ok) {
-          pos = head + g.need <= P.ring_bytes ? head : 0;
-          if (oldest == issued) break;
-          const int A = descs[oldest & (NS - 1)].off;
-          if (A < head ? (pos + g.need <= A || pos >= head) : (pos >= head && pos + g.need <= A)) break;
-          ok = wait_released(empty, NS, oldest++, P);
-        }
-        if (!ok) break;
-        head = pos + g.need;
-        write_desc(descs + s, g, q, pos);
-        stage = smem + plan.ring + pos;
-        mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
-        if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
+      // ring space: a free slot, then free bytes
+      while (ok && issued - oldest >= NS) ok = wait_released(empty, NS, oldest++, P);
+      int pos = 0;
+      while (ok) {
+        pos = head + g.need <= P.ring_bytes ? head : 0;
+        if (oldest == issued) break;
+        const int A = descs[oldest & (NS - 1)].off;
+        if (A < head ? (pos + g.need <= A || pos >= head) : (pos >= head && pos + g.need <= A)) break;
+        ok = wait_released(empty, NS, oldest++, P);
       }
+      if (!ok) break;
+      head = pos + g.need;
+      const int s = issued & (NS - 1);
+      write_desc(descs + s, g, q, pos);
+      uint8_t* stage = smem + plan.ring + pos;
+      mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
+      if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
       if (!dep_ok) {
         if (g.kind == kGateUp) {
           dep_ok = true;  // routed gate/up: gated by the routing flag (shared: waited above)
@@ -444,15 +404,6 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       (void)grp;
       ++issued;
     }
-    // prefetched stages whose activations were not issued (an error stopped
-    // the loop) still complete: give them their activation bytes
-    for (int q = issued; q < pre; ++q) {
-      const int s = q & (NS - 1);
-      uint8_t* adst = smem + plan.ring + descs[s].off + g.wb;
-      for (int m = 0; m < g.M; ++m) bulk_g2s(adst + m * g.per, asrc[0], g.per, &full[s]);
-      ++issued;
-    }
-    pre = 0;
     t = t_next;
   }
   // end marker (or error): hand the consumers an END descriptor in the next slot
@@ -747,13 +698,13 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   }
   consumer_sync();
   // One arrival of the routing on every 128-row block of z: a block is
-  // complete after its two down tiles of each of the n_sh + n_rent entries
-  // and this arrival, and whoever arrives last combines it.  A shared down tile that finishes before the
+  // complete after the down tile of each of the n_sh + n_rent entries and
+  // this arrival, and whoever arrives last combines it.  A shared down tile that finishes before the
   // routing is known can therefore never be taken for the last one, and a
   // layer with no down work for this batch (a shard none of whose experts
   // was chosen, with no shared expert) still gets y from the combine.
   {
-    const int last = 2 * (P.n_sh + *nrent_s);
+    const int last = P.n_sh + *nrent_s;
     for (int b = tid; b < P.n_dt; b += NT)
       if (atom_add_acq_rel(&P.d_cnt[b], 1) == last) pend[1 + atomicAdd(&pend[0], 1)] = b;
   }
@@ -1008,6 +959,7 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   uint32_t rph = 0;
   float keep[kGroup] = {0.f, 0.f, 0.f, 0.f};
   bool preloaded = false;
+  int n_rent_c = -1;  // (lane 0) routed entries, once known
   while (true) {
     if (!mbar_wait_bounded(&rfull[rs], rph, P.timeout_ns, P.status, kSiteRedFull, rs)) break;
     const Desc d = metas[rs];
@@ -1058,18 +1010,22 @@ __device__ void epilogue_loop(const SmallParams& P, uint8_t* smem, const SmemPla
         preloaded = true;
         if (preload_routing(P, smem, plan) && lane == 0) reinterpret_cast<int*>(smem + plan.flags)[3] = 1;
       }
-      const int row = d.rbt * 64 + d.group * 32 + lane;
+      const int row = d.rbt * 128 + d.group * 32 + lane;
       for (int m = 0; m < d.M; ++m) P.z[(int64_t)(d.slot0 + m) * P.H + row] = v[m];
       if (d.group == d.ngroups - 1) {
         __syncwarp();  // orders the lanes' z writes before lane 0's release
         if (lane == 0) {
-          // the 128-row block is complete after both halves of every entry's
-          // down tiles (2 (n_sh + n_rent)) and the routing's own arrival;
-          // n_rent is visible whenever the routing has arrived, and before
-          // that no tile can be the last one
-          const int blk = d.rbt >> 1;
+          // The block is complete after every entry's down tile (n_sh +
+          // n_rent) and the routing's own arrival, which comes after the
+          // routing is published.  So a tile whose increment finds the block
+          // complete has acquired the routing; it reads n_rent after the
+          // increment (once per block of this CTA: then it is cached).  Until
+          // the routing has arrived no tile can be the last one.
+          const int blk = d.rbt;
           const int old = atom_add_acq_rel(&P.d_cnt[blk], 1);
-          if (old == 2 * (P.n_sh + ld_acquire(&P.sync->n_rent))) {
+          if (n_rent_c < 0 && (d.entry >= P.n_sh || ld_acquire(&P.sync->routing_ready)))
+            n_rent_c = ld_acquire(&P.sync->n_rent);
+          if (n_rent_c >= 0 && old == P.n_sh + n_rent_c) {
             stamp_last(P.stamps, kTsLastDownDone);
             // this CTA combines the block when it leaves (with all its threads)
             int* pend = reinterpret_cast<int*>(smem + plan.pend);
@@ -1092,6 +1048,7 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
   const int* sp = reinterpret_cast<const int*>(smem + plan.escr + kMaxSmallT * kMaxTopK * 4);
   const int T = P.T, k = P.k;
   int* flags = reinterpret_cast<int*>(smem + plan.flags);
+  if (threadIdx.x == 0) stamp_last(P.stamps, kTsCombineStart);
   if (!flags[3]) {
     // not fetched by the epilogue warp (this CTA saw no routed down tile)
     if (threadIdx.x < 32) {
@@ -1101,6 +1058,7 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
     __syncthreads();
     if (!flags[2]) return;
   }
+  if (threadIdx.x == 0) stamp_last(P.stamps, kTsCombineReady);
   const int n = pend[0];
   for (int o = threadIdx.x; o < n * 128 * T; o += blockDim.x) {
     const int b = o / (128 * T), rem = o % (128 * T), t = rem / 128;
@@ -1139,6 +1097,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   griddep_launch_dependents();
   const uint64_t t_entry = globaltimer_ns();
   if (threadIdx.x == 0) {
+    // constant data only: warm L2 with one router tile's weights (tile = block)
+    if ((int)blockIdx.x < P.n_rg * P.n_kt) {
+      const int rg = blockIdx.x / P.n_kt, kt = blockIdx.x % P.n_kt;
+      const int nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * kt);
+      prefetch_l2(P.router + ((int64_t)rg * P.n_ks * 64 + kRouterTileChunks * 32 * kt) * kRows * 16,
+                  (uint32_t)(nbc * chunk_bytes(MOE_F32, kRouterCc)));
+    }
     pend[0] = 0;
     flags[3] = 0;  // the combine's routing arrays are not in shared memory yet
     for (int i = 0; i < P.n_stages; ++i) {
@@ -1152,15 +1117,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     mbar_init(reinterpret_cast<uint64_t*>(smem + plan.ebar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // barriers initialised before the producer's first copies
-  const int warp = threadIdx.x >> 5;
-  const bool producer = warp == kProducerWarp && (threadIdx.x & 31) == 0;
-  // the block's static first item: its first weight stages start loading
-  // now, while the previous kernel in the stream finishes (constant data only)
-  const int n_static = min((int)gridDim.x, P.n_rg * P.n_kt + P.n_sh * P.n_gu_sh);
-  const int t_static = (int)blockIdx.x < n_static ? (int)blockIdx.x : -1;
-  int n_pre = 0, head0 = 0;
-  if (producer && t_static >= 0) n_pre = producer_prefetch<L>(P, smem, plan, t_static, &head0);
   griddep_wait();  // x, the workspace and its counters are the previous launches' to finish with
   if (threadIdx.x == 0) {
     stamp_first_at(P.stamps, kTsEntry, t_entry);
@@ -1168,8 +1124,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   }
   __syncthreads();
 
+  const int warp = threadIdx.x >> 5;
   if (warp == kProducerWarp) {
-    if (producer) producer_loop<L>(P, smem, plan, t_static, n_pre, head0);
+    if ((threadIdx.x & 31) == 0) producer_loop<L>(P, smem, plan);
   } else if (warp == kEpilogueWarp) {
     epilogue_loop<L>(P, smem, plan);
   } else {

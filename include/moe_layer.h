@@ -173,7 +173,7 @@ int moe_layer_status(moe_layer* L, void* stream);
  * profiling: synchronises `stream`, then writes n (>= 1) int64 values to the
  * HOST array out_ns, in nanoseconds of the GPU's global timer relative to
  * the first of the launch's blocks to pass its dependency wait, -1 where the
- * event did not happen (or i >= 15).  The events, in order:
+ * event did not happen.  The events, in order:
  *   0 first block entered the kernel (before its dependency wait; negative
  *     when it started during the previous kernel)
  *   1 first block passed its dependency wait (0 by definition)
@@ -190,7 +190,10 @@ int moe_layer_status(moe_layer* L, void* stream);
  *  12 the last combine finished
  *  13 first block leaving
  *  14 last block leaving
- * The stamps cost a few atomic writes per block and are always recorded. */
+ *  15 the last combining block started its combine
+ *  16 the last combining block had the routing arrays it needs
+ * (-1 for i >= 17).  The stamps cost a few atomic writes per block and are
+ * always recorded. */
 int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream);
 
 /* Test hook for the bounded device-side waits (no fault is involved).
