@@ -77,7 +77,7 @@ __device__ __forceinline__ void record_timeout(int* status, int site, int detail
 // Waits spin on the non-blocking test first (a suspended thread takes a few
 // hundred cycles to resume, which would sit on the per-stage critical path),
 // then fall back to the suspending try_wait.
-constexpr int kSpin = 256;
+constexpr int kSpin = 32;
 
 // Single-thread bounded wait.
 __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t par, volatile int* abort, const LtGemmParams& p,

@@ -20,16 +20,16 @@ struct Entry {
 static_assert(sizeof(Entry) == 32, "Entry is copied as two 16-byte vectors");
 
 // Cross-CTA counters of the fused kernel.  All zero between launches: the
-// last CTA to leave resets them.
+// last CTA to leave resets them.  Each busy counter has an L2 line (128 B)
+// of its own, so that the blocks polling one flag do not queue behind the
+// atomics on another.
 struct Sync {
-  int queue;          // next tile to claim
-  int router_done;    // router tiles finished
-  int x_done;         // x slices converted to activation records
-  int routing_ready;  // routing published
-  int exit_cnt;       // CTAs that left
-  int n_rent;         // routed entries (written with the routing)
-  int routing_aux;    // ids, gates, offsets, perm, pos written (after routing_ready)
-  int pad;
+  alignas(128) int queue;          // next tile to claim
+  alignas(128) int router_done;    // router tiles finished (also: x records complete)
+  alignas(128) int routing_ready;  // routing published
+  int n_rent;                      // routed entries (written with the routing)
+  alignas(128) int routing_aux;    // ids, gates, offsets, perm, pos written (after routing_ready)
+  alignas(128) int exit_cnt;       // CTAs that left
 };
 
 // Phase stamps of one small-T launch (globaltimer, ns).  Each kind is kept

@@ -349,9 +349,9 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     }
     bool dep_ok = xslice;
     if (g.kind == kGateUp && shared_e) {
-      // the shared expert's records are read once they exist (the x records
-      // are written by the first row group's router tiles)
-      dep_ok = wait_flag_geq(&P.sync->x_done, P.T * P.n_rc, P.timeout_ns, P.status, kSiteX, t);
+      // the shared expert's records are read once they exist: the first row
+      // group's router tiles write them before they count themselves done
+      dep_ok = wait_flag_geq(&P.sync->router_done, P.n_rg * P.n_kt, P.timeout_ns, P.status, kSiteX, t);
       if (dep_ok) fence_proxy_async_global();
       else ok = false;
     }
@@ -834,8 +834,8 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       if (d_rg == 0) {
         // the first row group's tiles also turn their slice of x into the
         // activation records (one 32-column block per thread); the proxy
-        // fence makes them visible to the bulk copies that read them after
-        // x_done
+        // fence makes them visible to the bulk copies that read them once
+        // every router tile has counted itself done
         const int kt = d_ks / kRouterTileChunks, nb = cols / 32;
         constexpr int XEL = L == 2 ? 2 : 4;
         if (tid < T * nb) {
@@ -851,9 +851,9 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       for (int t = 0; t < kMaxSmallT; ++t)
         if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
       consumer_sync();
-      // (the barrier also orders every thread's record writes before thread 0's release)
-      if (d_rg == 0 && tid == 0 && atom_add_acq_rel(&P.sync->x_done, T * d.nbc) + T * d.nbc == T * P.n_rc)
-        stamp_last(P.stamps, kTsXDone);
+      // (the barriers also order every thread's record writes before thread
+      // 0's release of router_done, which the shared expert's records and,
+      // through the routing, the routed tiles' records wait for)
       if (tid < T * 32) {
         // this slice's share of logit (t, expert 32 rg + r), added as an
         // exact integer multiple of 2^-32: the total does not depend on the
@@ -873,7 +873,10 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       }
       consumer_sync();
       if (flags[0]) {
-        if (tid == 0) stamp_last(P.stamps, kTsRouterDone);
+        if (tid == 0) {
+          stamp_last(P.stamps, kTsXDone);  // the x records are written by router tiles
+          stamp_last(P.stamps, kTsRouterDone);
+        }
         finalize_routing(P, misc, reinterpret_cast<int*>(smem + plan.pend));
       }
       consumer_sync();
@@ -1059,26 +1062,55 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
     if (!flags[2]) return;
   }
   if (threadIdx.x == 0) stamp_last(P.stamps, kTsCombineReady);
+  // one pass: thread u takes 4 consecutive rows of one token of one block,
+  // with all of its z reads (128-bit) in flight at once
   const int n = pend[0];
-  for (int o = threadIdx.x; o < n * 128 * T; o += blockDim.x) {
-    const int b = o / (128 * T), rem = o % (128 * T), t = rem / 128;
-    const int r = pend[1 + b] * 128 + rem % 128;
-    float zv[kMaxTopK];
+  for (int u = threadIdx.x; u < n * 32 * T; u += blockDim.x) {
+    const int b = u / (32 * T), rem = u - b * (32 * T), t = rem / 32;
+    const int r = pend[1 + b] * 128 + (rem - t * 32) * 4;
+    float4 zv[kMaxTopK];
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) zv[j] = sp[t * k + j] >= 0 ? __ldcg(&P.z[(int64_t)sp[t * k + j] * P.H + r]) : 0.f;
-    const float zs = P.n_sh > 0 ? __ldcg(&P.z[(int64_t)(T * k + t) * P.H + r]) : 0.f;
-    float acc = 0.f;
+      if (j < k && sp[t * k + j] >= 0) zv[j] = __ldcg(reinterpret_cast<const float4*>(P.z + (int64_t)sp[t * k + j] * P.H + r));
+    const float4 zs = P.n_sh > 0 ? __ldcg(reinterpret_cast<const float4*>(P.z + (int64_t)(T * k + t) * P.H + r))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k && sp[t * k + j] >= 0) acc = fmaf(sg[t * k + j], zv[j], acc);
-    acc += zs;
+      if (j < k && sp[t * k + j] >= 0) {
+        const float g = sg[t * k + j];
+        acc.x = fmaf(g, zv[j].x, acc.x);
+        acc.y = fmaf(g, zv[j].y, acc.y);
+        acc.z = fmaf(g, zv[j].z, acc.z);
+        acc.w = fmaf(g, zv[j].w, acc.w);
+      }
+    acc.x += zs.x;
+    acc.y += zs.y;
+    acc.z += zs.z;
+    acc.w += zs.w;
+    const int64_t o = (int64_t)t * P.H + r;
     if (P.residual) {
-      if constexpr (L == 2) acc += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + r]);
-      else acc += reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + r];
+      if constexpr (L == 2) {
+        const uint2 xr = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(P.x) + o);
+        acc.x += __uint_as_float(xr.x << 16);
+        acc.y += __uint_as_float(xr.x & 0xFFFF0000u);
+        acc.z += __uint_as_float(xr.y << 16);
+        acc.w += __uint_as_float(xr.y & 0xFFFF0000u);
+      } else {
+        const float4 xr = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(P.x) + o);
+        acc.x += xr.x;
+        acc.y += xr.y;
+        acc.z += xr.z;
+        acc.w += xr.w;
+      }
     }
-    if (L == 2 && !P.out_f32) reinterpret_cast<__nv_bfloat16*>(P.y)[(int64_t)t * P.H + r] = __float2bfloat16_rn(acc);
-    else reinterpret_cast<float*>(P.y)[(int64_t)t * P.H + r] = acc;
+    if (L == 2 && !P.out_f32) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(P.y) + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(P.y) + o) = acc;
+    }
   }
 }
 
@@ -1166,7 +1198,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     if (threadIdx.x == 0) {
       P.sync->queue = 0;
       P.sync->router_done = 0;
-      P.sync->x_done = 0;
       P.sync->routing_ready = 0;
       P.sync->routing_aux = 0;
       P.sync->n_rent = 0;

@@ -177,7 +177,8 @@ int moe_layer_status(moe_layer* L, void* stream);
  *   0 first block entered the kernel (before its dependency wait; negative
  *     when it started during the previous kernel)
  *   1 first block passed its dependency wait (0 by definition)
- *   2 the activation records of x were complete
+ *   2 the activation records of x were complete (written by the router
+ *     tiles: the same time as 3)
  *   3 the last router tile finished (the routing starts)
  *   4 the routing was published
  *   5 first routed gate/up weight copy issued
