@@ -30,7 +30,7 @@ EXPORTS = (
 TIMELINE = ("entry", "start", "x_records", "router_done", "routing_ready", "first_routed_issue",
             "first_routed_compute", "shared_gate_up_done", "last_gate_up_done", "first_down_issue",
             "queue_exhausted", "last_down_block", "last_combine", "first_exit", "last_exit", "combine_start",
-            "combine_ready")
+            "combine_ready", "topk_done", "entries_done")
 
 
 class MoeTensor(_c.Structure):

@@ -57,6 +57,8 @@ enum Stamp : int {
   kTsLastExit,           // the last CTA is leaving
   kTsCombineStart,       // last: a combining CTA's roles are done (its combine starts)
   kTsCombineReady,       // last: a combining CTA has the routing arrays in shared memory
+  kTsTopkDone,           // the routing's top-k and gates are done
+  kTsEntriesDone,        // the routing's permutation and work entries are written
   kNumStamps
 };
 constexpr uint32_t kStampFirstMask = (1u << kTsEntry) | (1u << kTsStart) | (1u << kTsFirstRoutedIssue) |

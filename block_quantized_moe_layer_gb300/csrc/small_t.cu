@@ -454,21 +454,32 @@ __device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
 // values, a lower index; 0 = none) and keeps its largest.  Each round takes
 // the exact maximum key over the lanes (a warp max); if several lanes hold
 // it, the lowest expert index among them wins (a second warp min, only
-// then).  The winning lane clears that expert and takes the tree maximum of
-// what it has left.  The rounds are a loop, not unrolled: this code runs once
-// per launch, so its size (instruction fetch) matters more than its
-// per-round cost.
+// then).  The winning lane clears that expert and every lane takes the tree
+// maximum of what it holds: the rounds have no divergent branches.  A
+// separate (not inlined) function: it runs once per launch, and its
+// registers do not add to the pressure of the streaming loops.
 template <int NPER>
-__device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
+__device__ __noinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
   const int E = P.E, k = P.k;
+  // every load in flight before the first conversion
+  long long v[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
+  }
+  float b[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    b[i] = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
+  }
   uint64_t c[NPER];
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    const long long v = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
-    const float b = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
-    const float x = __ll2float_rn(v) * 0x1p-32f + b;
+    const float x = __ll2float_rn(v[i]) * 0x1p-32f + b[i];
     c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
   }
   uint64_t best = tree_max(c);
@@ -480,22 +491,17 @@ __device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids
     const uint32_t m = __reduce_max_sync(0xffffffffu, key);
     const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
     int wl = __ffs(holders) - 1;
-    if (holders & (holders - 1u))
+    if (holders & (holders - 1u))  // warp-uniform
       wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
     const int wi = (int)__shfl_sync(0xffffffffu, ~(uint32_t)best, wl);
     const float val = key_value(m);
-    if (j == 0) l0 = val;
-    if (lane == j) {
-      my_id = wi;
-      lv = val;
-    }
-    if (lane == wl) {
-      const int slot = wi >> 5;
+    l0 = j == 0 ? val : l0;
+    my_id = lane == j ? wi : my_id;
+    lv = lane == j ? val : lv;
+    const int slot = lane == wl ? (wi >> 5) : -1;
 #pragma unroll
-      for (int i = 0; i < NPER; ++i)
-        if (i == slot) c[i] = 0ull;
-      best = tree_max(c);
-    }
+    for (int i = 0; i < NPER; ++i) c[i] = i == slot ? 0ull : c[i];
+    best = tree_max(c);
   }
   const float ex = lane < k ? expf(lv - l0) : 0.f;
   float sum = ex;
@@ -569,6 +575,9 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
     else topk_token<kMaxE / 32>(P, t, sid + t * k, sl + t * k, sg + t * k);
   }
   consumer_sync();
+  // (stamps here come from warp 1: the release below is thread 0's, and a
+  // release waits for its own thread's earlier writes)
+  if (tid == 32) stamp_last(P.stamps, kTsTopkDone);
 
   // slot of each pair (experts ascending, tokens ascending within an
   // expert) and the routed entries (up to kGroup consecutive slots of one
@@ -690,6 +699,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   consumer_sync();
   // the barrier orders every thread's entry writes before thread 0's release
   int* nrent_s = reinterpret_cast<int*>(misc + f.end);
+  if (tid == 32) stamp_last(P.stamps, kTsEntriesDone);
   if (tid == 0) {
     P.sync->n_rent = n_rent;
     st_release(&P.sync->routing_ready, 1);
@@ -873,7 +883,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       }
       consumer_sync();
       if (flags[0]) {
-        if (tid == 0) {
+        if (tid == 32) {
           stamp_last(P.stamps, kTsXDone);  // the x records are written by router tiles
           stamp_last(P.stamps, kTsRouterDone);
         }

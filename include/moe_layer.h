@@ -193,7 +193,9 @@ int moe_layer_status(moe_layer* L, void* stream);
  *  14 last block leaving
  *  15 the last combining block started its combine
  *  16 the last combining block had the routing arrays it needs
- * (-1 for i >= 17).  The stamps cost a few atomic writes per block and are
+ *  17 the routing's top-k and gates were done
+ *  18 the routing's permutation and work entries were written
+ * (-1 for i >= 19).  The stamps cost a few atomic writes per block and are
  * always recorded. */
 int moe_layer_timeline(moe_layer* L, int64_t* out_ns, int32_t n, void* stream);
 
