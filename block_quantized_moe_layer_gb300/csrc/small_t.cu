@@ -454,12 +454,12 @@ __device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
 // values, a lower index; 0 = none) and keeps its largest.  Each round takes
 // the exact maximum key over the lanes (a warp max); if several lanes hold
 // it, the lowest expert index among them wins (a second warp min, only
-// then).  The winning lane clears that expert and every lane takes the tree
-// maximum of what it holds: the rounds have no divergent branches.  A
-// separate (not inlined) function: it runs once per launch, and its
-// registers do not add to the pressure of the streaming loops.
+// then).  The winning lane clears that expert and takes the tree maximum of
+// what it has left.  The rounds are a loop, not unrolled: this code runs
+// once per launch, so its size (instruction fetch) matters more than its
+// per-round cost.
 template <int NPER>
-__device__ __noinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
+__device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
   const int E = P.E, k = P.k;
   // every load in flight before the first conversion
@@ -491,17 +491,22 @@ __device__ __noinline__ void topk_token(const SmallParams& P, int t, int* ids, f
     const uint32_t m = __reduce_max_sync(0xffffffffu, key);
     const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
     int wl = __ffs(holders) - 1;
-    if (holders & (holders - 1u))  // warp-uniform
+    if (holders & (holders - 1u))
       wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
     const int wi = (int)__shfl_sync(0xffffffffu, ~(uint32_t)best, wl);
     const float val = key_value(m);
-    l0 = j == 0 ? val : l0;
-    my_id = lane == j ? wi : my_id;
-    lv = lane == j ? val : lv;
-    const int slot = lane == wl ? (wi >> 5) : -1;
+    if (j == 0) l0 = val;
+    if (lane == j) {
+      my_id = wi;
+      lv = val;
+    }
+    if (lane == wl) {
+      const int slot = wi >> 5;
 #pragma unroll
-    for (int i = 0; i < NPER; ++i) c[i] = i == slot ? 0ull : c[i];
-    best = tree_max(c);
+      for (int i = 0; i < NPER; ++i)
+        if (i == slot) c[i] = 0ull;
+      best = tree_max(c);
+    }
   }
   const float ex = lane < k ? expf(lv - l0) : 0.f;
   float sum = ex;
