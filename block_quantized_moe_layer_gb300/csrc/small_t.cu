@@ -469,17 +469,11 @@ __device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids
     const int e = lane + 32 * i;
     v[i] = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
   }
-  float b[NPER];
-#pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    b[i] = (e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f;
-  }
   uint64_t c[NPER];
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    const float x = __ll2float_rn(v[i]) * 0x1p-32f + b[i];
+    const float x = __ll2float_rn(v[i]) * 0x1p-32f + ((e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f);
     c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
   }
   uint64_t best = tree_max(c);
