@@ -22,6 +22,7 @@ int small_t_smem_bytes(const SmallParams& P);
 int finalize_misc_bytes(int T, int E, int k);
 cudaError_t small_t_configure(int L, int smem_bytes);
 cudaError_t small_t_launch(const SmallParams& P, int L, int grid, int smem_bytes, cudaStream_t st);
+cudaError_t small_t_init_logit_sums(const SmallParams& P, long long* lfx0, cudaStream_t st);
 bool large_t_enabled(const moe_layer* L);
 cudaError_t large_t_alloc(moe_layer* L);
 cudaError_t large_t_repack(moe_layer* L, int which, int e, const uint8_t* src, cudaStream_t st);
@@ -364,10 +365,11 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_gucnt = take((size_t)w_max * 4);
   const size_t o_ready = take((size_t)w_max * 4);
   const size_t o_dcnt = take((size_t)n_dt * 4);
-  const size_t o_lfx = take((size_t)E_pad * 8 * 8);  // zero between launches, like the counters
+  const size_t o_lfx = take((size_t)E_pad * 8 * 8);  // the bias between launches (reset by the last block)
   const size_t counters_end = off;
   const size_t o_status = take(16);
   const size_t o_stamps = take(2 * kNumStamps * 8);
+  const size_t o_lfx0 = take((size_t)E_pad * 8);
   const size_t o_ids = take((size_t)Tm * k * 4);
   const size_t o_gates = take((size_t)Tm * k * 4);
   const size_t o_pos = take((size_t)Tm * k * 4);
@@ -387,6 +389,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.d_cnt = reinterpret_cast<int*>(w + o_dcnt);
   sp.status = reinterpret_cast<int*>(w + o_status);
   sp.stamps = reinterpret_cast<unsigned long long*>(w + o_stamps);
+  sp.lfx0 = reinterpret_cast<const long long*>(w + o_lfx0);
   sp.lfx = reinterpret_cast<long long*>(w + o_lfx);
   sp.ids = reinterpret_cast<int*>(w + o_ids);
   sp.gates = reinterpret_cast<float*>(w + o_gates);
@@ -413,6 +416,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   // device limit, which bounds every layer's plan
   CK(small_t_configure(L_limbs, max_optin), "configure small-T kernel");
 
+  CK(small_t_init_logit_sums(sp, reinterpret_cast<long long*>(w + o_lfx0), st), "logit sums init");
   CK(cudaStreamSynchronize(st), "create sync");
   guard.keep = true;
   *out = L;
@@ -500,6 +504,8 @@ int moe_layer_status(moe_layer* L, void* stream) {
     // clear the word and every cross-CTA counter so the next call starts clean
     const size_t counters = reinterpret_cast<uint8_t*>(L->sp.status) - static_cast<uint8_t*>(L->ws);
     CK(cudaMemset(L->ws, 0, counters + 16), "status reset");
+    CK(small_t_init_logit_sums(L->sp, const_cast<long long*>(L->sp.lfx0), nullptr), "logit sums reset");
+    CK(cudaDeviceSynchronize(), "status reset sync");
     static const char* sites[] = {"?", "routing flag", "x records", "entry ready", "free stage", "full stage",
                                    "end marker", "copy drain"};
     const int site = (word[1] >= 0 && word[1] <= 7) ? word[1] : 0;

@@ -71,7 +71,7 @@ struct SmallParams {
   int e0, n_e;            // routed experts held by this layer: [e0, e0 + n_e) (all E unless sharded)
   int n_rg, n_ks, n_kt;   // router: row groups of 32 experts, 256-column repack blocks, 512-column tiles
   int n_rc;               // router: 128-column chunks (H / 128)
-  int Tp;                 // T rounded up to 4 (partial-logit row stride)
+  int Tp;                 // T rounded up to 4
   int n_gu, n_gu_sh;      // gate/up tiles per routed / shared entry (32 outputs each)
   int n_dt;               // down tiles per entry (128 outputs each; the unit of the combine)
   int n_sh;               // shared entries for this T
@@ -101,7 +101,8 @@ struct SmallParams {
   int* gu_cnt;       // [w_max]
   int* entry_ready;  // [w_max]
   int* d_cnt;        // [n_dt]
-  long long* lfx;    // [E_pad][Tp] router logits in units of 2^-32, summed with integer atomics
+  long long* lfx;    // [E_pad][8] router logits in units of 2^-32, summed with integer atomics from the bias
+  const long long* lfx0;  // [E_pad] the bias in units of 2^-32 (0 past E or without a bias): lfx's start
   int* ids;          // [T*k]
   float* gates;      // [T*k]
   int* pos;          // [T*k]

@@ -446,18 +446,18 @@ __device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
 
 // The k largest of one token's E logits by (value desc, index asc), one
 // warp, with the gates (softmax over the k selected logits, the sum by a
-// fixed shuffle tree), written in slot order.  Logit e is read from its
-// fixed-point sum (one rounding to fp32, an exact power-of-two scale, then
-// + bias; NaN counts as -inf).  Lane l holds experts l, l + 32, ... (NPER of
-// them) as 64-bit composites (order-preserving key of the value, then the
+// fixed shuffle tree), written in slot order.  Logit e is its fixed-point
+// sum (router slices plus the bias, in units of 2^-32) rounded once to fp32;
+// NaN counts as -inf.  Lane l holds experts l, l + 32, ... (NPER of them) as
+// 64-bit composites (order-preserving key of the value, then the
 // complemented index, so a larger composite is a larger value or, on equal
 // values, a lower index; 0 = none) and keeps its largest.  Each round takes
 // the exact maximum key over the lanes (a warp max); if several lanes hold
 // it, the lowest expert index among them wins (a second warp min, only
-// then).  The winning lane clears that expert and takes the tree maximum of
-// what it has left.  The rounds are a loop, not unrolled: this code runs
-// once per launch, so its size (instruction fetch) matters more than its
-// per-round cost.
+// then).  The winning lane writes the slot, clears that expert and takes the
+// tree maximum of what it has left.  The rounds are a loop, not unrolled:
+// this code runs once per launch, so its size (instruction fetch) matters
+// more than its per-round cost.
 template <int NPER>
 __device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
@@ -467,18 +467,16 @@ __device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? __ldcg(P.lfx + (int64_t)e * P.Tp + t) : 0ll;
+    v[i] = e < E ? __ldcg(P.lfx + (int64_t)e * kMaxSmallT + t) : 0ll;
   }
   uint64_t c[NPER];
 #pragma unroll
   for (int i = 0; i < NPER; ++i) {
     const int e = lane + 32 * i;
-    const float x = __ll2float_rn(v[i]) * 0x1p-32f + ((e < E && P.router_b) ? __ldg(P.router_b + e) : 0.f);
+    const float x = __ll2float_rn(v[i]) * 0x1p-32f;
     c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
   }
   uint64_t best = tree_max(c);
-  float l0 = 0.f, lv = 0.f;
-  int my_id = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
     const uint32_t key = (uint32_t)(best >> 32);
@@ -487,30 +485,24 @@ __device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids
     int wl = __ffs(holders) - 1;
     if (holders & (holders - 1u))
       wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
-    const int wi = (int)__shfl_sync(0xffffffffu, ~(uint32_t)best, wl);
-    const float val = key_value(m);
-    if (j == 0) l0 = val;
-    if (lane == j) {
-      my_id = wi;
-      lv = val;
-    }
     if (lane == wl) {
-      const int slot = wi >> 5;
+      const uint32_t wi = ~(uint32_t)best;
+      ids[j] = (int)wi;
+      vals[j] = key_value(m);
+      const int slot = (int)(wi >> 5);
 #pragma unroll
       for (int i = 0; i < NPER; ++i)
         if (i == slot) c[i] = 0ull;
       best = tree_max(c);
     }
   }
-  const float ex = lane < k ? expf(lv - l0) : 0.f;
+  __syncwarp();
+  const float l0 = vals[0];
+  const float ex = lane < k ? expf(vals[lane] - l0) : 0.f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    ids[lane] = my_id;
-    vals[lane] = lv;
-    gates[lane] = ex / sum;
-  }
+  if (lane < k) gates[lane] = ex / sum;
 }
 
 // Scratch of finalize_routing in the misc region (bytes, see finalize_misc_bytes).
@@ -865,12 +857,12 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       // through the routing, the routed tiles' records wait for)
       if (tid < T * 32) {
         // this slice's share of logit (t, expert 32 rg + r), added as an
-        // exact integer multiple of 2^-32: the total does not depend on the
-        // order in which the slices arrive
+        // exact integer multiple of 2^-32 to a sum that starts from the bias:
+        // the total does not depend on the order in which the slices arrive
         const int t = tid >> 5, r = tid & 31;
         float v = 0.f;
         for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
-        atomicAdd(reinterpret_cast<unsigned long long*>(P.lfx) + (int64_t)(d_rg * 32 + r) * P.Tp + t,
+        atomicAdd(reinterpret_cast<unsigned long long*>(P.lfx) + (int64_t)(d_rg * 32 + r) * kMaxSmallT + t,
                   (unsigned long long)__float2ll_rn(v * 4294967296.f));
       }
       // the barrier orders every thread's additions before thread 0's
@@ -1196,7 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.entry_ready[i] = 0;
     }
     for (int i = threadIdx.x; i < P.n_dt; i += blockDim.x) P.d_cnt[i] = 0;
-    for (int i = threadIdx.x; i < P.E_pad * P.Tp; i += blockDim.x) P.lfx[i] = 0;
+    // the logit sums start from the bias (2^-32 fixed point) for the next launch
+    for (int i = threadIdx.x; i < P.E_pad * kMaxSmallT; i += blockDim.x) P.lfx[i] = P.lfx0[i / kMaxSmallT];
     // this launch's phase stamps become the last completed launch's
     if (threadIdx.x < kNumStamps) {
       const unsigned long long v =
@@ -1219,6 +1212,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// The router logit sums' starting value: the bias in units of 2^-32 (exact
+// for |b| >= 2^-8, rounded to the nearest 2^-32 below that), written to the
+// table lfx0 and to every token column of lfx.
+__global__ void logit_sums_init_kernel(const float* __restrict__ bias, int E, int E_pad, long long* __restrict__ lfx0,
+                                       long long* __restrict__ lfx) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= E_pad * kMaxSmallT) return;
+  const int e = i / kMaxSmallT;
+  const long long v = (bias && e < E) ? __float2ll_rn(bias[e] * 4294967296.f) : 0ll;
+  lfx[i] = v;
+  if (i % kMaxSmallT == 0) lfx0[e] = v;
+}
+
+cudaError_t small_t_init_logit_sums(const SmallParams& P, long long* lfx0, cudaStream_t st) {
+  const int n = P.E_pad * kMaxSmallT;
+  logit_sums_init_kernel<<<(n + 255) / 256, 256, 0, st>>>(P.router_b, P.E, P.E_pad, lfx0, P.lfx);
+  return cudaGetLastError();
+}
+
 int small_t_smem_bytes(const SmallParams& P) {
   return smem_plan(P.n_stages, P.ring_bytes, P.misc_bytes, P.w_max).total;
 }

@@ -25,7 +25,8 @@
  *     fp32 mode).  Every block product is therefore exact, and block sums are
  *     scaled and accumulated in fp32.
  *   - The router logits are fp32 sums over 512-column slices, added across
- *     slices exactly (as integer multiples of 2^-32) and rounded once.
+ *     slices and to the bias exactly (as integer multiples of 2^-32) and
+ *     rounded once.
  *   - The same inputs give the same output bits on every call.
  *   - T > 8: weights are dequantised to bf16; bf16 tensor-core products with
  *     fp32 accumulation.
