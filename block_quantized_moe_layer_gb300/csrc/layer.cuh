@@ -102,6 +102,7 @@ struct SmallParams {
   int* entry_ready;  // [w_max]
   int* d_cnt;        // [n_dt]
   long long* lfx;    // [E_pad][8] router logits in units of 2^-32, summed with integer atomics from the bias
+                     // (restored to the bias by the routing block once it has read them)
   const long long* lfx0;  // [E_pad] the bias in units of 2^-32 (0 past E or without a bias): lfx's start
   int* ids;          // [T*k]
   float* gates;      // [T*k]

@@ -709,6 +709,16 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
     for (int b = tid; b < P.n_dt; b += NT)
       if (atom_add_acq_rel(&P.d_cnt[b], 1) == last) pend[1 + atomicAdd(&pend[0], 1)] = b;
   }
+  // The logit sums were read by this block only (the top-k, above): restore
+  // them to their starting value (the bias) for the next launch now, off the
+  // launch's tail.  Thread i takes experts i, i + 256, ...: one read of the
+  // bias table, then the expert's 8 token columns.
+  for (int e = tid; e < P.E_pad; e += NT) {
+    const long long v = P.lfx0[e];
+    longlong2* row = reinterpret_cast<longlong2*>(P.lfx + (int64_t)e * kMaxSmallT);
+#pragma unroll
+    for (int q = 0; q < kMaxSmallT / 2; ++q) row[q] = make_longlong2(v, v);
+  }
   // what only the combine and moe_get_routing read
   if (tid < Tk) {
     P.ids[tid] = sid[tid];
@@ -1188,8 +1198,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.entry_ready[i] = 0;
     }
     for (int i = threadIdx.x; i < P.n_dt; i += blockDim.x) P.d_cnt[i] = 0;
-    // the logit sums start from the bias (2^-32 fixed point) for the next launch
-    for (int i = threadIdx.x; i < P.E_pad * kMaxSmallT; i += blockDim.x) P.lfx[i] = P.lfx0[i / kMaxSmallT];
     // this launch's phase stamps become the last completed launch's
     if (threadIdx.x < kNumStamps) {
       const unsigned long long v =
