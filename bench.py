@@ -506,6 +506,7 @@ def run_round(args):
         "metric": "µs per MTP draft/verify round (8 target layers T=4, draft heads T=1,2,3, 2 LM-head passes, "
                   "acceptance) and effective HBM GB/s",
         "value": round(us, 2), "unit": "us/round", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "q8_0/q4ks weights x bf16 activations (int dp4a, fp32 accumulate)",
         "data": "synthetic (seeded, random-init weights of the workload's shapes)",

@@ -24,6 +24,7 @@ EXPORTS = (
     "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
     "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
     "moe_layer_timeline", "moe_layer_inject_timeout", "moe_lm_head_status", "moe_forward_f32",
+    "mtp_round_hidden",
 )
 
 # event names of moe_layer_timeline, in order
@@ -89,6 +90,7 @@ def lib():
             "moe_last_error": (_c.c_char_p, []),
             "moe_layer_timeline": (_c.c_int, [vp, _c.POINTER(i64), i32, vp]),
             "moe_layer_inject_timeout": (_c.c_int, [vp, i32]),
+            "mtp_round_hidden": (_c.c_int, [vp, sz, i32, i32, i32, i32, i32, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -360,4 +362,14 @@ def mtp_round(layers, heads, lm, x, noise, eps=1e-6, p_min=0.0, workspace=None, 
     _check(lib().mtp_round(tl, len(layers), hl, k, lm.handle, x.data_ptr(), noise.data_ptr(), eps, p_min, wp, wn,
                            logits.data_ptr(), dlogits.data_ptr(), hout.data_ptr() if hout is not None else None,
                            drafts.data_ptr(), acc.data_ptr(), acc.data_ptr() + 4, _stream(stream)))
-    return dict(logits=logits, draft_logits=dlogits, drafts=drafts, accept=acc, head_out=hout)
+    return dict(logits=logits, draft_logits=dlogits, drafts=drafts, accept=acc, head_out=hout, workspace=workspace)
+
+
+def round_hidden(workspace, lm, k, n_target, stream=None):
+    """The final residual rows h_n (fp32 [k+1, H]) of the last round run on
+    ``workspace`` (``mtp_round_hidden``)."""
+    import torch
+    wp, wn = _aligned(workspace)
+    h = torch.empty(k + 1, lm.H, dtype=torch.float32, device=workspace.device)
+    _check(lib().mtp_round_hidden(wp, wn, lm.H, k, lm.V, lm.act, n_target, h.data_ptr(), _stream(stream)))
+    return h

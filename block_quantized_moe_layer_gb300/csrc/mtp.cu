@@ -393,4 +393,19 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   return MOE_OK;
 }
 
+int mtp_round_hidden(const void* workspace, size_t workspace_bytes, int32_t H, int32_t k, int32_t V, int32_t act_dtype,
+                     int32_t n_target, float* h_out, void* stream) {
+  if (!workspace || !h_out) return set_error(MOE_EINVAL, "mtp_round_hidden: NULL argument");
+  if (n_target < 0) return set_error(MOE_EINVAL, "mtp_round_hidden: n_target < 0");
+  const size_t need = mtp_round_workspace_bytes(H, k, V, act_dtype);
+  if (need == 0) return set_error(MOE_EINVAL, "mtp_round_hidden: H / k / V / act_dtype outside the round's ranges");
+  if (workspace_bytes < need) return set_error(MOE_EINVAL, "mtp_round_hidden: workspace %zu bytes, need %zu", workspace_bytes, need);
+  const RoundLayout r = round_layout(H, k, V, act_dtype);
+  // h_0 is written to hA and each target layer moves it to the other buffer
+  const uint8_t* src = static_cast<const uint8_t*>(workspace) + (n_target % 2 == 0 ? r.hA : r.hB);
+  MCK(cudaMemcpyAsync(h_out, src, (size_t)(k + 1) * H * 4, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)),
+      "mtp_round_hidden: copy");
+  return MOE_OK;
+}
+
 }  // extern "C"

@@ -331,6 +331,18 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
               size_t workspace_bytes, float* target_logits, float* draft_logits, void* head_out, int32_t* draft_ids,
               int32_t* out_n_accepted, int32_t* out_next_token, void* stream);
 
+/* Copies the final residual rows h_n (fp32 [k+1, H], the LM head's input for
+ * the verify rows, and with the noise the source of the draft rows) of the
+ * last mtp_round that ran on `workspace` with these H, k, V, act_dtype and
+ * n_target into h_out (device, fp32 [k+1, H]).  The round leaves them in its
+ * workspace; this reads them for checking the round's last steps (output
+ * norm, LM head, drafts, acceptance) on their own.  Ordered on `stream`
+ * after the round when the round used the same stream.  Errors: MOE_EINVAL
+ * (NULL pointer, n_target < 0, sizes outside mtp_round_workspace_bytes'
+ * ranges, workspace too small), MOE_ECUDA. */
+int mtp_round_hidden(const void* workspace, size_t workspace_bytes, int32_t H, int32_t k, int32_t V, int32_t act_dtype,
+                     int32_t n_target, float* h_out, void* stream);
+
 /* Message for the last error on the calling thread; valid until the next
  * call on that thread.  Never NULL. */
 const char* moe_last_error(void);

@@ -17,12 +17,20 @@ XDT = {pkg.ACT_BF16: torch.bfloat16, pkg.ACT_F32: torch.float32}
 TOL = {pkg.ACT_BF16: 2e-2, pkg.ACT_F32: 1e-3}
 # Router margin below which a layer's expert choice for a token may differ
 # between the GPU chain and the fp64 oracle chain: the GPU's hidden state
-# carries the rounding of every earlier layer (bf16: ~2^-8 relative per
-# element), so its router logits differ from the oracle's by far more than
-# within one layer.  A token whose top-k boundary margin is below this in any
-# layer is reported and left out of the value comparisons (the per-layer
-# near-tie rule, widened to the chain's input perturbation).
-CHAIN_TIE = {pkg.ACT_BF16: 5e-2, pkg.ACT_F32: 1e-4}
+# carries the error of every earlier layer, so its router logits differ from
+# the oracle's by more than within one layer.  A token whose top-k boundary
+# margin is below this in any layer is reported and left out of the value
+# comparisons (the per-layer near-tie rule, widened to the chain's input
+# perturbation).  The margin is twice the bound that
+# test_mtp_round_teacher_forced_layers asserts on the chain's router-logit
+# drift (the oracle's router logits at the GPU chain's layer inputs against
+# those at the oracle chain's), measured on the full-size round:
+#   fp32: 1.9e-6 after 8 layers (layer errors ~2e-7 add up) -> bound 5e-6;
+#   bf16: 1.46e-2 -- each layer input is rounded to bf16, and where the two
+#   chains differ by ~1e-4 (the 16-bit records' error) that rounding moves
+#   a few percent of the elements by one bf16 step (2^-8 relative), ~3e-3 of
+#   router logit per layer -> bound 2.5e-2.
+CHAIN_TIE = {pkg.ACT_BF16: 5e-2, pkg.ACT_F32: 1e-5}
 # the oracle round in the same precision at the layer inputs: bf16 layers
 # take bf16 values, so in bf16 mode the oracle rounds them too (its routing
 # decisions then see the inputs the kernels see); outputs and the residual
@@ -190,20 +198,72 @@ def full_round_gpu(request):
 
 def test_mtp_round_full_size_acceptance(full_round_gpu, full_round_oracle):
     """The full-size round ("Support Step3.5/3.7 flash mtp3", "Overview",
-    Round 1 steps 1-5) on several input variants: the accepted count and the
-    next token equal the oracle's on every round whose deciding rows are
-    decided, and at least 3 rounds must be decided."""
+    Round 1 steps 1-5) end to end against the oracle round on the same inputs,
+    on several input variants: the accepted count and the next token equal
+    the oracle's on every round whose deciding rows are decided.  fp32: at
+    least 3 of at most 6 rounds must be decided.  bf16: the two chains part
+    at the bf16 rounding of every layer input (logits ~3e-3 apart after 8
+    layers, against top-1 margins of that order), so few rounds are decided
+    end to end; there the decided ones are asserted and the count is taken
+    by test_mtp_round_acceptance_from_round_hidden, which starts the oracle
+    from the round's own final hidden rows."""
     from tests._oracle_pool import OraclePool
     act, gpu = full_round_gpu
     r, ol_layers, ol_heads, ol_lm = full_round_oracle
     decided = []
+    n_var = 6 if act == pkg.ACT_F32 else 3
     with OraclePool() as pool:
-        for variant in range(6):
+        for variant in range(n_var):
             decided.append(_check_round(r, act, print, variant, pool, ol_layers, ol_heads, ol_lm, gpu=gpu))
             if sum(decided) >= 3 and len(decided) >= 4:
                 break
     print(f"mtp_round act={act}: {sum(decided)} of {len(decided)} rounds decided and asserted")
-    assert sum(decided) >= 3
+    if act == pkg.ACT_F32:
+        assert sum(decided) >= 3
+
+
+def test_mtp_round_acceptance_from_round_hidden(full_round_gpu, full_round_oracle):
+    """The round's last steps ("Support Step3.5/3.7 flash mtp3", "Overview",
+    steps 3-5: output norm and LM head on the verify rows, the draft rows and
+    their tokens, greedy acceptance) teacher-forced: the oracle starts from
+    the final residual rows h_n the GPU round itself produced
+    (mtp_round_hidden) and must give the same drafts, accepted count and next
+    token on every decided round; at least 3 of at least 4 rounds decided,
+    in both act dtypes.  The target stack that leads to h_n is held to the
+    oracle layer by layer in test_mtp_round_teacher_forced_layers."""
+    from tests._oracle_pool import OraclePool
+    act, (layers, heads, lm) = full_round_gpu
+    r, _, ol_heads, ol_lm = full_round_oracle
+    ws = pkg.round_workspace(lm.H, r.k, lm.V, lm.act, "cuda")
+    decided = []
+    with OraclePool() as pool:
+        fwd = pool.layer_forward({id(o): w for o, w in zip(ol_heads, r.heads)})
+        for variant in range(6):
+            x, noise = synth.round_inputs(r, "cuda", variant=variant)
+            out = pkg.mtp_round(layers, heads, lm, x.to(XDT[act]), noise, workspace=ws)
+            h = pkg.round_hidden(ws, lm, r.k, len(layers))
+            torch.cuda.synchronize()
+            logits, dlogits = to_np(out["logits"]), to_np(out["draft_logits"])
+            drafts = out["drafts"].cpu().tolist()
+            n_gpu, next_gpu = out["accept"].cpu().tolist()
+            # the oracle's round with no target layers on h_n is steps 3-5 from h_n
+            ref = omtp.mtp_round(to_np(h), [], ol_heads, ol_lm, to_np(noise), layer_forward=fwd, act=OACT[act])
+            scale = np.abs(ref["logits"]).max()
+            assert np.abs(logits - ref["logits"]).max() / scale < 1e-3
+            assert np.abs(dlogits - ref["draft_logits"]).max() / scale < 1e-3
+            row_dec = _rows_decided(ref["logits"], logits)
+            dr_dec = _rows_decided(ref["draft_logits"], dlogits)
+            n_ref = ref["n_accepted"]
+            ok = bool(row_dec[: n_ref + 1].all() and dr_dec[: min(n_ref + 1, r.k)].all())
+            if ok:
+                assert (n_gpu, next_gpu) == (n_ref, ref["next_token"]), (variant, n_gpu, next_gpu, n_ref)
+                assert drafts[: min(n_ref + 1, r.k)] == ref["drafts"][: min(n_ref + 1, r.k)]
+            decided.append(ok)
+            print(f"round from h_n act={act} variant {variant}: n_accepted gpu {n_gpu} oracle {n_ref}, next "
+                  f"{next_gpu}/{ref['next_token']}, {'decided, asserted' if ok else 'not decided'}")
+            if sum(decided) >= 3 and len(decided) >= 4:
+                break
+    assert sum(decided) >= 3 and len(decided) >= 4, decided
 
 
 def _rms(h, eps=1e-6):
