@@ -14,14 +14,6 @@
 
 namespace moe {
 
-__device__ __forceinline__ uint32_t field6(uint32_t w0, uint32_t w1, uint32_t w2, int f) {
-  const int p = 6 * f;
-  const int wi = p >> 5, sh = p & 31;
-  const uint32_t lo = wi == 0 ? w0 : (wi == 1 ? w1 : w2);
-  const uint32_t hi = wi == 0 ? w1 : (wi == 1 ? w2 : 0u);
-  return __funnelshift_r(lo, hi, sh) & 63u;
-}
-
 // Integer dot product of one 32-weight Q8_0 block (codes q0 | q1) with one
 // activation record: four independent dp4a chains of four, then the limbs
 // combined exactly (L = 2) or in fp32 (L = 4).
@@ -80,14 +72,6 @@ __device__ __forceinline__ void q4_unpack(const uint4 qv, uint32_t (&w)[8]) {
   w[6] = qv.w & 0x0F0F0F0Fu; w[7] = (qv.w >> 4) & 0x0F0F0F0Fu;
 }
 
-// a = d * sc[s], b = dmin * m[s] of sub-block s from a 16-byte superblock header
-__device__ __forceinline__ void q4_scales(const uint4 hd, int s, float& a, float& b) {
-  const float dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-  const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-  a = dd * (float)field6(hd.y, hd.z, hd.w, s);
-  b = dmin * (float)field6(hd.y, hd.z, hd.w, 8 + s);
-}
-
 // One chunk.  Lane l owns row l of the chunk; warp w owns blocks w, w + 8,
 // ... (a warp load of one block's 16-byte pieces covers the 32 rows in 512
 // contiguous bytes; the block's activation records are a broadcast read, one
@@ -113,13 +97,27 @@ __device__ __forceinline__ void gemv_chunk_m(const uint8_t* stage, const uint8_t
       }
     }
   } else {  // MOE_Q4KS
+    // Warp w takes blocks w, w + 8, ...: always sub-block w of a 256-column
+    // superblock (a chunk is whole superblocks), so where its two 6-bit
+    // fields sit in the header -- sc at bit 6w, m at bit 48 + 6w of the
+    // 96-bit field stream -- is fixed for the whole loop.
+    static_assert(kBlocksPerStep == 8, "one sub-block per warp");
     const uint8_t* hdr = stage + nbc * 512;
+    const uint32_t sh_sc = (uint32_t)(6 * warp) & 31u, sh_m = (uint32_t)(48 + 6 * warp) & 31u;
+    const bool sc_low = warp <= 5, m_low = warp <= 2;  // field starts in the first word of its pair
 #pragma unroll 2
     for (int b = warp; b < nbc; b += kBlocksPerStep) {
       const uint4 qv = *reinterpret_cast<const uint4*>(stage + ((int64_t)b * kRows + lane) * 16);
       const uint4 hd = *reinterpret_cast<const uint4*>(hdr + ((b >> 3) * kRows + lane) * 16);
-      float sa, sb;
-      q4_scales(hd, b & 7, sa, sb);
+      const float dd = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+      const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+      const uint32_t sc = __funnelshift_r(sc_low ? hd.y : hd.z, sc_low ? hd.z : hd.w, sh_sc) & 63u;
+      const uint32_t mm = __funnelshift_r(m_low ? hd.z : hd.w, m_low ? hd.w : 0u, sh_m) & 63u;
+      // a = d * sc, b = dmin * m, exact in fp32 (11 x 6 significant bits):
+      // 2^23 + v is the float with bits 0x4B000000 | v, and one fma removes
+      // the 2^23 term with a single (exact) rounding
+      const float sa = fmaf(dd, __uint_as_float(0x4B000000u | sc), -dd * 8388608.f);
+      const float sb = fmaf(dmin, __uint_as_float(0x4B000000u | mm), -dmin * 8388608.f);
       uint32_t w[8];
       q4_unpack(qv, w);
 #pragma unroll
