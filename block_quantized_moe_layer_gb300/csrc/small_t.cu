@@ -22,13 +22,15 @@
 //                    The last router tile to finish computes the routing
 //                    (top-k, gates, permutation, expert work entries).
 //   shared gate/up   32 outputs (16+16 gate/up rows, twice) x full K
-//   shared down      128 outputs x full I
 //   routed gate/up   per routed work entry (<= 4 tokens of one expert)
+//   shared down      128 outputs x full I
 //   routed down
-// The router tiles and the shared gate/up tiles go to blocks 0, 1, ... by
-// block index, and each of those blocks starts loading its item's weights
-// before it waits for the previous kernel in the stream; every later item is
-// claimed from a global queue.
+// Every item is claimed from one global queue.  A down tile's producer waits
+// for its inputs (the entry's gate/up outputs) before it copies them, so the
+// shared down tiles come after the routed gate/up ones: claimed earlier they
+// would hold their producers (and leave their rings empty) until the shared
+// gate/up finishes.  Before it waits for the previous kernel in the stream,
+// block i warms L2 with router tile i's weights (constant data).
 // Hand-offs use last-arriver counters: the last gate/up tile of an entry
 // publishes it (its activation records are complete); the last down tile of
 // a 128-row block combines that block of y in slot order.  No floating-point
@@ -287,10 +289,6 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
     } else if (t < NR + NSG) {
       entry = (t - NR) / P.n_gu_sh;
       rbt = (t - NR) % P.n_gu_sh;
-    } else if (t < NR + NSG + NSD) {
-      kind = kDown;
-      entry = (t - NR - NSG) / NDT;
-      rbt = (t - NR - NSG) % NDT;
     } else {
       if (n_rent < 0) {
         if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t)) {
@@ -309,15 +307,23 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
           if (!mbar_wait_bounded(ebar, 0, P.timeout_ns, P.status, kSiteEntry, -1)) { ok = false; break; }
         }
       }
-      const int A = NR + NSG + NSD;
+      // routed gate/up, then the shared expert's down tiles (claimed once
+      // every routed gate/up tile is, by when the shared gate/up outputs are
+      // long written: a down tile claimed before its inputs exist would hold
+      // its producer until they do), then routed down
+      const int A = NR + NSG;
       const int NG = n_rent * P.n_gu, ND = n_rent * NDT;
       if (t < A + NG) {
         entry = P.n_sh + (t - A) / P.n_gu;
         rbt = (t - A) % P.n_gu;
-      } else if (t < A + NG + ND) {
+      } else if (t < A + NG + NSD) {
         kind = kDown;
-        entry = P.n_sh + (t - A - NG) / NDT;
+        entry = (t - A - NG) / NDT;
         rbt = (t - A - NG) % NDT;
+      } else if (t < A + NG + NSD + ND) {
+        kind = kDown;
+        entry = P.n_sh + (t - A - NG - NSD) / NDT;
+        rbt = (t - A - NG - NSD) % NDT;
       } else {
         stamp_last(P.stamps, kTsLastIssue);
         break;  // queue exhausted
