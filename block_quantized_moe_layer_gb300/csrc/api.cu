@@ -242,15 +242,21 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
 
   CK(cudaGetDevice(&L->dev), "cudaGetDevice");
   CK(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->dev), "SM count");
-  // chunk sizes: the largest that let the shared-memory ring hold two stages
+  // chunk sizes: the largest that let the shared-memory ring hold two
+  // stages as they usually come, and any stage at all.  A stage is one
+  // weight chunk plus the activation records of its tokens.  Routed entries
+  // of the verify batch almost always hold one token (T tokens spread over
+  // T*k of E experts), so routed stages are double-buffered at one token and
+  // only have to fit the ring once at kGroup tokens; the shared expert
+  // always carries a full token group.
   int max_optin = 0;
   CK(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->dev), "smem attr");
   const int L_limbs = d->act_dtype == MOE_ACT_BF16 ? 2 : 4;
   const int RB = rec_bytes(L_limbs);
-  auto stage_need = [&](int f, Chunking ch) {
-    return chunk_bytes(f, ch.Kc) + (int64_t)kGroup * (ch.Kc / 32) * RB;
+  auto stage_need = [&](int f, Chunking ch, int tokens) {
+    return chunk_bytes(f, ch.Kc) + (int64_t)tokens * (ch.Kc / 32) * RB;
   };
-  int64_t stage = 0;
+  int64_t stage = 0, single = 0;  // the double-buffered stage, the largest stage
   for (int shift = 0; shift < 6; ++shift) {
     L->gu_ch = choose_chunking(fmt, d->H, shift);
     L->dn_ch = choose_chunking(fmt, d->I, shift);
@@ -263,14 +269,17 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
     // a router stage: room for one tile's weights (512 columns) and its x slice
     stage = kRouterTileChunks * chunk_bytes(MOE_F32, kRouterCc) +
             (int64_t)std::min(d->T_max, kMaxSmallT) * kRouterTileChunks * kRouterCc * (L_limbs == 2 ? 2 : 4);
-    stage = std::max(stage, stage_need(fmt, L->gu_ch));
-    stage = std::max(stage, stage_need(fmt, L->dn_ch));
+    single = stage;
+    stage = std::max(stage, stage_need(fmt, L->gu_ch, 1));
+    stage = std::max(stage, stage_need(fmt, L->dn_ch, 1));
+    single = std::max({single, stage_need(fmt, L->gu_ch, kGroup), stage_need(fmt, L->dn_ch, kGroup)});
     if (has_sh) {
-      stage = std::max(stage, stage_need(sfmt, L->sgu_ch));
-      stage = std::max(stage, stage_need(sfmt, L->sdn_ch));
+      stage = std::max({stage, stage_need(sfmt, L->sgu_ch, kGroup), stage_need(sfmt, L->sdn_ch, kGroup)});
+      single = std::max(single, stage);
     }
     stage = align_up(stage, 128);
-    if (2 * stage + 40 * 1024 <= max_optin) break;
+    single = align_up(single, 128);
+    if (2 * stage + 40 * 1024 <= max_optin && single + 40 * 1024 <= max_optin) break;
   }
   const int n_rg = (d->E + 31) / 32, n_ks = d->H / kRouterKc;
   const int E_pad = n_rg * 32;
@@ -409,8 +418,9 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.ring_bytes = 0;
   const int fixed = small_t_smem_bytes(sp);
   sp.ring_bytes = (int)((max_optin - fixed) / 128 * 128);
-  if (sp.ring_bytes < 2 * stage)
-    return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has (stage %lld B)", (long long)stage);
+  if (sp.ring_bytes < 2 * stage || sp.ring_bytes < single)
+    return fail(MOE_EINVAL, "layer shapes need more shared memory than the device has (stage %lld B, largest %lld B)",
+                (long long)stage, (long long)single);
   L->smem_bytes = small_t_smem_bytes(sp);
   // the attribute belongs to the kernel, not to this layer: set it to the
   // device limit, which bounds every layer's plan

@@ -25,7 +25,7 @@
 //   routed gate/up   per routed work entry (<= 4 tokens of one expert)
 //   shared down      128 outputs x full I
 //   routed down
-// Every item is claimed from one global queue.  A down tile's producer waits
+// Block b takes item b; every later item is claimed from one global queue.  A down tile's producer waits
 // for its inputs (the entry's gate/up outputs) before it copies them, so the
 // shared down tiles come after the routed gate/up ones: claimed earlier they
 // would hold their producers (and leave their rings empty) until the shared
@@ -280,9 +280,13 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
 
   const uint64_t wpol = l2_evict_first_policy();  // weights are read once per launch
   bool st_gu = false, st_dn = false;               // first routed gate/up / down copy stamped
-  int t = atomicAdd(&P.sync->queue, 1);
+  // Block b's first item is item b; later items are claimed from the
+  // counter (offset by the grid), one ahead, so the claim's latency overlaps
+  // the current item.  Claims on the one counter are served one at a time,
+  // so the launch's first items, needed by every block at once, skip it.
+  int t = blockIdx.x;
   while (ok) {
-    const int t_next = atomicAdd(&P.sync->queue, 1);  // claim one ahead: its latency overlaps this item
+    const int t_next = (int)gridDim.x + atomicAdd(&P.sync->queue, 1);
     int kind = kGateUp, entry = 0, rbt = 0;
     if (t < NR) {
       kind = kRouter;
