@@ -82,7 +82,7 @@ __device__ void lm_consume(const LmParams& P, uint8_t* smem, const LmPlan& plan,
       const int s = i % P.stages;
       if (!lm_wait(&full[s], (uint32_t)((i / P.stages) & 1), P, 2)) return;
       gemv_chunk_m<2, T>(smem + plan.ring + (int64_t)s * P.chunk, recs + (int64_t)c * T * nbc * kLmRecB, nbc, MOE_Q8_0,
-                         acc);
+                         0, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }

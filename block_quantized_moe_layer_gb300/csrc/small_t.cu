@@ -917,7 +917,7 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
 #pragma unroll
           for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
         }
-        gemv_chunk<L>(stage + j * cb, recs, d.nbc, d.fmt, d.M, acc);
+        gemv_chunk<L>(stage + j * cb, recs, d.nbc, d.fmt, j, d.M, acc);
         if (j == gps - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
