@@ -2,7 +2,7 @@
 //
 // One persistent CTA per SM (512 threads) claims work items from a global
 // queue.  An item multiplies one 128-row tile of a block-quantized weight
-// matrix (dequantised to bf16) by the bf16 activations of one token tile
+// matrix (dequantised to fp16) by the fp16 activations of one token tile
 // (n_pad <= 64 tokens), accumulating in fp32 in tensor memory (TMEM).
 //   warp 0      producer: 1-D bulk copies of raw weight stages (A ring) and
 //               activation K-slices (B ring);
@@ -10,7 +10,7 @@
 //               (M = 128, N = n_pad, K = 16, A from TMEM, B from shared memory);
 //   warps 4-11  dequantise, as two groups of four warps that take alternate A
 //               stages: thread (group, row r) turns its row's weights of the
-//               stage into bf16 pairs and stores them to TMEM;
+//               stage into fp16 pairs and stores them to TMEM;
 //   warps 12-15 epilogue: read the accumulator (double-buffered) and write
 //               SwiGLU outputs (gate/up), bf16 partial outputs z (down) or fp32
 //               router logits.
@@ -131,25 +131,8 @@ __device__ __forceinline__ uint64_t pack2(float a) {
   return ((uint64_t)u << 32) | u;
 }
 
-// Two Q8_0 codes held as the fp32 bit patterns 2^23 + 128 + q (the code byte
-// with its sign bit flipped, placed under the exponent of 2^23): subtracting
-// 2^23 + 128 gives q exactly, q * d is exact in fp32 (8 x 11 significant
-// bits), and the only rounding is the conversion to bf16.  Packed f32x2 math.
-__device__ __forceinline__ uint32_t q8_pair(uint32_t m0, uint32_t m1, uint64_t c2, uint64_t d2) {
-  uint32_t out;
-  asm("{\n\t.reg .b64 x;\n\t.reg .b32 lo, hi;\n\t"
-      "mov.b64 x, {%1, %2};\n\t"
-      "sub.rn.f32x2 x, x, %3;\n\t"
-      "mul.rn.f32x2 x, x, %4;\n\t"
-      "mov.b64 {lo, hi}, x;\n\t"
-      "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
-      : "=r"(out)
-      : "r"(m0), "r"(m1), "l"(c2), "l"(d2));
-  return out;
-}
-
 // Two Q4KS codes as 2^23 + q: w = a*q - b with one fp32 rounding (as the
-// format defines it), then bf16.
+// format defines it), then fp16.
 __device__ __forceinline__ uint32_t q4_pair(uint32_t m0, uint32_t m1, uint64_t c2, uint64_t a2, uint64_t nb2) {
   uint32_t out;
   asm("{\n\t.reg .b64 x;\n\t.reg .b32 lo, hi;\n\t"
@@ -157,26 +140,34 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t m0, uint32_t m1, uint64_t c
       "sub.rn.f32x2 x, x, %3;\n\t"
       "fma.rn.f32x2 x, x, %4, %5;\n\t"
       "mov.b64 {lo, hi}, x;\n\t"
-      "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+      "cvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
       : "=r"(out)
       : "r"(m0), "r"(m1), "l"(c2), "l"(a2), "l"(nb2));
   return out;
 }
 
-// 32 Q8_0 codes (8 words) of one block with scale d -> 16 bf16 pairs.
-__device__ __forceinline__ void dq_q8(const uint4& a, const uint4& b, float d, uint32_t (&v)[16]) {
+// 32 Q8_0 codes (8 words; the LT copy holds each code byte with its sign bit
+// flipped, u = q + 128) of one block with fp16 scale d -> 16 fp16 pairs.
+// A byte permute places u under the fp16 exponent of 1024 (0x64uu = 1024 + u),
+// subtracting 1152 gives q exactly, and the multiply by d rounds once:
+// fp16(q * d).
+__device__ __forceinline__ void dq_q8(const uint4& a, const uint4& b, uint32_t d2, uint32_t (&v)[16]) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  const uint64_t c2 = pack2(8388736.f), d2 = pack2(d);
+  const __half2 c = __half2half2(__ushort_as_half((unsigned short)0x6480u));  // 1152
+  const __half2 dd = *reinterpret_cast<const __half2*>(&d2);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t f = w[i] ^ 0x80808080u;
-    v[2 * i] = q8_pair(__byte_perm(f, 0x4B000000u, 0x7440), __byte_perm(f, 0x4B000000u, 0x7441), c2, d2);
-    v[2 * i + 1] = q8_pair(__byte_perm(f, 0x4B000000u, 0x7442), __byte_perm(f, 0x4B000000u, 0x7443), c2, d2);
+    uint32_t lo = __byte_perm(w[i], 0x64646464u, 0x5140), hi = __byte_perm(w[i], 0x64646464u, 0x7362);
+    const __half2 ql = __hsub2(*reinterpret_cast<const __half2*>(&lo), c);
+    const __half2 qh = __hsub2(*reinterpret_cast<const __half2*>(&hi), c);
+    const __half2 xl = __hmul2(ql, dd), xh = __hmul2(qh, dd);
+    v[2 * i] = *reinterpret_cast<const uint32_t*>(&xl);
+    v[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&xh);
   }
 }
 
 // 32 Q4KS codes of one sub-block (16 bytes, weight 2j in the low nibble of
-// byte j) -> 16 bf16 pairs of a*q - b.
+// byte j) -> 16 fp16 pairs of a*q - b.
 __device__ __forceinline__ void dq_q4(const uint4& c, float a, float b, uint32_t (&v)[16]) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   const uint64_t c2 = pack2(8388608.f), a2 = pack2(a), nb2 = pack2(-b);
@@ -404,7 +395,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         const uint32_t sb = nt % kNB;
         if (!wait1(&bfull[sb], (nt / kNB) & 1, abort, p, kSiteFull, (int)nt)) break;
         tc::fence_after();
-        const uint32_t idesc = tc::idesc_bf16(kLtRows, d.n_pad);
+        const uint32_t idesc = tc::idesc_f16(kLtRows, d.n_pad);
         const uint32_t bsm = smem_u32(sm + kOffB + sb * kBSlot);
         const uint32_t lbo = (uint32_t)d.n_pad * 16;
         for (int j = 0; j < d.nk; ++j) {
@@ -453,7 +444,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         // up to 4 blocks (two 64-column K-blocks x two halves)
         const int nb = d.cols / 32;
         uint4 c[4][2];
-        float sc[4];
+        uint32_t sc[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           if (b < nb) {
@@ -461,7 +452,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
             const int h = b & 1;
             c[b][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
             c[b][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
-            sc[b] = __half2float(*reinterpret_cast<const __half*>(kbp + 8192 + (h * 128 + r) * 2));
+            const uint32_t h16 = *reinterpret_cast<const unsigned short*>(kbp + 8192 + (h * 128 + r) * 2);
+            sc[b] = h16 | (h16 << 16);
           }
         }
         __syncwarp();
@@ -518,7 +510,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         }
         if (!good) break;
       } else {
-        // router plane: 64 columns of bf16, copied as they are
+        // router plane: 64 columns of fp16, copied as they are
         uint32_t v[2][16];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -568,8 +560,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
             const float u = __shfl_down_sync(0xffffffffu, gt, 16);
             if (lane < 16) {
               const float hv = gt / (1.f + expf(-gt)) * u;
-              *reinterpret_cast<__nv_bfloat16*>(stg + ((lane >> 3) * info.n_pad + c + m) * 16 + (lane & 7) * 2) =
-                  __float2bfloat16_rn(hv);
+              *reinterpret_cast<__half*>(stg + ((lane >> 3) * info.n_pad + c + m) * 16 + (lane & 7) * 2) =
+                  __float2half_rn(hv);
             }
           }
         } else if (info.kind == kItemDN) {

@@ -3,15 +3,16 @@
 // The steps of the layer (router, top-k and gates, permutation, SwiGLU
 // experts, combine; see the layer definition in moe_layer.h) run as a
 // sequence of launches on the caller's stream:
-//   1. lt_prep    : x -> token tiles of the shared expert / router (bf16 MMA
+//   1. lt_prep    : x -> token tiles of the shared expert / router (fp16 MMA
 //                   operand image), the work lists that need no routing;
-//   2. GEMM       : router logits (three bf16 planes of the fp32 router, so
-//                   the logits keep fp32 accuracy) + shared-expert gate/up;
+//   2. GEMM       : router logits (three scaled fp16 planes of the fp32
+//                   router, so the logits keep fp32 accuracy) + shared-expert
+//                   gate/up;
 //   3. lt_topk    : per token top-k (descending, ties to the lower index) and
 //                   renormalised gates;
 //   4. lt_perm    : histogram, scan, stable scatter -> offsets, perm, pos,
 //                   routed token tiles and the remaining work lists;
-//   5. lt_gather  : routed token tiles' activations (operand image);
+//   5. lt_gather  : routed token tiles' activations (fp16 operand image);
 //   6. GEMM       : routed gate/up + SwiGLU;
 //   7. GEMM       : routed and shared down projections -> z (bf16);
 //   8. lt_combine : y[t] = sum_j g[t,j] z[pos[t,j]] + z[shared t], in slot order.
@@ -88,7 +89,7 @@ __global__ void lt_repack_q8_kernel(const uint8_t* __restrict__ src, uint8_t* __
   for (int p = 0; p < 2; ++p) {
     uint8_t* q = chunk + ((h * 2 + p) * 128 + r) * 16;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = s[2 + 16 * p + j];
+    for (int j = 0; j < 16; ++j) q[j] = s[2 + 16 * p + j] ^ 0x80;  // u = q + 128 (sign bit flipped)
   }
   chunk[8192 + (h * 128 + r) * 2] = s[0];
   chunk[8192 + (h * 128 + r) * 2 + 1] = s[1];
@@ -113,8 +114,11 @@ __global__ void lt_repack_q4ks_kernel(const uint8_t* __restrict__ src, uint8_t* 
   }
 }
 
-// fp32 router [E, H] -> three bf16 planes (W1 = bf16(W), W2 = bf16(W - W1),
-// W3 = bf16(W - W1 - W2)), rows zero-padded to E_pad128, LT BF16 layout.
+// fp32 router [E, H] -> three fp16 planes, each holding the previous ones'
+// remainder scaled by 2^11 so that it stays a normal fp16 number:
+//   W1 = fp16(W), W2 = fp16(2^11 (W - W1)), W3 = fp16(2^11 (2^11 (W - W1) - W2)),
+// W = W1 + 2^-11 W2 + 2^-22 W3 up to fp32's own precision (33 bits kept; each
+// remainder is exact in fp32); rows zero-padded to E_pad128, LT 16-bit layout.
 __global__ void lt_repack_router_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int E, int E_pad,
                                         int H, int64_t plane_bytes) {
   const int n8 = H / 8;
@@ -131,10 +135,10 @@ __global__ void lt_repack_router_kernel(const float* __restrict__ src, uint8_t* 
     float v1 = row < E ? src[(int64_t)row * H + k0 + j + 1] : 0.f;
 #pragma unroll
     for (int pl = 0; pl < 3; ++pl) {
-      const __nv_bfloat16 b0 = __float2bfloat16_rn(v0), b1 = __float2bfloat16_rn(v1);
-      w[pl][j / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-      v0 -= __bfloat162float(b0);
-      v1 -= __bfloat162float(b1);
+      const __half b0 = __float2half_rn(v0), b1 = __float2half_rn(v1);
+      w[pl][j / 2] = (uint32_t)__half_as_ushort(b0) | ((uint32_t)__half_as_ushort(b1) << 16);
+      v0 = (v0 - __half2float(b0)) * 2048.f;
+      v1 = (v1 - __half2float(b1)) * 2048.f;
     }
   }
 #pragma unroll
@@ -145,6 +149,18 @@ __global__ void lt_repack_router_kernel(const float* __restrict__ src, uint8_t* 
 // ---------------------------------------------------------------------------
 // Forward kernels
 // ---------------------------------------------------------------------------
+
+// 8 bf16 values -> 8 fp16 values (exact for |v| in fp16's normal range;
+// round to nearest otherwise)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 struct PrepParams {
   const __nv_bfloat16* x;
@@ -174,7 +190,7 @@ __global__ void lt_prep_kernel(const PrepParams P) {
   for (int idx = threadIdx.x; idx < n_pad * nc; idx += blockDim.x) {
     const int r = idx % n_pad, c = c0 + idx / n_pad;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = *reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c);
+    if (r < n) v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c));
     dst[(int64_t)c * n_pad + r] = v;
   }
 }
@@ -197,7 +213,8 @@ __global__ void lt_topk_kernel(const float* __restrict__ logits, const float* __
     const int e = lane + 32 * i;
     float x = -INFINITY;
     if (e < E) {
-      x = ((l0[e] + l0[plane + e]) + l0[2 * plane + e]) + (bias ? bias[e] : 0.f);
+      // the planes' logits, scaled back by 2^-11 and 2^-22 (exact)
+      x = fmaf(l0[2 * plane + e], 0x1p-22f, fmaf(l0[plane + e], 0x1p-11f, l0[e])) + (bias ? bias[e] : 0.f);
       if (x != x) x = -INFINITY;
     }
     v[i] = x;
@@ -388,7 +405,7 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
   for (int idx = threadIdx.x; idx < tl.n_pad * nc; idx += blockDim.x) {
     const int r = idx % tl.n_pad, c = c0 + idx / tl.n_pad;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < tl.n) v = *reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c);
+    if (r < tl.n) v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c));
     dst[(int64_t)c * tl.n_pad + r] = v;
   }
 }

@@ -8,17 +8,18 @@
 // 64 rt + 16 q + i - 16 otherwise, so each 32-lane quarter of the
 // accumulator holds matching gate and up rows.  For down, tile row r is
 // output row 128 rt + r.
-//   Q8_0 : per (tile, K-block) 8704 bytes: quants [half h][piece p][128 rows][16 B]
-//          (half h = Q8_0 block 2 kb + h, piece p = its weights 16p..16p+15),
-//          then fp16 scales [h][128 rows].
+//   Q8_0 : per (tile, K-block) 8704 bytes: codes [half h][piece p][128 rows][16 B]
+//          (half h = Q8_0 block 2 kb + h, piece p = its weights 16p..16p+15;
+//          each code byte with its sign bit flipped, q + 128), then fp16
+//          scales [h][128 rows].
 //   Q4KS : per (tile, 256-column superblock) 18432 bytes: the serialised
 //          16-byte headers [128 rows][16 B], then for each of its 4 K-blocks
 //          codes [h][128 rows][16 B] (sub-block 2j + h, serialised nibble order).
-//   BF16 : per (tile, K-block) 16384 bytes: [h][piece p of 8][128 rows][16 B]
-//          (the router's three bf16 planes).
+//   16-bit (tag MOE_BF16): per (tile, K-block) 16384 bytes: [h][piece p of 8]
+//          [128 rows][16 B] (the router's three fp16 planes).
 // Activations that feed the MMA as its B operand (the gathered x of a token
 // tile and the SwiGLU outputs h) are stored per token tile as K-blocks of
-// [8 column chunks][n_pad rows][8 bf16]: one contiguous block of
+// [8 column chunks][n_pad rows][8 fp16]: one contiguous block of
 // n_pad * 128 bytes per K-block, which is the operand's shared-memory image
 // (8x8 core matrices, K-major, no swizzle).
 #pragma once
@@ -34,7 +35,7 @@ constexpr int kLtQ4Super = 18432;  // 128 rows x 256 columns of Q4KS
 constexpr int kLtQ4Hdr = 2048;
 constexpr int kLtQ4Codes = 4096;
 constexpr int kLtBf16Chunk = 16384;
-constexpr int kLtPlanes = 3;       // router: W = W1 + W2 + W3, each bf16
+constexpr int kLtPlanes = 3;       // router: W = W1 + 2^-11 W2 + 2^-22 W3, each fp16
 
 enum { kItemGU = 0, kItemDN = 1, kItemRT = 2 };
 
