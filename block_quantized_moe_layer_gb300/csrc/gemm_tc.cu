@@ -381,10 +381,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
+      // One thread issues every MMA of the CTA, and an MMA of N <= 64 takes
+      // the tensor core only ~45 cycles: the loop keeps its ring positions
+      // and phases as running counters (no divisions), steps the shared-
+      // memory descriptor by adding to its address field, and unrolls the
+      // usual 8 K-steps of a TMEM stage.
       uint32_t i = 0, a = 0;
+      uint32_t st = 0, tph = 0, sb = 0, bph = 0;
       for (uint32_t nt = 0;; ++nt) {
-        const uint32_t st = nt % kNT;
-        if (!wait1(&tfull[st], (nt / kNT) & 1, abort, p, kSiteDq, (int)nt)) break;
+        if (!wait1(&tfull[st], tph, abort, p, kSiteDq, (int)nt)) break;
         const TDesc d = tdescs[st];
         if (d.flags & kFlagEnd) break;
         if (d.flags & kFlagFirst) {
@@ -392,16 +397,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           const uint32_t u = i >> 1;
           if (u >= 1 && !wait1(&dempty[a], (u - 1) & 1, abort, p, kSiteAcc, (int)i)) break;
         }
-        const uint32_t sb = nt % kNB;
-        if (!wait1(&bfull[sb], (nt / kNB) & 1, abort, p, kSiteFull, (int)nt)) break;
+        if (!wait1(&bfull[sb], bph, abort, p, kSiteFull, (int)nt)) break;
         tc::fence_after();
         const uint32_t idesc = tc::idesc_f16(kLtRows, d.n_pad);
-        const uint32_t bsm = smem_u32(sm + kOffB + sb * kBSlot);
         const uint32_t lbo = (uint32_t)d.n_pad * 16;
-        for (int j = 0; j < d.nk; ++j) {
-          const uint64_t bdesc = tc::smem_desc(bsm + j * 2 * lbo, lbo, 128);
-          tc::mma_ts(tbase + kTmemAcc + 64 * a, tbase + 64 * st + 8 * j, bdesc, idesc,
-                     ((d.flags & kFlagFirst) && j == 0) ? 0u : 1u);
+        // K step of 16 = two core matrices along K: the address field (bits
+        // 0-13, address / 16; shared addresses stay below 2^18) grows by 2 lbo / 16
+        const uint64_t bdesc = tc::smem_desc(smem_u32(sm + kOffB + sb * kBSlot), lbo, 128);
+        const uint64_t bstep = (uint64_t)(lbo >> 3);
+        const uint32_t dacc = tbase + kTmemAcc + 64 * a, at = tbase + 64 * st;
+        const uint32_t acc0 = (d.flags & kFlagFirst) ? 0u : 1u;
+        if (d.nk == 8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
+        } else {
+          for (int j = 0; j < d.nk; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
         }
         tc::commit(&tempty[st]);
         tc::commit(&bempty[sb]);
@@ -409,6 +419,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           tc::commit(&dfull[a]);
           ++i;
         }
+        if (++st == kNT) { st = 0; tph ^= 1u; }
+        if (++sb == kNB) { sb = 0; bph ^= 1u; }
       }
       // all MMAs of this thread complete before the accumulators are freed
       tc::commit(finbar);
