@@ -30,9 +30,12 @@ namespace moe {
 
 namespace {
 
-constexpr int kNA = 7;            // raw weight slots
-constexpr int kNB = 5;            // activation slots
+constexpr int kNA = 6;            // raw weight slots
 constexpr int kNT = 6;            // TMEM A stages of 64 columns
+// activation slots: one per TMEM stage, indexed alike, so one MMA commit per
+// stage frees both (a commit costs the tensor pipe ~80 cycles, about two
+// small MMAs)
+constexpr int kNB = kNT;
 constexpr int kASlot = kLtQ4Super;  // 18432 >= Q8_0 (17408) >= a router K-block (16384)
 constexpr int kBSlot = kLtMaxN * 128 * 2;
 constexpr int kGemmThreads = 512;
@@ -44,7 +47,7 @@ constexpr int kTmemAcc = 384;
 constexpr int kOffB = kNA * kASlot;
 constexpr int kOffStaging = kOffB + kNB * kBSlot;          // 4 warps x 2 chunks x 64 rows x 16 B
 constexpr int kOffBars = kOffStaging + 4 * 2048;
-constexpr int kNumBars = 2 * kNA + 2 * kNB + 2 * kNT + 2 + 2 + 4 + 4 + 1;
+constexpr int kNumBars = 2 * kNA + kNB + 2 * kNT + 2 + 2 + 4 + 4 + 1;
 constexpr int kOffDescs = kOffBars + kNumBars * 8;
 constexpr int kOffTdescs = kOffDescs + kNA * 48;
 constexpr int kOffInfos = kOffTdescs + kNT * 16;
@@ -200,8 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   uint64_t* afull = bars;
   uint64_t* aempty = afull + kNA;
   uint64_t* bfull = aempty + kNA;
-  uint64_t* bempty = bfull + kNB;
-  uint64_t* tfull = bempty + kNB;
+  uint64_t* tfull = bfull + kNB;
   uint64_t* tempty = tfull + kNT;
   uint64_t* dfull = tempty + kNT;
   uint64_t* dempty = dfull + 2;
@@ -222,7 +224,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
     }
     for (int s = 0; s < kNB; ++s) {
       mbar_init(&bfull[s], 1);
-      mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < kNT; ++s) {
       mbar_init(&tfull[s], 4);
@@ -328,8 +329,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           // activation K-slices, one per TMEM stage
           for (int t = 0; t < nts; ++t, ++nt) {
             const int tc0 = c0 + 128 * t, tcols = min(128, cols - 128 * t);
+            // slot nt % kNB is free once the MMAs of TMEM stage nt - kNB completed
             const uint32_t sb = nt % kNB;
-            if (nt >= kNB && !(ok = wait1(&bempty[sb], ((nt / kNB) - 1) & 1, abort, p, kSiteFree, -(int)nt)))
+            if (nt >= kNB && !(ok = wait1(&tempty[sb], ((nt / kNB) - 1) & 1, abort, p, kSiteFree, -(int)nt)))
               break;
             const uint32_t bbytes = (uint32_t)tl.n_pad * tcols * 2;
             mbar_arrive_expect_tx(&bfull[sb], bbytes);
@@ -413,8 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         } else {
           for (int j = 0; j < d.nk; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
         }
-        tc::commit(&tempty[st]);
-        tc::commit(&bempty[sb]);
+        tc::commit(&tempty[st]);  // frees TMEM stage st and activation slot sb (== st)
         if (d.flags & kFlagLast) {
           tc::commit(&dfull[a]);
           ++i;
