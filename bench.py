@@ -247,17 +247,28 @@ E2E_NOTE = ("every step: inputs host->device from pinned memory, the step, resul
             "memory; copies on their own streams, buffers doubled, so copies overlap neighbouring steps")
 
 
-def traffic_record(kernel_src):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+KERNEL_SOURCES = {  # the files each path's kernels are compiled from
+    "small_t": ("small_t.cu", "gemv.cuh", "layer.cuh", "common.cuh"),
+    "large_t": ("gemm_tc.cu", "large_t.cuh", "tc.cuh", "layer.cuh", "common.cuh"),
+}
+
+
+def kernel_hash(path):
+    """Hash of the sources the path's dominant kernel is compiled from."""
     import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[path]:
+        h.update(open(os.path.join(ROOT, "block_quantized_moe_layer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(path, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources for this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    rec = d.get(h)
-    return rec
+    return json.load(open(p)).get(f"{kernel_hash(path)}:{workload}")
 
 
 def cpu_baseline_sample(w, budget_s=20.0):
@@ -374,8 +385,7 @@ def run_ours(args):
 
     peak, peak_src = measured_peaks()
     achieved = alg / (kern_us * 1e-6) / 1e9
-    src = os.path.join(ROOT, "block_quantized_moe_layer_gb300", "csrc", "small_t.cu" if w.T <= 8 else "gemm_tc.cu")
-    tr = traffic_record(src)
+    tr = traffic_record("small_t" if w.T <= 8 else "large_t", w.name)
     kname = "moe_small_t_kernel" if w.T <= 8 else "moe_forward (8 launches; the grouped tcgen05 GEMMs dominate)"
     out = {
         "metric": METRIC,
