@@ -161,7 +161,9 @@ int moe_forward_f32(moe_layer* L, const void* x, int32_t T, float* y, void* stre
 /* Copies the routing of the last moe_forward (device-to-device, async on
  * `stream`): ids int32 [T, k] and gates fp32 [T, k] in slot order, offsets
  * int32 [E+1], perm int32 [T*k] (pair ids t*k+j grouped by expert, ascending
- * within an expert).  Any pointer may be NULL to skip it. */
+ * within an expert).  Any pointer may be NULL to skip it.  The stream
+ * argument orders the copies after the forward on the caller's stream, so
+ * reading the routing never synchronises the device. */
 int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm,
                     void* stream);
 
@@ -244,6 +246,10 @@ int moe_quantize(int32_t fmt, const float* w, int64_t rows, int64_t cols, void* 
  *   bytes, 16-byte aligned, owned by the caller; it must be zero-filled
  *   before its first use and is left zero-filled by every call that
  *   completes.  Calls sharing one workspace must not overlap on the GPU.
+ *   The scratch is the caller's rather than the library's so that the call
+ *   never allocates (it stays capturable in a CUDA graph) and calls on
+ *   different workspaces may run concurrently; mtp_verify_accept_noalloc
+ *   below takes no workspace.
  *   Launched with programmatic stream serialization like moe_forward: it
  *   waits for the previous kernel in the stream before reading anything. */
 size_t mtp_verify_accept_workspace_bytes(int32_t k, int32_t V);
