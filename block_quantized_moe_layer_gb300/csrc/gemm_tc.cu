@@ -16,10 +16,10 @@
 //               router logits.
 // The three rings are released independently: a raw weight slot as soon as
 // its group holds the data in registers, an activation slot and a TMEM stage
-// when the MMAs that read them complete.  An A stage is 128 columns of Q8_0,
-// one 256-column superblock of Q4KS (two TMEM stages) or 64 columns of a
-// router plane.
-// TMEM columns: A stages at 64 s (s < 6), accumulators at 384 and 448.
+// when the MMAs that read them complete.  An A stage is 256 columns of Q8_0,
+// one 256-column superblock of Q4KS or 64 columns of a router plane, and
+// fills one TMEM stage of 128 columns (up to 16 MMAs).
+// TMEM columns: A stages at 128 s (s < 2), accumulators at 384 and 448.
 // Every wait is bounded; a timeout records its site in the status word, sets
 // an abort flag that the other roles see, and every role then leaves after
 // its own in-flight copies and MMAs have completed.
@@ -30,14 +30,26 @@ namespace moe {
 
 namespace {
 
-constexpr int kNA = 6;            // raw weight slots
-constexpr int kNT = 6;            // TMEM A stages of 64 columns
+// A stage covers up to 256 columns of K: one TMEM stage of 128 columns (16
+// MMAs of K = 16), so the issuer's fixed cost per stage (its waits, one
+// commit, its bookkeeping: ~700 cycles on a thread that shares its
+// scheduler with busy warps) is spread over 16 MMAs.
+constexpr int kStageK = 256;
+constexpr int kTmemStage = kStageK / 2;  // TMEM columns of one A stage (two fp16 per column)
+// The two dequant groups take alternate stages, so every ring they wait on
+// has an even number of slots: each slot then always belongs to the same
+// group, which sees all of its phases in order (a ring of odd size would let
+// a group wait on a phase two ahead, and the parity test pass early).
+constexpr int kNA = 4;            // raw weight slots
+constexpr int kNT = 2;            // TMEM A stages
+static_assert(kNA % 2 == 0 && kNT % 2 == 0, "rings shared by the two dequant groups must be even");
 // activation slots: one per TMEM stage, indexed alike, so one MMA commit per
 // stage frees both (a commit costs the tensor pipe ~80 cycles, about two
 // small MMAs)
 constexpr int kNB = kNT;
-constexpr int kASlot = kLtQ4Super;  // 18432 >= Q8_0 (17408) >= a router K-block (16384)
-constexpr int kBSlot = kLtMaxN * 128 * 2;
+constexpr int kASlot = 4 * kLtQ8Chunk;  // 34816: Q8_0 (256 columns) >= Q4KS superblock >= a router K-block
+constexpr int kBSlot = kLtMaxN * kStageK * 2;
+static_assert(kNT * kTmemStage <= 384, "A stages below the accumulators");
 constexpr int kGemmThreads = 512;
 constexpr int kDequantWarp0 = 4;
 constexpr int kEpiWarp0 = 12;
@@ -295,13 +307,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         if (i >= 4 && !(ok = wait1(&iempty[j], ((i >> 2) - 1) & 1, abort, p, kSiteItem, (int)i))) break;
         infos[j] = ItemInfo{0, kind, rt, tl.e, tl.slot0, tl.n, tl.n_pad, tl.prow0, plane, {0, 0, 0}};
         mbar_arrive(&ifull[j]);
-        const int span = fmt == MOE_Q8_0 ? 128 : (fmt == MOE_Q4KS ? 256 : 64);  // columns per A stage
+        const int span = fmt == MOE_Q8_0 ? kStageK : (fmt == MOE_Q4KS ? 256 : 64);  // columns per A stage
         const int nst = (K + span - 1) / span;
         for (int st = 0; st < nst; ++st, ++na) {
           const int c0 = st * span, cols = min(span, K - c0);
           const uint32_t sa = na % kNA;
           if (na >= kNA && !(ok = wait1(&aempty[sa], ((na / kNA) - 1) & 1, abort, p, kSiteFree, (int)na))) break;
-          const int nts = cols > 128 ? 2 : 1;
+          const int nts = 1;
           StageDesc d;
           d.flags = 0;
           d.fmt = fmt;
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           bulk_g2s(sm + sa * kASlot, asrc, abytes, &afull[sa]);
           // activation K-slices, one per TMEM stage
           for (int t = 0; t < nts; ++t, ++nt) {
-            const int tc0 = c0 + 128 * t, tcols = min(128, cols - 128 * t);
+            const int tc0 = c0 + kStageK * t, tcols = min(kStageK, cols - kStageK * t);
             // slot nt % kNB is free once the MMAs of TMEM stage nt - kNB completed
             const uint32_t sb = nt % kNB;
             if (nt >= kNB && !(ok = wait1(&tempty[sb], ((nt / kNB) - 1) & 1, abort, p, kSiteFree, -(int)nt)))
@@ -387,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
       // the tensor core only ~45 cycles: the loop keeps its ring positions
       // and phases as running counters (no divisions), steps the shared-
       // memory descriptor by adding to its address field, and unrolls the
-      // usual 8 K-steps of a TMEM stage.
+      // usual 16 K-steps of a TMEM stage.
       uint32_t i = 0, a = 0;
       uint32_t st = 0, tph = 0, sb = 0, bph = 0;
       for (uint32_t nt = 0;; ++nt) {
@@ -407,11 +419,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         // 0-13, address / 16; shared addresses stay below 2^18) grows by 2 lbo / 16
         const uint64_t bdesc = tc::smem_desc(smem_u32(sm + kOffB + sb * kBSlot), lbo, 128);
         const uint64_t bstep = (uint64_t)(lbo >> 3);
-        const uint32_t dacc = tbase + kTmemAcc + 64 * a, at = tbase + 64 * st;
+        const uint32_t dacc = tbase + kTmemAcc + 64 * a, at = tbase + kTmemStage * st;
         const uint32_t acc0 = (d.flags & kFlagFirst) ? 0u : 1u;
-        if (d.nk == 8) {
+        if (d.nk == 16) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
+          for (int j = 0; j < 16; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
         } else {
           for (int j = 0; j < d.nk; ++j) tc::mma_ts(dacc, at + 8 * j, bdesc + j * bstep, idesc, j == 0 ? acc0 : 1u);
         }
@@ -454,41 +466,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         break;
       }
       if (d.fmt == MOE_Q8_0) {
-        // up to 4 blocks (two 64-column K-blocks x two halves)
+        // up to 8 blocks (four 64-column K-blocks x two halves), in two
+        // halves of 4 (the second half's codes are read before the raw slot
+        // is released)
         const int nb = d.cols / 32;
-        uint4 c[4][2];
-        uint32_t sc[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (b < nb) {
-            const uint8_t* kbp = s + (b >> 1) * kLtQ8Chunk;
-            const int h = b & 1;
-            c[b][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
-            c[b][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
-            const uint32_t h16 = *reinterpret_cast<const unsigned short*>(kbp + 8192 + (h * 128 + r) * 2);
-            sc[b] = h16 | (h16 << 16);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aempty[sa]);
         const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
-        if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
-        tc::fence_after();
+        bool good = true;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (b < nb) {
-            uint32_t v[16];
-            dq_q8(c[b][0], c[b][1], sc[b], v);
-            tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16 * b, v);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint4 c[4][2];
+          uint32_t sc[4];
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int b = 4 * hf + bb;
+            if (b < nb) {
+              const uint8_t* kbp = s + (b >> 1) * kLtQ8Chunk;
+              const int h = b & 1;
+              c[bb][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
+              c[bb][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
+              const uint32_t h16 = *reinterpret_cast<const unsigned short*>(kbp + 8192 + (h * 128 + r) * 2);
+              sc[bb] = h16 | (h16 << 16);
+            }
+          }
+          if (hf == 0) {
+            if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) {
+              good = false;
+              break;
+            }
+            tc::fence_after();
+          } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[sa]);
+          }
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int b = 4 * hf + bb;
+            if (b < nb) {
+              uint32_t v[16];
+              dq_q8(c[bb][0], c[bb][1], sc[bb], v);
+              tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * b, v);
+            }
           }
         }
+        if (!good) break;
         tc::wait_st();
         tc::fence_before();
         if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nb * 2, 0};
         __syncwarp();
         if (lane == 0) mbar_arrive(&tfull[ts]);
       } else if (d.fmt == MOE_Q4KS) {
-        // one superblock: header, then 8 sub-blocks over two TMEM stages
+        // one superblock: header, then its 8 sub-blocks into one TMEM stage
         const uint4 hv = *reinterpret_cast<const uint4*>(s + r * 16);
         uint4 c[8];
 #pragma unroll
@@ -498,30 +525,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         if (lane == 0) mbar_arrive(&aempty[sa]);
         const float dd = __half2float(__ushort_as_half((unsigned short)(hv.x & 0xFFFFu)));
         const float dm = __half2float(__ushort_as_half((unsigned short)(hv.x >> 16)));
-        bool good = true;
+        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
+        if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
+        tc::fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t t = (uint32_t)d.nt0 + half, ts = t % kNT;
-          if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) {
-            good = false;
-            break;
-          }
-          tc::fence_after();
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int sb = 4 * half + k4;
-            uint32_t v[16];
-            dq_q4(c[sb], dd * (float)q4_field(hv.y, hv.z, hv.w, sb), dm * (float)q4_field(hv.y, hv.z, hv.w, 8 + sb),
-                  v);
-            tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16 * k4, v);
-          }
-          tc::wait_st();
-          tc::fence_before();
-          if (leader) tdescs[ts] = TDesc{d.tflags[half], d.n_pad, 8, 0};
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tfull[ts]);
+        for (int sb = 0; sb < 8; ++sb) {
+          uint32_t v[16];
+          dq_q4(c[sb], dd * (float)q4_field(hv.y, hv.z, hv.w, sb), dm * (float)q4_field(hv.y, hv.z, hv.w, 8 + sb), v);
+          tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * sb, v);
         }
-        if (!good) break;
+        tc::wait_st();
+        tc::fence_before();
+        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, 16, 0};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfull[ts]);
       } else {
         // router plane: 64 columns of fp16, copied as they are
         uint32_t v[2][16];
@@ -540,8 +557,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
         if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
         tc::fence_after();
-        tc::st_32x32b_x16(tbase + tlane + 64 * ts, v[0]);
-        tc::st_32x32b_x16(tbase + tlane + 64 * ts + 16, v[1]);
+        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts, v[0]);
+        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16, v[1]);
         tc::wait_st();
         tc::fence_before();
         if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, 4, 0};
