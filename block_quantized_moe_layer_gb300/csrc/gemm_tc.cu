@@ -8,14 +8,14 @@
 //               activation K-slices (B ring);
 //   warp 1      allocates the 512 TMEM columns; lane 0 issues the MMAs
 //               (M = 128, N = n_pad, K = 16, A from TMEM, B from shared memory);
-//   warps 4-11  dequantise, as two groups of four warps that take alternate A
-//               stages: thread (group, row r) turns its row's weights of the
-//               stage into fp16 pairs and stores them to TMEM;
+//   warps 4-11  dequantise, as two groups of four warps that share every A
+//               stage: thread (group g, row r) turns its row's weights in
+//               half g of the stage into fp16 pairs and stores them to TMEM;
 //   warps 12-15 epilogue: read the accumulator (double-buffered) and write
 //               SwiGLU outputs (gate/up), bf16 partial outputs z (down) or fp32
 //               router logits.
 // The three rings are released independently: a raw weight slot as soon as
-// its group holds the data in registers, an activation slot and a TMEM stage
+// both groups hold its data in registers, an activation slot and a TMEM stage
 // when the MMAs that read them complete.  An A stage is 256 columns of Q8_0,
 // one 256-column superblock of Q4KS or 64 columns of a router plane, and
 // fills one TMEM stage of 128 columns (up to 16 MMAs).
@@ -36,13 +36,11 @@ namespace {
 // scheduler with busy warps) is spread over 16 MMAs.
 constexpr int kStageK = 256;
 constexpr int kTmemStage = kStageK / 2;  // TMEM columns of one A stage (two fp16 per column)
-// The two dequant groups take alternate stages, so every ring they wait on
-// has an even number of slots: each slot then always belongs to the same
-// group, which sees all of its phases in order (a ring of odd size would let
-// a group wait on a phase two ahead, and the parity test pass early).
-constexpr int kNA = 4;            // raw weight slots
-constexpr int kNT = 2;            // TMEM A stages
-static_assert(kNA % 2 == 0 && kNT % 2 == 0, "rings shared by the two dequant groups must be even");
+// Both dequant groups work on every stage (each on half of its blocks), so
+// every waiter sees every phase of every ring in order, whatever the ring
+// sizes.
+constexpr int kNA = 3;            // raw weight slots
+constexpr int kNT = 3;            // TMEM A stages
 // activation slots: one per TMEM stage, indexed alike, so one MMA commit per
 // stage frees both (a commit costs the tensor pipe ~80 cycles, about two
 // small MMAs)
@@ -232,13 +230,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   if (tid == 0) {
     for (int s = 0; s < kNA; ++s) {
       mbar_init(&afull[s], 1);
-      mbar_init(&aempty[s], 4);
+      mbar_init(&aempty[s], 8);  // both dequant groups
     }
     for (int s = 0; s < kNB; ++s) {
       mbar_init(&bfull[s], 1);
     }
     for (int s = 0; s < kNT; ++s) {
-      mbar_init(&tfull[s], 4);
+      mbar_init(&tfull[s], 8);  // both dequant groups
       mbar_init(&tempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -354,8 +352,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         ++i;
         item = next;
       }
-      // end markers: one A stage for each dequant group; the first forwards
-      // the end to the MMA issuer
+      // end marker: one A stage, which both dequant groups see and forward
+      // to the MMA issuer
       if (ok) {
         const uint32_t j = i & 3;
         if (i < 4 || (ok = wait1(&iempty[j], ((i >> 2) - 1) & 1, abort, p, kSiteItem, (int)i))) {
@@ -363,7 +361,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           mbar_arrive(&ifull[j]);
         }
       }
-      for (int e = 0; e < 2 && ok; ++e, ++na) {
+      for (int e = 0; e < 1 && ok; ++e, ++na) {
         const uint32_t sa = na % kNA;
         if (na >= kNA && !(ok = wait1(&aempty[sa], ((na / kNA) - 1) & 1, abort, p, kSiteFree, (int)na))) break;
         descs[sa].flags = kFlagEnd | (e == 0 ? kFlagFwdEnd : 0);
@@ -448,16 +446,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   } else if (warp >= kDequantWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------------ dequantise
     const int q = warp & 3, g = (warp - kDequantWarp0) >> 2, r = 32 * q + lane;
-    const bool leader = warp == kDequantWarp0 + 4 * g && lane == 0;
+    const bool leader = warp == kDequantWarp0 && lane == 0;  // writes the TMEM stage's descriptor
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
-    for (uint32_t na = g;; na += 2) {
+    for (uint32_t na = 0;; ++na) {
       const uint32_t sa = na % kNA;
       if (!waitw(&afull[sa], (na / kNA) & 1, abort, p, kSiteFull, (int)na)) break;
       const StageDesc d = descs[sa];
       const uint8_t* s = sm + sa * kASlot;
+      const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
       if (d.flags & kFlagEnd) {
         if (d.flags & kFlagFwdEnd) {
-          const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
           if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
           if (leader) tdescs[ts] = TDesc{kFlagEnd, 0, 0, 0};
           __syncwarp();
@@ -465,106 +463,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         }
         break;
       }
+      int nk = 0;
       if (d.fmt == MOE_Q8_0) {
-        // up to 8 blocks (four 64-column K-blocks x two halves), in two
-        // halves of 4 (the second half's codes are read before the raw slot
-        // is released)
+        // up to 8 blocks (four 64-column K-blocks x two halves); group g
+        // takes blocks 4g .. 4g+3
         const int nb = d.cols / 32;
-        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
-        bool good = true;
+        uint4 c[4][2];
+        uint32_t sc[4];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint4 c[4][2];
-          uint32_t sc[4];
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const int b = 4 * hf + bb;
-            if (b < nb) {
-              const uint8_t* kbp = s + (b >> 1) * kLtQ8Chunk;
-              const int h = b & 1;
-              c[bb][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
-              c[bb][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
-              const uint32_t h16 = *reinterpret_cast<const unsigned short*>(kbp + 8192 + (h * 128 + r) * 2);
-              sc[bb] = h16 | (h16 << 16);
-            }
-          }
-          if (hf == 0) {
-            if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) {
-              good = false;
-              break;
-            }
-            tc::fence_after();
-          } else {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&aempty[sa]);
-          }
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const int b = 4 * hf + bb;
-            if (b < nb) {
-              uint32_t v[16];
-              dq_q8(c[bb][0], c[bb][1], sc[bb], v);
-              tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * b, v);
-            }
+        for (int bb = 0; bb < 4; ++bb) {
+          const int b = 4 * g + bb;
+          if (b < nb) {
+            const uint8_t* kbp = s + (b >> 1) * kLtQ8Chunk;
+            const int h = b & 1;
+            c[bb][0] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 0) * 128 + r) * 16);
+            c[bb][1] = *reinterpret_cast<const uint4*>(kbp + ((h * 2 + 1) * 128 + r) * 16);
+            const uint32_t h16 = *reinterpret_cast<const unsigned short*>(kbp + 8192 + (h * 128 + r) * 2);
+            sc[bb] = h16 | (h16 << 16);
           }
         }
-        if (!good) break;
-        tc::wait_st();
-        tc::fence_before();
-        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nb * 2, 0};
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tfull[ts]);
-      } else if (d.fmt == MOE_Q4KS) {
-        // one superblock: header, then its 8 sub-blocks into one TMEM stage
-        const uint4 hv = *reinterpret_cast<const uint4*>(s + r * 16);
-        uint4 c[8];
+        if (lane == 0) mbar_arrive(&aempty[sa]);
+        if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
+        tc::fence_after();
 #pragma unroll
-        for (int sb = 0; sb < 8; ++sb)
-          c[sb] = *reinterpret_cast<const uint4*>(s + kLtQ4Hdr + (sb >> 1) * kLtQ4Codes + ((sb & 1) * 128 + r) * 16);
+        for (int bb = 0; bb < 4; ++bb) {
+          const int b = 4 * g + bb;
+          if (b < nb) {
+            uint32_t v[16];
+            dq_q8(c[bb][0], c[bb][1], sc[bb], v);
+            tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * b, v);
+          }
+        }
+        nk = nb * 2;
+      } else if (d.fmt == MOE_Q4KS) {
+        // one superblock: header, then its 8 sub-blocks; group g takes
+        // sub-blocks 4g .. 4g+3
+        const uint4 hv = *reinterpret_cast<const uint4*>(s + r * 16);
+        uint4 c[4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int sb = 4 * g + k4;
+          c[k4] = *reinterpret_cast<const uint4*>(s + kLtQ4Hdr + (sb >> 1) * kLtQ4Codes + ((sb & 1) * 128 + r) * 16);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[sa]);
         const float dd = __half2float(__ushort_as_half((unsigned short)(hv.x & 0xFFFFu)));
         const float dm = __half2float(__ushort_as_half((unsigned short)(hv.x >> 16)));
-        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
         if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
         tc::fence_after();
 #pragma unroll
-        for (int sb = 0; sb < 8; ++sb) {
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int sb = 4 * g + k4;
           uint32_t v[16];
-          dq_q4(c[sb], dd * (float)q4_field(hv.y, hv.z, hv.w, sb), dm * (float)q4_field(hv.y, hv.z, hv.w, 8 + sb), v);
+          dq_q4(c[k4], dd * (float)q4_field(hv.y, hv.z, hv.w, sb), dm * (float)q4_field(hv.y, hv.z, hv.w, 8 + sb), v);
           tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * sb, v);
         }
-        tc::wait_st();
-        tc::fence_before();
-        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, 16, 0};
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tfull[ts]);
+        nk = 16;
       } else {
-        // router plane: 64 columns of fp16, copied as they are
-        uint32_t v[2][16];
+        // router plane: 64 columns of fp16, copied as they are; group g
+        // takes 32 of them
+        uint32_t v[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int pc = 0; pc < 4; ++pc) {
-            const uint4 x = *reinterpret_cast<const uint4*>(s + ((h * 4 + pc) * 128 + r) * 16);
-            v[h][4 * pc + 0] = x.x;
-            v[h][4 * pc + 1] = x.y;
-            v[h][4 * pc + 2] = x.z;
-            v[h][4 * pc + 3] = x.w;
-          }
+        for (int pc = 0; pc < 4; ++pc) {
+          const uint4 x = *reinterpret_cast<const uint4*>(s + ((g * 4 + pc) * 128 + r) * 16);
+          v[4 * pc + 0] = x.x;
+          v[4 * pc + 1] = x.y;
+          v[4 * pc + 2] = x.z;
+          v[4 * pc + 3] = x.w;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[sa]);
-        const uint32_t t = (uint32_t)d.nt0, ts = t % kNT;
         if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
         tc::fence_after();
-        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts, v[0]);
-        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16, v[1]);
-        tc::wait_st();
-        tc::fence_before();
-        if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, 4, 0};
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tfull[ts]);
+        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * g, v);
+        nk = 4;
       }
+      tc::wait_st();
+      tc::fence_before();
+      if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nk, 0};
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tfull[ts]);
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue
