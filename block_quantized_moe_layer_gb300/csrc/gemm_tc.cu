@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
       // memory descriptor by adding to its address field, and unrolls the
       // usual 16 K-steps of a TMEM stage.
       uint32_t i = 0, a = 0;
-      uint32_t st = 0, tph = 0, sb = 0, bph = 0;
+      uint32_t st = 0, tph = 0, sb = 0;
       for (uint32_t nt = 0;; ++nt) {
         if (!wait1(&tfull[st], tph, abort, p, kSiteDq, (int)nt)) break;
         const TDesc d = tdescs[st];
@@ -409,7 +409,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           const uint32_t u = i >> 1;
           if (u >= 1 && !wait1(&dempty[a], (u - 1) & 1, abort, p, kSiteAcc, (int)i)) break;
         }
-        if (!wait1(&bfull[sb], bph, abort, p, kSiteFull, (int)nt)) break;
+        // (the activation slot's copy was observed complete before the stage's
+        // barrier, by the dequant warp that writes the stage descriptor)
         tc::fence_after();
         const uint32_t idesc = tc::idesc_f16(kLtRows, d.n_pad);
         const uint32_t lbo = (uint32_t)d.n_pad * 16;
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
           ++i;
         }
         if (++st == kNT) { st = 0; tph ^= 1u; }
-        if (++sb == kNB) { sb = 0; bph ^= 1u; }
+        if (++sb == kNB) sb = 0;
       }
       // all MMAs of this thread complete before the accumulators are freed
       tc::commit(finbar);
@@ -541,8 +542,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
       }
       tc::wait_st();
       tc::fence_before();
-      if (leader) tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nk, 0};
-      __syncwarp();
+      bool bok = true;
+      if (leader) {
+        // the stage's activation slot (slot ts of the B ring) has landed: the
+        // issuer then waits on this stage's barrier alone
+        bok = wait1(&bfull[ts], (t / kNB) & 1, abort, p, kSiteFull, (int)t);
+        tdescs[ts] = TDesc{d.tflags[0], d.n_pad, nk, 0};
+      }
+      if (!__shfl_sync(0xffffffffu, (int)bok, 0)) break;
       if (lane == 0) mbar_arrive(&tfull[ts]);
     }
   } else if (warp >= kEpiWarp0) {
