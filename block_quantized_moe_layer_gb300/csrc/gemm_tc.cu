@@ -17,7 +17,7 @@
 // The three rings are released independently: a raw weight slot as soon as
 // both groups hold its data in registers, an activation slot and a TMEM stage
 // when the MMAs that read them complete.  An A stage is 256 columns of Q8_0,
-// one 256-column superblock of Q4KS or 64 columns of a router plane, and
+// one 256-column superblock of Q4KS or 128 columns of a router plane, and
 // fills one TMEM stage of 128 columns (up to 16 MMAs).
 // TMEM columns: A stages at 128 s (s < 2), accumulators at 384 and 448.
 // Every wait is bounded; a timeout records its site in the status word, sets
@@ -45,7 +45,7 @@ constexpr int kNT = 3;            // TMEM A stages
 // stage frees both (a commit costs the tensor pipe ~80 cycles, about two
 // small MMAs)
 constexpr int kNB = kNT;
-constexpr int kASlot = 4 * kLtQ8Chunk;  // 34816: Q8_0 (256 columns) >= Q4KS superblock >= a router K-block
+constexpr int kASlot = 4 * kLtQ8Chunk;  // 34816: Q8_0 (256 columns) >= two router K-blocks >= a Q4KS superblock
 constexpr int kBSlot = kLtMaxN * kStageK * 2;
 static_assert(kNT * kTmemStage <= 384, "A stages below the accumulators");
 constexpr int kGemmThreads = 512;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         if (i >= 4 && !(ok = wait1(&iempty[j], ((i >> 2) - 1) & 1, abort, p, kSiteItem, (int)i))) break;
         infos[j] = ItemInfo{0, kind, rt, tl.e, tl.slot0, tl.n, tl.n_pad, tl.prow0, plane, {0, 0, 0}};
         mbar_arrive(&ifull[j]);
-        const int span = fmt == MOE_Q8_0 ? kStageK : (fmt == MOE_Q4KS ? 256 : 64);  // columns per A stage
+        const int span = fmt == MOE_Q8_0 ? kStageK : (fmt == MOE_Q4KS ? 256 : 128);  // columns per A stage
         const int nst = (K + span - 1) / span;
         for (int st = 0; st < nst; ++st, ++na) {
           const int c0 = st * span, cols = min(span, K - c0);
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
             abytes = kLtQ4Super;
           } else {
             asrc = A + (int64_t)(c0 / 64) * kLtBf16Chunk;
-            abytes = kLtBf16Chunk;
+            abytes = (uint32_t)(cols / 64) * kLtBf16Chunk;
           }
           mbar_arrive_expect_tx(&afull[sa], abytes);
           bulk_g2s(sm + sa * kASlot, asrc, abytes, &afull[sa]);
@@ -522,23 +522,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
         }
         nk = 16;
       } else {
-        // router plane: 64 columns of fp16, copied as they are; group g
-        // takes 32 of them
-        uint32_t v[16];
+        // router plane: up to 128 columns of fp16 (two 64-column K-blocks),
+        // copied as they are; group g takes K-block g
+        const int nkb = d.cols / 64;
+        uint32_t v[2][16];
+        if (g < nkb) {
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const uint4 x = *reinterpret_cast<const uint4*>(s + ((g * 4 + pc) * 128 + r) * 16);
-          v[4 * pc + 0] = x.x;
-          v[4 * pc + 1] = x.y;
-          v[4 * pc + 2] = x.z;
-          v[4 * pc + 3] = x.w;
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+              const uint4 x = *reinterpret_cast<const uint4*>(s + g * kLtBf16Chunk + ((h * 4 + pc) * 128 + r) * 16);
+              v[h][4 * pc + 0] = x.x;
+              v[h][4 * pc + 1] = x.y;
+              v[h][4 * pc + 2] = x.z;
+              v[h][4 * pc + 3] = x.w;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[sa]);
         if (t >= kNT && !waitw(&tempty[ts], ((t / kNT) - 1) & 1, abort, p, kSiteFree, (int)t)) break;
         tc::fence_after();
-        tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 16 * g, v);
-        nk = 4;
+        if (g < nkb) {
+          tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 32 * g, v[0]);
+          tc::st_32x32b_x16(tbase + tlane + kTmemStage * ts + 32 * g + 16, v[1]);
+        }
+        nk = nkb * 4;
       }
       tc::wait_st();
       tc::fence_before();
