@@ -24,7 +24,7 @@ EXPORTS = (
     "mtp_verify_accept", "mtp_verify_accept_noalloc", "moe_forward_residual", "moe_lm_head_create",
     "moe_lm_head_forward", "moe_lm_head_destroy", "mtp_round_workspace_bytes", "mtp_round", "moe_last_error",
     "moe_layer_timeline", "moe_layer_inject_timeout", "moe_lm_head_status", "moe_forward_f32",
-    "mtp_round_hidden",
+    "mtp_round_hidden", "moe_forward_resnorm",
 )
 
 # event names of moe_layer_timeline, in order
@@ -91,6 +91,7 @@ def lib():
             "moe_layer_timeline": (_c.c_int, [vp, _c.POINTER(i64), i32, vp]),
             "moe_layer_inject_timeout": (_c.c_int, [vp, i32]),
             "mtp_round_hidden": (_c.c_int, [vp, sz, i32, i32, i32, i32, i32, vp, vp]),
+            "moe_forward_resnorm": (_c.c_int, [vp, vp, i32, vp, vp, vp, _c.c_float, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -202,6 +203,20 @@ class Layer:
         f = lib().moe_forward_f32 if out_f32 else (lib().moe_forward_residual if residual else lib().moe_forward)
         _check(f(self.handle, x.data_ptr() if T else None, T, y.data_ptr() if T else None, _stream(stream)))
         return y
+
+    def forward_resnorm(self, x, h_in, h_out=None, xn=None, eps=1e-6, stream=None):
+        """One residual-stream step (``moe_forward_resnorm``): h_out = h_in +
+        MoE(x) (fp32), xn = rmsnorm(h_out) (x's dtype).  Returns (h_out, xn)."""
+        import torch
+        T = x.shape[0]
+        if h_out is None:
+            h_out = torch.empty(h_in.shape, dtype=torch.float32, device=x.device)
+        if xn is None:
+            xn = torch.empty_like(x)
+        _check(lib().moe_forward_resnorm(self.handle, x.data_ptr() if T else None, T,
+                                         h_in.data_ptr() if T else None, h_out.data_ptr() if T else None,
+                                         xn.data_ptr() if T else None, eps, _stream(stream)))
+        return h_out, xn
 
     def routing(self, T, stream=None):
         """(ids [T,k] int32, gates [T,k] fp32, offsets [E+1] int32, perm [T*k] int32)."""

@@ -388,6 +388,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   const size_t o_xrec = take((size_t)Tm * (d->H / 32) * RB);
   const size_t o_hrec = take((size_t)P * (Imax / 32) * RB);
   const size_t o_z = take((size_t)P * d->H * 4);
+  const size_t o_ssq = take((size_t)kMaxSmallT * n_dt * 4);
   L->ws_bytes = off;
   CK(cudaMalloc(&L->ws, L->ws_bytes), "alloc workspace");
   CK(cudaMemsetAsync(L->ws, 0, L->ws_bytes, st), "zero workspace");
@@ -397,6 +398,7 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
   sp.entry_ready = reinterpret_cast<int*>(w + o_ready);
   sp.d_cnt = reinterpret_cast<int*>(w + o_dcnt);
   sp.status = reinterpret_cast<int*>(w + o_status);
+  sp.ssq = reinterpret_cast<float*>(w + o_ssq);
   sp.stamps = reinterpret_cast<unsigned long long*>(w + o_stamps);
   sp.lfx0 = reinterpret_cast<const long long*>(w + o_lfx0);
   sp.lfx = reinterpret_cast<long long*>(w + o_lfx);
@@ -437,7 +439,15 @@ int moe_layer_create(const moe_layer_desc* d, void* stream, moe_layer** out) {
 }  // extern "C"
 
 namespace {
-int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, bool residual, bool out_f32) {
+struct ResNorm {  // moe_forward_resnorm's outputs
+  const float* h_in;
+  float* h_out;
+  void* xn;
+  float eps;
+};
+
+int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, bool residual, bool out_f32,
+                 const ResNorm* rn = nullptr) {
   if (!L) return fail(MOE_EINVAL, "moe_forward: NULL layer");
   if (T < 0 || T > L->T_max) return fail(MOE_EINVAL, "moe_forward: T=%d outside 0..%d", T, L->T_max);
   if (T == 0) return MOE_OK;
@@ -463,6 +473,13 @@ int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, 
   P.y = y;
   P.residual = residual ? 1 : 0;
   P.out_f32 = out_f32 ? 1 : 0;
+  P.h_in = nullptr;
+  if (rn) {
+    P.h_in = rn->h_in;
+    P.h_out = rn->h_out;
+    P.xn = rn->xn;
+    P.eps = rn->eps;
+  }
   P.ready_target = 1;
   if (L->inject == 1) {
     P.ready_target = 2;  // published as 1: the routed tiles' wait runs out
@@ -485,6 +502,30 @@ int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* 
 
 int moe_forward_f32(moe_layer* L, const void* x, int32_t T, float* y, void* stream) {
   return forward_impl(L, x, T, y, stream, false, true);
+}
+
+int moe_forward_resnorm(moe_layer* L, const void* x, int32_t T, const float* h_in, float* h_out, void* xn, float eps,
+                        void* stream) {
+  if (!L) return fail(MOE_EINVAL, "moe_forward_resnorm: NULL layer");
+  if (T < 0 || T > kMaxSmallT || T > L->T_max)
+    return fail(MOE_EINVAL, "moe_forward_resnorm: T=%d outside 0..%d", T, std::min(kMaxSmallT, L->T_max));
+  if (T == 0) return MOE_OK;
+  if (!x || !h_in || !h_out || !xn) return fail(MOE_EINVAL, "moe_forward_resnorm: NULL argument");
+  if (!(eps >= 0.f) || eps > 1e30f) return fail(MOE_EINVAL, "moe_forward_resnorm: eps must be finite and >= 0");
+  if ((reinterpret_cast<uintptr_t>(h_in) | reinterpret_cast<uintptr_t>(h_out) | reinterpret_cast<uintptr_t>(xn)) & 15)
+    return fail(MOE_EINVAL, "moe_forward_resnorm: h_in, h_out and xn must be 16-byte aligned");
+  const size_t esz = L->act == MOE_ACT_BF16 ? 2 : 4, nh = (size_t)T * L->H * 4, nx = (size_t)T * L->H * esz;
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+  };
+  if (h_in != h_out && overlap(h_in, nh, h_out, nh))
+    return fail(MOE_EINVAL, "moe_forward_resnorm: h_in and h_out overlap without being the same rows");
+  if (overlap(x, nx, h_out, nh) || overlap(x, nx, xn, nx) || overlap(xn, nx, h_out, nh) || overlap(xn, nx, h_in, nh))
+    return fail(MOE_EINVAL, "moe_forward_resnorm: x, xn and h_out must not overlap (nor xn and h_in)");
+  const ResNorm rn{h_in, h_out, xn, eps};
+  // y is not written in this mode; h_out stands in for it in the checks
+  return forward_impl(L, x, T, h_out, stream, false, true, &rn);
 }
 
 int moe_get_routing(moe_layer* L, int32_t* ids, float* gates, int32_t* offsets, int32_t* perm, void* stream) {

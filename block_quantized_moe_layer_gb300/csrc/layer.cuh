@@ -30,6 +30,7 @@ struct Sync {
   int n_rent;                      // routed entries (written with the routing)
   alignas(128) int routing_aux;    // ids, gates, offsets, perm, pos written (after routing_ready)
   alignas(128) int exit_cnt;       // CTAs that left
+  alignas(128) int norm_cnt;       // residual-stream mode: 128-row blocks combined
 };
 
 // Phase stamps of one small-T launch (globaltimer, ns).  Each kind is kept
@@ -94,6 +95,15 @@ struct SmallParams {
   int residual;   // 1: y = x + MoE(x)
   int act_f32;    // 1: x and y are fp32 (check mode), else bf16
   int out_f32;    // 1: y is fp32 whatever the act dtype (moe_forward_f32)
+  // residual-stream mode (moe_forward_resnorm), when h_in is set: y is not
+  // written; h_out = h_in + MoE(x) in fp32 and xn = rmsnorm(h_out) in the act
+  // dtype (weight 1, eps); ssq [8][n_dt] holds each block's per-token sum of
+  // squares
+  const float* h_in;
+  float* h_out;
+  void* xn;
+  float eps;
+  float* ssq;
   // workspace
   Sync* sync;
   int* status;

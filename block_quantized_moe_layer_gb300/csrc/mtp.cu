@@ -1,13 +1,17 @@
 // mtp.cu -- the output head entry points and one MTP draft/verify round.
 //
 // mtp_round sequences, on the caller's stream: the pre-norm residual target
-// blocks, the output norm + LM head on the verify batch, the noisy draft rows,
+// blocks (one launch each: the layer adds its output to h and normalises the
+// next block's input), the output norm + LM head on the verify batch, the
+// noisy draft rows,
 // the draft heads, the LM head on the draft rows, their argmax, and greedy
 // acceptance.  Everything runs in this library's kernels; nothing allocates.
 // The residual stream (the hidden state h between blocks, and the noisy draft
 // rows) is kept in fp32 whatever the activation type; only the inputs and
 // outputs of the MoE layers are in the act dtype (as in the pages' runtime,
 // whose hidden states between operations are F32 tensors).
+#include <utility>
+
 #include "layer.cuh"
 
 namespace moe {
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const float* _
 size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct RoundLayout {
-  size_t hA, hB, xn, ytmp, hin, hout, rows, dlog, dprob, acc, total;
+  size_t hA, hB, xn, xn2, hin, hout, rows, dlog, dprob, acc, total;
 };
 RoundLayout round_layout(int H, int k, int V, int act) {
   const size_t esz = act == MOE_ACT_BF16 ? 2 : 4;
@@ -201,7 +205,7 @@ RoundLayout round_layout(int H, int k, int V, int act) {
   r.hA = take((size_t)(k + 1) * H * 4);  // residual stream: fp32
   r.hB = take((size_t)(k + 1) * H * 4);
   r.xn = take((size_t)(k + 1) * H * esz);
-  r.ytmp = take((size_t)(k + 1) * H * 4);  // layer outputs: fp32
+  r.xn2 = take((size_t)(k + 1) * H * esz);  // the normalised rows ping-pong with xn
   r.hin = take((size_t)k * k * H * esz);
   r.hout = take((size_t)k * k * H * esz);
   r.rows = take((size_t)k * H * 4);
@@ -346,7 +350,6 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   // target stack: pre-norm residual blocks h <- h + MoE(rmsnorm(h)); the
   // hidden state ping-pongs between hA and hB, xn holds the normalised rows
   void* xn = w + r.xn;
-  float* yt = reinterpret_cast<float*>(w + r.ytmp);
   float* hA = reinterpret_cast<float*>(w + r.hA);
   float* hB = reinterpret_cast<float*>(w + r.hB);
   // h_0 = x (to fp32), xn = rmsnorm(h_0)
@@ -355,16 +358,16 @@ int mtp_round(moe_layer* const* target_layers, int32_t n_target, moe_layer* cons
   else
     e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, x, (const float*)nullptr, hA, xn, H, eps);
   MCK(e, "mtp_round: norm");
+  // each layer adds its output to h in fp32 and normalises the next
+  // layer's input in the same launch (moe_forward_resnorm)
   float* cur = hA;
+  void* xin = xn;
+  void* xnext = w + r.xn2;
   for (int l = 0; l < n_target; ++l) {
     float* out = cur == hA ? hB : hA;
-    if ((rc = moe_forward_f32(target_layers[l], xn, k + 1, yt, stream))) return rc;
-    if (act == MOE_ACT_BF16)
-      e = launch_pdl(add_rmsnorm_kernel<2, 4>, k + 1, 256, 0, st, (const void*)cur, (const float*)yt, out, xn, H, eps);
-    else
-      e = launch_pdl(add_rmsnorm_kernel<4, 4>, k + 1, 256, 0, st, (const void*)cur, (const float*)yt, out, xn, H, eps);
-    MCK(e, "mtp_round: residual + norm");
+    if ((rc = moe_forward_resnorm(target_layers[l], xin, k + 1, cur, out, xnext, eps, stream))) return rc;
     cur = out;
+    std::swap(xin, xnext);
   }
   e = lm_forward(lm, cur, true, k + 1, eps, target_logits, st);
   MCK(e, "mtp_round: LM head (verify rows)");

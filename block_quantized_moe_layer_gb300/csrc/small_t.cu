@@ -1110,6 +1110,23 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
     acc.z += zs.z;
     acc.w += zs.w;
     const int64_t o = (int64_t)t * P.H + r;
+    if (P.h_in) {
+      // residual-stream mode: h_out = h_in + y in fp32 (h_in may be h_out),
+      // and this block's sum of squares of token t's row.  A warp's 32 lanes
+      // are one (block, token) here (32 units each; the CTA has whole
+      // warps), summed by a fixed shuffle tree.
+      const float4 hv = *reinterpret_cast<const float4*>(P.h_in + o);
+      acc.x += hv.x;
+      acc.y += hv.y;
+      acc.z += hv.z;
+      acc.w += hv.w;
+      *reinterpret_cast<float4*>(P.h_out + o) = acc;
+      float q = fmaf(acc.w, acc.w, fmaf(acc.z, acc.z, fmaf(acc.y, acc.y, acc.x * acc.x)));
+#pragma unroll
+      for (int off = 16; off; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+      if ((threadIdx.x & 31) == 0) P.ssq[t * P.n_dt + pend[1 + b]] = q;
+      continue;
+    }
     if (P.residual) {
       if constexpr (L == 2) {
         const uint2 xr = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(P.x) + o);
@@ -1133,6 +1150,45 @@ __device__ void combine_blocks(const SmallParams& P, uint8_t* smem, const SmemPl
       *reinterpret_cast<float4*>(reinterpret_cast<float*>(P.y) + o) = acc;
     }
   }
+}
+
+// Residual-stream mode, after this CTA combined `nb` blocks (all threads):
+// the CTA whose blocks complete the set normalises the rows,
+// xn[t] = h_out[t] / sqrt(mean(h_out[t]^2) + eps), from the blocks' sums of
+// squares taken in block order.  The other CTAs' h_out and sums were
+// released by their count increments (after a CTA barrier) and are acquired
+// by this CTA's own.
+template <int L>
+__device__ void norm_rows(const SmallParams& P, uint8_t* smem, const SmemPlan& plan, int nb) {
+  int* flags = reinterpret_cast<int*>(smem + plan.flags);
+  float* inv = reinterpret_cast<float*>(smem + plan.rred);  // free at this point
+  if (threadIdx.x == 0) {
+    const int old = atom_add_acq_rel(&P.sync->norm_cnt, nb);
+    flags[12] = (old + nb == P.n_dt);
+  }
+  __syncthreads();
+  if (!flags[12]) return;
+  if (threadIdx.x < P.T) {
+    float sq = 0.f;
+    for (int b = 0; b < P.n_dt; ++b) sq += __ldcg(P.ssq + threadIdx.x * P.n_dt + b);
+    inv[threadIdx.x] = 1.f / sqrtf(sq / (float)P.H + P.eps);
+  }
+  __syncthreads();
+  const int q4 = P.H / 4;
+  for (int u = threadIdx.x; u < P.T * q4; u += blockDim.x) {
+    const int t = u / q4;
+    const int64_t o = (int64_t)t * P.H + (int64_t)(u - t * q4) * 4;
+    const float4 h = __ldcg(reinterpret_cast<const float4*>(P.h_out + o));
+    const float s = inv[t];
+    if constexpr (L == 2) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(h.x * s, h.y * s), hi = __floats2bfloat162_rn(h.z * s, h.w * s);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(P.xn) + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(P.xn) + o) = make_float4(h.x * s, h.y * s, h.z * s, h.w * s);
+    }
+  }
+  if (threadIdx.x == 0) P.sync->norm_cnt = 0;  // every CTA has counted: ready for the next launch
 }
 
 template <int L>
@@ -1191,6 +1247,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     combine_blocks<L>(P, smem, plan, pend);
     __syncthreads();
     if (threadIdx.x == 0) stamp_last(P.stamps, kTsLastCombine);
+    if (P.h_in) norm_rows<L>(P, smem, plan, pend[0]);
   }
   // the last CTA out resets the cross-CTA counters for the next launch
   __syncthreads();

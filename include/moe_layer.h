@@ -158,6 +158,23 @@ int moe_forward_residual(moe_layer* L, const void* x, int32_t T, void* y, void* 
  * moe_forward, with y (4 T H bytes) 16-byte aligned and not overlapping x. */
 int moe_forward_f32(moe_layer* L, const void* x, int32_t T, float* y, void* stream);
 
+/* One pre-norm residual block's step of the residual stream, in the layer's
+ * own launch ("Support Step3.5/3.7 flash mtp3", "Overview": the target
+ * stack keeps F32 hidden states; the pre-norm residual reading of the block
+ * is this library's, h <- h + MoE(rmsnorm(h))):
+ *   h_out = h_in + MoE(x)                       (fp32 [T, H])
+ *   xn    = h_out / sqrt(mean(h_out^2) + eps)   (act dtype [T, H], weight 1)
+ * x [T, H] (act dtype) is the block's input, normally the previous step's
+ * xn.  The mean over the H columns of a row is summed per 128-column block
+ * and then over the blocks in order (fp32, deterministic).  Nothing is
+ * written to a y; the routing and the status are those of moe_forward.
+ *   0 <= T <= min(8, T_max); h_in, h_out, xn 16-byte aligned; h_in == h_out
+ *   (in place) or not overlapping it; x, xn, h_out pairwise disjoint, and xn
+ *   disjoint from h_in; eps finite and >= 0.  Asynchronous, no allocation.
+ * Errors: MOE_EINVAL (arguments), MOE_ECUDA. */
+int moe_forward_resnorm(moe_layer* L, const void* x, int32_t T, const float* h_in, float* h_out, void* xn, float eps,
+                        void* stream);
+
 /* Copies the routing of the last moe_forward (device-to-device, async on
  * `stream`): ids int32 [T, k] and gates fp32 [T, k] in slot order, offsets
  * int32 [E+1], perm int32 [T*k] (pair ids t*k+j grouped by expert, ascending
@@ -323,8 +340,10 @@ void moe_lm_head_destroy(moe_lm_head* lm);
  *   every draft);
  *   then greedy acceptance as mtp_verify_accept over the kept drafts.
  * The residual stream h and the noisy rows h~ are kept in fp32 in both
- * act dtypes: the target layers' inputs rmsnorm(h) are in act_dtype, their
- * outputs fp32 (moe_forward_f32); head outputs are in act_dtype.
+ * act dtypes: the target layers' inputs rmsnorm(h) are in act_dtype, and
+ * each layer adds its output to h in fp32 and normalises the next layer's
+ * input in its own launch (moe_forward_resnorm); head outputs are in
+ * act_dtype.
  * Every layer and the head must share act_dtype; all layers have hidden H,
  * T_max >= k+1.  noise fp32 [k][k][H] (device).  1 <= k <= 7.
  * workspace: device scratch of mtp_round_workspace_bytes(H, k, V, act)

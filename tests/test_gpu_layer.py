@@ -112,6 +112,44 @@ def test_verify_mixed_full_size(verify_mixed, T):
 
 
 @pytest.mark.parametrize("T", [1, 4, 8])
+def test_forward_resnorm_is_residual_add_then_rmsnorm(tiny, T):
+    """moe_forward_resnorm, one step of the residual stream: h_out = h_in + y
+    with y the fp32 output of moe_forward_f32, bit for bit (the same combine
+    sum, then one fp32 add); xn = rmsnorm(h_out) (weight 1, eps) up to the
+    fp32 summation order and, in bf16 mode, one rounding; y and xn against
+    the oracle within the layer's tolerance; in place (h_in is h_out) the
+    same; overlapping outputs are refused."""
+    w, L, ol, act = tiny
+    eps = 1e-6
+    g = torch.Generator(device="cuda").manual_seed(1234 + T)
+    h_in = torch.randn(T, w.H, generator=g, device="cuda", dtype=torch.float32)
+    x = (h_in / torch.sqrt((h_in * h_in).mean(dim=-1, keepdim=True) + eps)).to(XDT[act])
+    y32 = L.forward(x, out_f32=True)
+    h_out, xn = L.forward_resnorm(x, h_in, eps=eps)
+    torch.cuda.synchronize()
+    L.status()
+    assert torch.equal(h_out, h_in + y32)
+    ref_xn = h_out / torch.sqrt((h_out * h_out).mean(dim=-1, keepdim=True) + eps)
+    d = (xn.float() - ref_xn).abs()
+    if act == pkg.ACT_F32:
+        assert d.max().item() <= 1e-5 * ref_xn.abs().max().item()
+    else:
+        assert bool((d <= ref_xn.abs() * 2.0 ** -8 + 1e-6).all())
+    y_ref, r = omoe.forward(to_np(x), ol)
+    keep = ~omoe.near_tie_tokens(r["logits"], w.top_k)
+    assert omoe.max_rel_err(to_np(h_out - h_in)[keep], y_ref[keep]) <= TOL[act]
+    h_ref = to_np(h_in).astype(np.float64) + y_ref
+    xn_ref = h_ref / np.sqrt((h_ref * h_ref).mean(axis=-1, keepdims=True) + eps)
+    assert omoe.max_rel_err(to_np(xn)[keep], xn_ref[keep]) <= TOL[act]
+    h2 = h_in.clone()
+    _, xn2 = L.forward_resnorm(x, h2, h_out=h2, eps=eps)
+    torch.cuda.synchronize()
+    assert torch.equal(h2, h_out) and torch.equal(xn2, xn)
+    with pytest.raises(pkg.MoEError):
+        L.forward_resnorm(x, h_in, xn=x)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
 def test_forward_f32_is_the_unrounded_output(tiny, T):
     """moe_forward_f32 stores the combine's fp32 sum: in bf16 mode its rounding
     to bf16 is moe_forward's output bit for bit; in check mode it is that output."""
