@@ -26,6 +26,7 @@ constexpr int kLmThreads = (kLmConsumerWarps + 1) * 32;               // + the p
 constexpr int kLmTokens = 4;                                          // rows of x per launch (token group)
 constexpr int kLmMaxStages = 8;
 constexpr int kLmRecB = rec_bytes(2);                                 // 16-bit block fixed point
+constexpr int kLmRgBatch = 8;  // row groups whose warp partials are reduced together (one barrier pair)
 
 __global__ void lm_zero_kernel(uint8_t* __restrict__ p, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = 0;
@@ -43,14 +44,15 @@ struct LmParams {
 };
 
 struct LmPlan {
-  int ring, recs, red, bars, total;
+  int ring, recs, red, sq, bars, total;
 };
 __host__ __device__ inline LmPlan lm_plan(int H, int64_t chunk, int stages) {
   LmPlan p;
   p.ring = 0;
   p.recs = (int)(chunk * stages);
   p.red = p.recs + kLmTokens * (H / 32) * kLmRecB;
-  p.bars = p.red + kLmConsumerWarps * kLmTokens * 32 * 4 + kLmTokens * 8 * 4;
+  p.sq = p.red + kLmRgBatch * kLmConsumerWarps * kLmTokens * 32 * 4;
+  p.bars = p.sq + kLmTokens * 8 * 4;
   p.total = p.bars + 2 * kLmMaxStages * 8 + 16;
   return p;
 }
@@ -75,7 +77,25 @@ __device__ void lm_consume(const LmParams& P, uint8_t* smem, const LmPlan& plan,
   const int nbc = P.Kc / 32;
   float acc[kGroup];
   int i = 0;  // item (row group, chunk) counter of this block
-  for (int g = blockIdx.x; g < P.n_rg; g += gridDim.x) {
+  int j = 0;  // row groups of this block so far
+  // Each row group's per-warp partials go to their own slot; the slots of
+  // up to kLmRgBatch row groups are summed (in warp order) behind one
+  // barrier pair, so the consumers rarely stop streaming.
+  auto reduce = [&](int g_last, int n) {
+    consumer_sync();
+    for (int u = tid; u < n * T * 32; u += kLmConsumerWarps * 32) {
+      const int q = u / (T * 32), m = (u / 32) % T, l = u & 31;
+      const int gq = g_last - (n - 1 - q) * (int)gridDim.x;  // the row group of slot q
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kLmConsumerWarps; ++w) v += red[((q * kLmConsumerWarps + w) * kLmTokens + m) * 32 + l];
+      const int r = gq * 32 + l;
+      if (r < P.V) P.logits[(int64_t)m * P.V + r] = v;
+    }
+    consumer_sync();
+  };
+  int g = blockIdx.x;
+  for (; g < P.n_rg; g += gridDim.x, ++j) {
 #pragma unroll
     for (int m = 0; m < kGroup; ++m) acc[m] = 0.f;
     for (int c = 0; c < P.nch; ++c, ++i) {
@@ -86,19 +106,12 @@ __device__ void lm_consume(const LmParams& P, uint8_t* smem, const LmPlan& plan,
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // the 8 warps' shares of each row, summed in warp order
+    const int q = j % kLmRgBatch;
 #pragma unroll
-    for (int m = 0; m < T; ++m) red[(warp * kLmTokens + m) * 32 + lane] = acc[m];
-    consumer_sync();
-    if (tid < T * 32) {
-      const int m = tid >> 5, r = g * 32 + (tid & 31);
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kLmConsumerWarps; ++w) v += red[(w * kLmTokens + m) * 32 + (tid & 31)];
-      if (r < P.V) P.logits[(int64_t)m * P.V + r] = v;
-    }
-    consumer_sync();
+    for (int m = 0; m < T; ++m) red[((q * kLmConsumerWarps + warp) * kLmTokens + m) * 32 + lane] = acc[m];
+    if (q == kLmRgBatch - 1) reduce(g, kLmRgBatch);
   }
+  if (j % kLmRgBatch) reduce(g - (int)gridDim.x, j % kLmRgBatch);
 }
 
 template <int LIN>
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_stream_kernel(const __grid_c
       lm_wait(&full[j % P.stages], (uint32_t)((j / P.stages) & 1), P, 3);
   } else if (warp < kLmConsumerWarps) {
     // records of the normalised rows, [chunk][token][block] (consumers only)
-    float* sq = reinterpret_cast<float*>(smem + plan.red) + kLmConsumerWarps * kLmTokens * 32;  // [T][8]
+    float* sq = reinterpret_cast<float*>(smem + plan.sq);  // [T][8]
     for (int t = 0; t < P.T; ++t) {
       float ss = 0.f;
       for (int c = tid; c < P.H; c += kLmConsumerWarps * 32) {
@@ -159,18 +172,42 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_stream_kernel(const __grid_c
     }
     consumer_sync();
     const int nbc = P.Kc / 32;
-    for (int t = 0; t < P.T; ++t) {
+    float inv[kLmTokens];
+#pragma unroll
+    for (int t = 0; t < kLmTokens; ++t) {
       float ss = 0.f;
-      for (int w = 0; w < kLmConsumerWarps; ++w) ss += sq[t * 8 + w];
-      const float inv = 1.f / sqrtf(ss / (float)P.H + P.eps);
-      for (int b = warp; b < P.H / 32; b += kLmConsumerWarps) {
-        float v;
-        const int col = b * 32 + lane;
-        if constexpr (LIN == 2) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[(int64_t)t * P.H + col]);
-        else v = reinterpret_cast<const float*>(P.x)[(int64_t)t * P.H + col];
-        const int c = b / nbc, lb = b % nbc;
-        write_record<2>(v * inv, smem + plan.recs + (((int64_t)c * P.T + t) * nbc + lb) * kLmRecB);
-      }
+      if (t < P.T)
+        for (int w = 0; w < kLmConsumerWarps; ++w) ss += sq[t * 8 + w];
+      inv[t] = 1.f / sqrtf(ss / (float)P.H + P.eps);
+    }
+    // warp w takes blocks w, w + 8, ... of every row: 4 blocks x all rows are
+    // loaded at once, then turned into records (each a warp reduction), so
+    // the loads' latency is paid once per batch rather than per record
+    const int nb = P.H / 32;
+    for (int b0 = warp; b0 < nb; b0 += 4 * kLmConsumerWarps) {
+      float v[4][kLmTokens];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int t = 0; t < kLmTokens; ++t) {
+          const int b = b0 + i * kLmConsumerWarps;
+          v[i][t] = 0.f;
+          if (b < nb && t < P.T) {
+            const int64_t o = (int64_t)t * P.H + b * 32 + lane;
+            if constexpr (LIN == 2) v[i][t] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[o]);
+            else v[i][t] = reinterpret_cast<const float*>(P.x)[o];
+          }
+        }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int t = 0; t < kLmTokens; ++t) {
+          const int b = b0 + i * kLmConsumerWarps;
+          if (b < nb && t < P.T) {
+            const int c = b / nbc, lb = b - c * nbc;
+            write_record<2>(v[i][t] * inv[t], smem + plan.recs + (((int64_t)c * P.T + t) * nbc + lb) * kLmRecB);
+          }
+        }
     }
     consumer_sync();
     switch (P.T) {
@@ -192,9 +229,9 @@ size_t lm_weight_bytes(int V, int H, Chunking ch) {
   return (size_t)((V + 31) / 32) * ch.n * (size_t)chunk_bytes(MOE_Q8_0, ch.Kc);
 }
 
-// Chunking of the head's rows: chunks of at most 1024 columns, so that
-// several stages fit the ring beside the records.
-Chunking lm_chunking(int H) { return choose_chunking(MOE_Q8_0, H, 1); }
+// Chunking of the head's rows: chunks of at most 2048 columns (8 blocks per
+// consumer warp per stage), as large as two stages beside the records allow.
+Chunking lm_chunking(int H) { return choose_chunking(MOE_Q8_0, H, 0); }
 
 cudaError_t lm_repack(const uint8_t* src, uint8_t* dst, int V, int H, cudaStream_t st) {
   const Chunking ch = lm_chunking(H);
