@@ -284,29 +284,11 @@ __device__ __forceinline__ void write_record(float v, uint8_t* rec) {
     *reinterpret_cast<float4*>(rec + 32 * L) = make_float4(ldexpf(1.f, -s), record_sumx(sx, s), 0.f, 0.f);
 }
 
-// The same record as write_record, written by one thread for one block of 32
-// values read from shared memory (bf16 for L = 2, fp32 for L = 4).  The
-// arithmetic is the same.
+// The same record as write_record, written by one thread from the block's 32
+// values v (rec 16-byte aligned).  The arithmetic is the same, so the bytes
+// are the same.
 template <int L>
-__device__ __forceinline__ void write_record_lane(const uint8_t* src, uint8_t* rec) {
-  float v[32];
-#pragma unroll
-  for (int q = 0; q < (L == 2 ? 4 : 8); ++q) {
-    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
-    if constexpr (L == 2) {
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
-    } else {
-      v[4 * q] = __uint_as_float(u.x);
-      v[4 * q + 1] = __uint_as_float(u.y);
-      v[4 * q + 2] = __uint_as_float(u.z);
-      v[4 * q + 3] = __uint_as_float(u.w);
-    }
-  }
+__device__ __forceinline__ void record_from_values(const float (&v)[32], uint8_t* rec) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -336,6 +318,31 @@ __device__ __forceinline__ void write_record_lane(const uint8_t* src, uint8_t* r
   }
   *reinterpret_cast<float4*>(rec + 32 * L) =
       make_float4(ldexpf(1.f, -s), record_sumx(sx, s), 0.f, 0.f);
+}
+
+// The record of one block of 32 values read from shared memory (bf16 for
+// L = 2, fp32 for L = 4), by one thread.
+template <int L>
+__device__ __forceinline__ void write_record_lane(const uint8_t* src, uint8_t* rec) {
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < (L == 2 ? 4 : 8); ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
+    if constexpr (L == 2) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+      v[4 * q] = __uint_as_float(u.x);
+      v[4 * q + 1] = __uint_as_float(u.y);
+      v[4 * q + 2] = __uint_as_float(u.z);
+      v[4 * q + 3] = __uint_as_float(u.w);
+    }
+  }
+  record_from_values<L>(v, rec);
 }
 
 // Status bits written into the layer's status word.

@@ -180,34 +180,37 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_stream_kernel(const __grid_c
         for (int w = 0; w < kLmConsumerWarps; ++w) ss += sq[t * 8 + w];
       inv[t] = 1.f / sqrtf(ss / (float)P.H + P.eps);
     }
-    // warp w takes blocks w, w + 8, ... of every row: 4 blocks x all rows are
-    // loaded at once, then turned into records (each a warp reduction), so
-    // the loads' latency is paid once per batch rather than per record
+    // one thread per record (t, block): the block's 32 values of row t,
+    // times the row's 1/rms, into the record (no warp reductions)
     const int nb = P.H / 32;
-    for (int b0 = warp; b0 < nb; b0 += 4 * kLmConsumerWarps) {
-      float v[4][kLmTokens];
+    for (int u = tid; u < P.T * nb; u += kLmConsumerWarps * 32) {
+      const int t = u / nb, b = u - t * nb;
+      float v[32];
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(P.x) +
+                                                        ((int64_t)t * P.H + (int64_t)b * 32) * (LIN == 2 ? 2 : 4));
+      float sc = inv[0];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int m = 1; m < kLmTokens; ++m)
+        if (t == m) sc = inv[m];
 #pragma unroll
-        for (int t = 0; t < kLmTokens; ++t) {
-          const int b = b0 + i * kLmConsumerWarps;
-          v[i][t] = 0.f;
-          if (b < nb && t < P.T) {
-            const int64_t o = (int64_t)t * P.H + b * 32 + lane;
-            if constexpr (LIN == 2) v[i][t] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(P.x)[o]);
-            else v[i][t] = reinterpret_cast<const float*>(P.x)[o];
+      for (int q = 0; q < (LIN == 2 ? 4 : 8); ++q) {
+        const uint4 w4 = src[q];
+        if constexpr (LIN == 2) {
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * q + 2 * k] = __uint_as_float(w[k] << 16) * sc;
+            v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u) * sc;
           }
+        } else {
+          v[4 * q] = __uint_as_float(w4.x) * sc;
+          v[4 * q + 1] = __uint_as_float(w4.y) * sc;
+          v[4 * q + 2] = __uint_as_float(w4.z) * sc;
+          v[4 * q + 3] = __uint_as_float(w4.w) * sc;
         }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int t = 0; t < kLmTokens; ++t) {
-          const int b = b0 + i * kLmConsumerWarps;
-          if (b < nb && t < P.T) {
-            const int c = b / nbc, lb = b - c * nbc;
-            write_record<2>(v[i][t] * inv[t], smem + plan.recs + (((int64_t)c * P.T + t) * nbc + lb) * kLmRecB);
-          }
-        }
+      }
+      const int c = b / nbc, lb = b - c * nbc;
+      record_from_values<2>(v, smem + plan.recs + (((int64_t)c * P.T + t) * nbc + lb) * kLmRecB);
     }
     consumer_sync();
     switch (P.T) {
