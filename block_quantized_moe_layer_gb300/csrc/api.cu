@@ -482,7 +482,7 @@ int forward_impl(moe_layer* L, const void* x, int32_t T, void* y, void* stream, 
   }
   P.ready_target = 1;
   if (L->inject == 1) {
-    P.ready_target = 2;  // published as 1: the routed tiles' wait runs out
+    P.ready_target = 1 << 30;  // published as 1 + the routed entries: the routed tiles' wait runs out
     L->inject = 0;
   }
   CK(small_t_launch(P, L->act == MOE_ACT_BF16 ? 2 : 4, L->num_sms, L->smem_bytes, st), "moe_forward launch");
@@ -557,9 +557,10 @@ int moe_layer_status(moe_layer* L, void* stream) {
     CK(cudaMemset(L->ws, 0, counters + 16), "status reset");
     CK(small_t_init_logit_sums(L->sp, const_cast<long long*>(L->sp.lfx0), nullptr), "logit sums reset");
     CK(cudaDeviceSynchronize(), "status reset sync");
-    static const char* sites[] = {"?", "routing flag", "x records", "entry ready", "free stage", "full stage",
-                                   "end marker", "copy drain"};
-    const int site = (word[1] >= 0 && word[1] <= 7) ? word[1] : 0;
+    static const char* sites[] = {"?",          "routing flag",        "x records",           "entry ready",
+                                   "free stage", "full stage",          "end marker",          "copy drain",
+                                   "free reduction slot", "full reduction slot", "router logit words"};
+    const int site = (word[1] >= 0 && word[1] <= 10) ? word[1] : 0;
     return fail(MOE_ETIMEOUT, "a device-side wait timed out: %s (detail %d, block %d)", sites[site], word[2],
                 word[3]);
   }

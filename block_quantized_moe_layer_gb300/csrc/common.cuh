@@ -203,8 +203,20 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+// A strong (relaxed, GPU scope) 64-bit load: every call reads the word anew.
+__device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
+  long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Add with release semantics at GPU scope (no value returned).
+__device__ __forceinline__ void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Fetch-and-add with acquire and release semantics at GPU scope.
@@ -224,6 +236,17 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // Named barrier over the consumer warps only (the producer warp keeps going).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// The same barrier, returning whether any consumer thread passed true.
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r != 0;
 }
 
 // dp4a variants: a = weight bytes, b = activation limb bytes.

@@ -26,7 +26,7 @@ static_assert(sizeof(Entry) == 32, "Entry is copied as two 16-byte vectors");
 struct Sync {
   alignas(128) int queue;          // next tile to claim
   alignas(128) int router_done;    // router tiles finished (also: x records complete)
-  alignas(128) int routing_ready;  // routing published
+  alignas(128) int routing_ready;  // routing published: 1 + the routed entry count
   int n_rent;                      // routed entries (written with the routing)
   alignas(128) int routing_aux;    // ids, gates, offsets, perm, pos written (after routing_ready)
   alignas(128) int exit_cnt;       // CTAs that left
@@ -126,7 +126,7 @@ struct SmallParams {
   // shared-memory plan
   int n_stages, ring_bytes, misc_bytes;  // descriptor slots, bytes of the stage ring, router scratch
   uint64_t timeout_ns;
-  int ready_target;  // value of routing_ready the producers wait for: 1 (2 only under moe_layer_inject_timeout)
+  int ready_target;  // value of routing_ready the producers wait for: 1 (2^30 only under moe_layer_inject_timeout)
 };
 
 }  // namespace moe

@@ -103,15 +103,25 @@ __device__ inline void record_timeout(int* status, int site, int detail) {
 }
 
 enum WaitSite : int { kSiteRouting = 1, kSiteX = 2, kSiteEntry = 3, kSiteEmpty = 4, kSiteFull = 5, kSiteEnd = 6,
-                      kSiteDrain = 7, kSiteRedEmpty = 8, kSiteRedFull = 9 };
+                      kSiteDrain = 7, kSiteRedEmpty = 8, kSiteRedFull = 9, kSiteLogits = 10 };
 
-// Bounded spin on a global flag (acquire).  Returns false on timeout.
-__device__ inline bool wait_flag_geq(const int* p, int v, uint64_t limit_ns, int* status, int site, int detail) {
-  if (ld_acquire(p) >= v) return true;
+// Bounded spin on a global flag (acquire).  Returns false on timeout; the
+// value seen goes to *seen when given.
+__device__ inline bool wait_flag_geq(const int* p, int v, uint64_t limit_ns, int* status, int site, int detail,
+                                     int* seen = nullptr) {
+  int x = ld_acquire(p);
+  if (x >= v) {
+    if (seen) *seen = x;
+    return true;
+  }
   const uint64_t t0 = globaltimer_ns();
   int ns = 32;
   while (true) {
-    if (ld_acquire(p) >= v) return true;
+    x = ld_acquire(p);
+    if (x >= v) {
+      if (seen) *seen = x;
+      return true;
+    }
     if (ld_acquire(status) != 0) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       record_timeout(status, site, detail);
@@ -295,12 +305,14 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       rbt = (t - NR) % P.n_gu_sh;
     } else {
       if (n_rent < 0) {
-        if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t)) {
+        // the routing flag is published as 1 + the routed entry count
+        int ready = 0;
+        if (!wait_flag_geq(&P.sync->routing_ready, P.ready_target, P.timeout_ns, P.status, kSiteRouting, t, &ready)) {
           ok = false;
           break;
         }
         fence_proxy_async_global();
-        n_rent = __ldcg(&P.sync->n_rent);
+        n_rent = ready - 1;
         // the routed entries, in one bulk copy (their writers fenced them for
         // the async proxy before the routing flag)
         if (n_rent > 0) {
@@ -391,8 +403,10 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       const int s = issued & (NS - 1);
       write_desc(descs + s, g, q, pos);
       uint8_t* stage = smem + plan.ring + pos;
-      mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
-      if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
+      if (!(issued == 0 && (int)blockIdx.x < NR + NSG)) {  // (the first stage's weights are on their way)
+        mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
+        if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
+      }
       if (!dep_ok) {
         if (g.kind == kGateUp) {
           dep_ok = true;  // routed gate/up: gated by the routing flag (shared: waited above)
@@ -441,6 +455,43 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Batcher's odd-even merge sort network for N (a power of two) inputs, as a
+// comparator list in its iterative schedule (Knuth, TAOCP vol. 3, 5.3.4):
+// 63 comparators for N = 16, 191 for N = 32.
+struct SortNet {
+  int n;
+  unsigned char a[192], b[192];
+};
+template <int N>
+__host__ __device__ constexpr SortNet batcher_net() {
+  SortNet s{};
+  for (int p = 1; p < N; p <<= 1)
+    for (int k = p; k >= 1; k >>= 1)
+      for (int j = k % p; j + k < N; j += 2 * k)
+        for (int i = 0; i < k && i + j + k < N; ++i)
+          if ((i + j) / (2 * p) == (i + j + k) / (2 * p)) {
+            s.a[s.n] = (unsigned char)(i + j);
+            s.b[s.n] = (unsigned char)(i + j + k);
+            ++s.n;
+          }
+  return s;
+}
+
+// Sorts N 64-bit values into descending order in registers: comparator I
+// and then the rest, by recursion, so that every index is a compile-time
+// constant (entries known to be 0 fold away).
+template <int N, int I = 0>
+__device__ __forceinline__ void sort_desc(uint64_t (&c)[N]) {
+  constexpr SortNet net = batcher_net<N>();
+  if constexpr (I < net.n) {
+    constexpr int a = net.a[I], b = net.b[I];
+    const uint64_t x = c[a], y = c[b];
+    c[a] = x > y ? x : y;
+    c[b] = x > y ? y : x;
+    sort_desc<N, I + 1>(c);
+  }
+}
+
 // Largest of N values by a pairwise tree (depth log2 N).
 template <int N>
 __device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
@@ -454,65 +505,107 @@ __device__ __forceinline__ uint64_t tree_max(const uint64_t (&c)[N]) {
   return t[0];
 }
 
+__host__ __device__ constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 * pow2_at_least((n + 1) / 2); }
+
 // The k largest of one token's E logits by (value desc, index asc), one
 // warp, with the gates (softmax over the k selected logits, the sum by a
-// fixed shuffle tree), written in slot order.  Logit e is its fixed-point
-// sum (router slices plus the bias, in units of 2^-32) rounded once to fp32;
-// NaN counts as -inf.  Lane l holds experts l, l + 32, ... (NPER of them) as
-// 64-bit composites (order-preserving key of the value, then the
-// complemented index, so a larger composite is a larger value or, on equal
-// values, a lower index; 0 = none) and keeps its largest.  Each round takes
-// the exact maximum key over the lanes (a warp max); if several lanes hold
-// it, the lowest expert index among them wins (a second warp min, only
-// then).  The winning lane writes the slot, clears that expert and takes the
-// tree maximum of what it has left.  The rounds are a loop, not unrolled:
-// this code runs once per launch, so its size (instruction fetch) matters
-// more than its per-round cost.
+// fixed shuffle tree), written in slot order.
+//
+// Logit word (e, t) holds 256 S + n: S is the fixed-point sum (bias plus
+// router slices, in units of 2^-32) and n the number of slices added so far,
+// each slice one integer atomic.  The warp reads the token's words until
+// every one holds all n_kt slices (a bounded wait: false on timeout), so no
+// other flag has to order the slices before the read.  Logit e is S rounded
+// once to fp32.
+//
+// Lane l holds experts l, l + 32, ... (NPER of them) as 64-bit composites
+// (order-preserving key of the value, then the complemented index, so a
+// larger composite is a larger value or, on equal values, a lower index;
+// 0 = none) and sorts them.  Each round takes the exact maximum of the
+// lanes' heads (a warp max of the keys; if several lanes hold it, the lowest
+// expert index among them wins by a second warp min, only then); the winning
+// lane writes the slot and drops its head.
+//
 template <int NPER>
-__device__ __forceinline__ void topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
+__device__ __forceinline__ bool topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
   const int E = P.E, k = P.k;
-  // every load in flight before the first conversion
-  long long v[NPER];
+  constexpr int NP = pow2_at_least(NPER);
+  constexpr int NL = NP < kMaxTopK ? NP : kMaxTopK;  // (sorted lists) a lane wins at most k <= kMaxTopK rounds
+  uint64_t t0 = 0;
+  while (true) {
+    uint64_t c[NP];
+    bool done = true;
 #pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? __ldcg(P.lfx + (int64_t)e * kMaxSmallT + t) : 0ll;
-  }
-  uint64_t c[NPER];
-#pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    const float x = __ll2float_rn(v[i]) * 0x1p-32f;
-    c[i] = e < E ? ((uint64_t)order_key(x == x ? x : -INFINITY) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
-  }
-  uint64_t best = tree_max(c);
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const uint32_t key = (uint32_t)(best >> 32);
-    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t holders = __ballot_sync(0xffffffffu, best != 0ull && key == m);
-    int wl = __ffs(holders) - 1;
-    if (holders & (holders - 1u))
-      wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)best : 0x7fffffffu) & 31u);
-    if (lane == wl) {
-      const uint32_t wi = ~(uint32_t)best;
-      ids[j] = (int)wi;
-      vals[j] = key_value(m);
-      const int slot = (int)(wi >> 5);
-#pragma unroll
-      for (int i = 0; i < NPER; ++i)
-        if (i == slot) c[i] = 0ull;
-      best = tree_max(c);
+    for (int i = 0; i < NP; ++i) {
+      const int e = lane + 32 * i;
+      c[i] = 0ull;
+      if (i < NPER && e < E) {
+        const long long w = ld_relaxed_s64(P.lfx + (int64_t)e * kMaxSmallT + t);
+        if ((int)(w & 255) != P.n_kt) done = false;
+        const float x = __ll2float_rn(w >> 8) * 0x1p-32f;
+        c[i] = ((uint64_t)order_key(x) << 32) | (uint64_t)(~(uint32_t)e);
+      }
     }
-  }
-  __syncwarp();
-  const float l0 = vals[0];
-  const float ex = lane < k ? expf(vals[lane] - l0) : 0.f;
-  float sum = ex;
+    done = __all_sync(0xffffffffu, done);
+    if (done && t == 0 && lane == 0) stamp_last(P.stamps, kTsRouterDone);
+    if (done) {
+      // up to 16 per lane: sorted, the head dropped per win; more (E > 512):
+      // unsorted, the lane's best found again by a tree per win (a 32-input
+      // network needs more registers than the kernel has)
+      uint64_t best = 0ull;
+      if constexpr (NP <= 16) sort_desc(c);
+      else best = tree_max(c);
+#pragma unroll 1
+      for (int j = 0; j < k; ++j) {
+        const uint64_t b = NP <= 16 ? c[0] : best;
+        const uint32_t key = (uint32_t)(b >> 32);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t holders = __ballot_sync(0xffffffffu, b != 0ull && key == m);
+        int wl = __ffs(holders) - 1;
+        if (holders & (holders - 1u))
+          wl = (int)(__reduce_min_sync(0xffffffffu, (holders >> lane) & 1u ? ~(uint32_t)b : 0x7fffffffu) & 31u);
+        const bool win = lane == wl;
+        if (win) {
+          ids[j] = (int)~(uint32_t)b;
+          vals[j] = key_value(m);
+        }
+        if constexpr (NP <= 16) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) gates[lane] = ex / sum;
+          for (int i = 0; i + 1 < NL; ++i) c[i] = win ? c[i + 1] : c[i];
+          c[NL - 1] = win ? 0ull : c[NL - 1];
+        } else if (win) {
+          const int slot = (int)((~(uint32_t)b) >> 5);
+#pragma unroll
+          for (int i = 0; i < NP; ++i)
+            if (i == slot) c[i] = 0ull;
+          best = tree_max(c);
+        }
+      }
+      __syncwarp();
+      const float l0 = vals[0];
+      const float ex = lane < k ? expf(vals[lane] - l0) : 0.f;
+      float sum = ex;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane < k) gates[lane] = ex / sum;
+      __syncwarp();
+      break;
+    }
+    int stop = 0;
+    if (lane == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > P.timeout_ns) {
+        record_timeout(P.status, kSiteLogits, t);
+        stop = 1;
+      } else if (ld_acquire(P.status) != 0) {
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+  return true;
 }
 
 // Scratch of finalize_routing in the misc region (bytes, see finalize_misc_bytes).
@@ -536,9 +629,12 @@ __host__ __device__ inline FinLayout fin_layout(int T, int E, int k) {
 }
 int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).end + 16; }
 
-// Runs on the consumer threads of the CTA that finished the last router
-// tile: logits, top-k and gates, then the permutation and the routed work
-// entries.  The entries and their count are published first (routing_ready);
+// Runs on the consumer threads of one CTA: logits, top-k and gates, then the
+// permutation and the routed work entries.  Polled (the usual case: fewer
+// router tiles than CTAs): the last CTA, which has no router tile, runs it
+// as soon as every logit word holds all its slices; it acquires the router
+// count only to publish the x records with the routing.  Otherwise the CTA
+// that counted the last router tile runs it (the count orders the slices).  The entries and their count are published first (routing_ready);
 // ids, gates, offsets, perm and pos follow (routing_aux), since only the
 // combine and moe_get_routing read them.  A layer that holds only the routed
 // experts [e0, e0 + n_e) (one shard of an expert-parallel split) routes over
@@ -550,12 +646,14 @@ int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).end + 
 // slot is lt + rank (experts ascending, tokens ascending within an expert).
 // The first pair of an expert owns that expert's entries: its entry index is
 // the number of entries of all lower experts.
-__device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend) {
+//
+// Not inlined: one copy of the code for both callers (and both activation
+// widths), and its registers are its own.
+__device__ __noinline__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend, bool polled) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NT = kConsumerWarps * 32;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
   const FinLayout f = fin_layout(T, E, k);
-  float* lg = reinterpret_cast<float*>(misc + f.lg);    // [T*E]
   int* sid = reinterpret_cast<int*>(misc + f.sid);      // [Tk]
   float* sl = reinterpret_cast<float*>(misc + f.sl);    // [Tk]
   float* sg = reinterpret_cast<float*>(misc + f.sg);    // [Tk]
@@ -565,17 +663,28 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   int* srank = reinterpret_cast<int*>(misc + f.srank);  // [Tk] earlier pairs of the same expert
   int* sent = reinterpret_cast<int*>(misc + f.sent);    // [Tk] entries owned (first pair of an expert)
 
-  // (the router counter was taken with acquire semantics)
   // top-k and gates per token, one warp per token, straight from the
   // fixed-point logit sums
-  (void)lg;
-#pragma unroll 1
+  bool ok = true;
+  #pragma unroll 1
   for (int t = warp; t < T; t += kConsumerWarps) {
-    if (E <= 128) topk_token<4>(P, t, sid + t * k, sl + t * k, sg + t * k);
-    else if (E <= 384) topk_token<12>(P, t, sid + t * k, sl + t * k, sg + t * k);
-    else topk_token<kMaxE / 32>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    bool r;
+    if (E <= 128) r = topk_token<4>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    else if (E <= 384) r = topk_token<12>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    else r = topk_token<kMaxE / 32>(P, t, sid + t * k, sl + t * k, sg + t * k);
+    ok = ok && r;
   }
-  consumer_sync();
+  // polled: a warp without a token (warp 0 after its own, at T = 8) acquires
+  // the router count, so that thread 0's release of the routing below also
+  // publishes the x records
+  const int xw = T < kConsumerWarps ? T : 0;
+  if (polled && warp == xw && lane == 0) {
+    if (wait_flag_geq(&P.sync->router_done, P.n_rg * P.n_kt, P.timeout_ns, P.status, kSiteX, -1))
+      stamp_last(P.stamps, kTsXDone);
+    else
+      ok = false;
+  }
+  if (consumer_sync_or(!ok)) return;  // a wait timed out: the status word says which
   // (stamps here come from warp 1: the release below is thread 0's, and a
   // release waits for its own thread's earlier writes)
   if (tid == 32) stamp_last(P.stamps, kTsTopkDone);
@@ -593,7 +702,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
       const int ekey = act ? sid[lane] : 1024;
       int lt = 0;
       uint32_t eq = 0xffffffffu;
-#pragma unroll
+  #pragma unroll
       for (int b = 10; b >= 0; --b) {
         const bool bit = (ekey >> b) & 1;
         const uint32_t ones = __ballot_sync(0xffffffffu, bit);
@@ -617,7 +726,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
       const uint32_t starts = __ballot_sync(0xffffffffu, act && own && r_i % kGroup == 0);
       int tk[kGroup];
       tk[0] = tok;
-#pragma unroll
+  #pragma unroll
       for (int m = 1; m < kGroup; ++m) tk[m] = __shfl_down_sync(0xffffffffu, tok, m);
       if ((starts >> lane) & 1u) {
         const int M = min(kGroup, c_i - r_i);
@@ -636,11 +745,11 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
     if (tid < Tk) {
       const int p = tid, e = sid[p];
       int lt = 0, rank = 0, c = 0;
-#pragma unroll 4
+  #pragma unroll 4
       for (int q4 = 0; q4 < nq4; ++q4) {
         const int4 v = sid4[q4];
         const int ev[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
+  #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int q = 4 * q4 + u;
           if (q < Tk) {
@@ -663,22 +772,22 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
     if (tid < Tk && srank[tid] == 0) {
       const int e = sid[tid], lt = slt[tid], ne = sent[tid];
       int w0 = 0, c = 0;
-#pragma unroll 4
+  #pragma unroll 4
       for (int q4 = 0; q4 < nq4; ++q4) {
         const int4 v = sid4[q4], n = sent4[q4];
         const int ev[4] = {v.x, v.y, v.z, v.w}, nv[4] = {n.x, n.y, n.z, n.w};
-#pragma unroll
+  #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (4 * q4 + u < Tk) {
             w0 += ev[u] < e ? nv[u] : 0;
             c += ev[u] == e;
           }
       }
-#pragma unroll 1
+  #pragma unroll 1
       for (int g = 0; g < ne; ++g) {
         const int slot0 = lt + g * kGroup, M = min(kGroup, c - g * kGroup);
         int tok[kGroup];
-#pragma unroll
+  #pragma unroll
         for (int m = 0; m < kGroup; ++m) tok[m] = m < M ? sperm[slot0 + m] / k : 0;
         int4* dst = reinterpret_cast<int4*>(P.entries + P.n_sh + w0 + g);
         dst[0] = make_int4(e - P.e0, slot0, M, tok[0]);
@@ -687,11 +796,11 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
       fence_proxy_async_global();  // the producers fetch the entries with a bulk copy
     }
     if (tid == 0) {
-#pragma unroll 4
+  #pragma unroll 4
       for (int q4 = 0; q4 < nq4; ++q4) {
         const int4 n = sent4[q4];
         const int nv[4] = {n.x, n.y, n.z, n.w};
-#pragma unroll
+  #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (4 * q4 + u < Tk) n_rent += nv[u];
       }
@@ -703,7 +812,7 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
   if (tid == 32) stamp_last(P.stamps, kTsEntriesDone);
   if (tid == 0) {
     P.sync->n_rent = n_rent;
-    st_release(&P.sync->routing_ready, 1);
+    st_release(&P.sync->routing_ready, 1 + n_rent);
     stamp_last(P.stamps, kTsRoutingReady);
     *nrent_s = n_rent;
   }
@@ -749,40 +858,97 @@ __device__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend)
 
 // Router tile dot products: lane = expert row, warp w takes float4 columns
 // w, w + 8, ... of the slice; T tokens (compile time), four independent
-// accumulators per token (one per float4 component).
+// accumulators per token (one per float4 component).  A full 512-column
+// slice loads its columns in batches (weights and x first, then the FMAs),
+// so that the shared-memory latency is paid once per batch.
 template <int L, int T>
 __device__ __forceinline__ void router_dot(const float4* wst, const uint8_t* xs, int cols, float (&racc)[kMaxSmallT]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int XEL = L == 2 ? 2 : 4;
   float ra[T][4];
 #pragma unroll
   for (int t = 0; t < T; ++t)
 #pragma unroll
     for (int c = 0; c < 4; ++c) ra[t][c] = 0.f;
-  const int ncol4 = cols / 4;
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int k4 = warp + kConsumerWarps * i;
-    if (k4 < ncol4) {
-      const float4 w = wst[k4 * 32 + lane];
+  auto fma4 = [&](const float4& w, const uint8_t* xp, int t) {
+    float4 xv;
+    if constexpr (L == 2) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(xp);
+      xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
+                       __uint_as_float(raw.y & 0xFFFF0000u));
+    } else {
+      xv = *reinterpret_cast<const float4*>(xp);
+    }
+    ra[t][0] = fmaf(w.x, xv.x, ra[t][0]);
+    ra[t][1] = fmaf(w.y, xv.y, ra[t][1]);
+    ra[t][2] = fmaf(w.z, xv.z, ra[t][2]);
+    ra[t][3] = fmaf(w.w, xv.w, ra[t][3]);
+  };
+  if (cols == kRouterTileChunks * kRouterCc) {
+    constexpr int NI = kRouterTileChunks * kRouterCc / 4 / kConsumerWarps;  // 16 columns of float4 per warp
+    constexpr int B = (T <= 4 && L == 2) ? 8 : 4;                            // columns per batch
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
-        float4 xv;
-        if constexpr (L == 2) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(xs + (t * cols + k4 * 4) * 2);
-          xv = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-        } else {
-          xv = *reinterpret_cast<const float4*>(xs + (t * cols + k4 * 4) * 4);
+    for (int h = 0; h < NI / B; ++h) {
+      float4 w[B];
+      uint4 xr[B][T];  // the x values of column group k4 (8 or 16 bytes per token)
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        const int k4 = warp + kConsumerWarps * (B * h + i);
+        w[i] = wst[k4 * 32 + lane];
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          if constexpr (L == 2) {
+            const uint2 r = *reinterpret_cast<const uint2*>(xs + (t * cols + k4 * 4) * XEL);
+            xr[i][t] = make_uint4(r.x, r.y, 0u, 0u);
+          } else {
+            xr[i][t] = *reinterpret_cast<const uint4*>(xs + (t * cols + k4 * 4) * XEL);
+          }
         }
-        ra[t][0] = fmaf(w.x, xv.x, ra[t][0]);
-        ra[t][1] = fmaf(w.y, xv.y, ra[t][1]);
-        ra[t][2] = fmaf(w.z, xv.z, ra[t][2]);
-        ra[t][3] = fmaf(w.w, xv.w, ra[t][3]);
+      }
+#pragma unroll
+      for (int i = 0; i < B; ++i)
+#pragma unroll
+        for (int t = 0; t < T; ++t) fma4(w[i], reinterpret_cast<const uint8_t*>(&xr[i][t]), t);
+    }
+  } else {
+    const int ncol4 = cols / 4;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int k4 = warp + kConsumerWarps * i;
+      if (k4 < ncol4) {
+        const float4 w = wst[k4 * 32 + lane];
+#pragma unroll
+        for (int t = 0; t < T; ++t) fma4(w, xs + (t * cols + k4 * 4) * XEL, t);
       }
     }
   }
 #pragma unroll
   for (int t = 0; t < kMaxSmallT; ++t) racc[t] = t < T ? (ra[t][0] + ra[t][1]) + (ra[t][2] + ra[t][3]) : 0.f;
+}
+
+struct RouterAcc {
+  float v[kMaxSmallT];
+};
+
+// One router tile's dot products for T tokens (runtime).  Not inlined: a
+// router CTA runs this code once per launch, so its instructions are cold;
+// its consumer warps call it once on the stage before the dependency wait
+// (weights in flight, x not there yet, results discarded) and then find it
+// warm for the real call.
+template <int L>
+__device__ __noinline__ RouterAcc router_tile_dot(const float4* wst, const uint8_t* xs, int cols, int T) {
+  RouterAcc r;
+  switch (T) {
+    case 1: router_dot<L, 1>(wst, xs, cols, r.v); break;
+    case 2: router_dot<L, 2>(wst, xs, cols, r.v); break;
+    case 3: router_dot<L, 3>(wst, xs, cols, r.v); break;
+    case 4: router_dot<L, 4>(wst, xs, cols, r.v); break;
+    case 5: router_dot<L, 5>(wst, xs, cols, r.v); break;
+    case 6: router_dot<L, 6>(wst, xs, cols, r.v); break;
+    case 7: router_dot<L, 7>(wst, xs, cols, r.v); break;
+    default: router_dot<L, 8>(wst, xs, cols, r.v); break;
+  }
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -808,6 +974,10 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
   float acc[kGroup];
   float racc[kMaxSmallT];
   bool st_routed = false;  // (thread 0) first routed gate/up stage stamped
+  // With fewer router tiles than CTAs the last CTA has none (its items are
+  // all claimed past the router's); it routes first, polling the logits.
+  const bool polled = P.n_rg * P.n_kt < (int)gridDim.x;
+  if (polled && blockIdx.x == gridDim.x - 1) finalize_routing(P, misc, reinterpret_cast<int*>(smem + plan.pend), true);
 
   while (true) {
     if (!mbar_wait_bounded(&full[s], ph, P.timeout_ns, P.status, kSiteFull, s)) break;
@@ -842,65 +1012,68 @@ __device__ void consumer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       const int ncc = d.nbc, cols = ncc * kRouterCc;
       const float4* wst = reinterpret_cast<const float4*>(stage);
       const uint8_t* xs = stage + cols * kRows * 4;
-      switch (T) {
-        case 1: router_dot<L, 1>(wst, xs, cols, racc); break;
-        case 2: router_dot<L, 2>(wst, xs, cols, racc); break;
-        case 3: router_dot<L, 3>(wst, xs, cols, racc); break;
-        case 4: router_dot<L, 4>(wst, xs, cols, racc); break;
-        case 5: router_dot<L, 5>(wst, xs, cols, racc); break;
-        case 6: router_dot<L, 6>(wst, xs, cols, racc); break;
-        case 7: router_dot<L, 7>(wst, xs, cols, racc); break;
-        default: router_dot<L, 8>(wst, xs, cols, racc); break;
+      {
+        const RouterAcc r = router_tile_dot<L>(wst, xs, cols, T);
+#pragma unroll
+        for (int t = 0; t < kMaxSmallT; ++t) racc[t] = r.v[t];
+      }
+#pragma unroll
+      for (int t = 0; t < kMaxSmallT; ++t)
+        if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
+      consumer_sync();
+      if (tid < T * 32) {
+        // this slice's share of logit (t, expert 32 rg + r), added as an
+        // exact integer multiple of 2^-32 to a sum that starts from the bias,
+        // together with one count in the word's low 8 bits: the total does
+        // not depend on the order in which the slices arrive, and the word
+        // says by itself when it is complete.  A share saturates at 2^17 in
+        // magnitude (a NaN share counts as -2^17), so that n_kt <= 32 slices
+        // and the bias never overflow the word.
+        const int t = tid >> 5, r = tid & 31;
+        float v = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
+        const float q = fminf(fmaxf(v * 4294967296.f, -0x1p49f), 0x1p49f);
+        atomicAdd(reinterpret_cast<unsigned long long*>(P.lfx) + (int64_t)(d_rg * 32 + r) * kMaxSmallT + t,
+                  ((unsigned long long)__float2ll_rn(q) << 8) + 1ull);
       }
       if (d_rg == 0) {
-        // the first row group's tiles also turn their slice of x into the
-        // activation records (one 32-column block per thread); the proxy
+        // after the logit shares (they start the routing): the first row
+        // group's tiles also turn their slice of x into the activation
+        // records, one 32-column block per thread from warp 4 on; the proxy
         // fence makes them visible to the bulk copies that read them once
         // every router tile has counted itself done
         const int kt = d_ks / kRouterTileChunks, nb = cols / 32;
         constexpr int XEL = L == 2 ? 2 : 4;
-        if (tid < T * nb) {
-          const int t = tid / nb, b = tid - (tid / nb) * nb;
+        const int i = tid - 4 * 32;
+        if (i >= 0 && i < T * nb) {
+          const int t = i / nb, b = i - (i / nb) * nb;
           write_record_lane<L>(xs + (t * cols + b * 32) * XEL,
                                P.xrec + ((int64_t)t * (P.H / 32) + kt * (kRouterTileChunks * kRouterCc / 32) + b) * RB);
           fence_proxy_async_global();
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-      for (int t = 0; t < kMaxSmallT; ++t)
-        if (t < T) rred[(warp * kMaxSmallT + t) * 32 + lane] = racc[t];
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage (weights, x slice) is read
+      // the barrier orders every thread's record writes (and additions)
+      // before thread 0's release count, which the shared expert's records
+      // and, through the routing, the routed tiles' records wait for
       consumer_sync();
-      // (the barriers also order every thread's record writes before thread
-      // 0's release of router_done, which the shared expert's records and,
-      // through the routing, the routed tiles' records wait for)
-      if (tid < T * 32) {
-        // this slice's share of logit (t, expert 32 rg + r), added as an
-        // exact integer multiple of 2^-32 to a sum that starts from the bias:
-        // the total does not depend on the order in which the slices arrive
-        const int t = tid >> 5, r = tid & 31;
-        float v = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) v += rred[(w * kMaxSmallT + t) * 32 + r];
-        atomicAdd(reinterpret_cast<unsigned long long*>(P.lfx) + (int64_t)(d_rg * 32 + r) * kMaxSmallT + t,
-                  (unsigned long long)__float2ll_rn(v * 4294967296.f));
-      }
-      // the barrier orders every thread's additions before thread 0's
-      // release (acquire-release) count
-      consumer_sync();
-      if (tid == 0) {
-        const int old = atom_add_acq_rel(&P.sync->router_done, 1);
-        flags[0] = (old == P.n_rg * P.n_kt - 1);
-      }
-      consumer_sync();
-      if (flags[0]) {
-        if (tid == 32) {
-          stamp_last(P.stamps, kTsXDone);  // the x records are written by router tiles
-          stamp_last(P.stamps, kTsRouterDone);
+      if (polled) {
+        // the routing CTA reads the logit words by themselves; the count
+        // publishes this tile's x records
+        if (tid == 0) red_add_release(&P.sync->router_done, 1);
+      } else {
+        if (tid == 0) {
+          const int old = atom_add_acq_rel(&P.sync->router_done, 1);
+          flags[0] = (old == P.n_rg * P.n_kt - 1);
         }
-        finalize_routing(P, misc, reinterpret_cast<int*>(smem + plan.pend));
+        consumer_sync();
+        if (flags[0]) {
+          if (tid == 32) stamp_last(P.stamps, kTsXDone);  // the x records are written by router tiles
+          finalize_routing(P, misc, reinterpret_cast<int*>(smem + plan.pend), false);
+        }
+        consumer_sync();
       }
-      consumer_sync();
     } else {
       // gate/up or down: one chunk of a group, or gps whole groups of one
       // chunk each (their weights back to back, then the shared records)
@@ -1206,13 +1379,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
   griddep_launch_dependents();
   const uint64_t t_entry = globaltimer_ns();
   if (threadIdx.x == 0) {
-    // constant data only: warm L2 with one router tile's weights (tile = block)
-    if ((int)blockIdx.x < P.n_rg * P.n_kt) {
-      const int rg = blockIdx.x / P.n_kt, kt = blockIdx.x % P.n_kt;
-      const int nbc = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * kt);
-      prefetch_l2(P.router + ((int64_t)rg * P.n_ks * 64 + kRouterTileChunks * 32 * kt) * kRows * 16,
-                  (uint32_t)(nbc * chunk_bytes(MOE_F32, kRouterCc)));
-    }
     pend[0] = 0;
     flags[3] = 0;  // the combine's routing arrays are not in shared memory yet
     for (int i = 0; i < P.n_stages; ++i) {
@@ -1225,6 +1391,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     }
     mbar_init(reinterpret_cast<uint64_t*>(smem + plan.ebar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // constant data only: the weights of this block's first stage (its first
+  // item, a router tile or a shared gate/up tile, stage 0 at ring offset 0)
+  // are copied before the dependency wait, while the previous launch ends;
+  // the producer adds the activations to the same stage after it
+  const int n_early = P.n_rg * P.n_kt + P.n_sh * P.n_gu_sh;
+  if (threadIdx.x == kProducerWarp * 32 && (int)blockIdx.x < n_early) {
+    const int b = blockIdx.x, nr = P.n_rg * P.n_kt;
+    const Geo g = b < nr ? geo_router<L>(P, b / P.n_kt, b % P.n_kt)
+                         : geo_expert<L>(P, kGateUp, (b - nr) / P.n_gu_sh, (b - nr) % P.n_gu_sh, nullptr);
+    mbar_arrive_expect_tx(&full[0], g.wb + (uint32_t)g.M * g.per);
+    bulk_g2s_hint(smem + plan.ring, g.wbase, g.wb, &full[0], l2_evict_first_policy());
+  } else if ((threadIdx.x >> 5) < kConsumerWarps && (int)blockIdx.x < P.n_rg * P.n_kt) {
+    // warm the router tile's code on the stage (its bytes still arriving;
+    // the result is discarded, only its instructions are wanted)
+    const int cols = min(kRouterTileChunks, P.n_rc - kRouterTileChunks * ((int)blockIdx.x % P.n_kt)) * kRouterCc;
+    const RouterAcc r = router_tile_dot<L>(reinterpret_cast<const float4*>(smem + plan.ring),
+                                           smem + plan.ring + cols * kRows * 4, cols, P.T);
+    asm volatile("" ::"f"(r.v[0]));
   }
   griddep_wait();  // x, the workspace and its counters are the previous launches' to finish with
   if (threadIdx.x == 0) {
@@ -1287,15 +1473,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// The router logit sums' starting value: the bias in units of 2^-32 (exact
-// for |b| >= 2^-8, rounded to the nearest 2^-32 below that), written to the
+// The router logit words' starting value: the bias in units of 2^-32 (exact
+// for |b| >= 2^-8, rounded to the nearest 2^-32 below that; saturated at
+// 2^17 in magnitude), times 256 (no slices counted yet), written to the
 // table lfx0 and to every token column of lfx.
 __global__ void logit_sums_init_kernel(const float* __restrict__ bias, int E, int E_pad, long long* __restrict__ lfx0,
                                        long long* __restrict__ lfx) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= E_pad * kMaxSmallT) return;
   const int e = i / kMaxSmallT;
-  const long long v = (bias && e < E) ? __float2ll_rn(bias[e] * 4294967296.f) : 0ll;
+  const float q = (bias && e < E) ? fminf(fmaxf(bias[e] * 4294967296.f, -0x1p49f), 0x1p49f) : 0.f;
+  const long long v = (long long)((unsigned long long)__float2ll_rn(q) << 8);
   lfx[i] = v;
   if (i % kMaxSmallT == 0) lfx0[e] = v;
 }
