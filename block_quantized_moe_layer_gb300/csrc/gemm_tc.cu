@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kNA; ++s) {
       mbar_init(&afull[s], 1);
@@ -256,6 +257,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) lt_gemm_kernel(const LtGemmPa
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
+  // setup only above: the previous kernel in the stream wrote the items,
+  // operands and counters read below (or reads what this one writes)
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -644,8 +648,7 @@ cudaError_t lt_gemm_configure() {
 }
 
 cudaError_t lt_gemm_launch(const LtGemmParams& p, int grid, cudaStream_t st) {
-  lt_gemm_kernel<<<grid, kGemmThreads, kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(lt_gemm_kernel, grid, kGemmThreads, kSmemBytes, st, p);
 }
 
 }  // namespace moe

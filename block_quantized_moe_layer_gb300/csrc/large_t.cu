@@ -171,11 +171,14 @@ struct PrepParams {
 };
 
 constexpr int kColSlices = 8;  // column slices per token tile in the operand-image kernels
+constexpr int kImgBatch = 4;   // loads in flight per thread in the operand-image kernels
 
 // Block (tt, cs) writes column slice cs of plain token tile tt (x rows
 // [64 tt, 64 tt + 64)) into the operand image; block (0, 0) also writes the
 // plain token tiles, which the router and the shared expert use.
 __global__ void lt_prep_kernel(const PrepParams P) {
+  griddep_launch_dependents();
+  griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   const int tt = blockIdx.x, cs = blockIdx.y;
   const int n = min(kLtMaxN, P.T - kLtMaxN * tt), n_pad = round16(n);
   if (tt == 0 && cs == 0) {
@@ -187,11 +190,22 @@ __global__ void lt_prep_kernel(const PrepParams P) {
   }
   uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)kLtMaxN * tt * P.H * 2);
   const int nc = P.H / 8 / kColSlices, c0 = cs * nc;
-  for (int idx = threadIdx.x; idx < n_pad * nc; idx += blockDim.x) {
-    const int r = idx % n_pad, c = c0 + idx / n_pad;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c));
-    dst[(int64_t)c * n_pad + r] = v;
+  // kImgBatch independent 16-byte loads in flight per thread, then their stores
+  const int total = n_pad * nc;
+  for (int base = threadIdx.x; base < total; base += kImgBatch * blockDim.x) {
+    uint4 v[kImgBatch];
+#pragma unroll
+    for (int u = 0; u < kImgBatch; ++u) {
+      const int idx = base + u * blockDim.x;
+      const int r = idx % n_pad, c = c0 + idx / n_pad;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (idx < total && r < n) v[u] = *reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c);
+    }
+#pragma unroll
+    for (int u = 0; u < kImgBatch; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < total) dst[(int64_t)(c0 + idx / n_pad) * n_pad + idx % n_pad] = bf16x8_to_f16x8(v[u]);
+    }
   }
 }
 
@@ -203,6 +217,8 @@ __device__ __forceinline__ bool topk_better(float v, int i, float bv, int bi) {
 template <int NPER>
 __global__ void lt_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                                int E_pad, int k, int* __restrict__ ids, float* __restrict__ gates) {
+  griddep_launch_dependents();
+  griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const int64_t plane = (int64_t)T * E_pad;
@@ -313,6 +329,8 @@ constexpr int kPermChunk = 512;  // tokens per pass (16 bitmap words per expert)
 // passes.  The k experts of one token are distinct, so the order of pairs
 // within an expert is the order of their tokens.
 __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermParams P) {
+  griddep_launch_dependents();
+  griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   extern __shared__ int psm[];
   const int E = P.E, k = P.k, T = P.T;
   constexpr int W = kPermChunk / 32;
@@ -395,6 +413,8 @@ __global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermPara
 __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm,
                                  const LtTile* __restrict__ tiles, const int* __restrict__ counters, int n_sh, int k,
                                  int H, uint8_t* __restrict__ xg) {
+  griddep_launch_dependents();
+  griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   if ((int)blockIdx.x >= counters[9]) return;
   const LtTile tl = tiles[n_sh + blockIdx.x];
   __shared__ int tok[kLtMaxN];
@@ -402,11 +422,22 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
   __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>(xg + (int64_t)tl.prow0 * H * 2);
   const int nc = H / 8 / kColSlices, c0 = blockIdx.y * nc;
-  for (int idx = threadIdx.x; idx < tl.n_pad * nc; idx += blockDim.x) {
-    const int r = idx % tl.n_pad, c = c0 + idx / tl.n_pad;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < tl.n) v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c));
-    dst[(int64_t)c * tl.n_pad + r] = v;
+  // kImgBatch independent 16-byte loads in flight per thread, then their stores
+  const int total = tl.n_pad * nc;
+  for (int base = threadIdx.x; base < total; base += kImgBatch * blockDim.x) {
+    uint4 v[kImgBatch];
+#pragma unroll
+    for (int u = 0; u < kImgBatch; ++u) {
+      const int idx = base + u * blockDim.x;
+      const int r = idx % tl.n_pad, c = c0 + idx / tl.n_pad;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (idx < total && r < tl.n) v[u] = *reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c);
+    }
+#pragma unroll
+    for (int u = 0; u < kImgBatch; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < total) dst[(int64_t)(c0 + idx / tl.n_pad) * tl.n_pad + idx % tl.n_pad] = bf16x8_to_f16x8(v[u]);
+    }
   }
 }
 
@@ -417,6 +448,8 @@ __global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const flo
                                   const int* __restrict__ pos, const int* __restrict__ ids, int e0, int n_e, int T,
                                   int k, int H, bool shared, const __nv_bfloat16* __restrict__ xres,
                                   __nv_bfloat16* __restrict__ y) {
+  griddep_launch_dependents();
+  griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   const int t = blockIdx.x;
   __shared__ float g[kMaxTopK];
   __shared__ int ps[kMaxTopK];
@@ -440,11 +473,19 @@ __global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const flo
     float acc[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) acc[m] = 0.f;
-    for (int j = 0; j < kh; ++j) {
-      const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)ps[j] * H + 8 * c);
-      const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+    // the slots' loads in flight 8 at a time, then their sums (in slot order)
+    for (int j0 = 0; j0 < kh; j0 += 8) {
+      uint4 zu[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] += g[j] * __bfloat162float(b[m]);
+      for (int j = 0; j < 8; ++j)
+        if (j0 + j < kh) zu[j] = *reinterpret_cast<const uint4*>(z + (int64_t)ps[j0 + j] * H + 8 * c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j0 + j < kh) {
+          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&zu[j]);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) acc[m] += g[j0 + j] * __bfloat162float(b[m]);
+        }
     }
     if (shared) {
       const uint4 u = *reinterpret_cast<const uint4*>(z + (int64_t)(T * k + t) * H + 8 * c);
@@ -597,8 +638,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
 
   PrepParams pp{static_cast<const __nv_bfloat16*>(x), T, H, k, n_sh, n_rt_items + n_gu_sh * n_sh, S->tiles,
                 S->counters, S->xg};
-  lt_prep_kernel<<<dim3(n_sh, kColSlices), 256, 0, st>>>(pp);
-  LT_CK(cudaGetLastError());
+  LT_CK(launch_pdl(lt_prep_kernel, dim3(n_sh, kColSlices), 256, 0, st, pp));
 
   LtGemmParams g{};
   g.tiles = S->tiles;
@@ -621,25 +661,23 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   const int warps = 8;
   const unsigned tgrid = (unsigned)((T + warps - 1) / warps);
   const int nper = (E + 31) / 32;
-#define LT_TOPK(NP) \
-  lt_topk_kernel<NP><<<tgrid, warps * 32, 0, st>>>(S->logits, L->router_b, T, E, S->E_pad128, k, S->ids, S->gates)
-  if (nper <= 4) LT_TOPK(4);
-  else if (nper <= 8) LT_TOPK(8);
-  else if (nper <= 12) LT_TOPK(12);
-  else if (nper <= 16) LT_TOPK(16);
-  else LT_TOPK(32);
+#define LT_TOPK(NP)                                                                                               \
+  launch_pdl(lt_topk_kernel<NP>, tgrid, warps * 32, 0, st, (const float*)S->logits, (const float*)L->router_b, T, E, \
+             S->E_pad128, k, S->ids, S->gates)
+  if (nper <= 4) LT_CK(LT_TOPK(4));
+  else if (nper <= 8) LT_CK(LT_TOPK(8));
+  else if (nper <= 12) LT_CK(LT_TOPK(12));
+  else if (nper <= 16) LT_CK(LT_TOPK(16));
+  else LT_CK(LT_TOPK(32));
 #undef LT_TOPK
-  LT_CK(cudaGetLastError());
 
   PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, L->e0, L->n_e, S->offsets, S->perm, S->pos,
                S->tiles, S->counters};
-  lt_perm_kernel<<<1, kPermThreads, S->perm_smem, st>>>(P);
-  LT_CK(cudaGetLastError());
+  LT_CK(launch_pdl(lt_perm_kernel, 1, kPermThreads, S->perm_smem, st, P));
 
   const int max_routed = S->max_tiles - (L->T_max + kLtMaxN - 1) / kLtMaxN;
-  lt_gather_kernel<<<dim3(max_routed, kColSlices), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), S->perm,
-                                                                  S->tiles, S->counters, n_sh, k, H, S->xg);
-  LT_CK(cudaGetLastError());
+  LT_CK(launch_pdl(lt_gather_kernel, dim3(max_routed, kColSlices), 256, 0, st, static_cast<const __nv_bfloat16*>(x),
+                   (const int*)S->perm, (const LtTile*)S->tiles, (const int*)S->counters, n_sh, k, H, S->xg));
 
   // routed gate/up
   g.n_items = S->counters + 7; g.queue = S->counters + 1; g.exit_cnt = S->counters + 4;
@@ -650,10 +688,9 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   g.n_rt_items = 0; g.tile_kind = kItemDN; g.tile0 = L->Ish > 0 ? 0 : n_sh; g.n_rt_tile = H / 128;
   LT_CK(lt_gemm_launch(g, grid, st));
 
-  lt_combine_kernel<<<T, 256, 0, st>>>(S->z, S->gates, S->pos, S->ids, L->e0, L->n_e, T, k, H, L->Ish > 0,
-                                       residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
-                                       static_cast<__nv_bfloat16*>(y));
-  LT_CK(cudaGetLastError());
+  LT_CK(launch_pdl(lt_combine_kernel, T, 256, 0, st, (const __nv_bfloat16*)S->z, (const float*)S->gates,
+                   (const int*)S->pos, (const int*)S->ids, L->e0, L->n_e, T, k, H, L->Ish > 0,
+                   residual ? static_cast<const __nv_bfloat16*>(x) : nullptr, static_cast<__nv_bfloat16*>(y)));
   return cudaSuccess;
 }
 

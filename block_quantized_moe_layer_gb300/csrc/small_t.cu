@@ -401,9 +401,11 @@ __device__ void producer_loop(const SmallParams& P, uint8_t* smem, const SmemPla
       if (!ok) break;
       head = pos + g.need;
       const int s = issued & (NS - 1);
-      write_desc(descs + s, g, q, pos);
       uint8_t* stage = smem + plan.ring + pos;
-      if (!(issued == 0 && (int)blockIdx.x < NR + NSG)) {  // (the first stage's weights are on their way)
+      // (a block's first stage: its descriptor and weights were issued before
+      // the dependency wait)
+      if (!(issued == 0 && (int)blockIdx.x < NR + NSG)) {
+        write_desc(descs + s, g, q, pos);
         mbar_arrive_expect_tx(&full[s], g.wb + (uint32_t)g.M * g.per);
         if (g.wb) bulk_g2s_hint(stage, g.wbase + (int64_t)q * g.wb, g.wb, &full[s], wpol);
       }
@@ -526,6 +528,10 @@ __host__ __device__ constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 *
 // expert index among them wins by a second warp min, only then); the winning
 // lane writes the slot and drops its head.
 //
+// This code runs once per launch, so its instructions are cold: the first
+// read of the words, complete or not, also runs the selection (results
+// overwritten later), so that the pass on the complete words finds it warm.
+//
 template <int NPER>
 __device__ __forceinline__ bool topk_token(const SmallParams& P, int t, int* ids, float* vals, float* gates) {
   const int lane = threadIdx.x & 31;
@@ -533,6 +539,7 @@ __device__ __forceinline__ bool topk_token(const SmallParams& P, int t, int* ids
   constexpr int NP = pow2_at_least(NPER);
   constexpr int NL = NP < kMaxTopK ? NP : kMaxTopK;  // (sorted lists) a lane wins at most k <= kMaxTopK rounds
   uint64_t t0 = 0;
+  bool warm = false;
   while (true) {
     uint64_t c[NP];
     bool done = true;
@@ -549,7 +556,7 @@ __device__ __forceinline__ bool topk_token(const SmallParams& P, int t, int* ids
     }
     done = __all_sync(0xffffffffu, done);
     if (done && t == 0 && lane == 0) stamp_last(P.stamps, kTsRouterDone);
-    if (done) {
+    if (done || !warm) {
       // up to 16 per lane: sorted, the head dropped per win; more (E > 512):
       // unsorted, the lane's best found again by a tree per win (a 32-input
       // network needs more registers than the kernel has)
@@ -590,7 +597,8 @@ __device__ __forceinline__ bool topk_token(const SmallParams& P, int t, int* ids
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       if (lane < k) gates[lane] = ex / sum;
       __syncwarp();
-      break;
+      if (done) break;
+      warm = true;
     }
     int stop = 0;
     if (lane == 0) {
@@ -646,10 +654,7 @@ int finalize_misc_bytes(int T, int E, int k) { return fin_layout(T, E, k).end + 
 // slot is lt + rank (experts ascending, tokens ascending within an expert).
 // The first pair of an expert owns that expert's entries: its entry index is
 // the number of entries of all lower experts.
-//
-// Not inlined: one copy of the code for both callers (and both activation
-// widths), and its registers are its own.
-__device__ __noinline__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend, bool polled) {
+__device__ __forceinline__ void finalize_routing(const SmallParams& P, uint8_t* misc, int* pend, bool polled) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NT = kConsumerWarps * 32;
   const int T = P.T, E = P.E, k = P.k, Tk = P.T * P.k;
@@ -1402,6 +1407,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
     const int b = blockIdx.x, nr = P.n_rg * P.n_kt;
     const Geo g = b < nr ? geo_router<L>(P, b / P.n_kt, b % P.n_kt)
                          : geo_expert<L>(P, kGateUp, (b - nr) / P.n_gu_sh, (b - nr) % P.n_gu_sh, nullptr);
+    // the descriptor first: the arrival below releases it to the consumers
+    write_desc(reinterpret_cast<Desc*>(smem + plan.descs), g, 0, 0);
     mbar_arrive_expect_tx(&full[0], g.wb + (uint32_t)g.M * g.per);
     bulk_g2s_hint(smem + plan.ring, g.wbase, g.wb, &full[0], l2_evict_first_policy());
   } else if ((threadIdx.x >> 5) < kConsumerWarps && (int)blockIdx.x < P.n_rg * P.n_kt) {
