@@ -1473,7 +1473,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_small_t_kernel(const __grid_c
       P.sync->n_rent = 0;
       P.sync->exit_cnt = 0;
     }
-    __threadfence();
+    // (no fence: the grid's completion makes these writes visible to the
+    // next launch, whose dependency wait waits for it)
   }
 }
 
