@@ -40,6 +40,7 @@ struct LtState {
   int* status = nullptr;    // [4]
   float* logits = nullptr;  // [planes][T_max][E_pad128]
   int* ids = nullptr;
+  uint32_t* bits = nullptr;  // [E][ceil(T_max/32)] tokens that chose each expert (one bit per token)
   float* gates = nullptr;
   int* pos = nullptr;
   int* perm = nullptr;
@@ -48,12 +49,9 @@ struct LtState {
   uint8_t* xg = nullptr;
   uint8_t* h = nullptr;
   __nv_bfloat16* z = nullptr;
-  int perm_smem = 0;
 };
 
 namespace {
-
-constexpr int kPermThreads = 1024;
 
 __host__ __device__ inline int round16(int v) { return (v + 15) & ~15; }
 
@@ -168,6 +166,8 @@ struct PrepParams {
   LtTile* tiles;
   int* counters;
   uint8_t* xg;
+  uint32_t* bits;  // [E][ceil(T/32)], zeroed here for lt_topk
+  int n_bits;
 };
 
 constexpr int kColSlices = 8;  // column slices per token tile in the operand-image kernels
@@ -187,6 +187,10 @@ __global__ void lt_prep_kernel(const PrepParams P) {
       P.tiles[i] = LtTile{-1, P.T * P.k + kLtMaxN * i, ni, round16(ni), kLtMaxN * i, {0, 0, 0}};
     }
     if (threadIdx.x == 0) P.counters[6] = P.n_items1;
+  }
+  {
+    const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = b * blockDim.x + threadIdx.x; i < P.n_bits; i += nb * blockDim.x) P.bits[i] = 0u;
   }
   uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)kLtMaxN * tt * P.H * 2);
   const int nc = P.H / 8 / kColSlices, c0 = cs * nc;
@@ -216,7 +220,8 @@ __device__ __forceinline__ bool topk_better(float v, int i, float bv, int bi) {
 // One warp per token.  NPER = experts per lane (lane l holds e = l + 32 i).
 template <int NPER>
 __global__ void lt_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
-                               int E_pad, int k, int* __restrict__ ids, float* __restrict__ gates) {
+                               int E_pad, int k, int* __restrict__ ids, float* __restrict__ gates,
+                               uint32_t* __restrict__ bits) {
   griddep_launch_dependents();
   griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -270,47 +275,20 @@ __global__ void lt_topk_kernel(const float* __restrict__ logits, const float* __
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
       if (j < k) s += expf(sel[j] - sel[0]);
+    const int W = (T + 31) / 32;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
       if (j < k) {
         ids[t * k + j] = seli[j];
         gates[t * k + j] = expf(sel[j] - sel[0]) / s;
+        atomicOr(&bits[(int64_t)seli[j] * W + (t >> 5)], 1u << (t & 31));  // token t chose expert seli[j]
       }
   }
 }
 
-// Exclusive scan of one int per thread over the block (blockDim.x == 1024).
-__device__ int block_excl_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_tot[lane];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    warp_tot[lane] = wi - w;
-    if (lane == 31) warp_tot[32] = wi;
-  }
-  __syncthreads();
-  const int r = x - v + warp_tot[warp];
-  *total = warp_tot[32];
-  __syncthreads();
-  return r;
-}
-
 struct PermParams {
   const int* ids;
+  const uint32_t* bits;  // [E][ceil(T/32)]: bit t of expert e set when token t chose e
   int T, E, k, H, I, Ish, n_sh, prow_sh;
   int e0, n_e;  // routed experts held: token tiles only for [e0, e0 + n_e), by local index
   int* offsets;
@@ -320,88 +298,149 @@ struct PermParams {
   int* counters;
 };
 
-constexpr int kPermChunk = 512;  // tokens per pass (16 bitmap words per expert)
+constexpr int kPermWarps = 8;  // experts per block in lt_perm (one warp each)
 
-// Single CTA of 1024 threads.  Pair p = t*k + j goes to slot
-// offsets[e] + (number of tokens t' < t that chose e): an expert's tokens
-// are a bitmap over the tokens of a pass, and a pair's rank is the popcount
-// of the bits below its token plus the expert's count in earlier words and
-// passes.  The k experts of one token are distinct, so the order of pairs
-// within an expert is the order of their tokens.
-__global__ void __launch_bounds__(kPermThreads, 1) lt_perm_kernel(const PermParams P) {
+// Pair p = t*k + j goes to slot offsets[e] + (number of tokens t' < t that
+// chose e): expert e's tokens are the set bits of its bitmap row, so a
+// pair's rank is the popcount of the bits below its token.  The k experts of
+// one token are distinct, so the order of pairs within an expert is the
+// order of their tokens.
+//
+// Every block reads all the rows' popcounts (one warp reduction per expert)
+// and scans them, so it knows every expert's offset and tile position
+// without waiting for another block; then warp w scatters expert
+// blockIdx.x * kPermWarps + w and writes its token tiles.
+__global__ void __launch_bounds__(kPermWarps * 32) lt_perm_kernel(const PermParams P) {
   griddep_launch_dependents();
   griddep_wait();  // (the previous kernel in the stream wrote what this one reads, or reads what it writes)
-  extern __shared__ int psm[];
-  const int E = P.E, k = P.k, T = P.T;
-  constexpr int W = kPermChunk / 32;
-  int* cnt = psm;                                      // [E]
-  int* off = cnt + E;                                  // [E]
-  int* run = off + E;                                  // [E] tokens of e in earlier passes
-  unsigned* bits = reinterpret_cast<unsigned*>(run + E);  // [E][W]
-  int* pre = reinterpret_cast<int*>(bits + E * W);     // [E][W] exclusive word prefix
-  __shared__ int wtot[33];
-  const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += kPermThreads) {
-    cnt[e] = 0;
-    run[e] = 0;
-  }
-  __syncthreads();
-  for (int p = tid; p < T * k; p += kPermThreads) atomicAdd(&cnt[P.ids[p]], 1);
-  __syncthreads();
-  int total;
-  {
-    const int c = tid < E ? cnt[tid] : 0;
-    const int ex = block_excl_scan(c, wtot, &total);
-    if (tid < E) {
-      off[tid] = ex;
-      P.offsets[tid] = ex;
-    }
-    if (tid == 0) P.offsets[E] = total;
-  }
-  __syncthreads();
-  for (int t0 = 0; t0 < T; t0 += kPermChunk) {
-    const int nt = min(kPermChunk, T - t0);
-    for (int i = tid; i < E * W; i += kPermThreads) bits[i] = 0u;
-    __syncthreads();
-    for (int p = tid; p < nt * k; p += kPermThreads) {
-      const int tl = p / k;
-      atomicOr(&bits[P.ids[t0 * k + p] * W + (tl >> 5)], 1u << (tl & 31));
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kPermThreads) {
-      int s = run[e];
-      for (int w = 0; w < W; ++w) {
-        pre[e * W + w] = s;
-        s += __popc(bits[e * W + w]);
+  __shared__ int off_s[kMaxE + 1];  // exclusive prefix of the counts over all experts
+  __shared__ int tb_s[kMaxE];       // ... of the held experts' token tiles
+  __shared__ int pb_s[kMaxE];       // ... of their operand rows
+  __shared__ int wt[3][kPermWarps + 1];
+  const int E = P.E, k = P.k, T = P.T, W = (T + 31) / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // counts: warp w takes experts w, w + 8, ...; lane l the words l, l + 32, ...
+  for (int ea = warp; ea < E; ea += 4 * kPermWarps) {
+    int c[4] = {0, 0, 0, 0};
+    for (int g = lane; g < W; g += 32) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = ea + q * kPermWarps;
+        if (e < E) c[q] += __popc(P.bits[(int64_t)e * W + g]);
       }
-      run[e] = s;
     }
-    __syncthreads();
-    for (int p = tid; p < nt * k; p += kPermThreads) {
-      const int tl = p / k, e = P.ids[t0 * k + p];
-      const unsigned below = bits[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u);
-      const int dest = off[e] + pre[e * W + (tl >> 5)] + __popc(below);
-      P.perm[dest] = t0 * k + p;
-      P.pos[t0 * k + p] = dest;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = ea + q * kPermWarps;
+      const int n = __reduce_add_sync(0xffffffffu, c[q]);
+      if (lane == 0 && e < E) off_s[e] = n;  // the count, for now
     }
-    __syncthreads();
   }
-  // routed token tiles (E <= 1024: thread e handles expert e), for the
-  // experts this layer holds; a tile names its expert by local index
-  const int e = tid;
-  const int M = e < E && e >= P.e0 && e < P.e0 + P.n_e ? cnt[e] : 0;
-  const int ntt = (M + kLtMaxN - 1) / kLtMaxN;
-  const int rows = M > 0 ? kLtMaxN * (ntt - 1) + round16(M - kLtMaxN * (ntt - 1)) : 0;
-  int n_tiles, n_rows;
-  const int tb = block_excl_scan(ntt, wtot, &n_tiles);
-  const int pb = block_excl_scan(rows, wtot, &n_rows);
-  for (int i = 0; i < ntt; ++i) {
-    const int ni = min(kLtMaxN, M - kLtMaxN * i);
-    P.tiles[P.n_sh + tb + i] =
-        LtTile{e - P.e0, off[e] + kLtMaxN * i, ni, round16(ni), P.prow_sh + pb + kLtMaxN * i, {0, 0, 0}};
+  __syncthreads();
+  // exclusive scans of counts, tiles and rows over the experts: thread i
+  // takes experts 4i .. 4i + 3 (E <= 1024 = 4 x 256)
+  int cv[4], tv[4], rv[4], sc = 0, st = 0, sr = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = 4 * tid + q;
+    const int cnt = e < E ? off_s[e] : 0;
+    const int M = e >= P.e0 && e < P.e0 + P.n_e ? cnt : 0;
+    const int ntt = (M + kLtMaxN - 1) / kLtMaxN;
+    cv[q] = cnt;
+    tv[q] = ntt;
+    rv[q] = M > 0 ? kLtMaxN * (ntt - 1) + round16(M - kLtMaxN * (ntt - 1)) : 0;
+    sc += cv[q];
+    st += tv[q];
+    sr += rv[q];
   }
-  if (tid == 0) {
+  int ic = sc, it = st, ir = sr;  // inclusive warp scans
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yc = __shfl_up_sync(0xffffffffu, ic, o), yt = __shfl_up_sync(0xffffffffu, it, o),
+              yr = __shfl_up_sync(0xffffffffu, ir, o);
+    if (lane >= o) {
+      ic += yc;
+      it += yt;
+      ir += yr;
+    }
+  }
+  if (lane == 31) {
+    wt[0][warp] = ic;
+    wt[1][warp] = it;
+    wt[2][warp] = ir;
+  }
+  __syncthreads();  // (every count is read above before any offset is written below)
+  if (tid < 3) {
+    int run = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int v = wt[tid][w];
+      wt[tid][w] = run;
+      run += v;
+    }
+    wt[tid][kPermWarps] = run;
+  }
+  __syncthreads();
+  {
+    int bc = wt[0][warp] + ic - sc, bt = wt[1][warp] + it - st, br = wt[2][warp] + ir - sr;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = 4 * tid + q;
+      if (e < E) {
+        off_s[e] = bc;
+        tb_s[e] = bt;
+        pb_s[e] = br;
+      }
+      bc += cv[q];
+      bt += tv[q];
+      br += rv[q];
+    }
+    if (tid == 0) off_s[E] = wt[0][kPermWarps];
+  }
+  __syncthreads();
+  const int e = blockIdx.x * kPermWarps + warp;
+  if (e < E) {
+    // scatter: lane l takes words l, l + 32, ... of the row; a word's bits
+    // are ranked after the bits of the words before it
+    const int base = off_s[e];
+    int run = 0;
+    for (int g0 = 0; g0 < W; g0 += 32) {
+      const int g = g0 + lane;
+      uint32_t word = g < W ? P.bits[(int64_t)e * W + g] : 0u;
+      const int cw = __popc(word);
+      int incl = cw;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int r = run + incl - cw;
+      while (word) {
+        const int t = g * 32 + __ffs(word) - 1;
+        word &= word - 1u;
+        int j = 0;
+        for (int jj = 0; jj < k; ++jj)
+          if (P.ids[t * k + jj] == e) j = jj;
+        P.perm[base + r] = t * k + j;
+        P.pos[t * k + j] = base + r;
+        ++r;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) P.offsets[e] = base;
+    // routed token tiles of a held expert, by local index
+    if (e >= P.e0 && e < P.e0 + P.n_e) {
+      const int M = off_s[e + 1] - base, ntt = (M + kLtMaxN - 1) / kLtMaxN;
+      for (int i = lane; i < ntt; i += 32) {
+        const int ni = min(kLtMaxN, M - kLtMaxN * i);
+        P.tiles[P.n_sh + tb_s[e] + i] =
+            LtTile{e - P.e0, base + kLtMaxN * i, ni, round16(ni), P.prow_sh + pb_s[e] + kLtMaxN * i, {0, 0, 0}};
+      }
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    const int n_tiles = wt[1][kPermWarps];
     const int n_gu = P.I / 64, n_dn = P.H / 128;
+    P.offsets[E] = off_s[E];
     P.counters[7] = n_tiles * n_gu;                                   // routed gate/up items
     P.counters[8] = (P.Ish > 0 ? P.n_sh : 0) * n_dn + n_tiles * n_dn;  // down items
     P.counters[9] = n_tiles;
@@ -564,6 +603,7 @@ cudaError_t large_t_alloc(moe_layer* L) {
   const size_t o_status = take(16);
   const size_t o_logits = take((size_t)kLtPlanes * Tm * S->E_pad128 * 4);
   const size_t o_ids = take((size_t)Tk * 4);
+  const size_t o_bits = take((size_t)E * ((Tm + 31) / 32) * 4);
   const size_t o_gates = take((size_t)Tk * 4);
   const size_t o_pos = take((size_t)Tk * 4);
   const size_t o_perm = take((size_t)Tk * 4);
@@ -580,6 +620,7 @@ cudaError_t large_t_alloc(moe_layer* L) {
   S->status = reinterpret_cast<int*>(w + o_status);
   S->logits = reinterpret_cast<float*>(w + o_logits);
   S->ids = reinterpret_cast<int*>(w + o_ids);
+  S->bits = reinterpret_cast<uint32_t*>(w + o_bits);
   S->gates = reinterpret_cast<float*>(w + o_gates);
   S->pos = reinterpret_cast<int*>(w + o_pos);
   S->perm = reinterpret_cast<int*>(w + o_perm);
@@ -588,8 +629,6 @@ cudaError_t large_t_alloc(moe_layer* L) {
   S->xg = w + o_xg;
   S->h = w + o_h;
   S->z = reinterpret_cast<__nv_bfloat16*>(w + o_z);
-  S->perm_smem = (3 * E + 2 * E * (kPermChunk / 32)) * 4;
-  LT_CK(cudaFuncSetAttribute(lt_perm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S->perm_smem));
   LT_CK(lt_gemm_configure());
   return cudaSuccess;
 }
@@ -637,7 +676,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   const int n_gu_sh = L->Ish / 64;
 
   PrepParams pp{static_cast<const __nv_bfloat16*>(x), T, H, k, n_sh, n_rt_items + n_gu_sh * n_sh, S->tiles,
-                S->counters, S->xg};
+                S->counters, S->xg, S->bits, E * ((T + 31) / 32)};
   LT_CK(launch_pdl(lt_prep_kernel, dim3(n_sh, kColSlices), 256, 0, st, pp));
 
   LtGemmParams g{};
@@ -663,7 +702,7 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   const int nper = (E + 31) / 32;
 #define LT_TOPK(NP)                                                                                               \
   launch_pdl(lt_topk_kernel<NP>, tgrid, warps * 32, 0, st, (const float*)S->logits, (const float*)L->router_b, T, E, \
-             S->E_pad128, k, S->ids, S->gates)
+             S->E_pad128, k, S->ids, S->gates, S->bits)
   if (nper <= 4) LT_CK(LT_TOPK(4));
   else if (nper <= 8) LT_CK(LT_TOPK(8));
   else if (nper <= 12) LT_CK(LT_TOPK(12));
@@ -671,9 +710,9 @@ cudaError_t large_t_forward(moe_layer* L, const void* x, int T, void* y, bool re
   else LT_CK(LT_TOPK(32));
 #undef LT_TOPK
 
-  PermParams P{S->ids, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, L->e0, L->n_e, S->offsets, S->perm, S->pos,
+  PermParams P{S->ids, S->bits, T, E, k, H, L->I, L->Ish, n_sh, prow_sh, L->e0, L->n_e, S->offsets, S->perm, S->pos,
                S->tiles, S->counters};
-  LT_CK(launch_pdl(lt_perm_kernel, 1, kPermThreads, S->perm_smem, st, P));
+  LT_CK(launch_pdl(lt_perm_kernel, (E + kPermWarps - 1) / kPermWarps, kPermWarps * 32, 0, st, P));
 
   const int max_routed = S->max_tiles - (L->T_max + kLtMaxN - 1) / kLtMaxN;
   LT_CK(launch_pdl(lt_gather_kernel, dim3(max_routed, kColSlices), 256, 0, st, static_cast<const __nv_bfloat16*>(x),
