@@ -171,7 +171,39 @@ struct PrepParams {
 };
 
 constexpr int kColSlices = 8;  // column slices per token tile in the operand-image kernels
-constexpr int kImgBatch = 4;   // loads in flight per thread in the operand-image kernels
+constexpr int kImgSub = 16;    // 16-byte chunks per pass of an operand-image block's shared tile
+
+// One column slice (16-byte chunks [c0, c0 + nc)) of an fp16 operand image:
+// dst[c][r] for r < n_pad (rows past n zero), row r read from row(r).  Each
+// pass goes through a shared tile [kLtMaxN][kImgSub + 1] (the pad keeps the
+// transposed reads free of bank conflicts), so that the loads run along a
+// row and the stores along the rows of a chunk, both coalesced.
+template <typename RowFn>
+__device__ __forceinline__ void image_slice(RowFn row, int n, int n_pad, int c0, int nc, uint4* __restrict__ dst,
+                                            uint4 (*tile)[kImgSub + 1]) {
+  for (int cs = 0; cs < nc; cs += kImgSub) {
+    const int w = min(kImgSub, nc - cs);
+    const int total = n_pad * kImgSub;
+    uint4 v[kLtMaxN * kImgSub / 256];  // at most 4 per thread (256 threads)
+#pragma unroll
+    for (int u = 0; u < kLtMaxN * kImgSub / 256; ++u) {
+      const int idx = threadIdx.x + u * blockDim.x, r = idx / kImgSub, cc = idx % kImgSub;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (idx < total && r < n && cc < w) v[u] = row(r)[c0 + cs + cc];
+    }
+#pragma unroll
+    for (int u = 0; u < kLtMaxN * kImgSub / 256; ++u) {
+      const int idx = threadIdx.x + u * blockDim.x;
+      if (idx < total) tile[idx / kImgSub][idx % kImgSub] = bf16x8_to_f16x8(v[u]);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < w * n_pad; idx += blockDim.x) {
+      const int cc = idx / n_pad, r = idx - cc * n_pad;
+      dst[(int64_t)(c0 + cs + cc) * n_pad + r] = tile[r][cc];
+    }
+    __syncthreads();
+  }
+}
 
 // Block (tt, cs) writes column slice cs of plain token tile tt (x rows
 // [64 tt, 64 tt + 64)) into the operand image; block (0, 0) also writes the
@@ -192,25 +224,12 @@ __global__ void lt_prep_kernel(const PrepParams P) {
     const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = b * blockDim.x + threadIdx.x; i < P.n_bits; i += nb * blockDim.x) P.bits[i] = 0u;
   }
-  uint4* dst = reinterpret_cast<uint4*>(P.xg + (int64_t)kLtMaxN * tt * P.H * 2);
-  const int nc = P.H / 8 / kColSlices, c0 = cs * nc;
-  // kImgBatch independent 16-byte loads in flight per thread, then their stores
-  const int total = n_pad * nc;
-  for (int base = threadIdx.x; base < total; base += kImgBatch * blockDim.x) {
-    uint4 v[kImgBatch];
-#pragma unroll
-    for (int u = 0; u < kImgBatch; ++u) {
-      const int idx = base + u * blockDim.x;
-      const int r = idx % n_pad, c = c0 + idx / n_pad;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (idx < total && r < n) v[u] = *reinterpret_cast<const uint4*>(P.x + (int64_t)(kLtMaxN * tt + r) * P.H + 8 * c);
-    }
-#pragma unroll
-    for (int u = 0; u < kImgBatch; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < total) dst[(int64_t)(c0 + idx / n_pad) * n_pad + idx % n_pad] = bf16x8_to_f16x8(v[u]);
-    }
-  }
+  __shared__ uint4 tile[kLtMaxN][kImgSub + 1];
+  const int nc = P.H / 8 / kColSlices;
+  const uint4* x4 = reinterpret_cast<const uint4*>(P.x);
+  const int64_t rs = P.H / 8, r0 = (int64_t)kLtMaxN * tt;
+  image_slice([&](int r) { return x4 + (r0 + r) * rs; }, n, n_pad, cs * nc, nc,
+              reinterpret_cast<uint4*>(P.xg + r0 * P.H * 2), tile);
 }
 
 __device__ __forceinline__ bool topk_better(float v, int i, float bv, int bi) {
@@ -459,25 +478,12 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
   __shared__ int tok[kLtMaxN];
   for (int r = threadIdx.x; r < tl.n; r += blockDim.x) tok[r] = perm[tl.slot0 + r] / k;
   __syncthreads();
-  uint4* dst = reinterpret_cast<uint4*>(xg + (int64_t)tl.prow0 * H * 2);
-  const int nc = H / 8 / kColSlices, c0 = blockIdx.y * nc;
-  // kImgBatch independent 16-byte loads in flight per thread, then their stores
-  const int total = tl.n_pad * nc;
-  for (int base = threadIdx.x; base < total; base += kImgBatch * blockDim.x) {
-    uint4 v[kImgBatch];
-#pragma unroll
-    for (int u = 0; u < kImgBatch; ++u) {
-      const int idx = base + u * blockDim.x;
-      const int r = idx % tl.n_pad, c = c0 + idx / tl.n_pad;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (idx < total && r < tl.n) v[u] = *reinterpret_cast<const uint4*>(x + (int64_t)tok[r] * H + 8 * c);
-    }
-#pragma unroll
-    for (int u = 0; u < kImgBatch; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < total) dst[(int64_t)(c0 + idx / tl.n_pad) * tl.n_pad + idx % tl.n_pad] = bf16x8_to_f16x8(v[u]);
-    }
-  }
+  __shared__ uint4 tile[kLtMaxN][kImgSub + 1];
+  const int nc = H / 8 / kColSlices;
+  const uint4* x4 = reinterpret_cast<const uint4*>(x);
+  const int64_t rs = H / 8;
+  image_slice([&](int r) { return x4 + (int64_t)tok[r] * rs; }, tl.n, tl.n_pad, blockIdx.y * nc, nc,
+              reinterpret_cast<uint4*>(xg + (int64_t)tl.prow0 * H * 2), tile);
 }
 
 // y[t] = sum_j g[t,j] z[pos[t,j]] + z[T k + t]; one block per token, 8 columns per thread step.
