@@ -489,7 +489,7 @@ __global__ void lt_gather_kernel(const __nv_bfloat16* __restrict__ x, const int*
 // y[t] = sum_j g[t,j] z[pos[t,j]] + z[T k + t]; one block per token, 8 columns per thread step.
 // Pairs whose expert the layer does not hold (an expert-parallel shard) are
 // left out of the sum.
-__global__ void lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const float* __restrict__ gates,
+__global__ void __launch_bounds__(256, 4) lt_combine_kernel(const __nv_bfloat16* __restrict__ z, const float* __restrict__ gates,
                                   const int* __restrict__ pos, const int* __restrict__ ids, int e0, int n_e, int T,
                                   int k, int H, bool shared, const __nv_bfloat16* __restrict__ xres,
                                   __nv_bfloat16* __restrict__ y) {
