@@ -15,12 +15,16 @@
 // Work items, in order (each kind only waits on kinds before it, so every
 // item another item waits for has already been taken by a running CTA):
 //   router tiles     32 experts x 512 columns; each adds its share of the
-//                    logits to a global sum kept as exact 2^-32 fixed point
+//                    logits to a global sum kept as exact 2^-32 fixed point,
+//                    with a count of the shares in the word's low bits
 //                    (integer atomics, so the sum does not depend on the
-//                    order of arrival).  The tiles of the first 32 experts
-//                    also write the activation records of their slice of x.
-//                    The last router tile to finish computes the routing
-//                    (top-k, gates, permutation, expert work entries).
+//                    order of arrival, and a word says when it is complete).
+//                    The tiles of the first 32 experts also write the
+//                    activation records of their slice of x.  The routing
+//                    (top-k, gates, permutation, expert work entries) is
+//                    computed by the last CTA, which has no router tile,
+//                    as soon as it reads complete words (or, with as many
+//                    router tiles as CTAs, by the last router tile's CTA).
 //   shared gate/up   32 outputs (16+16 gate/up rows, twice) x full K
 //   routed gate/up   per routed work entry (<= 4 tokens of one expert)
 //   shared down      128 outputs x full I
@@ -30,7 +34,9 @@
 // shared down tiles come after the routed gate/up ones: claimed earlier they
 // would hold their producers (and leave their rings empty) until the shared
 // gate/up finishes.  Before it waits for the previous kernel in the stream,
-// block i warms L2 with router tile i's weights (constant data).
+// block b copies the weights of its first stage (router tile b or a shared
+// gate/up tile: constant data) and runs the router tile's code once, so that
+// the code is warm when the slice of x arrives.
 // Hand-offs use last-arriver counters: the last gate/up tile of an entry
 // publishes it (its activation records are complete); the last down tile of
 // a 128-row block combines that block of y in slot order.  No floating-point
